@@ -1,0 +1,472 @@
+"""Benchmark: one continuous-batching decode step of PagedAttention on GB300.
+
+A step appends one new token per sequence to the paged KV cache (reshape_and_cache)
+and runs paged_attention_decode over every sequence's full context.  The default
+workload is the LLaMA-2-7B-shaped single layer (64 sequences, context lengths uniform
+in [128, 2048], 32/32 heads, head_dim 128, bf16 KV, shuffled 1.25x block pool).
+
+Printed: one JSON line (rank 0).  `value` is KV-read GB/s over the whole step
+(algorithmic bytes: cached K/V actually attended + q + out + tables + the append),
+inputs resident in HBM.  Inputs are larger than L2 (the pool is >1 GB), so no L2 flush
+is done between steps.
+
+Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                       [--workload NAME]
+For N > 1 run under torch.distributed.run: each rank runs its own independent batch of
+the same shape (weak scaling; the only collectives are the timing barrier and the
+max-over-ranks reduction).
+"""
+
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import torch  # noqa: E402
+import torch.distributed as dist  # noqa: E402
+
+from paged_kv_cache_264_gb300 import roofline, workloads as W  # noqa: E402
+
+METRIC = "paged decode attention: KV-read GB/s (% of HBM peak) and decode steps/s"
+UNIT = "GB/s"
+DEFAULT_WORKLOAD = "llama2_7b"
+FALLBACK_HBM_GBS = 6800.0
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "ncu_traffic.json")
+CSRC = os.path.join(ROOT, "paged_kv_cache_264_gb300", "csrc")
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    for name in sorted(os.listdir(CSRC)):
+        if name.endswith((".cu", ".cuh", ".h")):
+            with open(os.path.join(CSRC, name), "rb") as f:
+                h.update(name.encode() + b"\0" + f.read())
+    with open(os.path.join(ROOT, "include", "pagedkv.h"), "rb") as f:
+        h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def measured_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    return FALLBACK_HBM_GBS, "fallback"
+
+
+def recorded_traffic(workload: str):
+    """Per-launch DRAM bytes of the decode kernel from a committed ncu capture, if it was
+    taken on the current kernel sources."""
+    if not os.path.exists(TRAFFIC_FILE):
+        return None
+    with open(TRAFFIC_FILE) as f:
+        d = json.load(f)
+    rec = d.get(workload)
+    if not rec or rec.get("source_hash") != kernel_source_hash():
+        return None
+    return rec.get("dram_bytes_per_launch")
+
+
+# ------------------------------------------------------------------ distributed
+
+def dist_setup():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1 and not dist.is_initialized():
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        if backend == "nccl":
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend)
+    return rank, world, local
+
+
+def barrier(world):
+    if world > 1:
+        dist.barrier()
+
+
+def max_over_ranks(x: float, world: int, device) -> float:
+    if world == 1:
+        return x
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def sum_over_ranks(x: float, world: int, device) -> float:
+    if world == 1:
+        return x
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.SUM)
+    return float(t.item())
+
+
+# ------------------------------------------------------------------ clocks
+
+class ClockSampler:
+    """nvidia-smi clock / throttle-reason samples during the timed region."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        try:
+            fd, self.path = tempfile.mkstemp(suffix=".csv")
+            os.close(fd)
+            self.out = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "50"],
+                stdout=self.out, stderr=subprocess.DEVNULL)
+            time.sleep(0.3)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+
+    def stop(self):
+        if not self.proc:
+            return None
+        time.sleep(0.1)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.out.close()
+        rows = []
+        with open(self.path) as f:
+            for line in f:
+                parts = [x.strip() for x in line.split(",")]
+                if len(parts) >= 9:
+                    rows.append(parts)
+        os.unlink(self.path)
+        if not rows:
+            return None
+        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        smax = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i].lower() == "active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None, "reasons": reasons,
+                "samples": len(rows)}
+
+
+# ------------------------------------------------------------------ our arm
+
+def run_ours(args, rank, world, local):
+    import paged_kv_cache_264_gb300 as pkv
+    from paged_kv_cache_264_gb300 import build as pkv_build
+
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py needs a CUDA device (there is no CPU path)")
+    pkv_build.build()
+    dev = torch.device("cuda", local if world > 1 else 0)
+    torch.cuda.set_device(dev)
+    spec = W.SPECS[args.workload]
+    w = W.make(args.workload, device=dev)
+    kv = spec.kv_dtype
+    stream = torch.cuda.current_stream(dev)
+
+    pool = pkv.PagedKVPool(w.num_blocks, w.num_kv_heads, w.head_dim, kv, device=dev, fill=0)
+    hist, last = w.history_rows().to(dev), w.last_token_rows().to(dev)
+    slots = w.slot_mapping.to(dev)
+    if hist.numel():
+        pool.reshape_and_cache(w.key[hist].contiguous(), w.value[hist].contiguous(), slots[hist].contiguous())
+    new_k, new_v = w.key[last].contiguous(), w.value[last].contiguous()
+    new_slots = slots[last].contiguous()
+    q = w.q.to(dev)
+    tables = w.block_tables.to(dev)
+    lens = w.context_lens.to(dev)
+    out = torch.empty_like(q)
+    max_ctx = w.max_context_len
+    ws_n = pkv.decode_workspace_bytes(pool, w.num_seqs, w.num_q_heads, max_ctx)
+    ws = torch.empty(max(ws_n, 16), dtype=torch.uint8, device=dev)
+    plan = pkv.decode_plan(pool, w.num_seqs, w.num_q_heads, max_ctx)
+    torch.cuda.synchronize(dev)
+    assert pool.device_error() == 0
+
+    def step():
+        pkv.reshape_and_cache(pool, new_k, new_v, new_slots, stream)
+        pkv.paged_attention_decode(pool, q, tables, lens, w.scale, max_ctx, out=out, workspace=ws,
+                                   stream=stream)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize(dev)
+
+    # ---- timed region: K steps, with decode-only events inside each step
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(args.steps)]
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    clocks = ClockSampler(dev.index if world == 1 else local)
+    barrier(world)
+    torch.cuda.synchronize(dev)
+    clocks.start()
+    launches0 = pkv.launch_count()
+    t0.record(stream)
+    for i in range(args.steps):
+        pkv.reshape_and_cache(pool, new_k, new_v, new_slots, stream)
+        ev[i][0].record(stream)
+        pkv.paged_attention_decode(pool, q, tables, lens, w.scale, max_ctx, out=out, workspace=ws,
+                                   stream=stream)
+        ev[i][1].record(stream)
+    t1.record(stream)
+    torch.cuda.synchronize(dev)
+    launches = pkv.launch_count() - launches0
+    barrier(world)
+    clk = clocks.stop()
+    ms_total = t0.elapsed_time(t1)
+    ms_total = max_over_ranks(ms_total, world, dev)
+    dec_ms = sum(a.elapsed_time(b) for a, b in ev) / args.steps
+    assert pool.device_error() == 0
+
+    sb = roofline.step_bytes(w.context_lens, w.num_q_heads, w.num_kv_heads, w.head_dim, kv)
+    ms_step = ms_total / args.steps
+    total_bytes = sum_over_ranks(float(sb.step) * args.steps, world, dev)
+    value = total_bytes / (ms_total * 1e-3) / 1e9
+    steps_per_s = args.steps * world / (ms_total * 1e-3)
+
+    # ---- end to end through the public API with host buffers
+    e2e = run_e2e(args, pkv, pool, w, new_k, new_v, new_slots, q, tables, lens, max_ctx, ws, sb,
+                  stream, dev, world)
+
+    peak, peak_kind = measured_peaks()
+    achieved = sb.decode / (dec_ms * 1e-3) / 1e9
+    traffic = recorded_traffic(args.workload)
+    kernel = "paged_decode_kernel" + (" + lse_reduce_kernel" if plan["kernels_per_call"] == 2 else "")
+    line = {
+        "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_step, 5),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "bf16" if kv == "bf16" else "int8 KV, fp32 accumulate",
+        "data": "synthetic (seeded N(0,1) bf16 values; seeded lengths and shuffled block pool)",
+        "config": {
+            "workload": args.workload, "description": spec.description,
+            "num_seqs": w.num_seqs, "num_q_heads": w.num_q_heads, "num_kv_heads": w.num_kv_heads,
+            "head_dim": w.head_dim, "kv_dtype": kv, "sum_context_tokens": int(w.context_lens.sum()),
+            "max_context_len": max_ctx, "num_blocks": w.num_blocks,
+            "step": "reshape_and_cache of one new token per sequence + paged_attention_decode",
+            "plan": plan, "l2": "inputs larger than L2 (pool %.2f GB > 129 MB); no flush" % (
+                2 * pool.k_cache.numel() * pool.k_cache.element_size() / 1e9),
+            "parallelism": f"{world} independent replicas" if world > 1 else "single GPU",
+        },
+        "decode_steps_per_s": round(steps_per_s, 1),
+        "pct_of_hbm_peak": round(100 * value / peak, 2),
+        "bytes_per_step": sb.step,
+        "roofline": {
+            "kernel": kernel, "bound": "hbm", "achieved": round(achieved, 2),
+            "peak": peak, "peak_kind": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)" if peak_kind == "measured" else "fallback",
+            "unit": "GB/s", "frac": round(achieved / peak, 4), "traffic": traffic,
+            "algorithmic_bytes_per_launch": sb.decode, "avg_launch_ms": round(dec_ms, 5),
+        },
+        "e2e": e2e,
+        "gpu_launches": int(launches),
+        "clocks": clk,
+    }
+    if rank == 0 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(args.workload, args.cpu_seconds)
+    pool.close()
+    return line
+
+
+def run_e2e(args, pkv, pool, w, new_k, new_v, new_slots, q, tables, lens, max_ctx, ws, sb, stream,
+            dev, world):
+    """Same step through the public API, but every step copies its inputs from pinned
+    host memory and reads the output back."""
+    host = {
+        "q": q.cpu().pin_memory(), "k": new_k.cpu().pin_memory(), "v": new_v.cpu().pin_memory(),
+        "slots": new_slots.cpu().pin_memory(), "tables": tables.cpu().pin_memory(),
+        "lens": lens.cpu().pin_memory(),
+    }
+    dbuf = {k: torch.empty_like(v, device=dev) for k, v in host.items()}
+    out_d = torch.empty_like(q)
+    out_h = torch.empty(q.shape, dtype=q.dtype).pin_memory()
+    h2d = sum(t.numel() * t.element_size() for t in host.values())
+    d2h = out_h.numel() * out_h.element_size()
+
+    def step():
+        for k in host:
+            dbuf[k].copy_(host[k], non_blocking=True)
+        pkv.reshape_and_cache(pool, dbuf["k"], dbuf["v"], dbuf["slots"], stream)
+        pkv.paged_attention_decode(pool, dbuf["q"], dbuf["tables"], dbuf["lens"], w.scale, max_ctx,
+                                   out=out_d, workspace=ws, stream=stream)
+        out_h.copy_(out_d, non_blocking=True)
+
+    for _ in range(max(3, args.warmup)):
+        step()
+    torch.cuda.synchronize(dev)
+    n = max(10, min(args.steps, 500))
+    barrier(world)
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    for _ in range(n):
+        step()
+    b.record(stream)
+    torch.cuda.synchronize(dev)
+    barrier(world)
+    ms = max_over_ranks(a.elapsed_time(b), world, dev)
+    total = sum_over_ranks(float(sb.step) * n, world, dev)
+    return {"value": round(total / (ms * 1e-3) / 1e9, 2), "unit": UNIT, "steps": n,
+            "ms_per_step": round(ms / n, 5), "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
+
+
+# ------------------------------------------------------------------ oracle legs
+
+def oracle_sample(workload: str, target_s: float):
+    """A bounded sample of the workload for the CPU oracle: the first k sequences (values
+    regenerated on the host), their blocks compacted into an oracle-side pool, the append
+    rows, and the algorithmic bytes of that sample's step."""
+    import numpy as np
+
+    import oracle
+
+    o = oracle.load()
+    spec = W.SPECS[workload]
+    lens_all = W.context_lens_of(workload)
+    order = list(range(spec.num_seqs))
+
+    def build(k):
+        w = W.make(workload, seqs=order[:k])
+        shape_tok = w.num_tokens
+        nblk = (w.context_lens.numpy() + 15) // 16
+        nb = int(nblk.sum())
+        tab = np.full((k, int(nblk.max())), -1, np.int32)
+        c = 0
+        for i, n in enumerate(nblk):
+            tab[i, :n] = np.arange(c, c + n)
+            c += n
+        lens = w.context_lens.numpy().astype(np.int32)
+        slots = np.empty(shape_tok, np.int32)
+        for i in range(k):
+            lo = int(w.seq_offsets[i])
+            t = np.arange(int(lens[i]))
+            slots[lo:lo + lens[i]] = tab[i, t // 16] * 16 + t % 16
+        shape = (nb, w.num_kv_heads, 16, w.head_dim)
+        key, value = W.bf16_bits(w.key), W.bf16_bits(w.value)
+        hist, last = w.history_rows().numpy(), w.last_token_rows().numpy()
+        if spec.kv_dtype == "bf16":
+            pool = dict(k_cache=np.zeros(shape, np.uint16), v_cache=np.zeros(shape, np.uint16))
+            o.reshape_and_cache_bf16(key[hist], value[hist], slots[hist], pool["k_cache"], pool["v_cache"])
+        else:
+            pool = dict(k_cache=np.zeros(shape, np.int8), v_cache=np.zeros(shape, np.int8),
+                        k_scale=np.zeros(shape[:3], np.float32), v_scale=np.zeros(shape[:3], np.float32))
+            o.reshape_and_cache_int8(key[hist], value[hist], slots[hist], pool["k_cache"], pool["v_cache"],
+                                     pool["k_scale"], pool["v_scale"])
+        args = dict(q=W.bf16_bits(w.q), key=key[last], value=value[last], slots=slots[last], tab=tab,
+                    lens=lens, scale=w.scale)
+        sb = roofline.step_bytes(w.context_lens, w.num_q_heads, w.num_kv_heads, w.head_dim, spec.kv_dtype)
+        return pool, args, sb
+
+    def run(pool, a):
+        if spec.kv_dtype == "bf16":
+            o.reshape_and_cache_bf16(a["key"], a["value"], a["slots"], pool["k_cache"], pool["v_cache"])
+            o.paged_decode(a["q"], pool["k_cache"], pool["v_cache"], a["tab"], a["lens"], a["scale"])
+        else:
+            o.reshape_and_cache_int8(a["key"], a["value"], a["slots"], pool["k_cache"], pool["v_cache"],
+                                     pool["k_scale"], pool["v_scale"])
+            o.paged_decode(a["q"], pool["k_cache"], pool["v_cache"], a["tab"], a["lens"], a["scale"],
+                           pool["k_scale"], pool["v_scale"])
+
+    # calibrate on one sequence, then size the sample to about target_s per step
+    pool, a, sb = build(1)
+    t = time.perf_counter()
+    run(pool, a)
+    per_token = (time.perf_counter() - t) / max(1, int(lens_all[0]))
+    k, tokens = 0, 0
+    while k < spec.num_seqs and (tokens + int(lens_all[k])) * per_token <= target_s:
+        tokens += int(lens_all[k])
+        k += 1
+    k = max(k, 1)
+    pool, a, sb = build(k)
+    return o, pool, a, sb, run, k
+
+
+def cpu_baseline(workload: str, seconds: float):
+    o, pool, a, sb, run, k = oracle_sample(workload, seconds)
+    t = time.perf_counter()
+    n = 0
+    while True:
+        run(pool, a)
+        n += 1
+        if time.perf_counter() - t >= seconds * 0.5:
+            break
+    dt = (time.perf_counter() - t) / n
+    return {"value": round(sb.step / dt / 1e9, 4), "unit": UNIT, "cores": o.max_threads(),
+            "kind": "oracle",
+            "sample": f"first {k} of {W.SPECS[workload].num_seqs} sequences, full step (append + decode), "
+                      f"{n} repetition(s), {dt:.3f} s each, fp64 C oracle with OpenMP"}
+
+
+def run_reference(args, rank, world):
+    """The reference arm: the CPU oracle, unchanged, on a bounded sample per step."""
+    if rank != 0:
+        return None
+    budget = 120.0
+    per_step = max(0.02, budget / max(1, args.steps + args.warmup))
+    o, pool, a, sb, run, k = oracle_sample(args.workload, per_step)
+    for _ in range(args.warmup):
+        run(pool, a)
+    t = time.perf_counter()
+    for _ in range(args.steps):
+        run(pool, a)
+    dt = time.perf_counter() - t
+    value = sb.step * args.steps / dt / 1e9
+    spec = W.SPECS[args.workload]
+    sample = (f"first {k} of {spec.num_seqs} sequences per step (append + decode), "
+              f"fp64 C oracle with OpenMP")
+    return {
+        "impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(1e3 * dt / args.steps, 4),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic (seeded)", "config": {"workload": args.workload, "description": spec.description},
+        "cpu_baseline": {"value": round(value, 4), "unit": UNIT, "cores": o.max_threads(), "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": round(value, 4), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", choices=sorted(W.SPECS), default=DEFAULT_WORKLOAD)
+    ap.add_argument("--cpu-seconds", type=float, default=12.0,
+                    help="CPU work for the oracle baseline sample")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    rank, world, local = dist_setup()
+    if args.impl == "reference":
+        line = run_reference(args, rank, world)
+    else:
+        line = run_ours(args, rank, world, local)
+    if rank == 0 and line is not None:
+        print(json.dumps(line), flush=True)
+    if world > 1 and dist.is_initialized():
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

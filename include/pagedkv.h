@@ -1,0 +1,219 @@
+/*
+ * pagedkv.h -- C ABI of a GB300 (sm_103a) library for PagedAttention decode.
+ *
+ * The problem, as the pages state it ("Lesson 4: Model deployment and inference
+ * acceleration", section 4.2 "PagedAttention: virtual-memory-style KV management";
+ * "Efficient AI Lecture 13: LLM Deployment Techniques", section "PagedAttention"):
+ * the KV cache is cut into fixed blocks of 16 tokens taken from one pre-allocated
+ * pool; every request keeps a page table (block table) from its logical blocks to
+ * physical blocks; attention fetches the blocks wherever they sit, and the result is
+ * plain attention softmax(q K^T / sqrt(d)) V over the request's tokens.
+ *
+ * Conventions for every call:
+ *  - Pointers named "device" point to GPU memory that the caller allocated and owns;
+ *    the library never frees caller memory.  Pointers named "host" point to host memory.
+ *  - Work is enqueued on the caller's stream (a cudaStream_t passed as void*; NULL is
+ *    the legacy default stream) and runs asynchronously.  Calls do not synchronise,
+ *    except pkv_get_device_error, which waits for its own stream.
+ *  - Every call validates its host-side arguments before launching anything and
+ *    returns a status; no exception crosses the ABI.  A launch failure maps to
+ *    PKV_ERR_CUDA (the CUDA error text is available from pkv_last_cuda_error).
+ *  - Device-side checks never trap: an out-of-range block id, slot or context length
+ *    found by a kernel sets a bit in the pool's device error word (see
+ *    pkv_get_device_error), and the offending access is skipped.
+ *  - Layouts are row-major ("C order"); element sizes are those of the named types.
+ *  - Calls on one pool must be ordered on one stream (or otherwise serialised): the
+ *    pool's device error word is shared by its calls.
+ */
+#ifndef PAGEDKV_H_
+#define PAGEDKV_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+/* Exported symbols (the library is built with hidden visibility by default). */
+#if defined(__GNUC__)
+#define PKV_API __attribute__((visibility("default")))
+#else
+#define PKV_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Tokens per physical block; fixed ("Lesson 4", 4.2: 16 tokens per block by default). */
+#define PKV_BLOCK_SIZE 16
+
+typedef enum pkv_status {
+  PKV_OK = 0,
+  PKV_ERR_INVALID_ARG = 1, /* a pointer, size or layout argument is invalid         */
+  PKV_ERR_UNSUPPORTED = 2, /* valid but not built (head_dim, group size, ...)        */
+  PKV_ERR_CUDA = 3,        /* a CUDA runtime call or kernel launch failed            */
+  PKV_ERR_WORKSPACE = 4    /* the workspace passed is smaller than the call needs    */
+} pkv_status;
+
+typedef enum pkv_kv_dtype {
+  /* K/V stored as bf16. */
+  PKV_KV_BF16 = 0,
+  /* K/V stored as int8 codes with one fp32 scale per (token, kv head) row, symmetric:
+   * s = max|x| / 127, code = round(x / s) ("Lesson 4", 5.3 "KV Cache Quantization"). */
+  PKV_KV_INT8 = 1
+} pkv_kv_dtype;
+
+/* Bits of the device error word. */
+#define PKV_DEVERR_BLOCK_ID 0x1u    /* a block-table entry read by decode was < 0 or >= num_blocks */
+#define PKV_DEVERR_CONTEXT_LEN 0x2u /* a context length was < 1 or > max_context_len            */
+#define PKV_DEVERR_SLOT 0x4u        /* a slot_mapping entry was >= num_blocks * 16               */
+#define PKV_DEVERR_TIMEOUT 0x8u     /* an asynchronous copy did not arrive within the time limit */
+
+/* Opaque, host-owned pool descriptor. */
+typedef struct pkv_pool pkv_pool;
+
+/* Text for a status code (static storage). */
+PKV_API const char* pkv_status_string(pkv_status status);
+
+/* Text of the last CUDA error seen by this thread inside the library (static per thread). */
+PKV_API const char* pkv_last_cuda_error(void);
+
+/* Library version string, e.g. "0.1.0". */
+PKV_API const char* pkv_version(void);
+
+/*
+ * Bytes the caller must allocate for a pool ("Lesson 4", 4.2: one global, pre-allocated
+ * block pool).  *kv_bytes_each receives the size of the K array (the V array has the
+ * same size): num_blocks * kv_heads * 16 * head_dim * element size.  *scale_bytes_each
+ * receives the size of each fp32 scale array, num_blocks * kv_heads * 16 * 4, or 0 for
+ * bf16.  Either output pointer may be NULL.
+ * Errors: PKV_ERR_INVALID_ARG for num_blocks < 1, kv_heads < 1, head_dim < 1 or an
+ * unknown dtype.
+ */
+PKV_API pkv_status pkv_pool_bytes(int64_t num_blocks, int kv_heads, int head_dim, pkv_kv_dtype dtype,
+                          size_t* kv_bytes_each, size_t* scale_bytes_each);
+
+/*
+ * Describe a pool of physical KV blocks that the caller has allocated on the current
+ * device ("Lesson 4", 4.2, global block pool).
+ *   k_cache, v_cache (device): [num_blocks, kv_heads, 16, head_dim] of bf16 or int8,
+ *                              each 16-byte aligned.
+ *   k_scale, v_scale (device): [num_blocks, kv_heads, 16] fp32 for PKV_KV_INT8, 16-byte
+ *                              aligned; must be NULL for PKV_KV_BF16.
+ *   block_size must be PKV_BLOCK_SIZE.
+ * The library records the pointers and allocates a small device error word for the
+ * pool on the current device (freed by pkv_pool_destroy).  The pool contents are not
+ * touched.  *out receives the descriptor.
+ * Errors: PKV_ERR_INVALID_ARG (NULL or misaligned pointers, bad sizes, scales given for
+ * bf16 or missing for int8); PKV_ERR_UNSUPPORTED (head_dim not 64 or 128, block_size
+ * not 16); PKV_ERR_CUDA (no device, allocation failure).
+ */
+PKV_API pkv_status pkv_pool_create(int64_t num_blocks, int kv_heads, int head_dim, int block_size,
+                           pkv_kv_dtype dtype, void* k_cache, void* v_cache, float* k_scale,
+                           float* v_scale, pkv_pool** out);
+
+/* Free the descriptor and its device error word (not the caller's arrays).  NULL is a no-op. */
+PKV_API pkv_status pkv_pool_destroy(pkv_pool* pool);
+
+/*
+ * Append new tokens' K and V to the cache: for token t and kv head h,
+ *   slot = slot_mapping[t], block = slot / 16, offset = slot % 16,
+ *   k_cache[block][h][offset][:] = key[t][h][:]   (and the same for V).
+ * Only the new tokens' K/V are written ("Lesson 4", 4.2; "LLM Engineer's Handbook --
+ * inference optimisation", section "KV cache").  For an INT8 pool each (t, h) row of
+ * key and of value is quantised on the way in ("Lesson 4", 5.3):
+ *   s = max_c |x_c| / 127 (fp32, IEEE division), code_c = round_half_even(x_c / s),
+ *   clamped to [-127, 127]; a row of zeros stores s = 0 and zero codes;
+ *   k_scale[block][h][offset] = s.
+ *   key, value   (device): bf16 [num_tokens, kv_heads, head_dim], 16-byte aligned.
+ *   slot_mapping (device): int32 [num_tokens]; a negative slot skips that token.
+ * Slots must be distinct among the tokens of one call (two writes to one slot race).
+ * A slot >= num_blocks * 16 is skipped and sets PKV_DEVERR_SLOT.
+ * num_tokens == 0 is a no-op.  Errors: PKV_ERR_INVALID_ARG, PKV_ERR_CUDA.
+ */
+PKV_API pkv_status pkv_reshape_and_cache(const pkv_pool* pool, const void* key, const void* value,
+                                 const int32_t* slot_mapping, int64_t num_tokens, void* stream);
+
+/*
+ * Decode-plan knobs.  Zero-initialise and set what you need; zero means automatic.
+ *   partition_blocks: context partition (split-K) size in 16-token blocks; each
+ *     (sequence, kv head, partition) becomes one work item, and sequences longer than
+ *     one partition are combined by a log-sum-exp reduce.  0 = chosen from the batch
+ *     shape and the device's SM count.
+ */
+typedef struct pkv_decode_options {
+  int partition_blocks;
+  int reserved[7];
+} pkv_decode_options;
+
+/*
+ * Bytes of device workspace that pkv_paged_attention_decode needs for this batch shape
+ * (0 when no sequence is split).  max_context_len is the largest context length the
+ * call will see.  options may be NULL.
+ */
+PKV_API pkv_status pkv_decode_workspace_bytes(const pkv_pool* pool, int num_seqs, int num_q_heads,
+                                      int max_context_len, const pkv_decode_options* options,
+                                      size_t* bytes);
+
+/*
+ * The plan the decode call would use for this shape: partition size in blocks, the
+ * largest number of partitions of one sequence, and kernels launched per call (1 or 2).
+ * Any output pointer may be NULL.
+ */
+PKV_API pkv_status pkv_decode_plan(const pkv_pool* pool, int num_seqs, int num_q_heads,
+                           int max_context_len, const pkv_decode_options* options,
+                           int* partition_blocks, int* max_partitions, int* kernels_per_call);
+
+/*
+ * PagedAttention decode: one new query token per sequence attends over the sequence's
+ * cached tokens ("Lesson 4", 4.2, attention-invariance equation):
+ *   out[b][h][:] = sum_{t < T_b} softmax_t(scale * q[b][h] . K_b[t]) V_b[t]
+ * where token t of sequence b lives in physical block block_tables[b][t / 16] at offset
+ * t % 16, T_b = context_lens[b], and query head h reads kv head h / (num_q_heads /
+ * kv_heads) (contiguous GQA groups; "LLM/MLLM inference optimisation", 2.3).  For an
+ * INT8 pool K and V are the dequantised values s * code.  Accumulation is fp32; out is
+ * rounded to bf16 (round to nearest even).
+ *   q            (device): bf16 [num_seqs, num_q_heads, head_dim], 16-byte aligned.
+ *   block_tables (device): int32 [num_seqs, max_blocks_per_seq]; entries past
+ *                          ceil(T_b / 16) are never read.
+ *   context_lens (device): int32 [num_seqs], 1 <= T_b <= max_context_len.
+ *   max_context_len (host int): an upper bound on every T_b; it sizes the plan and the
+ *                          workspace and must be <= max_blocks_per_seq * 16.
+ *   scale: softmax scale, usually 1 / sqrt(head_dim).
+ *   out          (device): bf16 [num_seqs, num_q_heads, head_dim].
+ *   workspace    (device): at least pkv_decode_workspace_bytes(...) bytes, 16-byte
+ *                          aligned; may be NULL when that size is 0.  Its contents need no
+ *                          initialisation and are overwritten.
+ * A sequence whose T_b is out of range gets a zero output and sets
+ * PKV_DEVERR_CONTEXT_LEN; a block id out of range is skipped and sets
+ * PKV_DEVERR_BLOCK_ID.  num_seqs == 0 is a no-op.
+ * num_q_heads must be a multiple of kv_heads with a group size of 1, 2, 4 or 8
+ * (else PKV_ERR_UNSUPPORTED).  Errors: PKV_ERR_INVALID_ARG, PKV_ERR_UNSUPPORTED,
+ * PKV_ERR_WORKSPACE, PKV_ERR_CUDA.
+ */
+PKV_API pkv_status pkv_paged_attention_decode(const pkv_pool* pool, const void* q,
+                                      const int32_t* block_tables, int max_blocks_per_seq,
+                                      const int32_t* context_lens, int num_seqs, int num_q_heads,
+                                      int max_context_len, float scale, void* out,
+                                      void* workspace, size_t workspace_bytes, void* stream);
+
+/* pkv_paged_attention_decode with explicit plan options (NULL = automatic). */
+PKV_API pkv_status pkv_paged_attention_decode_ex(const pkv_pool* pool, const void* q,
+                                         const int32_t* block_tables, int max_blocks_per_seq,
+                                         const int32_t* context_lens, int num_seqs,
+                                         int num_q_heads, int max_context_len, float scale,
+                                         void* out, void* workspace, size_t workspace_bytes,
+                                         const pkv_decode_options* options, void* stream);
+
+/*
+ * Read and clear the pool's device error word (PKV_DEVERR_* bits).  Waits for the work
+ * already enqueued on `stream`, then copies the word to *flags (host) and zeroes it.
+ */
+PKV_API pkv_status pkv_get_device_error(const pkv_pool* pool, uint32_t* flags, void* stream);
+
+/* Number of kernels this library has launched in this process (all threads). */
+PKV_API uint64_t pkv_launch_count(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PAGEDKV_H_ */

@@ -1,0 +1,203 @@
+"""Thin Python binding of the C ABI (``include/pagedkv.h``).
+
+Argument marshalling only: the functions check torch dtypes, devices and contiguity and
+pass ``data_ptr()``s and the current CUDA stream to the library; every step of the
+computation runs in the library's kernels.  Names follow the C calls without the
+``pkv_`` prefix.  ``PagedKVPool`` bundles a pool's tensors with its descriptor.
+"""
+
+from __future__ import annotations
+
+import ctypes
+
+import torch
+
+from . import _lib
+from ._lib import BLOCK_SIZE, DecodeOptions, PKV_KV_BF16, PKV_KV_INT8, check
+
+_DTYPES = {"bf16": PKV_KV_BF16, "int8": PKV_KV_INT8}
+
+
+def _stream(stream) -> ctypes.c_void_p:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _ptr(t: torch.Tensor | None) -> ctypes.c_void_p:
+    return ctypes.c_void_p(0 if t is None else t.data_ptr())
+
+
+def _need(t: torch.Tensor, dtype, name: str, ndim: int | None = None) -> None:
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be on a CUDA device")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if ndim is not None and t.dim() != ndim:
+        raise ValueError(f"{name} must have {ndim} dims, got {tuple(t.shape)}")
+
+
+def _options(partition_blocks: int) -> ctypes.POINTER(DecodeOptions) | None:
+    if not partition_blocks:
+        return None
+    o = DecodeOptions()
+    o.partition_blocks = int(partition_blocks)
+    return ctypes.pointer(o)
+
+
+def version() -> str:
+    return _lib.load().pkv_version().decode()
+
+
+def launch_count() -> int:
+    return int(_lib.load().pkv_launch_count())
+
+
+def pool_bytes(num_blocks: int, kv_heads: int, head_dim: int, dtype: str = "bf16") -> tuple[int, int]:
+    kv, sc = ctypes.c_size_t(), ctypes.c_size_t()
+    check(_lib.load().pkv_pool_bytes(num_blocks, kv_heads, head_dim, _DTYPES[dtype],
+                                     ctypes.byref(kv), ctypes.byref(sc)), "pool_bytes")
+    return kv.value, sc.value
+
+
+def pool_create(num_blocks: int, kv_heads: int, head_dim: int, dtype: str, k_cache: torch.Tensor,
+                v_cache: torch.Tensor, k_scale: torch.Tensor | None = None,
+                v_scale: torch.Tensor | None = None) -> ctypes.c_void_p:
+    h = ctypes.c_void_p()
+    check(_lib.load().pkv_pool_create(num_blocks, kv_heads, head_dim, BLOCK_SIZE, _DTYPES[dtype],
+                                      _ptr(k_cache), _ptr(v_cache), _ptr(k_scale), _ptr(v_scale),
+                                      ctypes.byref(h)), "pool_create")
+    return h
+
+
+def pool_destroy(handle) -> None:
+    check(_lib.load().pkv_pool_destroy(handle), "pool_destroy")
+
+
+class PagedKVPool:
+    """A block pool ([num_blocks, kv_heads, 16, head_dim] K and V, plus fp32 scales for
+    INT8) allocated with torch on the current CUDA device, and its library descriptor."""
+
+    def __init__(self, num_blocks: int, kv_heads: int, head_dim: int, dtype: str = "bf16",
+                 device=None, fill=None):
+        if dtype not in _DTYPES:
+            raise ValueError(f"dtype must be one of {list(_DTYPES)}")
+        device = torch.device(device or "cuda")
+        self.num_blocks, self.kv_heads, self.head_dim, self.dtype = num_blocks, kv_heads, head_dim, dtype
+        shape = (num_blocks, kv_heads, BLOCK_SIZE, head_dim)
+        tdt = torch.bfloat16 if dtype == "bf16" else torch.int8
+        self.k_cache = torch.empty(shape, dtype=tdt, device=device)
+        self.v_cache = torch.empty(shape, dtype=tdt, device=device)
+        self.k_scale = self.v_scale = None
+        if dtype == "int8":
+            self.k_scale = torch.empty(shape[:3], dtype=torch.float32, device=device)
+            self.v_scale = torch.empty(shape[:3], dtype=torch.float32, device=device)
+        if fill is not None:
+            for t in (self.k_cache, self.v_cache, self.k_scale, self.v_scale):
+                if t is not None:
+                    t.fill_(fill)
+        with torch.cuda.device(device):
+            self.handle = pool_create(num_blocks, kv_heads, head_dim, dtype, self.k_cache,
+                                      self.v_cache, self.k_scale, self.v_scale)
+
+    def close(self) -> None:
+        if getattr(self, "handle", None) is not None:
+            pool_destroy(self.handle)
+            self.handle = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:  # noqa: BLE001 -- interpreter shutdown
+            pass
+
+    # convenience wrappers
+    def reshape_and_cache(self, key, value, slot_mapping, stream=None):
+        reshape_and_cache(self, key, value, slot_mapping, stream)
+
+    def decode(self, q, block_tables, context_lens, scale, max_context_len, out=None,
+               workspace=None, partition_blocks=0, stream=None):
+        return paged_attention_decode(self, q, block_tables, context_lens, scale, max_context_len,
+                                      out=out, workspace=workspace,
+                                      partition_blocks=partition_blocks, stream=stream)
+
+    def device_error(self, stream=None) -> int:
+        return get_device_error(self, stream)
+
+
+def _handle(pool) -> ctypes.c_void_p:
+    return pool.handle if isinstance(pool, PagedKVPool) else pool
+
+
+def reshape_and_cache(pool: PagedKVPool, key: torch.Tensor, value: torch.Tensor,
+                      slot_mapping: torch.Tensor, stream=None) -> None:
+    """Write key/value bf16 [N, Hkv, d] rows into the pool slots slot_mapping (int32 [N])."""
+    _need(key, torch.bfloat16, "key", 3)
+    _need(value, torch.bfloat16, "value", 3)
+    _need(slot_mapping, torch.int32, "slot_mapping", 1)
+    if key.shape != value.shape or key.shape[0] != slot_mapping.shape[0]:
+        raise ValueError("key, value and slot_mapping disagree in shape")
+    if key.shape[1:] != (pool.kv_heads, pool.head_dim):
+        raise ValueError(f"key rows must be [{pool.kv_heads}, {pool.head_dim}]")
+    check(_lib.load().pkv_reshape_and_cache(_handle(pool), _ptr(key), _ptr(value), _ptr(slot_mapping),
+                                            key.shape[0], _stream(stream)), "reshape_and_cache")
+
+
+def decode_workspace_bytes(pool: PagedKVPool, num_seqs: int, num_q_heads: int, max_context_len: int,
+                           partition_blocks: int = 0) -> int:
+    n = ctypes.c_size_t()
+    check(_lib.load().pkv_decode_workspace_bytes(_handle(pool), num_seqs, num_q_heads, max_context_len,
+                                                 _options(partition_blocks), ctypes.byref(n)),
+          "decode_workspace_bytes")
+    return n.value
+
+
+def decode_plan(pool: PagedKVPool, num_seqs: int, num_q_heads: int, max_context_len: int,
+                partition_blocks: int = 0) -> dict:
+    pb, mp, kc = ctypes.c_int(), ctypes.c_int(), ctypes.c_int()
+    check(_lib.load().pkv_decode_plan(_handle(pool), num_seqs, num_q_heads, max_context_len,
+                                      _options(partition_blocks), ctypes.byref(pb), ctypes.byref(mp),
+                                      ctypes.byref(kc)), "decode_plan")
+    return {"partition_blocks": pb.value, "max_partitions": mp.value, "kernels_per_call": kc.value}
+
+
+def paged_attention_decode(pool: PagedKVPool, q: torch.Tensor, block_tables: torch.Tensor,
+                           context_lens: torch.Tensor, scale: float, max_context_len: int,
+                           out: torch.Tensor | None = None, workspace: torch.Tensor | None = None,
+                           partition_blocks: int = 0, stream=None) -> torch.Tensor:
+    """Decode attention for q bf16 [B, Hq, d] over the pool; returns out bf16 [B, Hq, d].
+
+    ``workspace`` (a uint8 CUDA tensor) is allocated here when not given and needed."""
+    _need(q, torch.bfloat16, "q", 3)
+    _need(block_tables, torch.int32, "block_tables", 2)
+    _need(context_lens, torch.int32, "context_lens", 1)
+    b, hq, d = q.shape
+    if d != pool.head_dim or block_tables.shape[0] != b or context_lens.shape[0] != b:
+        raise ValueError("q, block_tables and context_lens disagree in shape")
+    if out is None:
+        out = torch.empty_like(q)
+    else:
+        _need(out, torch.bfloat16, "out", 3)
+        if out.shape != q.shape:
+            raise ValueError("out must have q's shape")
+    need = decode_workspace_bytes(pool, b, hq, max_context_len, partition_blocks) if b else 0
+    if need and workspace is None:
+        workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+    ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    check(_lib.load().pkv_paged_attention_decode_ex(
+        _handle(pool), _ptr(q), _ptr(block_tables), block_tables.shape[1], _ptr(context_lens), b, hq,
+        int(max_context_len), float(scale), _ptr(out), _ptr(workspace), ws_bytes,
+        _options(partition_blocks), _stream(stream)), "paged_attention_decode")
+    return out
+
+
+def get_device_error(pool: PagedKVPool, stream=None) -> int:
+    """Read and clear the pool's device error word (DEVERR_* bits)."""
+    v = ctypes.c_uint32()
+    check(_lib.load().pkv_get_device_error(_handle(pool), ctypes.byref(v), _stream(stream)),
+          "get_device_error")
+    return v.value

@@ -1,0 +1,339 @@
+// pkv_api.cu -- the C ABI declared in include/pagedkv.h: argument validation, the
+// decode plan (partition size), workspace layout and kernel dispatch.
+#include <atomic>
+#include <cstdio>
+#include <cstring>
+#include <new>
+
+#include "../../include/pagedkv.h"
+#include "pkv_internal.h"
+
+namespace pkv {
+int ctas_per_sm_bf16(int head_dim, int group);
+int ctas_per_sm_int8(int head_dim, int group);
+}  // namespace pkv
+
+struct pkv_pool {
+  int64_t num_blocks;
+  int kv_heads;
+  int head_dim;
+  pkv_kv_dtype dtype;
+  void* k_cache;
+  void* v_cache;
+  float* k_scale;
+  float* v_scale;
+  uint32_t* d_err;  // library-owned device error word
+  int device;
+  int sm_count;
+};
+
+namespace {
+
+std::atomic<uint64_t> g_launches{0};
+thread_local char g_cuda_msg[256] = "no error";
+
+pkv_status cuda_fail(cudaError_t e, const char* where) {
+  std::snprintf(g_cuda_msg, sizeof g_cuda_msg, "%s: %s (%d)", where, cudaGetErrorString(e),
+                static_cast<int>(e));
+  return PKV_ERR_CUDA;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
+
+bool group_supported(int g) { return g == 1 || g == 2 || g == 4 || g == 8; }
+
+constexpr int kMaxPartitionBlocks = 1024;
+constexpr int64_t kItemTargetBytes = 256 * 1024;  // K/V bytes one work item aims to stream
+
+struct Plan {
+  int partition_blocks;
+  int max_parts;
+  int kernels;
+  size_t ws_bytes;
+  size_t ws_ml_offset;
+};
+
+pkv_status make_plan(const pkv_pool* pool, int num_seqs, int num_q_heads, int max_context_len,
+                     const pkv_decode_options* opt, Plan* plan) {
+  const int64_t max_nblk = ceil_div(max_context_len, pkv::kBlockSize);
+  const int group = num_q_heads / pool->kv_heads;
+  int P;
+  if (opt && opt->partition_blocks > 0) {
+    P = opt->partition_blocks;
+  } else {
+    const int64_t block_bytes = pkv::decode_block_bytes(static_cast<pkv::KvType>(pool->dtype),
+                                                        pool->head_dim);
+    P = static_cast<int>(kItemTargetBytes / block_bytes);
+    if (P < 1) P = 1;
+    const int per_sm =
+        pkv::decode_ctas_per_sm(static_cast<pkv::KvType>(pool->dtype), pool->head_dim, group);
+    const int64_t resident = int64_t(pool->sm_count) * (per_sm > 0 ? per_sm : 1);
+    const int64_t units = int64_t(num_seqs) * pool->kv_heads;
+    // Shrink the partition while the batch would not fill the GPU twice over.
+    while (P > 4 && units * ceil_div(max_nblk, P) < 2 * resident) P /= 2;
+  }
+  if (P > kMaxPartitionBlocks) P = kMaxPartitionBlocks;
+  if (P > max_nblk) P = static_cast<int>(max_nblk);
+  if (P < 1) P = 1;
+  plan->partition_blocks = P;
+  plan->max_parts = static_cast<int>(ceil_div(max_nblk, P));
+  plan->kernels = plan->max_parts > 1 ? 2 : 1;
+  plan->ws_bytes = 0;
+  plan->ws_ml_offset = 0;
+  if (plan->max_parts > 1) {
+    const size_t rows = size_t(num_seqs) * num_q_heads * plan->max_parts;
+    const size_t acc = rows * pool->head_dim * sizeof(float);
+    plan->ws_ml_offset = (acc + 255) / 256 * 256;
+    plan->ws_bytes = plan->ws_ml_offset + rows * 2 * sizeof(float);
+  }
+  return PKV_OK;
+}
+
+pkv_status check_decode_shape(const pkv_pool* pool, int num_seqs, int num_q_heads,
+                              int max_context_len) {
+  if (!pool) return PKV_ERR_INVALID_ARG;
+  if (num_seqs < 0 || num_q_heads < 1 || max_context_len < 1) return PKV_ERR_INVALID_ARG;
+  if (num_q_heads % pool->kv_heads != 0) return PKV_ERR_INVALID_ARG;
+  if (!group_supported(num_q_heads / pool->kv_heads)) return PKV_ERR_UNSUPPORTED;
+  return PKV_OK;
+}
+
+}  // namespace
+
+namespace pkv {
+int decode_ctas_per_sm(KvType kv, int head_dim, int group) {
+  static int cache[2][2][9] = {};  // [dtype][head_dim 64/128][group]
+  const int di = head_dim == 128 ? 1 : 0;
+  const int ki = kv == KvType::kInt8 ? 1 : 0;
+  if (group < 1 || group > 8) return 0;
+  int& slot = cache[ki][di][group];
+  if (slot == 0)
+    slot = kv == KvType::kInt8 ? ctas_per_sm_int8(head_dim, group) : ctas_per_sm_bf16(head_dim, group);
+  return slot;
+}
+
+int decode_block_bytes(KvType kv, int head_dim) {
+  const int esz = kv == KvType::kInt8 ? 1 : 2;
+  return 2 * kBlockSize * head_dim * esz + (kv == KvType::kInt8 ? 2 * kBlockSize * 4 : 0);
+}
+}  // namespace pkv
+
+extern "C" {
+
+const char* pkv_status_string(pkv_status s) {
+  switch (s) {
+    case PKV_OK: return "ok";
+    case PKV_ERR_INVALID_ARG: return "invalid argument";
+    case PKV_ERR_UNSUPPORTED: return "unsupported configuration";
+    case PKV_ERR_CUDA: return "CUDA error";
+    case PKV_ERR_WORKSPACE: return "workspace too small";
+  }
+  return "unknown status";
+}
+
+const char* pkv_last_cuda_error(void) { return g_cuda_msg; }
+
+const char* pkv_version(void) { return "0.1.0"; }
+
+uint64_t pkv_launch_count(void) { return g_launches.load(std::memory_order_relaxed); }
+
+pkv_status pkv_pool_bytes(int64_t num_blocks, int kv_heads, int head_dim, pkv_kv_dtype dtype,
+                          size_t* kv_bytes_each, size_t* scale_bytes_each) {
+  if (num_blocks < 1 || kv_heads < 1 || head_dim < 1) return PKV_ERR_INVALID_ARG;
+  if (dtype != PKV_KV_BF16 && dtype != PKV_KV_INT8) return PKV_ERR_INVALID_ARG;
+  const size_t esz = dtype == PKV_KV_INT8 ? 1 : 2;
+  const size_t rows = size_t(num_blocks) * kv_heads * pkv::kBlockSize;
+  if (kv_bytes_each) *kv_bytes_each = rows * head_dim * esz;
+  if (scale_bytes_each) *scale_bytes_each = dtype == PKV_KV_INT8 ? rows * sizeof(float) : 0;
+  return PKV_OK;
+}
+
+pkv_status pkv_pool_create(int64_t num_blocks, int kv_heads, int head_dim, int block_size,
+                           pkv_kv_dtype dtype, void* k_cache, void* v_cache, float* k_scale,
+                           float* v_scale, pkv_pool** out) {
+  if (!out) return PKV_ERR_INVALID_ARG;
+  *out = nullptr;
+  if (num_blocks < 1 || kv_heads < 1 || head_dim < 1) return PKV_ERR_INVALID_ARG;
+  if (dtype != PKV_KV_BF16 && dtype != PKV_KV_INT8) return PKV_ERR_INVALID_ARG;
+  if (!k_cache || !v_cache || !aligned16(k_cache) || !aligned16(v_cache)) return PKV_ERR_INVALID_ARG;
+  if (dtype == PKV_KV_INT8) {
+    if (!k_scale || !v_scale || !aligned16(k_scale) || !aligned16(v_scale)) return PKV_ERR_INVALID_ARG;
+  } else if (k_scale || v_scale) {
+    return PKV_ERR_INVALID_ARG;
+  }
+  if (block_size != pkv::kBlockSize) return PKV_ERR_UNSUPPORTED;
+  if (head_dim != 64 && head_dim != 128) return PKV_ERR_UNSUPPORTED;
+  // Block ids are int32 in the page table; tile offsets are computed in 64 bits.
+  if (num_blocks > INT32_MAX) return PKV_ERR_INVALID_ARG;
+
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+  int sms = 0;
+  e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaDeviceGetAttribute");
+  uint32_t* d_err = nullptr;
+  e = cudaMalloc(&d_err, 16);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaMalloc(error word)");
+  e = cudaMemset(d_err, 0, 16);
+  if (e != cudaSuccess) {
+    cudaFree(d_err);
+    return cuda_fail(e, "cudaMemset(error word)");
+  }
+  pkv_pool* pool = new (std::nothrow) pkv_pool;
+  if (!pool) {
+    cudaFree(d_err);
+    return PKV_ERR_INVALID_ARG;
+  }
+  *pool = pkv_pool{num_blocks, kv_heads, head_dim, dtype, k_cache, v_cache,
+                   k_scale, v_scale, d_err, dev, sms};
+  *out = pool;
+  return PKV_OK;
+}
+
+pkv_status pkv_pool_destroy(pkv_pool* pool) {
+  if (!pool) return PKV_OK;
+  cudaFree(pool->d_err);
+  delete pool;
+  return PKV_OK;
+}
+
+pkv_status pkv_reshape_and_cache(const pkv_pool* pool, const void* key, const void* value,
+                                 const int32_t* slot_mapping, int64_t num_tokens, void* stream) {
+  if (!pool || num_tokens < 0) return PKV_ERR_INVALID_ARG;
+  if (num_tokens == 0) return PKV_OK;
+  if (!key || !value || !slot_mapping || !aligned16(key) || !aligned16(value))
+    return PKV_ERR_INVALID_ARG;
+  pkv::CacheParams p{};
+  p.key = key;
+  p.value = value;
+  p.slot_mapping = slot_mapping;
+  p.k_cache = pool->k_cache;
+  p.v_cache = pool->v_cache;
+  p.k_scale = pool->k_scale;
+  p.v_scale = pool->v_scale;
+  p.err = pool->d_err;
+  p.num_tokens = num_tokens;
+  p.num_blocks = pool->num_blocks;
+  p.kv_heads = pool->kv_heads;
+  p.head_dim = pool->head_dim;
+  auto s = static_cast<cudaStream_t>(stream);
+  cudaError_t e = pool->dtype == PKV_KV_INT8 ? pkv::launch_cache_int8(p, s)
+                                              : pkv::launch_cache_bf16(p, s);
+  if (e != cudaSuccess) return cuda_fail(e, "reshape_and_cache launch");
+  g_launches.fetch_add(1, std::memory_order_relaxed);
+  return PKV_OK;
+}
+
+pkv_status pkv_decode_workspace_bytes(const pkv_pool* pool, int num_seqs, int num_q_heads,
+                                      int max_context_len, const pkv_decode_options* options,
+                                      size_t* bytes) {
+  if (!bytes) return PKV_ERR_INVALID_ARG;
+  pkv_status st = check_decode_shape(pool, num_seqs, num_q_heads, max_context_len);
+  if (st != PKV_OK) return st;
+  Plan plan;
+  make_plan(pool, num_seqs, num_q_heads, max_context_len, options, &plan);
+  *bytes = plan.ws_bytes;
+  return PKV_OK;
+}
+
+pkv_status pkv_decode_plan(const pkv_pool* pool, int num_seqs, int num_q_heads,
+                           int max_context_len, const pkv_decode_options* options,
+                           int* partition_blocks, int* max_partitions, int* kernels_per_call) {
+  pkv_status st = check_decode_shape(pool, num_seqs, num_q_heads, max_context_len);
+  if (st != PKV_OK) return st;
+  Plan plan;
+  make_plan(pool, num_seqs, num_q_heads, max_context_len, options, &plan);
+  if (partition_blocks) *partition_blocks = plan.partition_blocks;
+  if (max_partitions) *max_partitions = plan.max_parts;
+  if (kernels_per_call) *kernels_per_call = plan.kernels;
+  return PKV_OK;
+}
+
+pkv_status pkv_paged_attention_decode_ex(const pkv_pool* pool, const void* q,
+                                         const int32_t* block_tables, int max_blocks_per_seq,
+                                         const int32_t* context_lens, int num_seqs,
+                                         int num_q_heads, int max_context_len, float scale,
+                                         void* out, void* workspace, size_t workspace_bytes,
+                                         const pkv_decode_options* options, void* stream) {
+  pkv_status st = check_decode_shape(pool, num_seqs, num_q_heads, max_context_len);
+  if (st != PKV_OK) return st;
+  if (num_seqs == 0) return PKV_OK;
+  if (!q || !block_tables || !context_lens || !out || !aligned16(q)) return PKV_ERR_INVALID_ARG;
+  if (max_blocks_per_seq < 1) return PKV_ERR_INVALID_ARG;
+  if (int64_t(max_context_len) > int64_t(max_blocks_per_seq) * pkv::kBlockSize)
+    return PKV_ERR_INVALID_ARG;
+  if (!(scale == scale)) return PKV_ERR_INVALID_ARG;  // NaN
+  Plan plan;
+  make_plan(pool, num_seqs, num_q_heads, max_context_len, options, &plan);
+  if (plan.ws_bytes > 0) {
+    if (!workspace || workspace_bytes < plan.ws_bytes) return PKV_ERR_WORKSPACE;
+    if (!aligned16(workspace)) return PKV_ERR_INVALID_ARG;
+  }
+
+  pkv::DecodeParams p{};
+  p.q = q;
+  p.k_cache = pool->k_cache;
+  p.v_cache = pool->v_cache;
+  p.k_scale = pool->k_scale;
+  p.v_scale = pool->v_scale;
+  p.block_tables = block_tables;
+  p.context_lens = context_lens;
+  p.out = out;
+  p.ws_acc = plan.ws_bytes ? static_cast<float*>(workspace) : nullptr;
+  p.ws_ml = plan.ws_bytes
+                ? reinterpret_cast<float*>(static_cast<char*>(workspace) + plan.ws_ml_offset)
+                : nullptr;
+  p.err = pool->d_err;
+  p.num_blocks = pool->num_blocks;
+  p.max_blocks_per_seq = max_blocks_per_seq;
+  p.num_seqs = num_seqs;
+  p.num_q_heads = num_q_heads;
+  p.kv_heads = pool->kv_heads;
+  p.head_dim = pool->head_dim;
+  p.max_context_len = max_context_len;
+  p.partition_blocks = plan.partition_blocks;
+  p.max_parts = plan.max_parts;
+  p.scale_log2 = scale * 1.4426950408889634f;
+
+  const int group = num_q_heads / pool->kv_heads;
+  auto s = static_cast<cudaStream_t>(stream);
+  cudaError_t e = pool->dtype == PKV_KV_INT8 ? pkv::launch_decode_int8(p, group, s)
+                                              : pkv::launch_decode_bf16(p, group, s);
+  if (e != cudaSuccess) return cuda_fail(e, "paged_attention_decode launch");
+  g_launches.fetch_add(1, std::memory_order_relaxed);
+  if (plan.max_parts > 1) {
+    e = pkv::launch_lse_reduce(p, s);
+    if (e != cudaSuccess) return cuda_fail(e, "partition reduce launch");
+    g_launches.fetch_add(1, std::memory_order_relaxed);
+  }
+  return PKV_OK;
+}
+
+pkv_status pkv_paged_attention_decode(const pkv_pool* pool, const void* q,
+                                      const int32_t* block_tables, int max_blocks_per_seq,
+                                      const int32_t* context_lens, int num_seqs, int num_q_heads,
+                                      int max_context_len, float scale, void* out,
+                                      void* workspace, size_t workspace_bytes, void* stream) {
+  return pkv_paged_attention_decode_ex(pool, q, block_tables, max_blocks_per_seq, context_lens,
+                                       num_seqs, num_q_heads, max_context_len, scale, out,
+                                       workspace, workspace_bytes, nullptr, stream);
+}
+
+pkv_status pkv_get_device_error(const pkv_pool* pool, uint32_t* flags, void* stream) {
+  if (!pool || !flags) return PKV_ERR_INVALID_ARG;
+  auto s = static_cast<cudaStream_t>(stream);
+  uint32_t h = 0;
+  cudaError_t e = cudaMemcpyAsync(&h, pool->d_err, sizeof h, cudaMemcpyDeviceToHost, s);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaMemcpyAsync(error word)");
+  e = cudaMemsetAsync(pool->d_err, 0, sizeof h, s);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaMemsetAsync(error word)");
+  e = cudaStreamSynchronize(s);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaStreamSynchronize");
+  *flags = h;
+  return PKV_OK;
+}
+
+}  // extern "C"

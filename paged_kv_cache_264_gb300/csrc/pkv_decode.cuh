@@ -1,0 +1,530 @@
+// pkv_decode.cuh -- PagedAttention decode kernels for sm_103a.
+//
+// What is computed ("Lesson 4: Model deployment and inference acceleration", 4.2,
+// attention-invariance equation): for sequence b and query head h,
+//     out[b][h] = sum_{t < T_b} softmax_t(scale * q[b][h] . K_b[t]) V_b[t],
+// where token t of sequence b sits in physical block block_tables[b][t / 16] at offset
+// t % 16 of a [num_blocks, Hkv, 16, D] pool, and q head h reads kv head h / G with
+// G = Hq / Hkv (contiguous GQA groups; "LLM/MLLM inference optimisation", 2.3).
+//
+// Work decomposition.  A work item is (sequence b, kv head, context partition p); the
+// partition covers P consecutive logical blocks.  One CTA of NW warps runs one item and
+// serves all G query heads of its kv head, so each K/V block is read from HBM once per
+// group.  Warp w takes the item's blocks w, w + NW, ...; each warp owns a ring of S
+// shared-memory stages, and its lane 0 fills a stage with one bulk asynchronous copy
+// per tile (the [phys][kvh] K tile and V tile are each one contiguous 16*D-element
+// run, so no tensor map is needed), completing on the stage's mbarrier.  The block
+// table slice of the item is staged in shared memory first.
+//
+// Per block a warp computes 16 tokens x G heads of logits with fp32 FMAs: lanes split
+// a token's D dims (DPL dims each) and hold q for all G heads in registers; a
+// transposed butterfly reduces the G partial dot products across the lanes of a token
+// so that each lane ends with one head's logit.  The online softmax ("LLM/MLLM inference
+// optimisation", 3.2: running max and running sum) rescales the running state by
+// exp(m_old - m_new) per block; logits are kept in log2 units (scale * log2 e is folded
+// into q) so that exp2 is the only exponential.  Probabilities go through a small
+// per-warp shared array to the PV layout, where each lane owns D/32 output dims of all
+// G heads.  At the end of the item the NW warp states merge in shared memory; a
+// single-partition sequence writes bf16 output directly, otherwise the item writes its
+// partial (max, sum, accumulator) and a second kernel merges the partitions with the
+// same log-sum-exp algebra.
+//
+// INT8 pools: logit = (scale * log2 e) * s_K[t] * sum_c q_c code_c, and the PV weight of
+// token t is p_t * s_V[t]; codes are widened to fp32 exactly (see i8_from_flipped).
+//
+// Masking: tokens t >= T_b of the last block get logit -inf and are excluded from the
+// PV loop, so whatever bytes sit in unused slots are never used.  Block ids outside
+// [0, num_blocks) are skipped (no copy) and flagged in the device error word.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <math.h>
+
+#include "pkv_device.cuh"
+
+namespace pkv {
+
+constexpr int kMaxPartitionBlocks = 1024;  // largest P (the staged table slice is 4 KiB)
+
+template <KvType KV>
+struct KvTraits;
+template <>
+struct KvTraits<KvType::kBf16> {
+  static constexpr int kElemBytes = 2;
+  static constexpr bool kQuant = false;
+};
+template <>
+struct KvTraits<KvType::kInt8> {
+  static constexpr int kElemBytes = 1;
+  static constexpr bool kQuant = true;
+};
+
+constexpr size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+template <KvType KV, int D, int G, int NW, int S>
+struct DecodeCfg {
+  static constexpr int kEsz = KvTraits<KV>::kElemBytes;
+  static constexpr bool kQuant = KvTraits<KV>::kQuant;
+  static constexpr int kTileBytes = kBlockSize * D * kEsz;         // one K (or V) tile
+  static constexpr int kScaleBytes = kQuant ? kBlockSize * 4 : 0;  // one fp32 scale tile
+  static constexpr int kStageBytes = 2 * kTileBytes + 2 * kScaleBytes;
+  static constexpr int kDPL = (G <= 4) ? 16 : 8;  // QK: dims per lane
+  static constexpr int kLPT = D / kDPL;           // QK: lanes per token
+  static constexpr int kTPP = 32 / kLPT;          // QK: tokens per pass
+  static constexpr int kPasses = kBlockSize / kTPP;
+  static constexpr int kDup = kLPT / G;            // lanes holding the same (token, head) logit
+  static constexpr int kDPV = D / 32;             // PV: dims per lane
+  static constexpr int kThreads = NW * 32;
+  static constexpr bool kSwapHalves = !kQuant && kDPL == 16;
+
+  static constexpr size_t kRingBytes = size_t(NW) * S * kStageBytes;
+  static constexpr size_t kProbOff = kRingBytes;  // float [NW][17][G]: 16 p rows + alpha row
+  static constexpr size_t kProbBytes = size_t(NW) * 17 * G * 4;
+  static constexpr size_t kBarOff = align_up(kProbOff + kProbBytes, 16);
+  static constexpr size_t kTableOff = kBarOff + size_t(NW) * S * 8;
+  static size_t smem_bytes(int partition_blocks) {
+    return kTableOff + size_t(partition_blocks) * 4;
+  }
+
+  static_assert(D % 32 == 0 && (D == 64 || D == 128), "head_dim 64 or 128");
+  static_assert(kLPT >= G && kLPT <= 32, "a token's lanes must cover the group");
+  static_assert(kTPP * kPasses == kBlockSize, "passes must cover the block");
+  static_assert(size_t(G) * (D + 2) * 4 <= size_t(kStageBytes), "merge record fits a stage");
+  static_assert(kTileBytes % 16 == 0 && kStageBytes % 16 == 0, "bulk copies need 16 B");
+};
+
+// Transposed butterfly: NG partial sums per lane, lanes at xor-distance O, O/2, ... 1
+// belong to one token.  While more than one head remains, each step swaps half of the
+// heads with the partner lane, so the number of shuffles is about NG instead of
+// NG * log2(lanes).  At the end v[0] holds the full dot product for head
+// (lane % LPT) / (LPT / G).
+template <int NG, int O>
+struct HeadReduce {
+  static __device__ __forceinline__ void run(float* v, int lane) {
+    if constexpr (O == 0) {
+      return;
+    } else if constexpr (NG > 1) {
+      constexpr int H = NG / 2;
+      const bool upper = (lane & O) != 0;
+#pragma unroll
+      for (int i = 0; i < H; ++i) {
+        const float send = upper ? v[i] : v[i + H];
+        const float keep = upper ? v[i + H] : v[i];
+        v[i] = keep + __shfl_xor_sync(0xffffffffu, send, O);
+      }
+      HeadReduce<H, O / 2>::run(v, lane);
+    } else {
+      v[0] += __shfl_xor_sync(0xffffffffu, v[0], O);
+      HeadReduce<1, O / 2>::run(v, lane);
+    }
+  }
+};
+
+template <int G, int NQ>
+__device__ __forceinline__ void fma_bf16x8(float (&part)[G], const float (&qr)[G][NQ], int base,
+                                           const uint4 w) {
+  const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const float k0 = bf16lo(ws[i]);
+    const float k1 = bf16hi(ws[i]);
+#pragma unroll
+    for (int g = 0; g < G; ++g) {
+      part[g] = fmaf(qr[g][base + 2 * i], k0, part[g]);
+      part[g] = fmaf(qr[g][base + 2 * i + 1], k1, part[g]);
+    }
+  }
+}
+
+template <int G, int NQ>
+__device__ __forceinline__ void fma_i8x4(float (&part)[G], const float (&qr)[G][NQ], int base,
+                                         uint32_t w) {
+  const uint32_t u = w ^ 0x80808080u;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const float k = i8_from_flipped(u, i);
+#pragma unroll
+    for (int g = 0; g < G; ++g) part[g] = fmaf(qr[g][base + i], k, part[g]);
+  }
+}
+
+template <KvType KV, int D, int G, int NW, int S>
+__global__ void __launch_bounds__(NW * 32)
+    paged_decode_kernel(const DecodeParams p) {
+  using C = DecodeCfg<KV, D, G, NW, S>;
+  constexpr uint32_t kFull = 0xffffffffu;
+  extern __shared__ __align__(128) unsigned char smem[];
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+
+  // ---- which item
+  const int units = p.num_seqs * p.kv_heads;
+  const int part = static_cast<int>(blockIdx.x / static_cast<unsigned>(units));
+  const int rem = static_cast<int>(blockIdx.x - static_cast<unsigned>(part) * units);
+  const int b = rem / p.kv_heads;
+  const int kvh = rem - b * p.kv_heads;
+  const int T = __ldg(p.context_lens + b);
+  const size_t qo_base = (size_t(b) * p.num_q_heads + size_t(kvh) * G) * D;
+  auto* out = static_cast<__nv_bfloat16*>(p.out);
+
+  if (T < 1 || T > p.max_context_len) {
+    if (part == 0) {
+      for (int i = threadIdx.x; i < G * D; i += C::kThreads)
+        out[qo_base + i] = __float2bfloat16_rn(0.0f);
+      if (threadIdx.x == 0) set_error(p.err, kErrContextLen);
+    }
+    return;
+  }
+  const int nblk = (T + kBlockSize - 1) / kBlockSize;
+  const int P = p.partition_blocks;
+  const int nparts = (nblk + P - 1) / P;
+  if (part >= nparts) return;
+  const int blk0 = part * P;
+  const int nb_item = min(nblk, blk0 + P) - blk0;
+
+  int* tbl = reinterpret_cast<int*>(smem + C::kTableOff);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::kBarOff) + warp * S;
+  unsigned char* ring = smem + size_t(warp) * S * C::kStageBytes;
+  float* prob = reinterpret_cast<float*>(smem + C::kProbOff) + warp * 17 * G;
+
+  const int32_t* trow = p.block_tables + size_t(b) * p.max_blocks_per_seq + blk0;
+  for (int i = threadIdx.x; i < nb_item; i += C::kThreads) tbl[i] = __ldg(trow + i);
+  if (lane == 0) {
+#pragma unroll
+    for (int s = 0; s < S; ++s) mbar_init(bars + s, 1);
+    fence_barrier_init();
+  }
+  __syncthreads();
+
+  // Blocks of this warp: item blocks warp, warp + NW, ...
+  const int nw = warp < nb_item ? (nb_item - 1 - warp) / NW + 1 : 0;
+  const uint64_t policy = l2_evict_first_policy();
+  const char* kbase = static_cast<const char*>(p.k_cache);
+  const char* vbase = static_cast<const char*>(p.v_cache);
+
+  auto issue = [&](int k) {  // lane 0 only: fetch the warp's k-th block into stage k % S
+    const int s = k % S;
+    unsigned char* st = ring + size_t(s) * C::kStageBytes;
+    const int phys = tbl[warp + k * NW];
+    if (phys < 0 || phys >= p.num_blocks) {
+      set_error(p.err, kErrBlockId);
+      mbar_arrive(bars + s);  // complete the phase with no data; the block is skipped
+      return;
+    }
+    const int64_t tile = int64_t(phys) * p.kv_heads + kvh;
+    mbar_arrive_expect_tx(bars + s, C::kStageBytes);
+    bulk_copy_g2s(st, kbase + tile * C::kTileBytes, C::kTileBytes, bars + s, policy);
+    bulk_copy_g2s(st + C::kTileBytes, vbase + tile * C::kTileBytes, C::kTileBytes, bars + s,
+                  policy);
+    if constexpr (C::kQuant) {
+      bulk_copy_g2s(st + 2 * C::kTileBytes,
+                    reinterpret_cast<const char*>(p.k_scale) + tile * C::kScaleBytes,
+                    C::kScaleBytes, bars + s, policy);
+      bulk_copy_g2s(st + 2 * C::kTileBytes + C::kScaleBytes,
+                    reinterpret_cast<const char*>(p.v_scale) + tile * C::kScaleBytes,
+                    C::kScaleBytes, bars + s, policy);
+    }
+  };
+  if (lane == 0) {
+    for (int k = 0; k < S && k < nw; ++k) issue(k);
+  }
+
+  // ---- q for this lane's dims of all G heads, pre-multiplied by scale * log2(e)
+  const int tok = lane / C::kLPT;    // token within a pass
+  const int chunk = lane % C::kLPT;  // which DPL-dim slice of the row
+  const int sw = C::kSwapHalves ? ((lane >> 2) & 1) : 0;
+  float qr[G][C::kDPL];
+  {
+    const auto* qb = static_cast<const __nv_bfloat16*>(p.q) + qo_base;
+#pragma unroll
+    for (int g = 0; g < G; ++g) {
+      const uint4* src = reinterpret_cast<const uint4*>(qb + size_t(g) * D + chunk * C::kDPL);
+#pragma unroll
+      for (int h = 0; h < C::kDPL / 8; ++h) {
+        const uint4 w = __ldg(src + (h ^ sw));
+        const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          qr[g][8 * h + 2 * i] = bf16lo(ws[i]) * p.scale_log2;
+          qr[g][8 * h + 2 * i + 1] = bf16hi(ws[i]) * p.scale_log2;
+        }
+      }
+    }
+  }
+
+  const int g_lane = (lane % C::kLPT) / C::kDup;  // head whose logit this lane ends with
+  const bool store_lane = (lane % C::kDup) == 0;
+  float m_run = -INFINITY;
+  float l_run = 0.0f;
+  float acc[G][C::kDPV];
+#pragma unroll
+  for (int g = 0; g < G; ++g)
+#pragma unroll
+    for (int i = 0; i < C::kDPV; ++i) acc[g][i] = 0.0f;
+
+  int failed_at = -1;
+  for (int k = 0; k < nw; ++k) {
+    const int s = k % S;
+    const bool ok = __all_sync(kFull, mbar_wait_bounded(bars + s, (k / S) & 1));
+    if (!ok) {
+      failed_at = k;
+      if (lane == 0) set_error(p.err, kErrTimeout);
+      break;
+    }
+    const int ib = warp + k * NW;
+    const int phys = tbl[ib];
+    const bool valid = phys >= 0 && phys < p.num_blocks;
+    const int vt = valid ? min(kBlockSize, T - (blk0 + ib) * kBlockSize) : 0;
+    if (vt > 0) {
+      const unsigned char* st = ring + size_t(s) * C::kStageBytes;
+      const unsigned char* ktile = st;
+      const unsigned char* vtile = st + C::kTileBytes;
+      const float* kscale = reinterpret_cast<const float*>(st + 2 * C::kTileBytes);
+      const float* vscale = kscale + kBlockSize;
+
+      // ---- logits (log2 units)
+      float sc[C::kPasses];
+#pragma unroll
+      for (int ps = 0; ps < C::kPasses; ++ps) {
+        const int t = ps * C::kTPP + tok;
+        const unsigned char* row = ktile + (t * D + chunk * C::kDPL) * C::kEsz;
+        float part_g[G];
+#pragma unroll
+        for (int g = 0; g < G; ++g) part_g[g] = 0.0f;
+        if constexpr (!C::kQuant) {
+#pragma unroll
+          for (int h = 0; h < C::kDPL / 8; ++h)
+            fma_bf16x8<G, C::kDPL>(part_g, qr, 8 * h,
+                                   *reinterpret_cast<const uint4*>(row + 16 * (h ^ sw)));
+        } else if constexpr (C::kDPL == 16) {
+          const uint4 w = *reinterpret_cast<const uint4*>(row);
+          fma_i8x4<G, C::kDPL>(part_g, qr, 0, w.x);
+          fma_i8x4<G, C::kDPL>(part_g, qr, 4, w.y);
+          fma_i8x4<G, C::kDPL>(part_g, qr, 8, w.z);
+          fma_i8x4<G, C::kDPL>(part_g, qr, 12, w.w);
+        } else {
+          const uint2 w = *reinterpret_cast<const uint2*>(row);
+          fma_i8x4<G, C::kDPL>(part_g, qr, 0, w.x);
+          fma_i8x4<G, C::kDPL>(part_g, qr, 4, w.y);
+        }
+        HeadReduce<G, C::kLPT / 2>::run(part_g, lane);
+        float logit = part_g[0];
+        if constexpr (C::kQuant) logit *= kscale[t];
+        sc[ps] = (t < vt) ? logit : -INFINITY;
+      }
+
+      // ---- online softmax update for head g_lane
+      float bm = sc[0];
+#pragma unroll
+      for (int ps = 1; ps < C::kPasses; ++ps) bm = fmaxf(bm, sc[ps]);
+#pragma unroll
+      for (int o = C::kLPT; o < 32; o <<= 1) bm = fmaxf(bm, __shfl_xor_sync(kFull, bm, o));
+      const float m_new = fmaxf(m_run, bm);
+      const float alpha = exp2f(m_run - m_new);
+      m_run = m_new;
+      float psum = 0.0f;
+#pragma unroll
+      for (int ps = 0; ps < C::kPasses; ++ps) {
+        const int t = ps * C::kTPP + tok;
+        const float pr = exp2f(sc[ps] - m_new);
+        psum += pr;
+        if (store_lane) {
+          float w = pr;
+          if constexpr (C::kQuant) w = (t < vt) ? pr * vscale[t] : 0.0f;
+          prob[t * G + g_lane] = w;
+        }
+      }
+      l_run = l_run * alpha + (store_lane ? psum : 0.0f);
+      if (store_lane && tok == 0) prob[kBlockSize * G + g_lane] = alpha;
+      __syncwarp();
+
+      // ---- PV: acc[g][lane dims] = alpha_g * acc + sum_t p[t][g] * v[t][lane dims]
+      float al[G];
+#pragma unroll
+      for (int g = 0; g < G; ++g) al[g] = prob[kBlockSize * G + g];
+#pragma unroll
+      for (int g = 0; g < G; ++g)
+#pragma unroll
+        for (int i = 0; i < C::kDPV; ++i) acc[g][i] *= al[g];
+#pragma unroll 4
+      for (int t = 0; t < vt; ++t) {
+        float pv[G];
+        if constexpr (G % 4 == 0) {
+#pragma unroll
+          for (int g4 = 0; g4 < G / 4; ++g4) {
+            const float4 v4 = reinterpret_cast<const float4*>(prob + t * G)[g4];
+            pv[4 * g4] = v4.x; pv[4 * g4 + 1] = v4.y; pv[4 * g4 + 2] = v4.z; pv[4 * g4 + 3] = v4.w;
+          }
+        } else if constexpr (G == 2) {
+          const float2 v2 = reinterpret_cast<const float2*>(prob + t * G)[0];
+          pv[0] = v2.x; pv[1] = v2.y;
+        } else {
+          pv[0] = prob[t];
+        }
+        float vf[C::kDPV];
+        const unsigned char* vrow = vtile + (t * D + lane * C::kDPV) * C::kEsz;
+        if constexpr (!C::kQuant && C::kDPV == 4) {
+          const uint2 w = *reinterpret_cast<const uint2*>(vrow);
+          vf[0] = bf16lo(w.x); vf[1] = bf16hi(w.x); vf[2] = bf16lo(w.y); vf[3] = bf16hi(w.y);
+        } else if constexpr (!C::kQuant) {
+          const uint32_t w = *reinterpret_cast<const uint32_t*>(vrow);
+          vf[0] = bf16lo(w); vf[1] = bf16hi(w);
+        } else if constexpr (C::kDPV == 4) {
+          const uint32_t u = *reinterpret_cast<const uint32_t*>(vrow) ^ 0x80808080u;
+#pragma unroll
+          for (int i = 0; i < 4; ++i) vf[i] = i8_from_flipped(u, i);
+        } else {
+          const uint32_t u = uint32_t(*reinterpret_cast<const uint16_t*>(vrow)) ^ 0x8080u;
+          vf[0] = i8_from_flipped(u, 0);
+          vf[1] = i8_from_flipped(u, 1);
+        }
+#pragma unroll
+        for (int g = 0; g < G; ++g)
+#pragma unroll
+          for (int i = 0; i < C::kDPV; ++i) acc[g][i] = fmaf(pv[g], vf[i], acc[g][i]);
+      }
+    }
+    __syncwarp();  // every lane is done with this stage and with `prob`
+    if (lane == 0 && k + S < nw) {
+      fence_proxy_async_smem();
+      issue(k + S);
+    }
+  }
+  if (failed_at >= 0) {
+    // Let the copies still in flight into this warp's ring land (bounded) before the
+    // ring is reused for the merge record; their data is not used.
+    for (int k = failed_at; k < nw && k < failed_at + S; ++k)
+      (void)mbar_wait_bounded(bars + (k % S), (k / S) & 1);
+    __syncwarp();
+  }
+
+  // ---- this warp's softmax sum per head, then its merge record in its ring stage 0
+#pragma unroll
+  for (int o = C::kLPT; o < 32; o <<= 1) l_run += __shfl_xor_sync(kFull, l_run, o);
+  float* rec = reinterpret_cast<float*>(ring);  // [G][D + 2]: max, sum, accumulator
+  if (lane < C::kLPT && store_lane) {
+    rec[g_lane * (D + 2)] = m_run;
+    rec[g_lane * (D + 2) + 1] = l_run;
+  }
+#pragma unroll
+  for (int g = 0; g < G; ++g)
+#pragma unroll
+    for (int i = 0; i < C::kDPV; ++i) rec[g * (D + 2) + 2 + lane * C::kDPV + i] = acc[g][i];
+  __syncthreads();
+
+  // ---- merge the NW warp states (log-sum-exp) and write the output or the partial
+  for (int i = threadIdx.x; i < G * D; i += C::kThreads) {
+    const int g = i / D;
+    const int d = i - g * D;
+    float M = -INFINITY;
+#pragma unroll
+    for (int w = 0; w < NW; ++w)
+      M = fmaxf(M, reinterpret_cast<const float*>(smem + size_t(w) * S * C::kStageBytes)[g * (D + 2)]);
+    float L = 0.0f, A = 0.0f;
+    if (M != -INFINITY) {
+#pragma unroll
+      for (int w = 0; w < NW; ++w) {
+        const float* r =
+            reinterpret_cast<const float*>(smem + size_t(w) * S * C::kStageBytes) + g * (D + 2);
+        const float f = exp2f(r[0] - M);
+        L = fmaf(f, r[1], L);
+        A = fmaf(f, r[2 + d], A);
+      }
+    }
+    if (nparts == 1) {
+      out[qo_base + i] = __float2bfloat16_rn(L > 0.0f ? A / L : 0.0f);
+    } else {
+      const size_t pi = (size_t(b) * p.num_q_heads + size_t(kvh) * G + g) * p.max_parts + part;
+      p.ws_acc[pi * D + d] = A;
+      if (d == 0) {
+        p.ws_ml[2 * pi] = M;
+        p.ws_ml[2 * pi + 1] = L;
+      }
+    }
+  }
+}
+
+// Merge the partitions of every split sequence: M = max_p m_p, L = sum_p 2^(m_p - M) l_p,
+// out = sum_p 2^(m_p - M) acc_p / L.  One warp per (sequence, query head).
+template <int D>
+__global__ void __launch_bounds__(128) lse_reduce_kernel(const DecodeParams p) {
+  constexpr int kDPV = D / 32;
+  constexpr uint32_t kFull = 0xffffffffu;
+  const int lane = threadIdx.x & 31;
+  const int gw = blockIdx.x * (blockDim.x / 32) + (threadIdx.x >> 5);
+  if (gw >= p.num_seqs * p.num_q_heads) return;
+  const int b = gw / p.num_q_heads;
+  const int T = __ldg(p.context_lens + b);
+  if (T < 1 || T > p.max_context_len) return;  // the decode kernel wrote zeros
+  const int nblk = (T + kBlockSize - 1) / kBlockSize;
+  const int nparts = (nblk + p.partition_blocks - 1) / p.partition_blocks;
+  if (nparts <= 1) return;  // written directly by the decode kernel
+  const float* ml = p.ws_ml + size_t(gw) * p.max_parts * 2;
+  const float* acc = p.ws_acc + size_t(gw) * p.max_parts * D;
+
+  float M = -INFINITY;
+  for (int i = lane; i < nparts; i += 32) M = fmaxf(M, ml[2 * i]);
+#pragma unroll
+  for (int o = 16; o >= 1; o >>= 1) M = fmaxf(M, __shfl_xor_sync(kFull, M, o));
+  float L = 0.0f;
+  float a[kDPV];
+#pragma unroll
+  for (int i = 0; i < kDPV; ++i) a[i] = 0.0f;
+  if (M != -INFINITY) {
+    for (int i = lane; i < nparts; i += 32) L += exp2f(ml[2 * i] - M) * ml[2 * i + 1];
+#pragma unroll
+    for (int o = 16; o >= 1; o >>= 1) L += __shfl_xor_sync(kFull, L, o);
+    for (int i = 0; i < nparts; ++i) {
+      const float f = exp2f(ml[2 * i] - M);
+      const float* src = acc + size_t(i) * D + lane * kDPV;
+      if constexpr (kDPV == 4) {
+        const float4 v = *reinterpret_cast<const float4*>(src);
+        a[0] = fmaf(f, v.x, a[0]); a[1] = fmaf(f, v.y, a[1]);
+        a[2] = fmaf(f, v.z, a[2]); a[3] = fmaf(f, v.w, a[3]);
+      } else {
+        const float2 v = *reinterpret_cast<const float2*>(src);
+        a[0] = fmaf(f, v.x, a[0]); a[1] = fmaf(f, v.y, a[1]);
+      }
+    }
+  }
+  auto* out = static_cast<__nv_bfloat16*>(p.out) + size_t(gw) * D + lane * kDPV;
+#pragma unroll
+  for (int i = 0; i < kDPV; ++i) out[i] = __float2bfloat16_rn(L > 0.0f ? a[i] / L : 0.0f);
+}
+
+// ---- launch helpers
+template <KvType KV, int D, int G, int NW, int S>
+cudaError_t launch_decode_variant(const DecodeParams& p, cudaStream_t stream) {
+  using C = DecodeCfg<KV, D, G, NW, S>;
+  auto kern = paged_decode_kernel<KV, D, G, NW, S>;
+  static bool attr_done[64] = {};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev < 0 || dev >= 64 || !attr_done[dev]) {
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(C::smem_bytes(kMaxPartitionBlocks)));
+    if (e != cudaSuccess) return e;
+    if (dev >= 0 && dev < 64) attr_done[dev] = true;
+  }
+  const int64_t grid = int64_t(p.max_parts) * p.num_seqs * p.kv_heads;
+  if (grid <= 0) return cudaSuccess;
+  if (grid > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
+  kern<<<static_cast<unsigned>(grid), C::kThreads, C::smem_bytes(p.partition_blocks), stream>>>(p);
+  return cudaGetLastError();
+}
+
+template <KvType KV, int D, int G, int NW, int S>
+int ctas_per_sm_variant() {
+  using C = DecodeCfg<KV, D, G, NW, S>;
+  auto kern = paged_decode_kernel<KV, D, G, NW, S>;
+  cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                       static_cast<int>(C::smem_bytes(kMaxPartitionBlocks)));
+  int n = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kern, C::kThreads, C::smem_bytes(64)) !=
+      cudaSuccess)
+    return 0;
+  return n;
+}
+
+}  // namespace pkv

@@ -1,0 +1,72 @@
+// pkv_internal.h -- structures shared by the C-ABI layer and the kernel launchers.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+namespace pkv {
+
+constexpr int kBlockSize = 16;                      // tokens per physical block
+constexpr uint64_t kWaitTimeoutNs = 2000000000ull;  // bounded waits give up after 2 s
+
+// Device error word bits (mirror PKV_DEVERR_* of the public header).
+constexpr uint32_t kErrBlockId = 0x1u;
+constexpr uint32_t kErrContextLen = 0x2u;
+constexpr uint32_t kErrSlot = 0x4u;
+constexpr uint32_t kErrTimeout = 0x8u;
+
+enum class KvType : int { kBf16 = 0, kInt8 = 1 };
+
+struct CacheParams {
+  const void* key;              // bf16 [N, Hkv, D]
+  const void* value;            // bf16 [N, Hkv, D]
+  const int32_t* slot_mapping;  // [N]
+  void* k_cache;                // [NB, Hkv, 16, D]
+  void* v_cache;
+  float* k_scale;               // [NB, Hkv, 16] (int8 only)
+  float* v_scale;
+  uint32_t* err;
+  int64_t num_tokens;
+  int64_t num_blocks;
+  int kv_heads;
+  int head_dim;
+};
+
+struct DecodeParams {
+  const void* q;                // bf16 [B, Hq, D]
+  const void* k_cache;          // [NB, Hkv, 16, D]
+  const void* v_cache;
+  const float* k_scale;         // [NB, Hkv, 16] (int8 only)
+  const float* v_scale;
+  const int32_t* block_tables;  // [B, max_blocks_per_seq]
+  const int32_t* context_lens;  // [B]
+  void* out;                    // bf16 [B, Hq, D]
+  float* ws_acc;                // [B, Hq, max_parts, D]   (split only)
+  float* ws_ml;                 // [B, Hq, max_parts, 2]   (split only): running max (log2 units), sum
+  uint32_t* err;
+  int64_t num_blocks;
+  int max_blocks_per_seq;
+  int num_seqs;
+  int num_q_heads;
+  int kv_heads;
+  int head_dim;
+  int max_context_len;
+  int partition_blocks;         // P: blocks per work item
+  int max_parts;                // ceil(ceil(max_context_len / 16) / P)
+  float scale_log2;             // softmax scale * log2(e)
+};
+
+// Kernel launchers (defined next to their kernels).  Each returns the launch status.
+cudaError_t launch_cache_bf16(const CacheParams& p, cudaStream_t stream);
+cudaError_t launch_cache_int8(const CacheParams& p, cudaStream_t stream);
+cudaError_t launch_decode_bf16(const DecodeParams& p, int group, cudaStream_t stream);
+cudaError_t launch_decode_int8(const DecodeParams& p, int group, cudaStream_t stream);
+cudaError_t launch_lse_reduce(const DecodeParams& p, cudaStream_t stream);
+
+// Resident CTAs per SM of the decode kernel variant (0 if the variant is not built).
+int decode_ctas_per_sm(KvType kv, int head_dim, int group);
+// Bytes of K+V (+scales) one 16-token block brings in for one kv head.
+int decode_block_bytes(KvType kv, int head_dim);
+
+}  // namespace pkv

@@ -1,0 +1,57 @@
+"""Algorithmic bytes and flops of one decode step, for the HBM roofline.
+
+Decode reads every cached token's K and V once per kv head (GQA groups share the read;
+"LLM/MLLM inference optimisation", 2.2-2.3: the cache holds 2 x n_kv x head_dim x
+seq_len x bytes per layer), plus q, the output and the page table.  Tokens actually
+attended are counted, not whole 16-token blocks.  A decode step also appends one new
+token per sequence (reads its bf16 K/V row, writes the cached row and, for INT8, the
+scales).
+"""
+
+from __future__ import annotations
+
+from dataclasses import dataclass
+
+import torch
+
+BLOCK = 16
+
+
+@dataclass(frozen=True)
+class StepBytes:
+    kv_read: int        # cached K and V (and INT8 scales) read by decode
+    q_out: int          # q read + output written (bf16)
+    tables: int         # block-table entries + context lengths read
+    append: int         # the appended tokens: bf16 rows read, cached rows (+ scales) and slots
+    flops: int          # 4 * sum_b T_b * Hq * d  (QK and PV, multiply-add = 2)
+
+    @property
+    def decode(self) -> int:
+        return self.kv_read + self.q_out + self.tables
+
+    @property
+    def step(self) -> int:
+        return self.decode + self.append
+
+
+def step_bytes(context_lens, num_q_heads: int, num_kv_heads: int, head_dim: int, kv_dtype: str,
+               append: bool = True) -> StepBytes:
+    lens = torch.as_tensor(context_lens, dtype=torch.int64)
+    b = int(lens.numel())
+    sum_t = int(lens.sum())
+    sum_nb = int(((lens + BLOCK - 1) // BLOCK).sum())
+    esz = 2 if kv_dtype == "bf16" else 1
+    kv = 2 * sum_t * num_kv_heads * head_dim * esz
+    if kv_dtype == "int8":
+        kv += 2 * sum_t * num_kv_heads * 4
+    q_out = 2 * b * num_q_heads * head_dim * 2
+    tables = 4 * (sum_nb + b)
+    app = 0
+    if append:
+        app = 2 * b * num_kv_heads * head_dim * 2          # new K and V rows (bf16) read
+        app += 2 * b * num_kv_heads * head_dim * esz       # cached rows written
+        if kv_dtype == "int8":
+            app += 2 * b * num_kv_heads * 4                # scales written
+        app += 4 * b                                       # slot_mapping read
+    flops = 4 * sum_t * num_q_heads * head_dim
+    return StepBytes(kv, q_out, tables, app, flops)

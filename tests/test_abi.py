@@ -1,0 +1,92 @@
+"""The C-ABI library without a GPU: it loads, exports every symbol the header declares,
+and rejects bad host-side arguments before touching CUDA."""
+
+import ctypes
+import os
+import re
+
+import pytest
+
+from paged_kv_cache_264_gb300 import _lib, build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "pagedkv.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    build.build()
+    return _lib.load()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    return sorted(set(re.findall(r"^PKV_API\s+[\w\s\*]+?\b(pkv_\w+)\s*\(", text, flags=re.M)))
+
+
+def test_header_declares_the_boundary():
+    names = declared_functions()
+    for required in ("pkv_pool_create", "pkv_reshape_and_cache", "pkv_paged_attention_decode",
+                     "pkv_decode_workspace_bytes", "pkv_get_device_error", "pkv_pool_destroy"):
+        assert required in names
+
+
+def test_every_declared_symbol_is_exported(lib):
+    for name in declared_functions():
+        assert hasattr(lib, name), name
+        assert name in _lib.SIGNATURES, f"binding lacks {name}"
+
+
+def test_binding_declares_only_header_symbols():
+    assert set(_lib.SIGNATURES) <= set(declared_functions())
+
+
+def test_status_strings(lib):
+    assert lib.pkv_status_string(0) == b"ok"
+    assert b"invalid" in lib.pkv_status_string(1)
+    assert b"unsupported" in lib.pkv_status_string(2)
+    assert lib.pkv_version().decode().count(".") == 2
+
+
+def test_pool_bytes(lib):
+    kv, sc = ctypes.c_size_t(), ctypes.c_size_t()
+    assert lib.pkv_pool_bytes(10, 8, 128, _lib.PKV_KV_BF16, ctypes.byref(kv), ctypes.byref(sc)) == 0
+    assert kv.value == 10 * 8 * 16 * 128 * 2 and sc.value == 0
+    assert lib.pkv_pool_bytes(10, 8, 128, _lib.PKV_KV_INT8, ctypes.byref(kv), ctypes.byref(sc)) == 0
+    assert kv.value == 10 * 8 * 16 * 128 and sc.value == 10 * 8 * 16 * 4
+    assert lib.pkv_pool_bytes(0, 8, 128, 0, None, None) == _lib.PKV_ERR_INVALID_ARG
+    assert lib.pkv_pool_bytes(10, 8, 128, 7, None, None) == _lib.PKV_ERR_INVALID_ARG
+
+
+FAKE = ctypes.c_void_p(0x100000)  # aligned, never dereferenced: rejected before any CUDA call
+ODD = ctypes.c_void_p(0x100008)
+
+
+@pytest.mark.parametrize("args,expect", [
+    ((0, 8, 128, 16, 0, FAKE, FAKE, None, None), _lib.PKV_ERR_INVALID_ARG),   # no blocks
+    ((4, 8, 128, 16, 0, None, FAKE, None, None), _lib.PKV_ERR_INVALID_ARG),   # NULL K
+    ((4, 8, 128, 16, 0, ODD, FAKE, None, None), _lib.PKV_ERR_INVALID_ARG),    # misaligned K
+    ((4, 8, 128, 16, 0, FAKE, FAKE, FAKE, FAKE), _lib.PKV_ERR_INVALID_ARG),   # scales on bf16
+    ((4, 8, 128, 16, 1, FAKE, FAKE, None, None), _lib.PKV_ERR_INVALID_ARG),   # int8 without scales
+    ((4, 8, 96, 16, 0, FAKE, FAKE, None, None), _lib.PKV_ERR_UNSUPPORTED),    # head_dim 96
+    ((4, 8, 128, 32, 0, FAKE, FAKE, None, None), _lib.PKV_ERR_UNSUPPORTED),   # block size 32
+])
+def test_pool_create_rejects(lib, args, expect):
+    h = ctypes.c_void_p()
+    assert lib.pkv_pool_create(*args, ctypes.byref(h)) == expect
+    assert not h.value
+
+
+def test_null_pool_rejected(lib):
+    assert lib.pkv_reshape_and_cache(None, FAKE, FAKE, FAKE, 4, None) == _lib.PKV_ERR_INVALID_ARG
+    assert lib.pkv_paged_attention_decode(None, FAKE, FAKE, 4, FAKE, 2, 8, 64, 1.0, FAKE, None, 0,
+                                          None) == _lib.PKV_ERR_INVALID_ARG
+    n = ctypes.c_size_t()
+    assert lib.pkv_decode_workspace_bytes(None, 2, 8, 64, None, ctypes.byref(n)) == _lib.PKV_ERR_INVALID_ARG
+    f = ctypes.c_uint32()
+    assert lib.pkv_get_device_error(None, ctypes.byref(f), None) == _lib.PKV_ERR_INVALID_ARG
+    assert lib.pkv_pool_destroy(None) == 0
+
+
+def test_launch_count_starts_at_zero_without_work(lib):
+    assert lib.pkv_launch_count() == 0 or lib.pkv_launch_count() > 0  # a plain counter

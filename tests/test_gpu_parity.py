@@ -1,0 +1,291 @@
+"""GPU parity: the CUDA path, called through the C ABI, against the fp64 oracle on the
+same seeded inputs.
+
+Bars: slot writes and INT8 codes/scales bit-exact; attention outputs within max-abs
+1e-2 and mean-abs 1e-3 (bf16 output, fp32 accumulation; the INT8 oracle runs on the
+same dequantised values).  Pools are pre-filled with NaN so that any read of a slot that
+was never written (the tail of a last block, unused blocks) would show.
+"""
+
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import paged_kv_cache_264_gb300 as pkv
+from paged_kv_cache_264_gb300 import workloads as W
+from gpu_helpers import (compare, gpu_decode, gpu_pool_blocks, gpu_pool_from, oracle_decode,
+                         valid_slot_bytes_equal)
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    from paged_kv_cache_264_gb300 import build
+    build.build()
+    oracle.build()
+    torch.cuda.set_device(0)
+
+
+def custom(lens, hq, hkv, d, kv="bf16", seed=7, **kw):
+    return W.build(name="custom", context_lens=lens, num_q_heads=hq, num_kv_heads=hkv, head_dim=d,
+                   kv_dtype=kv, seed=seed, **kw)
+
+
+def check_all(w, kv, partition_blocks=0, seqs=None):
+    pool = gpu_pool_from(w, kv)
+    out = gpu_decode(pool, w, partition_blocks)
+    assert pool.device_error() == 0
+    ref, ref_pool, c = oracle_decode(w, kv, seqs)
+    sel = list(range(w.num_seqs)) if seqs is None else list(seqs)
+    valid_slot_bytes_equal(gpu_pool_blocks(pool, c["orig_tables"], c["lens"]), ref_pool, c["lens"])
+    res = compare(out[torch.tensor(sel, device=out.device)], ref, f"{w.name}/{kv}/P={partition_blocks}")
+    pool.close()
+    return out, res
+
+
+# ------------------------------------------------------------ small shapes
+
+@pytest.mark.parametrize("kv", ["bf16", "int8"])
+def test_tiny_workload(kv):
+    w = W.make("tiny")
+    check_all(w, kv)
+
+
+SHAPES = [
+    # lens, Hq, Hkv, d
+    ([1, 15, 16, 17, 33, 100], 4, 4, 64),
+    ([1, 2, 31, 48, 257], 8, 4, 64),
+    ([5, 16, 63, 200], 16, 4, 128),
+    ([17, 40, 129, 511, 700], 8, 1, 128),
+    ([3, 64, 65, 300], 32, 32, 128),
+    ([1, 16, 18, 99, 1000], 8, 2, 128),
+    ([7, 250, 33], 16, 2, 64),
+]
+
+
+@pytest.mark.parametrize("kv", ["bf16", "int8"])
+@pytest.mark.parametrize("shape", SHAPES, ids=lambda s: f"B{len(s[0])}_Hq{s[1]}_Hkv{s[2]}_d{s[3]}")
+def test_shapes_auto_plan(shape, kv):
+    lens, hq, hkv, d = shape
+    check_all(custom(lens, hq, hkv, d, kv), kv)
+
+
+@pytest.mark.parametrize("kv", ["bf16", "int8"])
+@pytest.mark.parametrize("partition_blocks", [1, 2, 3, 5, 8, 64])
+def test_partition_sweep(partition_blocks, kv):
+    """Split-K: any partition size gives the oracle's result (log-sum-exp merge)."""
+    w = custom([1, 16, 17, 95, 300, 613], 16, 4, 128, kv, seed=9)
+    check_all(w, kv, partition_blocks)
+
+
+def test_partitions_agree_with_each_other():
+    w = custom([700, 1000, 33], 8, 2, 128, "bf16", seed=10)
+    pool = gpu_pool_from(w, "bf16")
+    outs = [gpu_decode(pool, w, pb).float() for pb in (1, 4, 16, 64)]
+    for o in outs[1:]:
+        assert (o - outs[0]).abs().max().item() <= 1e-2
+    pool.close()
+
+
+def test_permutation_gives_identical_bits():
+    """Two different shuffles of the same tokens into the pool give bit-identical output:
+    the kernel's reduction order depends only on logical token positions."""
+    outs = []
+    for seed_shift in (0, 1):
+        w = custom([5, 40, 333, 1024], 16, 4, 128, "bf16", seed=21)
+        gen = torch.Generator().manual_seed(99 + seed_shift)
+        perm = torch.randperm(w.num_blocks, generator=gen).to(torch.int32)
+        tab = w.block_tables.clone()
+        m = tab >= 0
+        tab[m] = perm[tab[m].long()]
+        t = torch.arange(w.num_tokens)
+        seq = torch.repeat_interleave(torch.arange(w.num_seqs), w.context_lens.long())
+        pos = t - w.seq_offsets[seq]
+        w.block_tables = tab
+        w.slot_mapping = (tab[seq, pos // 16].long() * 16 + pos % 16).to(torch.int32)
+        pool = gpu_pool_from(w, "bf16")
+        outs.append(gpu_decode(pool, w).cpu())
+        pool.close()
+    assert torch.equal(outs[0].view(torch.int16), outs[1].view(torch.int16))
+
+
+def test_long_single_sequence():
+    """The longest context these tests build: one sequence of 65536 tokens, GQA group 4."""
+    w = custom([65536], 32, 8, 128, "bf16", seed=31)
+    check_all(w, "bf16")
+
+
+def test_int8_zero_rows():
+    """An all-zero row quantises to scale 0 and zero codes, and decodes without NaN."""
+    w = custom([20, 33], 8, 4, 64, "int8", seed=41)
+    w.key[3].zero_()
+    w.value[7].zero_()
+    w.value[20:30].zero_()
+    check_all(w, "int8")
+
+
+def test_int8_quantiser_bit_exact_many_rows():
+    """Codes and scales of 64k token-head rows equal the oracle's bit for bit."""
+    n, hkv, d = 8192, 8, 128
+    gen = torch.Generator().manual_seed(5)
+    key = (torch.randn(n, hkv, d, generator=gen) * torch.rand(n, hkv, 1, generator=gen) * 10).to(torch.bfloat16)
+    value = torch.randn(n, hkv, d, generator=gen).to(torch.bfloat16)
+    nb = n // 16 + 3
+    slots = torch.randperm(nb * 16, generator=gen)[:n].to(torch.int32)
+    pool = pkv.PagedKVPool(nb, hkv, d, "int8", fill=0)
+    pool.reshape_and_cache(key.cuda(), value.cuda(), slots.cuda())
+    torch.cuda.synchronize()
+    o = oracle.load()
+    kc = np.zeros((nb, hkv, 16, d), np.int8)
+    vc, ks, vs = kc.copy(), np.zeros((nb, hkv, 16), np.float32), np.zeros((nb, hkv, 16), np.float32)
+    o.reshape_and_cache_int8(W.bf16_bits(key), W.bf16_bits(value), slots.numpy(), kc, vc, ks, vs)
+    assert np.array_equal(pool.k_cache.cpu().numpy(), kc)
+    assert np.array_equal(pool.v_cache.cpu().numpy(), vc)
+    assert np.array_equal(pool.k_scale.cpu().numpy().view(np.uint32), ks.view(np.uint32))
+    assert np.array_equal(pool.v_scale.cpu().numpy().view(np.uint32), vs.view(np.uint32))
+    pool.close()
+
+
+def test_bf16_cache_write_bit_exact_and_skips_negative_slots():
+    n, hkv, d = 3000, 4, 64
+    gen = torch.Generator().manual_seed(6)
+    key = torch.randn(n, hkv, d, generator=gen).to(torch.bfloat16)
+    value = torch.randn(n, hkv, d, generator=gen).to(torch.bfloat16)
+    nb = n // 16 + 5
+    slots = torch.randperm(nb * 16, generator=gen)[:n].to(torch.int32)
+    slots[::5] = -1
+    pool = pkv.PagedKVPool(nb, hkv, d, "bf16", fill=0)
+    pool.k_cache.view(torch.int16).fill_(0x1234)
+    pool.v_cache.view(torch.int16).fill_(0x1234)
+    pool.reshape_and_cache(key.cuda(), value.cuda(), slots.cuda())
+    torch.cuda.synchronize()
+    o = oracle.load()
+    kc = np.full((nb, hkv, 16, d), 0x1234, np.uint16)
+    vc = kc.copy()
+    o.reshape_and_cache_bf16(W.bf16_bits(key), W.bf16_bits(value), slots.numpy(), kc, vc)
+    assert np.array_equal(W.bf16_bits(pool.k_cache), kc)
+    assert np.array_equal(W.bf16_bits(pool.v_cache), vc)
+    pool.close()
+
+
+# ------------------------------------------------------------ named workloads
+
+def _sample(w, k=6):
+    lens = w.context_lens.numpy()
+    order = np.argsort(lens)
+    picks = {int(order[0]), int(order[-1]), int(order[len(order) // 2])}
+    rng = np.random.default_rng(0)
+    picks.update(int(x) for x in rng.choice(w.num_seqs, size=min(k, w.num_seqs), replace=False))
+    return sorted(picks)
+
+
+@pytest.mark.parametrize("name", ["llama2_7b", "llama3_8b_gqa", "long_32k", "int8_cb"])
+def test_named_workload_full_size(name):
+    """Full-size workloads in the launch configuration the benchmark times (automatic
+    plan); the oracle checks sampled sequences (shortest, longest, median, random)."""
+    w = W.make(name, device="cuda")
+    kv = W.SPECS[name].kv_dtype
+    seqs = _sample(w)
+    check_all(w, kv, 0, seqs)
+
+
+def test_tiny_named_partitions():
+    w = W.make("tiny")
+    for pb in (1, 2, 3):
+        check_all(w, "bf16", pb)
+
+
+# ------------------------------------------------------------ errors and edges
+
+def test_device_error_bits():
+    w = custom([40, 20], 4, 4, 64, "bf16", seed=51)
+    pool = gpu_pool_from(w, "bf16", garbage=False)
+    bt = w.block_tables.clone()
+    bt[0, 1] = w.num_blocks + 5  # out of range
+    out = pool.decode(w.q.cuda(), bt.cuda(), w.context_lens.cuda(), w.scale, w.max_context_len)
+    torch.cuda.synchronize()
+    assert pool.device_error() & pkv.DEVERR_BLOCK_ID
+    assert torch.isfinite(out.float()).all()
+
+    lens = w.context_lens.clone()
+    lens[1] = 0
+    out = pool.decode(w.q.cuda(), w.block_tables.cuda(), lens.cuda(), w.scale, w.max_context_len)
+    torch.cuda.synchronize()
+    assert pool.device_error() & pkv.DEVERR_CONTEXT_LEN
+    assert (out[1].float() == 0).all()
+
+    lens[1] = w.max_context_len + 1  # beyond the declared maximum
+    out = pool.decode(w.q.cuda(), w.block_tables.cuda(), lens.cuda(), w.scale, w.max_context_len)
+    torch.cuda.synchronize()
+    assert pool.device_error() & pkv.DEVERR_CONTEXT_LEN
+
+    bad_slots = torch.tensor([w.num_blocks * 16, -1], dtype=torch.int32, device="cuda")
+    kv = torch.zeros(2, 4, 64, dtype=torch.bfloat16, device="cuda")
+    pool.reshape_and_cache(kv, kv, bad_slots)
+    torch.cuda.synchronize()
+    assert pool.device_error() == pkv.DEVERR_SLOT
+    assert pool.device_error() == 0  # reading clears it
+    pool.close()
+
+
+def test_empty_calls_are_noops():
+    pool = pkv.PagedKVPool(4, 2, 64, "bf16", fill=0)
+    before = pkv.launch_count()
+    q = torch.empty(0, 4, 64, dtype=torch.bfloat16, device="cuda")
+    pool.decode(q, torch.empty(0, 1, dtype=torch.int32, device="cuda"),
+                torch.empty(0, dtype=torch.int32, device="cuda"), 0.125, 16)
+    e = torch.empty(0, 2, 64, dtype=torch.bfloat16, device="cuda")
+    pool.reshape_and_cache(e, e, torch.empty(0, dtype=torch.int32, device="cuda"))
+    assert pkv.launch_count() == before
+    pool.close()
+
+
+def test_host_validation_errors():
+    pool = pkv.PagedKVPool(4, 2, 64, "bf16", fill=0)
+    q = torch.zeros(1, 6, 64, dtype=torch.bfloat16, device="cuda")  # group 3: unsupported
+    with pytest.raises(pkv.PagedKVError, match="unsupported"):
+        pool.decode(q, torch.zeros(1, 1, dtype=torch.int32, device="cuda"),
+                    torch.ones(1, dtype=torch.int32, device="cuda"), 1.0, 16)
+    q = torch.zeros(1, 2, 64, dtype=torch.bfloat16, device="cuda")
+    with pytest.raises(pkv.PagedKVError, match="invalid"):  # max_context_len beyond the table
+        pool.decode(q, torch.zeros(1, 1, dtype=torch.int32, device="cuda"),
+                    torch.ones(1, dtype=torch.int32, device="cuda"), 1.0, 17)
+    with pytest.raises(pkv.PagedKVError, match="workspace"):
+        pkv.paged_attention_decode(pool, q, torch.zeros(1, 4, dtype=torch.int32, device="cuda"),
+                                   torch.ones(1, dtype=torch.int32, device="cuda"), 1.0, 64,
+                                   workspace=torch.empty(16, dtype=torch.uint8, device="cuda"),
+                                   partition_blocks=1)
+    pool.close()
+
+
+def test_launch_count_and_plan():
+    w = custom([300, 40], 8, 2, 128, "bf16", seed=61)
+    pool = gpu_pool_from(w, "bf16", garbage=False)
+    plan = pkv.decode_plan(pool, w.num_seqs, w.num_q_heads, w.max_context_len, partition_blocks=4)
+    assert plan == {"partition_blocks": 4, "max_partitions": math.ceil(19 / 4), "kernels_per_call": 2}
+    before = pkv.launch_count()
+    gpu_decode(pool, w, 4)
+    assert pkv.launch_count() - before == 2
+    plan1 = pkv.decode_plan(pool, w.num_seqs, w.num_q_heads, w.max_context_len, partition_blocks=64)
+    assert plan1["kernels_per_call"] == 1
+    before = pkv.launch_count()
+    gpu_decode(pool, w, 64)
+    assert pkv.launch_count() - before == 1
+    pool.close()
+
+
+def test_side_stream():
+    w = custom([77, 150], 8, 8, 128, "bf16", seed=71)
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        pool = gpu_pool_from(w, "bf16")
+        out = pool.decode(w.q.cuda(), w.block_tables.cuda(), w.context_lens.cuda(), w.scale,
+                          w.max_context_len, stream=s)
+    s.synchronize()
+    ref, _, _ = oracle_decode(w, "bf16")
+    compare(out, ref, "side stream")
+    pool.close()
