@@ -204,6 +204,41 @@ PKV_API pkv_status pkv_paged_attention_decode_ex(const pkv_pool* pool, const voi
                                          const pkv_decode_options* options, void* stream);
 
 /*
+ * Size of the fixed device scratch array used by
+ * pkv_paged_attention_decode_static_scratch (16 MiB).
+ */
+#define PKV_STATIC_SCRATCH_BYTES (16u << 20)
+
+/*
+ * pkv_paged_attention_decode for callers that cannot allocate device memory.  The pages
+ * have no counterpart to this call; it exists for users of this library, not for the
+ * method.  Some callers cannot allocate where they decode -- for example a plugin hosted
+ * by another runtime that owns the whole device-memory budget and gives its plugins no
+ * allocator, or a latency-critical serving loop that must not call cudaMalloc.  This call
+ * takes the same arguments as pkv_paged_attention_decode minus the workspace, and keeps
+ * the split-K scratch in a fixed array of PKV_STATIC_SCRATCH_BYTES inside the library's
+ * device image instead; it calls no cudaMalloc, cudaFree or other allocating routine.
+ *  - Every GPU that loads the library holds that array until the process exits.
+ *  - The first call on a device looks up the array's device address (with that device
+ *    current) and caches it; make that first call before any stream capture.
+ *  - Call it with the pool's device current.
+ *  - All calls on a device share the array, which keeps the last call's contents.
+ *    Nothing in it needs to start at zero: each call writes every partial it reads.
+ *    Calls whose work overlaps on the GPU (other streams, other host threads) race on
+ *    the array; serialise them.
+ * Errors: as pkv_paged_attention_decode, and PKV_ERR_WORKSPACE when the batch shape
+ * needs more scratch than PKV_STATIC_SCRATCH_BYTES (pkv_static_scratch_error() then
+ * gives the sizes); nothing is launched in that case.
+ */
+PKV_API pkv_status pkv_paged_attention_decode_static_scratch(
+    const pkv_pool* pool, const void* q, const int32_t* block_tables, int max_blocks_per_seq,
+    const int32_t* context_lens, int num_seqs, int num_q_heads, int max_context_len, float scale,
+    void* out, void* stream);
+
+/* Text of the last static-scratch error in this thread (static per thread). */
+PKV_API const char* pkv_static_scratch_error(void);
+
+/*
  * Read and clear the pool's device error word (PKV_DEVERR_* bits).  Waits for the work
  * already enqueued on `stream`, then copies the word to *flags (host) and zeroes it.
  */

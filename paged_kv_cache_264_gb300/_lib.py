@@ -51,7 +51,12 @@ SIGNATURES = {
                                              ctypes.POINTER(DecodeOptions), _vp]),
     "pkv_get_device_error": (_i32, [_vp, ctypes.POINTER(ctypes.c_uint32), _vp]),
     "pkv_launch_count": (ctypes.c_uint64, []),
+    "pkv_paged_attention_decode_static_scratch": (_i32, [_vp, _vp, _vp, _i32, _vp, _i32, _i32, _i32, _f32,
+                                                         _vp, _vp]),
+    "pkv_static_scratch_error": (ctypes.c_char_p, []),
 }
+
+STATIC_SCRATCH_BYTES = 16 << 20
 
 _LOCK = threading.Lock()
 _LIB: ctypes.CDLL | None = None

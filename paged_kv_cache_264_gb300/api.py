@@ -201,3 +201,29 @@ def get_device_error(pool: PagedKVPool, stream=None) -> int:
     check(_lib.load().pkv_get_device_error(_handle(pool), ctypes.byref(v), _stream(stream)),
           "get_device_error")
     return v.value
+
+
+def paged_attention_decode_static_scratch(pool: PagedKVPool, q: torch.Tensor, block_tables: torch.Tensor,
+                                          context_lens: torch.Tensor, scale: float, max_context_len: int,
+                                          out: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """paged_attention_decode for callers that cannot allocate device memory: the split-K
+    scratch lives in a fixed 16 MiB array inside the library instead of a workspace the
+    caller allocates.  Calls that overlap on the GPU share that array and must be
+    serialised; shapes that need more scratch raise."""
+    _need(q, torch.bfloat16, "q", 3)
+    _need(block_tables, torch.int32, "block_tables", 2)
+    _need(context_lens, torch.int32, "context_lens", 1)
+    if out is None:
+        out = torch.empty_like(q)
+    else:
+        _need(out, torch.bfloat16, "out", 3)
+    b, hq, _ = q.shape
+    lib = _lib.load()
+    st = lib.pkv_paged_attention_decode_static_scratch(
+        _handle(pool), _ptr(q), _ptr(block_tables), block_tables.shape[1], _ptr(context_lens), b, hq,
+        int(max_context_len), float(scale), _ptr(out), _stream(stream))
+    if st == _lib.PKV_ERR_WORKSPACE:
+        raise _lib.PagedKVError(st, "paged_attention_decode_static_scratch (" +
+                                lib.pkv_static_scratch_error().decode() + ")")
+    check(st, "paged_attention_decode_static_scratch")
+    return out
