@@ -43,7 +43,7 @@ METRIC = "paged decode attention: KV-read GB/s (% of HBM peak) and decode steps/
 UNIT = "GB/s"
 DEFAULT_WORKLOAD = "llama2_7b"
 FALLBACK_HBM_GBS = 6800.0
-TRAFFIC_FILE = os.path.join(ROOT, "profiles", "ncu_traffic.json")
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "decode_traffic.txt")
 CSRC = os.path.join(ROOT, "paged_kv_cache_264_gb300", "csrc")
 
 
@@ -72,12 +72,15 @@ def recorded_traffic(workload: str):
     taken on the current kernel sources."""
     if not os.path.exists(TRAFFIC_FILE):
         return None
+    current = kernel_source_hash()
     with open(TRAFFIC_FILE) as f:
-        d = json.load(f)
-    rec = d.get(workload)
-    if not rec or rec.get("source_hash") != kernel_source_hash():
-        return None
-    return rec.get("dram_bytes_per_launch")
+        for line in f:
+            if line.startswith("#") or "=" not in line:
+                continue
+            rec = dict(kv.split("=", 1) for kv in line.split())
+            if rec.get("workload") == workload and rec.get("source_hash") == current:
+                return int(rec["dram_bytes"])
+    return None
 
 
 # ------------------------------------------------------------------ distributed
@@ -193,6 +196,9 @@ def run_ours(args, rank, world, local):
         pool.reshape_and_cache(w.key[hist].contiguous(), w.value[hist].contiguous(), slots[hist].contiguous())
     new_k, new_v = w.key[last].contiguous(), w.value[last].contiguous()
     new_slots = slots[last].contiguous()
+    w.key = w.value = None  # the history now lives in the pool; keep only the step's rows
+    del hist, slots
+    torch.cuda.empty_cache()
     q = w.q.to(dev)
     tables = w.block_tables.to(dev)
     lens = w.context_lens.to(dev)

@@ -138,10 +138,32 @@ PKV_API pkv_status pkv_reshape_and_cache(const pkv_pool* pool, const void* key, 
  *     (sequence, kv head, partition) becomes one work item, and sequences longer than
  *     one partition are combined by a log-sum-exp reduce.  0 = chosen from the batch
  *     shape and the device's SM count.
+ *   kernel: which decode kernel family runs.  PKV_KERNEL_AUTO (0) picks the tensor-core
+ *     kernel where it is built (GQA group 2, 4 or 8; bf16 head_dim 64/128 or INT8
+ *     head_dim 128) and the CUDA-core kernel otherwise; PKV_KERNEL_CUDA_CORE (1) and
+ *     PKV_KERNEL_TENSOR_CORE (2) force one (PKV_ERR_UNSUPPORTED if it is not built for
+ *     the shape).  Both compute the same function.
+ *   schedule: how CTAs map to work items.  PKV_SCHEDULE_AUTO (0) picks;
+ *     PKV_SCHEDULE_GRID (1) launches one CTA per (partition slot, sequence, kv head), slots
+ *     past a sequence's partition count exiting at once; PKV_SCHEDULE_PERSISTENT (2)
+ *     launches about one wave of CTAs that take items from a counter in the pool's device
+ *     memory (batches of up to 4096 sequences; larger batches use the grid).
+ *   stages: shared-memory ring depth per warp of the tensor-core kernel (0 = automatic;
+ *     otherwise one of the built depths, PKV_ERR_UNSUPPORTED for others).  Shallower rings
+ *     fit more CTAs on an SM.
  */
+#define PKV_KERNEL_AUTO 0
+#define PKV_KERNEL_CUDA_CORE 1
+#define PKV_KERNEL_TENSOR_CORE 2
+#define PKV_SCHEDULE_AUTO 0
+#define PKV_SCHEDULE_GRID 1
+#define PKV_SCHEDULE_PERSISTENT 2
 typedef struct pkv_decode_options {
   int partition_blocks;
-  int reserved[7];
+  int kernel;
+  int schedule;
+  int stages;
+  int reserved[4];
 } pkv_decode_options;
 
 /*
@@ -155,12 +177,15 @@ PKV_API pkv_status pkv_decode_workspace_bytes(const pkv_pool* pool, int num_seqs
 
 /*
  * The plan the decode call would use for this shape: partition size in blocks, the
- * largest number of partitions of one sequence, and kernels launched per call (1 or 2).
- * Any output pointer may be NULL.
+ * largest number of partitions of one sequence, kernels launched per call (1 or 2) and
+ * the kernel family (PKV_KERNEL_CUDA_CORE or PKV_KERNEL_TENSOR_CORE).  Any output pointer
+ * may be NULL.  Errors: as pkv_decode_workspace_bytes, and PKV_ERR_UNSUPPORTED when the
+ * options force a kernel family that is not built for the shape.
  */
 PKV_API pkv_status pkv_decode_plan(const pkv_pool* pool, int num_seqs, int num_q_heads,
                            int max_context_len, const pkv_decode_options* options,
-                           int* partition_blocks, int* max_partitions, int* kernels_per_call);
+                           int* partition_blocks, int* max_partitions, int* kernels_per_call,
+                           int* kernel);
 
 /*
  * PagedAttention decode: one new query token per sequence attends over the sequence's

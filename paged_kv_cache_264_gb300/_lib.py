@@ -32,8 +32,19 @@ _pi32 = ctypes.POINTER(ctypes.c_int)
 _psz = ctypes.POINTER(ctypes.c_size_t)
 
 
+KERNEL_AUTO = 0
+KERNEL_CUDA_CORE = 1
+KERNEL_TENSOR_CORE = 2
+
+
+SCHEDULE_AUTO = 0
+SCHEDULE_GRID = 1
+SCHEDULE_PERSISTENT = 2
+
+
 class DecodeOptions(ctypes.Structure):
-    _fields_ = [("partition_blocks", ctypes.c_int), ("reserved", ctypes.c_int * 7)]
+    _fields_ = [("partition_blocks", ctypes.c_int), ("kernel", ctypes.c_int), ("schedule", ctypes.c_int),
+                ("stages", ctypes.c_int), ("reserved", ctypes.c_int * 4)]
 
 
 SIGNATURES = {
@@ -45,7 +56,8 @@ SIGNATURES = {
     "pkv_pool_destroy": (_i32, [_vp]),
     "pkv_reshape_and_cache": (_i32, [_vp, _vp, _vp, _vp, _i64, _vp]),
     "pkv_decode_workspace_bytes": (_i32, [_vp, _i32, _i32, _i32, ctypes.POINTER(DecodeOptions), _psz]),
-    "pkv_decode_plan": (_i32, [_vp, _i32, _i32, _i32, ctypes.POINTER(DecodeOptions), _pi32, _pi32, _pi32]),
+    "pkv_decode_plan": (_i32, [_vp, _i32, _i32, _i32, ctypes.POINTER(DecodeOptions), _pi32, _pi32, _pi32,
+                               _pi32]),
     "pkv_paged_attention_decode": (_i32, [_vp, _vp, _vp, _i32, _vp, _i32, _i32, _i32, _f32, _vp, _vp, _sz, _vp]),
     "pkv_paged_attention_decode_ex": (_i32, [_vp, _vp, _vp, _i32, _vp, _i32, _i32, _i32, _f32, _vp, _vp, _sz,
                                              ctypes.POINTER(DecodeOptions), _vp]),

@@ -41,11 +41,18 @@ def _need(t: torch.Tensor, dtype, name: str, ndim: int | None = None) -> None:
         raise ValueError(f"{name} must have {ndim} dims, got {tuple(t.shape)}")
 
 
-def _options(partition_blocks: int) -> ctypes.POINTER(DecodeOptions) | None:
-    if not partition_blocks:
+_KERNELS = {0: 0, "auto": 0, 1: 1, "cuda_core": 1, 2: 2, "tensor_core": 2}
+_SCHEDULES = {0: 0, "auto": 0, 1: 1, "grid": 1, 2: 2, "persistent": 2}
+
+
+def _options(partition_blocks: int = 0, kernel=0, schedule=0, stages=0) -> ctypes.POINTER(DecodeOptions) | None:
+    if not partition_blocks and not _KERNELS[kernel] and not _SCHEDULES[schedule] and not stages:
         return None
     o = DecodeOptions()
     o.partition_blocks = int(partition_blocks)
+    o.kernel = _KERNELS[kernel]
+    o.schedule = _SCHEDULES[schedule]
+    o.stages = int(stages)
     return ctypes.pointer(o)
 
 
@@ -120,10 +127,10 @@ class PagedKVPool:
         reshape_and_cache(self, key, value, slot_mapping, stream)
 
     def decode(self, q, block_tables, context_lens, scale, max_context_len, out=None,
-               workspace=None, partition_blocks=0, stream=None):
+               workspace=None, partition_blocks=0, kernel=0, schedule=0, stages=0, stream=None):
         return paged_attention_decode(self, q, block_tables, context_lens, scale, max_context_len,
-                                      out=out, workspace=workspace,
-                                      partition_blocks=partition_blocks, stream=stream)
+                                      out=out, workspace=workspace, partition_blocks=partition_blocks,
+                                      kernel=kernel, schedule=schedule, stages=stages, stream=stream)
 
     def device_error(self, stream=None) -> int:
         return get_device_error(self, stream)
@@ -148,27 +155,29 @@ def reshape_and_cache(pool: PagedKVPool, key: torch.Tensor, value: torch.Tensor,
 
 
 def decode_workspace_bytes(pool: PagedKVPool, num_seqs: int, num_q_heads: int, max_context_len: int,
-                           partition_blocks: int = 0) -> int:
+                           partition_blocks: int = 0, kernel=0) -> int:
     n = ctypes.c_size_t()
     check(_lib.load().pkv_decode_workspace_bytes(_handle(pool), num_seqs, num_q_heads, max_context_len,
-                                                 _options(partition_blocks), ctypes.byref(n)),
+                                                 _options(partition_blocks, kernel), ctypes.byref(n)),
           "decode_workspace_bytes")
     return n.value
 
 
 def decode_plan(pool: PagedKVPool, num_seqs: int, num_q_heads: int, max_context_len: int,
-                partition_blocks: int = 0) -> dict:
-    pb, mp, kc = ctypes.c_int(), ctypes.c_int(), ctypes.c_int()
+                partition_blocks: int = 0, kernel=0) -> dict:
+    pb, mp, kc, kf = ctypes.c_int(), ctypes.c_int(), ctypes.c_int(), ctypes.c_int()
     check(_lib.load().pkv_decode_plan(_handle(pool), num_seqs, num_q_heads, max_context_len,
-                                      _options(partition_blocks), ctypes.byref(pb), ctypes.byref(mp),
-                                      ctypes.byref(kc)), "decode_plan")
-    return {"partition_blocks": pb.value, "max_partitions": mp.value, "kernels_per_call": kc.value}
+                                      _options(partition_blocks, kernel), ctypes.byref(pb), ctypes.byref(mp),
+                                      ctypes.byref(kc), ctypes.byref(kf)), "decode_plan")
+    return {"partition_blocks": pb.value, "max_partitions": mp.value, "kernels_per_call": kc.value,
+            "kernel": {1: "cuda_core", 2: "tensor_core"}.get(kf.value, str(kf.value))}
 
 
 def paged_attention_decode(pool: PagedKVPool, q: torch.Tensor, block_tables: torch.Tensor,
                            context_lens: torch.Tensor, scale: float, max_context_len: int,
                            out: torch.Tensor | None = None, workspace: torch.Tensor | None = None,
-                           partition_blocks: int = 0, stream=None) -> torch.Tensor:
+                           partition_blocks: int = 0, kernel=0, schedule=0, stages=0,
+                           stream=None) -> torch.Tensor:
     """Decode attention for q bf16 [B, Hq, d] over the pool; returns out bf16 [B, Hq, d].
 
     ``workspace`` (a uint8 CUDA tensor) is allocated here when not given and needed."""
@@ -184,14 +193,14 @@ def paged_attention_decode(pool: PagedKVPool, q: torch.Tensor, block_tables: tor
         _need(out, torch.bfloat16, "out", 3)
         if out.shape != q.shape:
             raise ValueError("out must have q's shape")
-    need = decode_workspace_bytes(pool, b, hq, max_context_len, partition_blocks) if b else 0
+    need = decode_workspace_bytes(pool, b, hq, max_context_len, partition_blocks, kernel) if b else 0
     if need and workspace is None:
         workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
     ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
     check(_lib.load().pkv_paged_attention_decode_ex(
         _handle(pool), _ptr(q), _ptr(block_tables), block_tables.shape[1], _ptr(context_lens), b, hq,
         int(max_context_len), float(scale), _ptr(out), _ptr(workspace), ws_bytes,
-        _options(partition_blocks), _stream(stream)), "paged_attention_decode")
+        _options(partition_blocks, kernel, schedule, stages), _stream(stream)), "paged_attention_decode")
     return out
 
 

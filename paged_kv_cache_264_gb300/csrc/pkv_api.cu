@@ -1,8 +1,11 @@
 // pkv_api.cu -- the C ABI declared in include/pagedkv.h: argument validation, the
 // decode plan (partition size), workspace layout and kernel dispatch.
+#include <cudaTypedefs.h>
+
 #include <atomic>
 #include <cstdio>
 #include <cstring>
+#include <mutex>
 #include <new>
 
 #include "../../include/pagedkv.h"
@@ -25,6 +28,9 @@ struct pkv_pool {
   uint32_t* d_err;  // library-owned device error word
   int device;
   int sm_count;
+  bool has_tmaps;    // tensor maps below are valid (the tensor-core kernel can run)
+  CUtensorMap tmap_k;
+  CUtensorMap tmap_v;
 };
 
 namespace {
@@ -45,9 +51,14 @@ int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
 bool group_supported(int g) { return g == 1 || g == 2 || g == 4 || g == 8; }
 
 constexpr int kMaxPartitionBlocks = 1024;
-constexpr int64_t kItemTargetBytes = 256 * 1024;  // K/V bytes one work item aims to stream
+constexpr int kItemBlocksCudaCore = 128;   // blocks per work item, before shrinking to fill the GPU
+constexpr int kItemBlocksTensorCore = 64;
 
 struct Plan {
+  int kernel;  // PKV_KERNEL_CUDA_CORE or PKV_KERNEL_TENSOR_CORE
+  int stages;  // tensor-core ring depth
+  int persistent;
+  int ctas_per_sm;
   int partition_blocks;
   int max_parts;
   int kernels;
@@ -59,17 +70,37 @@ pkv_status make_plan(const pkv_pool* pool, int num_seqs, int num_q_heads, int ma
                      const pkv_decode_options* opt, Plan* plan) {
   const int64_t max_nblk = ceil_div(max_context_len, pkv::kBlockSize);
   const int group = num_q_heads / pool->kv_heads;
+  const auto kv = static_cast<pkv::KvType>(pool->dtype);
+  const bool mma_ok = pool->has_tmaps && pkv::mma_supported(kv, pool->head_dim, group);
+  const int want = opt ? opt->kernel : PKV_KERNEL_AUTO;
+  if (want == PKV_KERNEL_TENSOR_CORE && !mma_ok) return PKV_ERR_UNSUPPORTED;
+  if (want != PKV_KERNEL_AUTO && want != PKV_KERNEL_CUDA_CORE && want != PKV_KERNEL_TENSOR_CORE)
+    return PKV_ERR_INVALID_ARG;
+  plan->kernel = (want == PKV_KERNEL_CUDA_CORE || !mma_ok) ? PKV_KERNEL_CUDA_CORE
+                                                           : PKV_KERNEL_TENSOR_CORE;
+  const int sched = opt ? opt->schedule : PKV_SCHEDULE_AUTO;
+  if (sched != PKV_SCHEDULE_AUTO && sched != PKV_SCHEDULE_GRID && sched != PKV_SCHEDULE_PERSISTENT)
+    return PKV_ERR_INVALID_ARG;
+  plan->persistent = 0;  // decided below, once the partition size is known
+  plan->stages = 0;
+  if (plan->kernel == PKV_KERNEL_TENSOR_CORE) {
+    plan->stages = (opt && opt->stages) ? opt->stages : pkv::mma_default_stages(kv, pool->head_dim);
+    if (!pkv::mma_stages_built(kv, pool->head_dim, plan->stages)) return PKV_ERR_UNSUPPORTED;
+  } else if (opt && opt->stages) {
+    return PKV_ERR_UNSUPPORTED;
+  }
+  const int per_sm = plan->kernel == PKV_KERNEL_TENSOR_CORE
+                         ? pkv::mma_ctas_per_sm(kv, pool->head_dim, group, plan->stages)
+                         : pkv::decode_ctas_per_sm(kv, pool->head_dim, group);
+  plan->ctas_per_sm = per_sm > 0 ? per_sm : 1;
   int P;
   if (opt && opt->partition_blocks > 0) {
     P = opt->partition_blocks;
   } else {
-    const int64_t block_bytes = pkv::decode_block_bytes(static_cast<pkv::KvType>(pool->dtype),
-                                                        pool->head_dim);
-    P = static_cast<int>(kItemTargetBytes / block_bytes);
-    if (P < 1) P = 1;
-    const int per_sm =
-        pkv::decode_ctas_per_sm(static_cast<pkv::KvType>(pool->dtype), pool->head_dim, group);
-    const int64_t resident = int64_t(pool->sm_count) * (per_sm > 0 ? per_sm : 1);
+    // Measured on GB300: items of 128 blocks (CUDA-core kernel) or 64 blocks (tensor-core
+    // kernel, which consumes a block faster) balance fewer partials against load balance.
+    P = plan->kernel == PKV_KERNEL_TENSOR_CORE ? kItemBlocksTensorCore : kItemBlocksCudaCore;
+    const int64_t resident = int64_t(pool->sm_count) * plan->ctas_per_sm;
     const int64_t units = int64_t(num_seqs) * pool->kv_heads;
     // Shrink the partition while the batch would not fill the GPU twice over.
     while (P > 4 && units * ceil_div(max_nblk, P) < 2 * resident) P /= 2;
@@ -79,6 +110,12 @@ pkv_status make_plan(const pkv_pool* pool, int num_seqs, int num_q_heads, int ma
   if (P < 1) P = 1;
   plan->partition_blocks = P;
   plan->max_parts = static_cast<int>(ceil_div(max_nblk, P));
+  // Persistent CTAs pay off when the grid would hold idle slots, i.e. when sequences split
+  // into different numbers of partitions; with one partition each, the grid is exact.
+  if (num_seqs <= pkv::kMaxSchedSeqs) {
+    if (sched == PKV_SCHEDULE_PERSISTENT) plan->persistent = 1;
+    else if (sched == PKV_SCHEDULE_AUTO) plan->persistent = plan->max_parts > 1;
+  }
   plan->kernels = plan->max_parts > 1 ? 2 : 1;
   plan->ws_bytes = 0;
   plan->ws_ml_offset = 0;
@@ -89,6 +126,42 @@ pkv_status make_plan(const pkv_pool* pool, int num_seqs, int num_q_heads, int ma
     plan->ws_bytes = plan->ws_ml_offset + rows * 2 * sizeof(float);
   }
   return PKV_OK;
+}
+
+// cuTensorMapEncodeTiled from the driver, looked up once.
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+  static std::once_flag once;
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  std::call_once(once, [] {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
+  });
+  return fn;
+}
+
+// A 2-D tensor map over a [rows, head_dim] pool: 128-byte boxes of 16 rows, 128-byte
+// swizzle.  Returns false when the layout does not qualify (rows not a whole number of
+// 128-byte spans, more than 2^31 rows, or no driver entry point).
+bool make_pool_tensor_map(CUtensorMap* map, void* base, pkv_kv_dtype dtype, int head_dim,
+                          int64_t rows) {
+  const int esz = dtype == PKV_KV_INT8 ? 1 : 2;
+  if ((head_dim * esz) % 128 != 0 || rows >= (int64_t(1) << 31)) return false;
+  auto encode = tensor_map_encoder();
+  if (!encode) return false;
+  const cuuint64_t dims[2] = {cuuint64_t(head_dim), cuuint64_t(rows)};
+  const cuuint64_t strides[1] = {cuuint64_t(head_dim) * esz};
+  const cuuint32_t box[2] = {cuuint32_t(128 / esz), cuuint32_t(pkv::kBlockSize)};
+  const cuuint32_t elem_strides[2] = {1, 1};
+  const CUresult r = encode(
+      map, dtype == PKV_KV_INT8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
+      2, base, dims, strides, box, elem_strides, CU_TENSOR_MAP_INTERLEAVE_NONE,
+      CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+      CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
 }
 
 pkv_status check_decode_shape(const pkv_pool* pool, int num_seqs, int num_q_heads,
@@ -187,8 +260,20 @@ pkv_status pkv_pool_create(int64_t num_blocks, int kv_heads, int head_dim, int b
     cudaFree(d_err);
     return PKV_ERR_INVALID_ARG;
   }
-  *pool = pkv_pool{num_blocks, kv_heads, head_dim, dtype, k_cache, v_cache,
-                   k_scale, v_scale, d_err, dev, sms};
+  pool->num_blocks = num_blocks;
+  pool->kv_heads = kv_heads;
+  pool->head_dim = head_dim;
+  pool->dtype = dtype;
+  pool->k_cache = k_cache;
+  pool->v_cache = v_cache;
+  pool->k_scale = k_scale;
+  pool->v_scale = v_scale;
+  pool->d_err = d_err;
+  pool->device = dev;
+  pool->sm_count = sms;
+  const int64_t rows = num_blocks * kv_heads * pkv::kBlockSize;
+  pool->has_tmaps = make_pool_tensor_map(&pool->tmap_k, k_cache, dtype, head_dim, rows) &&
+                    make_pool_tensor_map(&pool->tmap_v, v_cache, dtype, head_dim, rows);
   *out = pool;
   return PKV_OK;
 }
@@ -234,21 +319,25 @@ pkv_status pkv_decode_workspace_bytes(const pkv_pool* pool, int num_seqs, int nu
   pkv_status st = check_decode_shape(pool, num_seqs, num_q_heads, max_context_len);
   if (st != PKV_OK) return st;
   Plan plan;
-  make_plan(pool, num_seqs, num_q_heads, max_context_len, options, &plan);
+  st = make_plan(pool, num_seqs, num_q_heads, max_context_len, options, &plan);
+  if (st != PKV_OK) return st;
   *bytes = plan.ws_bytes;
   return PKV_OK;
 }
 
 pkv_status pkv_decode_plan(const pkv_pool* pool, int num_seqs, int num_q_heads,
                            int max_context_len, const pkv_decode_options* options,
-                           int* partition_blocks, int* max_partitions, int* kernels_per_call) {
+                           int* partition_blocks, int* max_partitions, int* kernels_per_call,
+                           int* kernel) {
   pkv_status st = check_decode_shape(pool, num_seqs, num_q_heads, max_context_len);
   if (st != PKV_OK) return st;
   Plan plan;
-  make_plan(pool, num_seqs, num_q_heads, max_context_len, options, &plan);
+  st = make_plan(pool, num_seqs, num_q_heads, max_context_len, options, &plan);
+  if (st != PKV_OK) return st;
   if (partition_blocks) *partition_blocks = plan.partition_blocks;
   if (max_partitions) *max_partitions = plan.max_parts;
   if (kernels_per_call) *kernels_per_call = plan.kernels;
+  if (kernel) *kernel = plan.kernel;
   return PKV_OK;
 }
 
@@ -267,7 +356,8 @@ pkv_status pkv_paged_attention_decode_ex(const pkv_pool* pool, const void* q,
     return PKV_ERR_INVALID_ARG;
   if (!(scale == scale)) return PKV_ERR_INVALID_ARG;  // NaN
   Plan plan;
-  make_plan(pool, num_seqs, num_q_heads, max_context_len, options, &plan);
+  st = make_plan(pool, num_seqs, num_q_heads, max_context_len, options, &plan);
+  if (st != PKV_OK) return st;
   if (plan.ws_bytes > 0) {
     if (!workspace || workspace_bytes < plan.ws_bytes) return PKV_ERR_WORKSPACE;
     if (!aligned16(workspace)) return PKV_ERR_INVALID_ARG;
@@ -287,6 +377,13 @@ pkv_status pkv_paged_attention_decode_ex(const pkv_pool* pool, const void* q,
                 ? reinterpret_cast<float*>(static_cast<char*>(workspace) + plan.ws_ml_offset)
                 : nullptr;
   p.err = pool->d_err;
+  p.sched = pool->d_err + 1;
+  p.persistent = plan.persistent;
+  {
+    const int64_t items = int64_t(plan.max_parts) * num_seqs * pool->kv_heads;
+    const int64_t resident = int64_t(pool->sm_count) * plan.ctas_per_sm;
+    p.grid = static_cast<int>(items < resident ? items : resident);
+  }
   p.num_blocks = pool->num_blocks;
   p.max_blocks_per_seq = max_blocks_per_seq;
   p.num_seqs = num_seqs;
@@ -300,8 +397,13 @@ pkv_status pkv_paged_attention_decode_ex(const pkv_pool* pool, const void* q,
 
   const int group = num_q_heads / pool->kv_heads;
   auto s = static_cast<cudaStream_t>(stream);
-  cudaError_t e = pool->dtype == PKV_KV_INT8 ? pkv::launch_decode_int8(p, group, s)
-                                              : pkv::launch_decode_bf16(p, group, s);
+  cudaError_t e;
+  if (plan.kernel == PKV_KERNEL_TENSOR_CORE)
+    e = pkv::launch_decode_mma(p, &pool->tmap_k, &pool->tmap_v,
+                               static_cast<pkv::KvType>(pool->dtype), group, plan.stages, s);
+  else
+    e = pool->dtype == PKV_KV_INT8 ? pkv::launch_decode_int8(p, group, s)
+                                   : pkv::launch_decode_bf16(p, group, s);
   if (e != cudaSuccess) return cuda_fail(e, "paged_attention_decode launch");
   g_launches.fetch_add(1, std::memory_order_relaxed);
   if (plan.max_parts > 1) {

@@ -61,6 +61,12 @@ struct KvTraits<KvType::kInt8> {
 
 constexpr size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
+// Shared memory of the persistent-grid scheduler: the batch's partition prefix sum
+// (num_seqs + 1 ints), two control ints and one scan slot per thread.
+__host__ __device__ constexpr size_t sched_smem_bytes(int num_seqs, int threads) {
+  return (size_t(num_seqs) + 1 + 2 + threads) * 4;
+}
+
 template <KvType KV, int D, int G, int NW, int S>
 struct DecodeCfg {
   static constexpr int kEsz = KvTraits<KV>::kElemBytes;
@@ -82,8 +88,8 @@ struct DecodeCfg {
   static constexpr size_t kProbBytes = size_t(NW) * 17 * G * 4;
   static constexpr size_t kBarOff = align_up(kProbOff + kProbBytes, 16);
   static constexpr size_t kTableOff = kBarOff + size_t(NW) * S * 8;
-  static size_t smem_bytes(int partition_blocks) {
-    return kTableOff + size_t(partition_blocks) * 4;
+  static size_t smem_bytes(int partition_blocks, int sched_seqs) {
+    return kTableOff + size_t(partition_blocks) * 4 + sched_smem_bytes(sched_seqs, kThreads);
   }
 
   static_assert(D % 32 == 0 && (D == 64 || D == 128), "head_dim 64 or 128");
@@ -148,6 +154,182 @@ __device__ __forceinline__ void fma_i8x4(float (&part)[G], const float (&qr)[G][
   }
 }
 
+// ---------------------------------------------------------------- work scheduling
+//
+// A work item is (sequence b, kv head, partition).  Two ways to map CTAs to items:
+//  * classic grid (large batches): one CTA per (partition slot, sequence, kv head), where
+//    slots past a sequence's own partition count exit at once;
+//  * persistent grid (batches up to kMaxSchedSeqs sequences): a few CTAs per SM build, in
+//    shared memory, the prefix sum of every sequence's partition count and take items from
+//    a ticket counter in global memory, one item ahead, until the tickets run out.  The
+//    last CTA to finish resets the counters to zero for the next call.  Nothing waits on
+//    another CTA.
+// A sequence whose context length is out of range counts as one item that writes zeros.
+
+struct ItemInfo {
+  int b, kvh, part, nparts, T;
+  bool bad_len;
+};
+
+// Shared-memory tail after the block-table slice: cum[B + 1] | slot[2] | scan[NT].
+struct SchedSmem {
+  int* cum;
+  int* slot;  // [0]: current item, [1]: abort flag
+  int* scan;
+};
+
+__device__ __forceinline__ SchedSmem sched_smem(unsigned char* tail, int num_seqs) {
+  int* base = reinterpret_cast<int*>(tail);
+  return SchedSmem{base, base + num_seqs + 1, base + num_seqs + 3};
+}
+
+__device__ __forceinline__ int seq_parts(const DecodeParams& p, int T) {
+  if (T < 1 || T > p.max_context_len) return 1;
+  const int nblk = (T + kBlockSize - 1) / kBlockSize;
+  return (nblk + p.partition_blocks - 1) / p.partition_blocks;
+}
+
+// First item of this CTA, or -1.  Builds the prefix sum in persistent mode.  Ends with a
+// barrier (so it also publishes the mbarrier initialisation done before it).
+template <int NT>
+__device__ __forceinline__ int first_item(const DecodeParams& p, const SchedSmem& ss) {
+  if (!p.persistent) {
+    __syncthreads();
+    return blockIdx.x;
+  }
+  const int B = p.num_seqs;
+  const int per = (B + NT - 1) / NT;
+  const int lo = min(B, int(threadIdx.x) * per);
+  const int hi = min(B, lo + per);
+  int sum = 0;
+  for (int b = lo; b < hi; ++b) {
+    const int c = seq_parts(p, __ldg(p.context_lens + b));
+    ss.cum[b + 1] = c;
+    sum += c;
+  }
+  ss.scan[threadIdx.x] = sum;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    int run = 0;
+    for (int i = 0; i < NT; ++i) {
+      const int v = ss.scan[i];
+      ss.scan[i] = run;
+      run += v;
+    }
+    ss.cum[0] = 0;
+    ss.slot[0] = static_cast<int>(atomicAdd(p.sched, 1u));
+    ss.slot[1] = 0;
+  }
+  __syncthreads();
+  int run = ss.scan[threadIdx.x];
+  for (int b = lo; b < hi; ++b) {
+    run += ss.cum[b + 1];
+    ss.cum[b + 1] = run;
+  }
+  __syncthreads();
+  const int item = ss.slot[0];
+  return item < ss.cum[B] * p.kv_heads ? item : -1;
+}
+
+// Ticket for the item after this one (thread 0 fetches it now; its value is used at the
+// end of the item, so the atomic's latency overlaps the item's work).
+__device__ __forceinline__ int prefetch_ticket(const DecodeParams& p) {
+  return (p.persistent && threadIdx.x == 0) ? static_cast<int>(atomicAdd(p.sched, 1u)) : 0;
+}
+
+__device__ __forceinline__ int next_item(const DecodeParams& p, const SchedSmem& ss, int ticket) {
+  if (!p.persistent) return -1;
+  __syncthreads();  // this item's shared memory is free again
+  if (threadIdx.x == 0) ss.slot[0] = ticket;
+  __syncthreads();
+  const int item = ss.slot[0];
+  if (ss.slot[1]) return -1;  // a bounded wait gave up: stop taking work
+  return item < ss.cum[p.num_seqs] * p.kv_heads ? item : -1;
+}
+
+__device__ __forceinline__ void finish_items(const DecodeParams& p) {
+  if (!p.persistent || threadIdx.x != 0) return;
+  __threadfence();
+  if (atomicAdd(p.sched + 1, 1u) == gridDim.x - 1) {
+    atomicExch(p.sched, 0u);
+    atomicExch(p.sched + 1, 0u);
+  }
+}
+
+// (b, kv head, partition) of an item; false for an idle classic-grid slot.
+__device__ __forceinline__ bool locate_item(const DecodeParams& p, const SchedSmem& ss, int item,
+                                            ItemInfo& it) {
+  if (p.persistent) {
+    const int u = item / p.kv_heads;
+    it.kvh = item - u * p.kv_heads;
+    int lo = 0, hi = p.num_seqs;  // cum[lo] <= u < cum[hi]
+    while (hi - lo > 1) {
+      const int mid = (lo + hi) >> 1;
+      if (ss.cum[mid] <= u) lo = mid; else hi = mid;
+    }
+    it.b = lo;
+    it.part = u - ss.cum[lo];
+  } else {
+    const int units = p.num_seqs * p.kv_heads;
+    it.part = item / units;
+    const int rem = item - it.part * units;
+    it.b = rem / p.kv_heads;
+    it.kvh = rem - it.b * p.kv_heads;
+  }
+  it.T = __ldg(p.context_lens + it.b);
+  it.bad_len = it.T < 1 || it.T > p.max_context_len;
+  it.nparts = seq_parts(p, it.T);
+  return it.part < it.nparts;
+}
+
+// Zero output and an error bit for a sequence with an out-of-range context length.
+template <int G, int D, int NT>
+__device__ __forceinline__ void write_bad_len(const DecodeParams& p, const ItemInfo& it, size_t qo_base) {
+  if (it.part != 0) return;
+  auto* out = static_cast<__nv_bfloat16*>(p.out);
+  for (int i = threadIdx.x; i < G * D; i += NT) out[qo_base + i] = __float2bfloat16_rn(0.0f);
+  if (threadIdx.x == 0) set_error(p.err, kErrContextLen);
+}
+
+// Merge the NW per-warp states of one work item by log-sum-exp and write the bf16 output
+// (single-partition sequences) or the item's partial (m, l, acc) to the workspace.  Warp w's
+// record is [G][D + 2] floats (running max in log2 units, sum, accumulator) at
+// smem + w * warp_stride.
+template <int G, int D, int NW>
+__device__ __forceinline__ void merge_warp_records(const unsigned char* smem, size_t warp_stride,
+                                                   const DecodeParams& p, int b, int kvh, int part,
+                                                   int nparts, size_t qo_base) {
+  auto* out = static_cast<__nv_bfloat16*>(p.out);
+  for (int i = threadIdx.x; i < G * D; i += NW * 32) {
+    const int g = i / D;
+    const int d = i - g * D;
+    float M = -INFINITY;
+#pragma unroll
+    for (int w = 0; w < NW; ++w)
+      M = fmaxf(M, reinterpret_cast<const float*>(smem + size_t(w) * warp_stride)[g * (D + 2)]);
+    float L = 0.0f, A = 0.0f;
+    if (M != -INFINITY) {
+#pragma unroll
+      for (int w = 0; w < NW; ++w) {
+        const float* r = reinterpret_cast<const float*>(smem + size_t(w) * warp_stride) + g * (D + 2);
+        const float f = exp2f(r[0] - M);
+        L = fmaf(f, r[1], L);
+        A = fmaf(f, r[2 + d], A);
+      }
+    }
+    if (nparts == 1) {
+      out[qo_base + i] = __float2bfloat16_rn(L > 0.0f ? A / L : 0.0f);
+    } else {
+      const size_t pi = (size_t(b) * p.num_q_heads + size_t(kvh) * G + g) * p.max_parts + part;
+      p.ws_acc[pi * D + d] = A;
+      if (d == 0) {
+        p.ws_ml[2 * pi] = M;
+        p.ws_ml[2 * pi + 1] = L;
+      }
+    }
+  }
+}
+
 template <KvType KV, int D, int G, int NW, int S>
 __global__ void __launch_bounds__(NW * 32)
     paged_decode_kernel(const DecodeParams p) {
@@ -158,43 +340,34 @@ __global__ void __launch_bounds__(NW * 32)
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
 
-  // ---- which item
-  const int units = p.num_seqs * p.kv_heads;
-  const int part = static_cast<int>(blockIdx.x / static_cast<unsigned>(units));
-  const int rem = static_cast<int>(blockIdx.x - static_cast<unsigned>(part) * units);
-  const int b = rem / p.kv_heads;
-  const int kvh = rem - b * p.kv_heads;
-  const int T = __ldg(p.context_lens + b);
-  const size_t qo_base = (size_t(b) * p.num_q_heads + size_t(kvh) * G) * D;
-  auto* out = static_cast<__nv_bfloat16*>(p.out);
-
-  if (T < 1 || T > p.max_context_len) {
-    if (part == 0) {
-      for (int i = threadIdx.x; i < G * D; i += C::kThreads)
-        out[qo_base + i] = __float2bfloat16_rn(0.0f);
-      if (threadIdx.x == 0) set_error(p.err, kErrContextLen);
-    }
-    return;
-  }
-  const int nblk = (T + kBlockSize - 1) / kBlockSize;
-  const int P = p.partition_blocks;
-  const int nparts = (nblk + P - 1) / P;
-  if (part >= nparts) return;
-  const int blk0 = part * P;
-  const int nb_item = min(nblk, blk0 + P) - blk0;
-
   int* tbl = reinterpret_cast<int*>(smem + C::kTableOff);
+  const SchedSmem ss = sched_smem(smem + C::kTableOff + size_t(p.partition_blocks) * 4,
+                                  p.persistent ? p.num_seqs : 0);
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::kBarOff) + warp * S;
   unsigned char* ring = smem + size_t(warp) * S * C::kStageBytes;
   float* prob = reinterpret_cast<float*>(smem + C::kProbOff) + warp * 17 * G;
-
-  const int32_t* trow = p.block_tables + size_t(b) * p.max_blocks_per_seq + blk0;
-  for (int i = threadIdx.x; i < nb_item; i += C::kThreads) tbl[i] = __ldg(trow + i);
   if (lane == 0) {
 #pragma unroll
     for (int s = 0; s < S; ++s) mbar_init(bars + s, 1);
     fence_barrier_init();
   }
+  const int P = p.partition_blocks;
+  uint32_t kb = 0;  // blocks this warp has consumed over all its items: stage and phase counter
+
+  for (int item = first_item<C::kThreads>(p, ss); item >= 0;) {
+  const int ticket = prefetch_ticket(p);
+  ItemInfo it;
+  if (locate_item(p, ss, item, it)) {
+  const int b = it.b, kvh = it.kvh, part = it.part, nparts = it.nparts, T = it.T;
+  const size_t qo_base = (size_t(b) * p.num_q_heads + size_t(kvh) * G) * D;
+  if (it.bad_len) {
+    write_bad_len<G, D, C::kThreads>(p, it, qo_base);
+  } else {
+  const int nblk = (T + kBlockSize - 1) / kBlockSize;
+  const int blk0 = part * P;
+  const int nb_item = min(nblk, blk0 + P) - blk0;
+  const int32_t* trow = p.block_tables + size_t(b) * p.max_blocks_per_seq + blk0;
+  for (int i = threadIdx.x; i < nb_item; i += C::kThreads) tbl[i] = __ldg(trow + i);
   __syncthreads();
 
   // Blocks of this warp: item blocks warp, warp + NW, ...
@@ -203,8 +376,8 @@ __global__ void __launch_bounds__(NW * 32)
   const char* kbase = static_cast<const char*>(p.k_cache);
   const char* vbase = static_cast<const char*>(p.v_cache);
 
-  auto issue = [&](int k) {  // lane 0 only: fetch the warp's k-th block into stage k % S
-    const int s = k % S;
+  auto issue = [&](int k) {  // lane 0 only: fetch the warp's k-th block of the item
+    const int s = (kb + k) % S;
     unsigned char* st = ring + size_t(s) * C::kStageBytes;
     const int phys = tbl[warp + k * NW];
     if (phys < 0 || phys >= p.num_blocks) {
@@ -265,8 +438,8 @@ __global__ void __launch_bounds__(NW * 32)
 
   int failed_at = -1;
   for (int k = 0; k < nw; ++k) {
-    const int s = k % S;
-    const bool ok = __all_sync(kFull, mbar_wait_bounded(bars + s, (k / S) & 1));
+    const int s = (kb + k) % S;
+    const bool ok = __all_sync(kFull, mbar_wait_bounded(bars + s, ((kb + k) / S) & 1));
     if (!ok) {
       failed_at = k;
       if (lane == 0) set_error(p.err, kErrTimeout);
@@ -393,11 +566,14 @@ __global__ void __launch_bounds__(NW * 32)
   }
   if (failed_at >= 0) {
     // Let the copies still in flight into this warp's ring land (bounded) before the
-    // ring is reused for the merge record; their data is not used.
+    // ring is reused for the merge record; their data is not used.  The CTA then takes no
+    // further items.
     for (int k = failed_at; k < nw && k < failed_at + S; ++k)
-      (void)mbar_wait_bounded(bars + (k % S), (k / S) & 1);
+      (void)mbar_wait_bounded(bars + ((kb + k) % S), ((kb + k) / S) & 1);
+    if (lane == 0 && p.persistent) ss.slot[1] = 1;
     __syncwarp();
   }
+  kb += failed_at >= 0 ? min(nw, failed_at + S) : nw;
 
   // ---- this warp's softmax sum per head, then its merge record in its ring stage 0
 #pragma unroll
@@ -413,36 +589,12 @@ __global__ void __launch_bounds__(NW * 32)
     for (int i = 0; i < C::kDPV; ++i) rec[g * (D + 2) + 2 + lane * C::kDPV + i] = acc[g][i];
   __syncthreads();
 
-  // ---- merge the NW warp states (log-sum-exp) and write the output or the partial
-  for (int i = threadIdx.x; i < G * D; i += C::kThreads) {
-    const int g = i / D;
-    const int d = i - g * D;
-    float M = -INFINITY;
-#pragma unroll
-    for (int w = 0; w < NW; ++w)
-      M = fmaxf(M, reinterpret_cast<const float*>(smem + size_t(w) * S * C::kStageBytes)[g * (D + 2)]);
-    float L = 0.0f, A = 0.0f;
-    if (M != -INFINITY) {
-#pragma unroll
-      for (int w = 0; w < NW; ++w) {
-        const float* r =
-            reinterpret_cast<const float*>(smem + size_t(w) * S * C::kStageBytes) + g * (D + 2);
-        const float f = exp2f(r[0] - M);
-        L = fmaf(f, r[1], L);
-        A = fmaf(f, r[2 + d], A);
-      }
-    }
-    if (nparts == 1) {
-      out[qo_base + i] = __float2bfloat16_rn(L > 0.0f ? A / L : 0.0f);
-    } else {
-      const size_t pi = (size_t(b) * p.num_q_heads + size_t(kvh) * G + g) * p.max_parts + part;
-      p.ws_acc[pi * D + d] = A;
-      if (d == 0) {
-        p.ws_ml[2 * pi] = M;
-        p.ws_ml[2 * pi + 1] = L;
-      }
-    }
-  }
+  merge_warp_records<G, D, NW>(smem, size_t(S) * C::kStageBytes, p, b, kvh, part, nparts, qo_base);
+  }  // valid context length
+  }  // item located
+  item = next_item(p, ss, ticket);
+  }  // items
+  finish_items(p);
 }
 
 // Merge the partitions of every split sequence: M = max_p m_p, L = sum_p 2^(m_p - M) l_p,
@@ -503,14 +655,15 @@ cudaError_t launch_decode_variant(const DecodeParams& p, cudaStream_t stream) {
   cudaGetDevice(&dev);
   if (dev < 0 || dev >= 64 || !attr_done[dev]) {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         static_cast<int>(C::smem_bytes(kMaxPartitionBlocks)));
+                                         static_cast<int>(C::smem_bytes(kMaxPartitionBlocks, kMaxSchedSeqs)));
     if (e != cudaSuccess) return e;
     if (dev >= 0 && dev < 64) attr_done[dev] = true;
   }
-  const int64_t grid = int64_t(p.max_parts) * p.num_seqs * p.kv_heads;
+  const int64_t grid =
+      p.persistent ? int64_t(p.grid) : int64_t(p.max_parts) * p.num_seqs * p.kv_heads;
   if (grid <= 0) return cudaSuccess;
   if (grid > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
-  kern<<<static_cast<unsigned>(grid), C::kThreads, C::smem_bytes(p.partition_blocks), stream>>>(p);
+  kern<<<static_cast<unsigned>(grid), C::kThreads, C::smem_bytes(p.partition_blocks, p.persistent ? p.num_seqs : 0), stream>>>(p);
   return cudaGetLastError();
 }
 
@@ -519,9 +672,9 @@ int ctas_per_sm_variant() {
   using C = DecodeCfg<KV, D, G, NW, S>;
   auto kern = paged_decode_kernel<KV, D, G, NW, S>;
   cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                       static_cast<int>(C::smem_bytes(kMaxPartitionBlocks)));
+                       static_cast<int>(C::smem_bytes(kMaxPartitionBlocks, kMaxSchedSeqs)));
   int n = 0;
-  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kern, C::kThreads, C::smem_bytes(64)) !=
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kern, C::kThreads, C::smem_bytes(64, 256)) !=
       cudaSuccess)
     return 0;
   return n;

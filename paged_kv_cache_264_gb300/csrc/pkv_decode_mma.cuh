@@ -1,0 +1,433 @@
+// pkv_decode_mma.cuh -- PagedAttention decode on the tensor cores (mma.sync) for GQA
+// groups of 2, 4 or 8 query heads, head_dim 128 (bf16 or INT8 pools) or 64 (bf16).
+//
+// Same work decomposition and result as paged_decode_kernel (pkv_decode.cuh): one CTA
+// per (sequence, kv head, context partition), NW warps taking the item's blocks in turn,
+// a per-warp ring of S shared-memory stages, an online softmax and a log-sum-exp merge.
+// What changes is how a 16-token block is consumed:
+//
+//  * Tiles arrive by TMA tensor copies (cp.async.bulk.tensor.2d) through a tensor map of
+//    the pool viewed as rows of head_dim elements, in 128-byte boxes with the 128-byte
+//    swizzle, so that the shared-memory reads below are free of bank conflicts.
+//  * Logits for all heads of the group come from m16n8k16 MMAs with fp32 accumulation:
+//    S[16 tokens x 8 heads] = K[16 x d] q^T[d x 8] (heads past G are zero columns).
+//  * The probabilities stay in registers: the accumulator fragment of S, packed to 16-bit
+//    pairs and transposed with movmatrix, is exactly the B operand of the PV product
+//    O^T[d x 8] += V^T[d x 16] P[16 x 8], whose A operand is V read transposed by ldmatrix.
+//    The row (dims) of O^T that a lane holds and the column (head) of its softmax state
+//    coincide, so rescaling needs no data movement, and it is skipped whenever no head's
+//    running max moved in a block.
+//  * INT8: codes become fp16 exactly (see f16x2_from_flipped) and both products run in
+//    fp16.  q is scaled by a power of two into fp16 range (exact for bf16 values), the
+//    K scale multiplies the fp32 logits, and the V scale is folded into P together with a
+//    power-of-two block exponent that keeps P in [0, 2): O^T is kept in units of 2^E and E
+//    only grows, like the running max, so the rescale stays rare.  Within one k-step the
+//    dims a lane handles are permuted (the same permutation on K and q), which lets each
+//    lane read its codes with 16-byte loads.
+#pragma once
+
+#include <limits.h>
+
+#include "pkv_decode.cuh"
+
+namespace pkv {
+
+template <KvType KV, int D, int G, int NW, int S>
+struct MmaCfg {
+  static constexpr int kEsz = KvTraits<KV>::kElemBytes;
+  static constexpr bool kQuant = KvTraits<KV>::kQuant;
+  static constexpr int kRowBytes = D * kEsz;           // one token row of one tile
+  static constexpr int kBoxCols = 128 / kEsz;          // elements in a 128-byte box row
+  static constexpr int kBoxes = kRowBytes / 128;       // boxes per tile
+  static constexpr int kBoxBytes = kBlockSize * 128;   // 2 KiB, 1 KiB aligned in the ring
+  static constexpr int kTileBytes = kBoxes * kBoxBytes;
+  static constexpr int kStageBytes = 2 * kTileBytes;   // K tile, V tile
+  static constexpr int kScaleStage = kQuant ? 2 * kBlockSize * 4 : 0;  // K and V scales
+  static constexpr int kKSteps = D / 16;
+  static constexpr int kMTiles = D / 16;
+  static constexpr int kThreads = NW * 32;
+  static constexpr size_t kRingBytes = size_t(NW) * S * kStageBytes;
+  static constexpr size_t kScaleOff = kRingBytes;
+  static constexpr size_t kBarOff = align_up(kScaleOff + size_t(NW) * S * kScaleStage, 16);
+  static constexpr size_t kTableOff = kBarOff + size_t(NW) * S * 8;
+  static size_t smem_bytes(int partition_blocks, int sched_seqs) {
+    return 1024 /* alignment slack */ + kTableOff + size_t(partition_blocks) * 4 +
+           sched_smem_bytes(sched_seqs, kThreads);
+  }
+
+  static_assert(kRowBytes % 128 == 0, "rows must be whole 128-byte swizzle spans");
+  static_assert(!kQuant || D == 128, "INT8 tensor-core path is built for head_dim 128");
+  static_assert(G == 2 || G == 4 || G == 8, "group of 2, 4 or 8 query heads");
+  static_assert(size_t(G) * (D + 2) * 4 <= size_t(S) * kStageBytes, "merge record fits the ring");
+};
+
+// Shared-memory address of 16-byte chunk `c` of token row `t` in a tile whose 128-byte
+// boxes were written with the 128-byte swizzle (chunk index xor row index mod 8).
+__device__ __forceinline__ uint32_t swz(uint32_t tile, int t, int c) {
+  return tile + (c >> 3) * 2048 + t * 128 + (((c & 7) ^ (t & 7)) << 4);
+}
+
+template <KvType KV, int D, int G, int NW, int S>
+__global__ void __launch_bounds__(NW * 32)
+    paged_decode_mma_kernel(const __grid_constant__ CUtensorMap tmap_k,
+                            const __grid_constant__ CUtensorMap tmap_v, const DecodeParams p) {
+  using C = MmaCfg<KV, D, G, NW, S>;
+  constexpr uint32_t kFull = 0xffffffffu;
+  extern __shared__ unsigned char smem_raw[];
+  unsigned char* smem = reinterpret_cast<unsigned char*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int gi = lane >> 2;  // fragment row group
+  const int gj = lane & 3;   // fragment column pair
+
+  int* tbl = reinterpret_cast<int*>(smem + C::kTableOff);
+  const SchedSmem ss = sched_smem(smem + C::kTableOff + size_t(p.partition_blocks) * 4,
+                                  p.persistent ? p.num_seqs : 0);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::kBarOff) + warp * S;
+  unsigned char* ring = smem + size_t(warp) * S * C::kStageBytes;
+  float* scl = reinterpret_cast<float*>(smem + C::kScaleOff) + warp * S * (C::kScaleStage / 4);
+  if (lane == 0) {
+#pragma unroll
+    for (int s = 0; s < S; ++s) mbar_init(bars + s, 1);
+    fence_barrier_init();
+  }
+  if (threadIdx.x == 0) {
+    prefetch_tensor_map(&tmap_k);
+    prefetch_tensor_map(&tmap_v);
+  }
+  const int P = p.partition_blocks;
+  uint32_t kb = 0;  // blocks this warp has consumed over all its items: stage and phase counter
+
+  for (int item = first_item<C::kThreads>(p, ss); item >= 0;) {
+  const int ticket = prefetch_ticket(p);
+  ItemInfo it;
+  if (locate_item(p, ss, item, it)) {
+  const int b = it.b, kvh = it.kvh, part = it.part, nparts = it.nparts, T = it.T;
+  const size_t qo_base = (size_t(b) * p.num_q_heads + size_t(kvh) * G) * D;
+  if (it.bad_len) {
+    write_bad_len<G, D, C::kThreads>(p, it, qo_base);
+  } else {
+  const int nblk = (T + kBlockSize - 1) / kBlockSize;
+  const int blk0 = part * P;
+  const int nb_item = min(nblk, blk0 + P) - blk0;
+  const int32_t* trow = p.block_tables + size_t(b) * p.max_blocks_per_seq + blk0;
+  for (int i = threadIdx.x; i < nb_item; i += C::kThreads) tbl[i] = __ldg(trow + i);
+  __syncthreads();
+
+  const int nw = warp < nb_item ? (nb_item - 1 - warp) / NW + 1 : 0;
+  const uint64_t policy = l2_evict_first_policy();
+
+  auto issue = [&](int k) {  // lane 0 only: fetch the warp's k-th block of the item
+    const int s = (kb + k) % S;
+    unsigned char* st = ring + size_t(s) * C::kStageBytes;
+    const int phys = tbl[warp + k * NW];
+    if (phys < 0 || phys >= p.num_blocks) {
+      set_error(p.err, kErrBlockId);
+      mbar_arrive(bars + s);
+      return;
+    }
+    const int tile = phys * p.kv_heads + kvh;  // pools with tensor maps have < 2^27 tiles
+    const int row = tile * kBlockSize;
+    mbar_arrive_expect_tx(bars + s, C::kStageBytes + C::kScaleStage);
+#pragma unroll
+    for (int x = 0; x < C::kBoxes; ++x) {
+      tma_load_2d(st + x * C::kBoxBytes, &tmap_k, x * C::kBoxCols, row, bars + s, policy);
+      tma_load_2d(st + C::kTileBytes + x * C::kBoxBytes, &tmap_v, x * C::kBoxCols, row, bars + s,
+                  policy);
+    }
+    if constexpr (C::kQuant) {
+      float* sc = scl + s * (C::kScaleStage / 4);
+      bulk_copy_g2s(sc, p.k_scale + int64_t(tile) * kBlockSize, kBlockSize * 4, bars + s, policy);
+      bulk_copy_g2s(sc + kBlockSize, p.v_scale + int64_t(tile) * kBlockSize, kBlockSize * 4,
+                    bars + s, policy);
+    }
+  };
+  if (lane == 0) {
+    for (int k = 0; k < S && k < nw; ++k) issue(k);
+  }
+
+  // ---- q as the B operand of S = K q^T: lane (gi, gj) holds head gi, k pairs 2gj, 2gj+8.
+  uint32_t qf[C::kKSteps][2];
+  float logit_factor = p.scale_log2;
+  {
+    const auto* qb = static_cast<const __nv_bfloat16*>(p.q) + qo_base;
+    if constexpr (!C::kQuant) {
+#pragma unroll
+      for (int s = 0; s < C::kKSteps; ++s) {
+        qf[s][0] = gi < G ? __ldg(reinterpret_cast<const uint32_t*>(qb + gi * D + 16 * s + 2 * gj)) : 0u;
+        qf[s][1] = gi < G ? __ldg(reinterpret_cast<const uint32_t*>(qb + gi * D + 16 * s + 2 * gj + 8)) : 0u;
+      }
+    } else {
+      // fp16 operands: bring q into fp16 range with a power of two (exact for bf16 values);
+      // its inverse goes into the logit factor.
+      float amax = 0.0f;
+      for (int i = lane; i < G * D; i += 32) amax = fmaxf(amax, fabsf(__bfloat162float(qb[i])));
+#pragma unroll
+      for (int o = 16; o >= 1; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(kFull, amax, o));
+      int e = 0;
+      if (amax > 0.0f) e = min(100, max(-100, int((__float_as_uint(amax) >> 23) & 0xff) - 127 - 14));
+      const float qs = __uint_as_float(uint32_t(127 - e) << 23);
+      logit_factor = p.scale_log2 * __uint_as_float(uint32_t(127 + e) << 23);
+#pragma unroll
+      for (int s = 0; s < C::kKSteps; ++s) {
+        if (gi < G) {
+          const __nv_bfloat16* r = qb + gi * D + 32 * gj + 4 * s;  // permuted dims, see K below
+          qf[s][0] = pack_f16x2(__bfloat162float(r[0]) * qs, __bfloat162float(r[1]) * qs);
+          qf[s][1] = pack_f16x2(__bfloat162float(r[2]) * qs, __bfloat162float(r[3]) * qs);
+        } else {
+          qf[s][0] = qf[s][1] = 0u;
+        }
+      }
+    }
+  }
+
+  // ldmatrix row assignment: lane gives the row address of matrix lane / 8.
+  const int mi = lane >> 3;
+  const int tok_k = (lane & 7) + (mi & 1) * 8;   // K (A of S): matrices (rows 0-7|8-15) x (k lo|hi)
+  const int ck = mi >> 1;
+  const int tok_v = (lane & 7) + (mi >> 1) * 8;  // V^T (A of O^T, transposed load)
+  const int cv = mi & 1;
+
+  float o[C::kMTiles][4];
+#pragma unroll
+  for (int t = 0; t < C::kMTiles; ++t) o[t][0] = o[t][1] = o[t][2] = o[t][3] = 0.0f;
+  float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.0f, l1 = 0.0f;
+  int e_run = INT_MIN;  // INT8: O^T is kept in units of 2^e_run
+
+  int failed_at = -1;
+  for (int k = 0; k < nw; ++k) {
+    const int s = (kb + k) % S;
+    const bool ok = __all_sync(kFull, mbar_wait_bounded(bars + s, ((kb + k) / S) & 1));
+    if (!ok) {
+      failed_at = k;
+      if (lane == 0) set_error(p.err, kErrTimeout);
+      break;
+    }
+    const int ib = warp + k * NW;
+    const int phys = tbl[ib];
+    const bool valid = phys >= 0 && phys < p.num_blocks;
+    const int vt = valid ? min(kBlockSize, T - (blk0 + ib) * kBlockSize) : 0;
+    if (vt > 0) {
+      const unsigned char* st = ring + size_t(s) * C::kStageBytes;
+      const uint32_t ktile = smem_addr(st);
+      const uint32_t vtile = ktile + C::kTileBytes;
+
+      // ---- S = K q^T (fp32): sacc = {S[gi][2gj], S[gi][2gj+1], S[gi+8][2gj], S[gi+8][2gj+1]}
+      float sacc[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+      if constexpr (!C::kQuant) {
+#pragma unroll
+        for (int s2 = 0; s2 < C::kKSteps; ++s2) {
+          uint32_t a[4];
+          ldmatrix_x4(a, swz(ktile, tok_k, 2 * s2 + ck));
+          mma_bf16_16816(sacc, a, qf[s2][0], qf[s2][1]);
+        }
+      } else {
+        // Lane (gi, gj) reads dims 32gj..32gj+31 of tokens gi and gi+8; k-step s2 pairs
+        // dims 32gj+4s2+{0,1} with k slots 2gj, 2gj+1 and +{2,3} with 2gj+8, 2gj+9.
+        const uint4 x0 = *reinterpret_cast<const uint4*>(st + gi * 128 + (((2 * gj) ^ gi) << 4));
+        const uint4 x1 = *reinterpret_cast<const uint4*>(st + gi * 128 + (((2 * gj + 1) ^ gi) << 4));
+        const uint4 y0 = *reinterpret_cast<const uint4*>(st + (gi + 8) * 128 + (((2 * gj) ^ gi) << 4));
+        const uint4 y1 = *reinterpret_cast<const uint4*>(st + (gi + 8) * 128 + (((2 * gj + 1) ^ gi) << 4));
+        const uint32_t wa[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
+        const uint32_t wb[8] = {y0.x, y0.y, y0.z, y0.w, y1.x, y1.y, y1.z, y1.w};
+#pragma unroll
+        for (int s2 = 0; s2 < 8; ++s2) {
+          const uint32_t ua = wa[s2] ^ 0x80808080u, ub = wb[s2] ^ 0x80808080u;
+          const uint32_t a[4] = {f16x2_from_flipped(ua, 0x4140u), f16x2_from_flipped(ub, 0x4140u),
+                                 f16x2_from_flipped(ua, 0x4342u), f16x2_from_flipped(ub, 0x4342u)};
+          mma_f16_16816(sacc, a, qf[s2][0], qf[s2][1]);
+        }
+      }
+
+      // ---- logits in log2 units, masked past the context
+      float f0 = logit_factor, f1 = logit_factor;
+      if constexpr (C::kQuant) {
+        const float* ks = scl + s * (C::kScaleStage / 4);
+        f0 *= ks[gi];
+        f1 *= ks[gi + 8];
+      }
+      const bool v0 = gi < vt, v1 = gi + 8 < vt;
+      const float sc0 = v0 ? sacc[0] * f0 : -INFINITY;
+      const float sc1 = v0 ? sacc[1] * f0 : -INFINITY;
+      const float sc2 = v1 ? sacc[2] * f1 : -INFINITY;
+      const float sc3 = v1 ? sacc[3] * f1 : -INFINITY;
+
+      // ---- online softmax for heads 2gj and 2gj+1
+      float bm0 = fmaxf(sc0, sc2), bm1 = fmaxf(sc1, sc3);
+#pragma unroll
+      for (int ofs = 4; ofs < 32; ofs <<= 1) {
+        bm0 = fmaxf(bm0, __shfl_xor_sync(kFull, bm0, ofs));
+        bm1 = fmaxf(bm1, __shfl_xor_sync(kFull, bm1, ofs));
+      }
+      const float mn0 = fmaxf(m0, bm0), mn1 = fmaxf(m1, bm1);
+      float r0 = exp2f(m0 - mn0), r1 = exp2f(m1 - mn1);
+      m0 = mn0;
+      m1 = mn1;
+      const float p0 = exp2f(sc0 - mn0), p1 = exp2f(sc1 - mn1);
+      const float p2 = exp2f(sc2 - mn0), p3 = exp2f(sc3 - mn1);
+      l0 = fmaf(l0, r0, p0 + p2);
+      l1 = fmaf(l1, r1, p1 + p3);
+
+      uint32_t x01, x23;
+      if constexpr (!C::kQuant) {
+        x01 = pack_bf16x2(p0, p1);
+        x23 = pack_bf16x2(p2, p3);
+      } else {
+        const float* vs = scl + s * (C::kScaleStage / 4) + kBlockSize;
+        const float sv0 = v0 ? vs[gi] : 0.0f, sv1 = v1 ? vs[gi + 8] : 0.0f;
+        float svm = fmaxf(sv0, sv1);
+#pragma unroll
+        for (int ofs = 4; ofs < 32; ofs <<= 1) svm = fmaxf(svm, __shfl_xor_sync(kFull, svm, ofs));
+        const int eb = int((__float_as_uint(svm) >> 23) & 0xff) - 127;
+        const int e_new = e_run == INT_MIN ? eb : max(e_run, eb);
+        if (e_run != INT_MIN && e_new != e_run) {
+          const float f = ldexpf(1.0f, e_run - e_new);
+          r0 *= f;
+          r1 *= f;
+        }
+        e_run = e_new;
+        const float pe = ldexpf(1.0f, -e_new);
+        x01 = pack_f16x2(p0 * sv0 * pe, p1 * sv0 * pe);
+        x23 = pack_f16x2(p2 * sv1 * pe, p3 * sv1 * pe);
+      }
+      if (__any_sync(kFull, r0 != 1.0f || r1 != 1.0f)) {
+#pragma unroll
+        for (int t = 0; t < C::kMTiles; ++t) {
+          o[t][0] *= r0; o[t][1] *= r1; o[t][2] *= r0; o[t][3] *= r1;
+        }
+      }
+      // P as the B operand of O^T += V^T P: lane (gi, gj) needs P[tokens 2gj, 2gj+1][head gi].
+      const uint32_t pb0 = movmatrix_trans(x01);
+      const uint32_t pb1 = movmatrix_trans(x23);
+
+      // ---- O^T += V^T P
+      if constexpr (!C::kQuant) {
+        // Slots past the context in the last block may hold anything, NaN included, and
+        // 0 * NaN would poison the sum: zero those tokens' V.  Lane (gi, gj) holds tokens
+        // 2gj, 2gj+1 in A registers 0-1 and 2gj+8, 2gj+9 in registers 2-3 (low half first).
+        const bool tail = vt < kBlockSize;
+        const uint32_t mlo = (2 * gj < vt ? 0x0000ffffu : 0u) | (2 * gj + 1 < vt ? 0xffff0000u : 0u);
+        const uint32_t mhi = (2 * gj + 8 < vt ? 0x0000ffffu : 0u) | (2 * gj + 9 < vt ? 0xffff0000u : 0u);
+#pragma unroll
+        for (int t = 0; t < C::kMTiles; ++t) {
+          uint32_t a[4];
+          ldmatrix_x4_trans(a, swz(vtile, tok_v, 2 * t + cv));
+          if (tail) {
+            a[0] &= mlo; a[1] &= mlo; a[2] &= mhi; a[3] &= mhi;
+          }
+          mma_bf16_16816(o[t], a, pb0, pb1);
+        }
+      } else {
+        // INT8 codes are always finite, and masked tokens have a zero weight in P.
+        // Lane (gi, gj) reads dims 16gi..16gi+15 of tokens 2gj, 2gj+1, 2gj+8, 2gj+9; m-tile t
+        // row gi is dim 16gi+2t and row gi+8 is dim 16gi+2t+1.
+        const unsigned char* vt8 = st + C::kTileBytes;
+        const uint4 va = *reinterpret_cast<const uint4*>(vt8 + (2 * gj) * 128 + ((gi ^ (2 * gj)) << 4));
+        const uint4 vb = *reinterpret_cast<const uint4*>(vt8 + (2 * gj + 1) * 128 + ((gi ^ (2 * gj + 1)) << 4));
+        const uint4 vc = *reinterpret_cast<const uint4*>(vt8 + (2 * gj + 8) * 128 + ((gi ^ (2 * gj)) << 4));
+        const uint4 vd = *reinterpret_cast<const uint4*>(vt8 + (2 * gj + 9) * 128 + ((gi ^ (2 * gj + 1)) << 4));
+        const uint32_t wa[4] = {va.x ^ 0x80808080u, va.y ^ 0x80808080u, va.z ^ 0x80808080u, va.w ^ 0x80808080u};
+        const uint32_t wb[4] = {vb.x ^ 0x80808080u, vb.y ^ 0x80808080u, vb.z ^ 0x80808080u, vb.w ^ 0x80808080u};
+        const uint32_t wc[4] = {vc.x ^ 0x80808080u, vc.y ^ 0x80808080u, vc.z ^ 0x80808080u, vc.w ^ 0x80808080u};
+        const uint32_t wd[4] = {vd.x ^ 0x80808080u, vd.y ^ 0x80808080u, vd.z ^ 0x80808080u, vd.w ^ 0x80808080u};
+#pragma unroll
+        for (int t = 0; t < C::kMTiles; ++t) {
+          const uint32_t sel = (t & 1) ? 0x7362u : 0x5140u;  // interleave the two tokens' bytes
+          const uint32_t ab = __byte_perm(wa[t >> 1], wb[t >> 1], sel);
+          const uint32_t cd = __byte_perm(wc[t >> 1], wd[t >> 1], sel);
+          const uint32_t a[4] = {f16x2_from_flipped(ab, 0x4140u), f16x2_from_flipped(ab, 0x4342u),
+                                 f16x2_from_flipped(cd, 0x4140u), f16x2_from_flipped(cd, 0x4342u)};
+          mma_f16_16816(o[t], a, pb0, pb1);
+        }
+      }
+    }
+    __syncwarp();
+    if (lane == 0 && k + S < nw) {
+      fence_proxy_async_smem();
+      issue(k + S);
+    }
+  }
+  if (failed_at >= 0) {
+    // Let the copies in flight land (bounded) before the ring holds the merge record; the
+    // CTA then takes no further items.
+    for (int k = failed_at; k < nw && k < failed_at + S; ++k)
+      (void)mbar_wait_bounded(bars + ((kb + k) % S), ((kb + k) / S) & 1);
+    if (lane == 0 && p.persistent) ss.slot[1] = 1;
+    __syncwarp();
+  }
+  kb += failed_at >= 0 ? min(nw, failed_at + S) : nw;
+
+  // ---- this warp's state -> merge record [G][D + 2] in its ring
+#pragma unroll
+  for (int ofs = 4; ofs < 32; ofs <<= 1) {
+    l0 += __shfl_xor_sync(kFull, l0, ofs);
+    l1 += __shfl_xor_sync(kFull, l1, ofs);
+  }
+  float oscale = 1.0f;
+  if constexpr (C::kQuant) oscale = e_run == INT_MIN ? 0.0f : ldexpf(1.0f, e_run);
+  float* rec = reinterpret_cast<float*>(ring);
+  const int h0 = 2 * gj, h1 = 2 * gj + 1;
+  if (gi == 0) {
+    if (h0 < G) { rec[h0 * (D + 2)] = m0; rec[h0 * (D + 2) + 1] = l0; }
+    if (h1 < G) { rec[h1 * (D + 2)] = m1; rec[h1 * (D + 2) + 1] = l1; }
+  }
+#pragma unroll
+  for (int t = 0; t < C::kMTiles; ++t) {
+    const int d0 = C::kQuant ? 16 * gi + 2 * t : 16 * t + gi;
+    const int d1 = C::kQuant ? d0 + 1 : d0 + 8;
+    if (h0 < G) {
+      rec[h0 * (D + 2) + 2 + d0] = o[t][0] * oscale;
+      rec[h0 * (D + 2) + 2 + d1] = o[t][2] * oscale;
+    }
+    if (h1 < G) {
+      rec[h1 * (D + 2) + 2 + d0] = o[t][1] * oscale;
+      rec[h1 * (D + 2) + 2 + d1] = o[t][3] * oscale;
+    }
+  }
+  __syncthreads();
+  merge_warp_records<G, D, NW>(smem, size_t(S) * C::kStageBytes, p, b, kvh, part, nparts, qo_base);
+  }  // valid context length
+  }  // item located
+  item = next_item(p, ss, ticket);
+  }  // items
+  finish_items(p);
+}
+
+template <KvType KV, int D, int G, int NW, int S>
+cudaError_t launch_mma_variant(const DecodeParams& p, const CUtensorMap& tk, const CUtensorMap& tv,
+                               cudaStream_t stream) {
+  using C = MmaCfg<KV, D, G, NW, S>;
+  auto kern = paged_decode_mma_kernel<KV, D, G, NW, S>;
+  static bool attr_done[64] = {};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev < 0 || dev >= 64 || !attr_done[dev]) {
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(C::smem_bytes(kMaxPartitionBlocks, kMaxSchedSeqs)));
+    if (e != cudaSuccess) return e;
+    if (dev >= 0 && dev < 64) attr_done[dev] = true;
+  }
+  const int64_t grid =
+      p.persistent ? int64_t(p.grid) : int64_t(p.max_parts) * p.num_seqs * p.kv_heads;
+  if (grid <= 0) return cudaSuccess;
+  if (grid > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
+  kern<<<static_cast<unsigned>(grid), C::kThreads, C::smem_bytes(p.partition_blocks, p.persistent ? p.num_seqs : 0), stream>>>(tk, tv, p);
+  return cudaGetLastError();
+}
+
+template <KvType KV, int D, int G, int NW, int S>
+int mma_ctas_per_sm_variant() {
+  using C = MmaCfg<KV, D, G, NW, S>;
+  auto kern = paged_decode_mma_kernel<KV, D, G, NW, S>;
+  cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                       static_cast<int>(C::smem_bytes(kMaxPartitionBlocks, kMaxSchedSeqs)));
+  int n = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kern, C::kThreads, C::smem_bytes(64, 256)) !=
+      cudaSuccess)
+    return 0;
+  return n;
+}
+
+}  // namespace pkv

@@ -1,6 +1,7 @@
 // pkv_internal.h -- structures shared by the C-ABI layer and the kernel launchers.
 #pragma once
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <stddef.h>
 #include <stdint.h>
@@ -9,6 +10,7 @@ namespace pkv {
 
 constexpr int kBlockSize = 16;                      // tokens per physical block
 constexpr uint64_t kWaitTimeoutNs = 2000000000ull;  // bounded waits give up after 2 s
+constexpr int kMaxSchedSeqs = 4096;  // largest batch scheduled by the persistent grid
 
 // Device error word bits (mirror PKV_DEVERR_* of the public header).
 constexpr uint32_t kErrBlockId = 0x1u;
@@ -45,6 +47,9 @@ struct DecodeParams {
   float* ws_acc;                // [B, Hq, max_parts, D]   (split only)
   float* ws_ml;                 // [B, Hq, max_parts, 2]   (split only): running max (log2 units), sum
   uint32_t* err;
+  unsigned* sched;              // [2] work ticket and finished-CTA counters (zero between calls)
+  int persistent;               // 1: persistent grid taking items from the ticket counter
+  int grid;                     // CTAs to launch in persistent mode
   int64_t num_blocks;
   int max_blocks_per_seq;
   int num_seqs;
@@ -64,7 +69,16 @@ cudaError_t launch_decode_bf16(const DecodeParams& p, int group, cudaStream_t st
 cudaError_t launch_decode_int8(const DecodeParams& p, int group, cudaStream_t stream);
 cudaError_t launch_lse_reduce(const DecodeParams& p, cudaStream_t stream);
 
-// Resident CTAs per SM of the decode kernel variant (0 if the variant is not built).
+// Tensor-core decode (GQA groups 2/4/8): tk/tv are 2-D tensor maps of the K and V pools
+// (rows of head_dim elements, 128-byte boxes of 16 rows, 128-byte swizzle).
+bool mma_supported(KvType kv, int head_dim, int group);
+int mma_default_stages(KvType kv, int head_dim);
+bool mma_stages_built(KvType kv, int head_dim, int stages);
+cudaError_t launch_decode_mma(const DecodeParams& p, const CUtensorMap* tk, const CUtensorMap* tv,
+                              KvType kv, int group, int stages, cudaStream_t stream);
+int mma_ctas_per_sm(KvType kv, int head_dim, int group, int stages);
+
+// Resident CTAs per SM of the CUDA-core decode kernel variant (0 if not built).
 int decode_ctas_per_sm(KvType kv, int head_dim, int group);
 // Bytes of K+V (+scales) one 16-token block brings in for one kv head.
 int decode_block_bytes(KvType kv, int head_dim);

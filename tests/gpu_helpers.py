@@ -48,9 +48,10 @@ def gpu_pool_from(w: W.Workload, kv: str, device="cuda", garbage=True, split_las
 
 
 def gpu_decode(pool: pkv.PagedKVPool, w: W.Workload, partition_blocks=0, device="cuda",
-               max_context_len=None) -> torch.Tensor:
+               max_context_len=None, kernel=0) -> torch.Tensor:
     out = pool.decode(w.q.to(device), w.block_tables.to(device), w.context_lens.to(device), w.scale,
-                      max_context_len or w.max_context_len, partition_blocks=partition_blocks)
+                      max_context_len or w.max_context_len, partition_blocks=partition_blocks,
+                      kernel=kernel)
     torch.cuda.synchronize()
     return out
 
@@ -122,13 +123,19 @@ def gpu_pool_blocks(pool: pkv.PagedKVPool, tables: np.ndarray, lens: np.ndarray)
     return res
 
 
-def compare(out_gpu: torch.Tensor, ref: np.ndarray, what=""):
+def compare(out_gpu: torch.Tensor, ref: np.ndarray, what="", output_rounding=False):
+    """Element-wise comparison with the fp64 oracle.
+
+    ``output_rounding`` widens the mean-abs bound by the bf16 rounding of the output
+    itself (bf16 keeps 8 significant bits, so rounding moves x by at most 2^-8 |x|); it is
+    used where the outputs are single O(1) values rather than averages over many tokens."""
     got = out_gpu.float().cpu().numpy().astype(np.float64)
     assert got.shape == ref.shape, (got.shape, ref.shape)
     assert np.all(np.isfinite(got)), f"{what}: non-finite output"
     err = np.abs(got - ref)
+    mean_bound = MEAN_ABS + (2.0 ** -8 * np.abs(ref).mean() if output_rounding else 0.0)
     assert err.max() <= MAX_ABS, f"{what}: max abs err {err.max():.3e}"
-    assert err.mean() <= MEAN_ABS, f"{what}: mean abs err {err.mean():.3e}"
+    assert err.mean() <= mean_bound, f"{what}: mean abs err {err.mean():.3e} > {mean_bound:.3e}"
     return float(err.max()), float(err.mean())
 
 

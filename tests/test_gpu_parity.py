@@ -35,14 +35,33 @@ def custom(lens, hq, hkv, d, kv="bf16", seed=7, **kw):
                    kv_dtype=kv, seed=seed, **kw)
 
 
-def check_all(w, kv, partition_blocks=0, seqs=None):
+KERNELS = ["cuda_core", "tensor_core"]
+
+
+def supported(w, kv, kernel):
+    """Whether the kernel family is built for this shape (the plan call says so)."""
+    pool = pkv.PagedKVPool(1, w.num_kv_heads, w.head_dim, kv, fill=0)
+    try:
+        pkv.decode_plan(pool, w.num_seqs, w.num_q_heads, 16, kernel=kernel)
+        return True
+    except pkv.PagedKVError as e:
+        assert "unsupported" in str(e)
+        return False
+    finally:
+        pool.close()
+
+
+def check_all(w, kv, partition_blocks=0, seqs=None, kernel=0, output_rounding=False):
+    if kernel and not supported(w, kv, kernel):
+        pytest.skip(f"{kernel} kernel not built for this shape")
     pool = gpu_pool_from(w, kv)
-    out = gpu_decode(pool, w, partition_blocks)
+    out = gpu_decode(pool, w, partition_blocks, kernel=kernel)
     assert pool.device_error() == 0
     ref, ref_pool, c = oracle_decode(w, kv, seqs)
     sel = list(range(w.num_seqs)) if seqs is None else list(seqs)
     valid_slot_bytes_equal(gpu_pool_blocks(pool, c["orig_tables"], c["lens"]), ref_pool, c["lens"])
-    res = compare(out[torch.tensor(sel, device=out.device)], ref, f"{w.name}/{kv}/P={partition_blocks}")
+    res = compare(out[torch.tensor(sel, device=out.device)], ref, f"{w.name}/{kv}/P={partition_blocks}/{kernel}",
+                  output_rounding=output_rounding)
     pool.close()
     return out, res
 
@@ -74,12 +93,45 @@ def test_shapes_auto_plan(shape, kv):
     check_all(custom(lens, hq, hkv, d, kv), kv)
 
 
+@pytest.mark.parametrize("kernel", KERNELS)
+@pytest.mark.parametrize("kv", ["bf16", "int8"])
+@pytest.mark.parametrize("shape", SHAPES, ids=lambda s: f"B{len(s[0])}_Hq{s[1]}_Hkv{s[2]}_d{s[3]}")
+def test_shapes_each_kernel(shape, kv, kernel):
+    lens, hq, hkv, d = shape
+    check_all(custom(lens, hq, hkv, d, kv), kv, kernel=kernel)
+
+
+@pytest.mark.parametrize("kernel", KERNELS)
 @pytest.mark.parametrize("kv", ["bf16", "int8"])
 @pytest.mark.parametrize("partition_blocks", [1, 2, 3, 5, 8, 64])
-def test_partition_sweep(partition_blocks, kv):
+def test_partition_sweep(partition_blocks, kv, kernel):
     """Split-K: any partition size gives the oracle's result (log-sum-exp merge)."""
     w = custom([1, 16, 17, 95, 300, 613], 16, 4, 128, kv, seed=9)
-    check_all(w, kv, partition_blocks)
+    check_all(w, kv, partition_blocks, kernel=kernel)
+
+
+@pytest.mark.parametrize("kernel", KERNELS)
+@pytest.mark.parametrize("qscale", [3e4, 1e-5])
+def test_int8_extreme_query_magnitudes(qscale, kernel):
+    """Very large and very small queries: the tensor-core path brings q into fp16 range
+    with a power of two, which must not change the result.  Large queries make the
+    softmax one-hot, so each output is a single O(1) value of V and its own bf16 rounding
+    is counted in the mean bound."""
+    w = custom([40, 333], 16, 4, 128, "int8", seed=12)
+    w.q = (w.q.float() * qscale).to(torch.bfloat16)
+    check_all(w, "int8", kernel=kernel, output_rounding=qscale > 1)
+
+
+@pytest.mark.parametrize("kernel", KERNELS)
+def test_int8_value_scales_spanning_binades(kernel):
+    """V rows whose scales differ by up to 2^14 across and within blocks (the tensor-core
+    path keeps P in fp16 with a growing block exponent).  Values stay below 4x N(0,1) so
+    that the absolute tolerance still applies to the bf16 output."""
+    w = custom([500, 70], 16, 4, 128, "int8", seed=13)
+    g = torch.Generator().manual_seed(3)
+    mult = torch.pow(2.0, torch.randint(-12, 3, (w.value.shape[0], 1, 1), generator=g).float())
+    w.value = (w.value.float() * mult).to(torch.bfloat16)
+    check_all(w, "int8", kernel=kernel)
 
 
 def test_partitions_agree_with_each_other():
@@ -91,7 +143,8 @@ def test_partitions_agree_with_each_other():
     pool.close()
 
 
-def test_permutation_gives_identical_bits():
+@pytest.mark.parametrize("kernel", KERNELS)
+def test_permutation_gives_identical_bits(kernel):
     """Two different shuffles of the same tokens into the pool give bit-identical output:
     the kernel's reduction order depends only on logical token positions."""
     outs = []
@@ -108,7 +161,7 @@ def test_permutation_gives_identical_bits():
         w.block_tables = tab
         w.slot_mapping = (tab[seq, pos // 16].long() * 16 + pos % 16).to(torch.int32)
         pool = gpu_pool_from(w, "bf16")
-        outs.append(gpu_decode(pool, w).cpu())
+        outs.append(gpu_decode(pool, w, kernel=kernel).cpu())
         pool.close()
     assert torch.equal(outs[0].view(torch.int16), outs[1].view(torch.int16))
 
@@ -193,6 +246,13 @@ def test_named_workload_full_size(name):
     check_all(w, kv, 0, seqs)
 
 
+@pytest.mark.parametrize("name", ["llama3_8b_gqa", "int8_cb"])
+def test_named_workload_cuda_core_kernel(name):
+    """The GQA workloads through the CUDA-core kernel too (auto picks the tensor cores)."""
+    w = W.make(name, device="cuda")
+    check_all(w, W.SPECS[name].kv_dtype, 0, _sample(w, 3), kernel="cuda_core")
+
+
 def test_tiny_named_partitions():
     w = W.make("tiny")
     for pb in (1, 2, 3):
@@ -266,7 +326,10 @@ def test_launch_count_and_plan():
     w = custom([300, 40], 8, 2, 128, "bf16", seed=61)
     pool = gpu_pool_from(w, "bf16", garbage=False)
     plan = pkv.decode_plan(pool, w.num_seqs, w.num_q_heads, w.max_context_len, partition_blocks=4)
-    assert plan == {"partition_blocks": 4, "max_partitions": math.ceil(19 / 4), "kernels_per_call": 2}
+    assert plan == {"partition_blocks": 4, "max_partitions": math.ceil(19 / 4), "kernels_per_call": 2,
+                    "kernel": "tensor_core"}
+    assert pkv.decode_plan(pool, w.num_seqs, w.num_q_heads, w.max_context_len,
+                           kernel="cuda_core")["kernel"] == "cuda_core"
     before = pkv.launch_count()
     gpu_decode(pool, w, 4)
     assert pkv.launch_count() - before == 2
@@ -289,3 +352,32 @@ def test_side_stream():
     ref, _, _ = oracle_decode(w, "bf16")
     compare(out, ref, "side stream")
     pool.close()
+
+
+@pytest.mark.parametrize("kernel", KERNELS)
+def test_repeated_calls_identical(kernel):
+    """The persistent grid takes items from counters that the last CTA of each call resets;
+    consecutive calls (and a split and an unsplit plan in between) give identical bits."""
+    w = custom([5, 700, 40, 1500, 16, 333], 16, 4, 128, "bf16", seed=81)
+    pool = gpu_pool_from(w, "bf16")
+    outs = []
+    for pb in (0, 0, 64, 0, 3, 0):
+        out = torch.full_like(w.q.cuda(), float("nan"))
+        pool.decode(w.q.cuda(), w.block_tables.cuda(), w.context_lens.cuda(), w.scale, w.max_context_len,
+                    out=out, partition_blocks=pb, kernel=kernel)
+        torch.cuda.synchronize()
+        if pb == 0:
+            outs.append(out.cpu())
+    for o in outs[1:]:
+        assert torch.equal(o.view(torch.int16), outs[0].view(torch.int16))
+    assert pool.device_error() == 0
+    pool.close()
+
+
+@pytest.mark.parametrize("kernel", KERNELS)
+def test_large_batch_classic_grid(kernel):
+    """More sequences than the persistent scheduler holds (4096): one CTA per item slot."""
+    g = torch.Generator().manual_seed(91)
+    lens = torch.randint(1, 70, (4200,), generator=g)
+    w = custom(lens, 8, 2, 64, "bf16", seed=92)
+    check_all(w, "bf16", kernel=kernel, seqs=list(range(0, 4200, 97)))

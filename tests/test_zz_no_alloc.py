@@ -39,12 +39,19 @@ def _close(a, b):
     assert err.max().item() <= MAX_ABS and err.mean().item() <= MEAN_ABS, (err.max().item(), err.mean().item())
 
 
-@pytest.mark.parametrize("name", ["llama2_7b", "long_32k"])
+def _workload(name):
+    if name == "gqa_split":  # 16 sequences of 4000-4096 tokens, 32/8 heads: split on the tensor cores
+        lens = torch.randint(4000, 4097, (16,), generator=torch.Generator().manual_seed(5))
+        return W.build(name=name, context_lens=lens, num_q_heads=32, num_kv_heads=8, head_dim=128,
+                       seed=17, device="cuda"), "bf16"
+    return W.make(name, device="cuda"), W.SPECS[name].kv_dtype
+
+
+@pytest.mark.parametrize("name", ["long_32k", "gqa_split"])
 def test_static_scratch_matches_workspace_entry_point(name):
     build.build()
     lib = _lib.load()
-    w = W.make(name, device="cuda")
-    kv = W.SPECS[name].kv_dtype
+    w, kv = _workload(name)
     pool = _pool_with(w, kv)
     q, tab, lens = w.q.cuda(), w.block_tables.cuda(), w.context_lens.cuda()
     need = pkv.decode_workspace_bytes(pool, w.num_seqs, w.num_q_heads, w.max_context_len)
