@@ -148,9 +148,10 @@ PKV_API pkv_status pkv_reshape_and_cache(const pkv_pool* pool, const void* key, 
  *     past a sequence's partition count exiting at once; PKV_SCHEDULE_PERSISTENT (2)
  *     launches about one wave of CTAs that take items from a counter in the pool's device
  *     memory (batches of up to 4096 sequences; larger batches use the grid).
- *   stages: shared-memory ring depth per warp of the tensor-core kernel (0 = automatic;
- *     otherwise one of the built depths, PKV_ERR_UNSUPPORTED for others).  Shallower rings
- *     fit more CTAs on an SM.
+ *   stages, blocks_per_stage: shape of each warp's shared-memory ring in the tensor-core
+ *     kernel (0 = automatic; otherwise a built shape, PKV_ERR_UNSUPPORTED for others).
+ *     Shallower rings fit more CTAs on an SM; two blocks per stage run the softmax once
+ *     per 32 tokens.
  */
 #define PKV_KERNEL_AUTO 0
 #define PKV_KERNEL_CUDA_CORE 1
@@ -163,7 +164,8 @@ typedef struct pkv_decode_options {
   int kernel;
   int schedule;
   int stages;
-  int reserved[4];
+  int blocks_per_stage;
+  int reserved[3];
 } pkv_decode_options;
 
 /*

@@ -44,7 +44,7 @@ SCHEDULE_PERSISTENT = 2
 
 class DecodeOptions(ctypes.Structure):
     _fields_ = [("partition_blocks", ctypes.c_int), ("kernel", ctypes.c_int), ("schedule", ctypes.c_int),
-                ("stages", ctypes.c_int), ("reserved", ctypes.c_int * 4)]
+                ("stages", ctypes.c_int), ("blocks_per_stage", ctypes.c_int), ("reserved", ctypes.c_int * 3)]
 
 
 SIGNATURES = {

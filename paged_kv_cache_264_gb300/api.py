@@ -45,14 +45,16 @@ _KERNELS = {0: 0, "auto": 0, 1: 1, "cuda_core": 1, 2: 2, "tensor_core": 2}
 _SCHEDULES = {0: 0, "auto": 0, 1: 1, "grid": 1, 2: 2, "persistent": 2}
 
 
-def _options(partition_blocks: int = 0, kernel=0, schedule=0, stages=0) -> ctypes.POINTER(DecodeOptions) | None:
-    if not partition_blocks and not _KERNELS[kernel] and not _SCHEDULES[schedule] and not stages:
+def _options(partition_blocks: int = 0, kernel=0, schedule=0, stages=0,
+             blocks_per_stage=0) -> ctypes.POINTER(DecodeOptions) | None:
+    if not (partition_blocks or _KERNELS[kernel] or _SCHEDULES[schedule] or stages or blocks_per_stage):
         return None
     o = DecodeOptions()
     o.partition_blocks = int(partition_blocks)
     o.kernel = _KERNELS[kernel]
     o.schedule = _SCHEDULES[schedule]
     o.stages = int(stages)
+    o.blocks_per_stage = int(blocks_per_stage)
     return ctypes.pointer(o)
 
 
@@ -127,10 +129,12 @@ class PagedKVPool:
         reshape_and_cache(self, key, value, slot_mapping, stream)
 
     def decode(self, q, block_tables, context_lens, scale, max_context_len, out=None,
-               workspace=None, partition_blocks=0, kernel=0, schedule=0, stages=0, stream=None):
+               workspace=None, partition_blocks=0, kernel=0, schedule=0, stages=0,
+               blocks_per_stage=0, stream=None):
         return paged_attention_decode(self, q, block_tables, context_lens, scale, max_context_len,
                                       out=out, workspace=workspace, partition_blocks=partition_blocks,
-                                      kernel=kernel, schedule=schedule, stages=stages, stream=stream)
+                                      kernel=kernel, schedule=schedule, stages=stages,
+                                      blocks_per_stage=blocks_per_stage, stream=stream)
 
     def device_error(self, stream=None) -> int:
         return get_device_error(self, stream)
@@ -177,7 +181,7 @@ def paged_attention_decode(pool: PagedKVPool, q: torch.Tensor, block_tables: tor
                            context_lens: torch.Tensor, scale: float, max_context_len: int,
                            out: torch.Tensor | None = None, workspace: torch.Tensor | None = None,
                            partition_blocks: int = 0, kernel=0, schedule=0, stages=0,
-                           stream=None) -> torch.Tensor:
+                           blocks_per_stage=0, stream=None) -> torch.Tensor:
     """Decode attention for q bf16 [B, Hq, d] over the pool; returns out bf16 [B, Hq, d].
 
     ``workspace`` (a uint8 CUDA tensor) is allocated here when not given and needed."""
@@ -200,7 +204,8 @@ def paged_attention_decode(pool: PagedKVPool, q: torch.Tensor, block_tables: tor
     check(_lib.load().pkv_paged_attention_decode_ex(
         _handle(pool), _ptr(q), _ptr(block_tables), block_tables.shape[1], _ptr(context_lens), b, hq,
         int(max_context_len), float(scale), _ptr(out), _ptr(workspace), ws_bytes,
-        _options(partition_blocks, kernel, schedule, stages), _stream(stream)), "paged_attention_decode")
+        _options(partition_blocks, kernel, schedule, stages, blocks_per_stage), _stream(stream)),
+        "paged_attention_decode")
     return out
 
 

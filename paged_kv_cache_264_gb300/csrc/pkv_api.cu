@@ -56,7 +56,7 @@ constexpr int kItemBlocksTensorCore = 64;
 
 struct Plan {
   int kernel;  // PKV_KERNEL_CUDA_CORE or PKV_KERNEL_TENSOR_CORE
-  int stages;  // tensor-core ring depth
+  int shape;   // tensor-core ring shape index
   int persistent;
   int ctas_per_sm;
   int partition_blocks;
@@ -82,15 +82,17 @@ pkv_status make_plan(const pkv_pool* pool, int num_seqs, int num_q_heads, int ma
   if (sched != PKV_SCHEDULE_AUTO && sched != PKV_SCHEDULE_GRID && sched != PKV_SCHEDULE_PERSISTENT)
     return PKV_ERR_INVALID_ARG;
   plan->persistent = 0;  // decided below, once the partition size is known
-  plan->stages = 0;
+  plan->shape = 0;
+  const int want_stages = opt ? opt->stages : 0;
+  const int want_bps = opt ? opt->blocks_per_stage : 0;
   if (plan->kernel == PKV_KERNEL_TENSOR_CORE) {
-    plan->stages = (opt && opt->stages) ? opt->stages : pkv::mma_default_stages(kv, pool->head_dim);
-    if (!pkv::mma_stages_built(kv, pool->head_dim, plan->stages)) return PKV_ERR_UNSUPPORTED;
-  } else if (opt && opt->stages) {
+    plan->shape = pkv::mma_ring_shape(kv, pool->head_dim, want_stages, want_bps);
+    if (plan->shape < 0) return PKV_ERR_UNSUPPORTED;
+  } else if (want_stages || want_bps) {
     return PKV_ERR_UNSUPPORTED;
   }
   const int per_sm = plan->kernel == PKV_KERNEL_TENSOR_CORE
-                         ? pkv::mma_ctas_per_sm(kv, pool->head_dim, group, plan->stages)
+                         ? pkv::mma_ctas_per_sm(kv, pool->head_dim, group, plan->shape)
                          : pkv::decode_ctas_per_sm(kv, pool->head_dim, group);
   plan->ctas_per_sm = per_sm > 0 ? per_sm : 1;
   int P;
@@ -400,7 +402,7 @@ pkv_status pkv_paged_attention_decode_ex(const pkv_pool* pool, const void* q,
   cudaError_t e;
   if (plan.kernel == PKV_KERNEL_TENSOR_CORE)
     e = pkv::launch_decode_mma(p, &pool->tmap_k, &pool->tmap_v,
-                               static_cast<pkv::KvType>(pool->dtype), group, plan.stages, s);
+                               static_cast<pkv::KvType>(pool->dtype), group, plan.shape, s);
   else
     e = pool->dtype == PKV_KV_INT8 ? pkv::launch_decode_int8(p, group, s)
                                    : pkv::launch_decode_bf16(p, group, s);

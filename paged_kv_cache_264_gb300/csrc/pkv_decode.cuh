@@ -494,13 +494,13 @@ __global__ void __launch_bounds__(NW * 32)
 #pragma unroll
       for (int o = C::kLPT; o < 32; o <<= 1) bm = fmaxf(bm, __shfl_xor_sync(kFull, bm, o));
       const float m_new = fmaxf(m_run, bm);
-      const float alpha = exp2f(m_run - m_new);
+      const float alpha = fast_exp2(m_run - m_new);
       m_run = m_new;
       float psum = 0.0f;
 #pragma unroll
       for (int ps = 0; ps < C::kPasses; ++ps) {
         const int t = ps * C::kTPP + tok;
-        const float pr = exp2f(sc[ps] - m_new);
+        const float pr = fast_exp2(sc[ps] - m_new);
         psum += pr;
         if (store_lane) {
           float w = pr;

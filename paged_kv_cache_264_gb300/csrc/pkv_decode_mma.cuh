@@ -32,7 +32,7 @@
 
 namespace pkv {
 
-template <KvType KV, int D, int G, int NW, int S>
+template <KvType KV, int D, int G, int NW, int S, int BPS>
 struct MmaCfg {
   static constexpr int kEsz = KvTraits<KV>::kElemBytes;
   static constexpr bool kQuant = KvTraits<KV>::kQuant;
@@ -41,8 +41,8 @@ struct MmaCfg {
   static constexpr int kBoxes = kRowBytes / 128;       // boxes per tile
   static constexpr int kBoxBytes = kBlockSize * 128;   // 2 KiB, 1 KiB aligned in the ring
   static constexpr int kTileBytes = kBoxes * kBoxBytes;
-  static constexpr int kStageBytes = 2 * kTileBytes;   // K tile, V tile
-  static constexpr int kScaleStage = kQuant ? 2 * kBlockSize * 4 : 0;  // K and V scales
+  static constexpr int kStageBytes = 2 * BPS * kTileBytes;   // BPS K tiles, then BPS V tiles
+  static constexpr int kScaleStage = kQuant ? 2 * BPS * kBlockSize * 4 : 0;  // K then V scales
   static constexpr int kKSteps = D / 16;
   static constexpr int kMTiles = D / 16;
   static constexpr int kThreads = NW * 32;
@@ -58,6 +58,7 @@ struct MmaCfg {
   static_assert(kRowBytes % 128 == 0, "rows must be whole 128-byte swizzle spans");
   static_assert(!kQuant || D == 128, "INT8 tensor-core path is built for head_dim 128");
   static_assert(G == 2 || G == 4 || G == 8, "group of 2, 4 or 8 query heads");
+  static_assert(BPS == 1 || BPS == 2, "one or two blocks per ring stage");
   static_assert(size_t(G) * (D + 2) * 4 <= size_t(S) * kStageBytes, "merge record fits the ring");
 };
 
@@ -67,11 +68,11 @@ __device__ __forceinline__ uint32_t swz(uint32_t tile, int t, int c) {
   return tile + (c >> 3) * 2048 + t * 128 + (((c & 7) ^ (t & 7)) << 4);
 }
 
-template <KvType KV, int D, int G, int NW, int S>
+template <KvType KV, int D, int G, int NW, int S, int BPS>
 __global__ void __launch_bounds__(NW * 32)
     paged_decode_mma_kernel(const __grid_constant__ CUtensorMap tmap_k,
                             const __grid_constant__ CUtensorMap tmap_v, const DecodeParams p) {
-  using C = MmaCfg<KV, D, G, NW, S>;
+  using C = MmaCfg<KV, D, G, NW, S, BPS>;
   constexpr uint32_t kFull = 0xffffffffu;
   extern __shared__ unsigned char smem_raw[];
   unsigned char* smem = reinterpret_cast<unsigned char*>(
@@ -116,32 +117,53 @@ __global__ void __launch_bounds__(NW * 32)
   for (int i = threadIdx.x; i < nb_item; i += C::kThreads) tbl[i] = __ldg(trow + i);
   __syncthreads();
 
-  const int nw = warp < nb_item ? (nb_item - 1 - warp) / NW + 1 : 0;
+  // The item's blocks are taken BPS at a time (one ring stage); warp w takes stages
+  // w, w + NW, ... of the item.
+  const int nst = (nb_item + BPS - 1) / BPS;
+  const int nw = warp < nst ? (nst - 1 - warp) / NW + 1 : 0;
   const uint64_t policy = l2_evict_first_policy();
 
-  auto issue = [&](int k) {  // lane 0 only: fetch the warp's k-th block of the item
+  auto issue = [&](int k) {  // lane 0 only: fetch the warp's k-th stage of the item
     const int s = (kb + k) % S;
     unsigned char* st = ring + size_t(s) * C::kStageBytes;
-    const int phys = tbl[warp + k * NW];
-    if (phys < 0 || phys >= p.num_blocks) {
-      set_error(p.err, kErrBlockId);
-      mbar_arrive(bars + s);
+    float* sc = scl + s * (C::kScaleStage / 4);
+    const int ib0 = (warp + k * NW) * BPS;
+    int tiles[BPS];
+    uint32_t bytes = 0;
+#pragma unroll
+    for (int j = 0; j < BPS; ++j) {
+      tiles[j] = -1;
+      if (ib0 + j >= nb_item) continue;
+      const int phys = tbl[ib0 + j];
+      if (phys < 0 || phys >= p.num_blocks) {
+        set_error(p.err, kErrBlockId);
+        continue;
+      }
+      tiles[j] = phys * p.kv_heads + kvh;  // pools with tensor maps have < 2^27 tiles
+      bytes += 2 * C::kTileBytes + (C::kQuant ? 2 * kBlockSize * 4 : 0);
+    }
+    if (bytes == 0) {
+      mbar_arrive(bars + s);  // complete the phase with no data; the blocks are skipped
       return;
     }
-    const int tile = phys * p.kv_heads + kvh;  // pools with tensor maps have < 2^27 tiles
-    const int row = tile * kBlockSize;
-    mbar_arrive_expect_tx(bars + s, C::kStageBytes + C::kScaleStage);
+    mbar_arrive_expect_tx(bars + s, bytes);
 #pragma unroll
-    for (int x = 0; x < C::kBoxes; ++x) {
-      tma_load_2d(st + x * C::kBoxBytes, &tmap_k, x * C::kBoxCols, row, bars + s, policy);
-      tma_load_2d(st + C::kTileBytes + x * C::kBoxBytes, &tmap_v, x * C::kBoxCols, row, bars + s,
-                  policy);
-    }
-    if constexpr (C::kQuant) {
-      float* sc = scl + s * (C::kScaleStage / 4);
-      bulk_copy_g2s(sc, p.k_scale + int64_t(tile) * kBlockSize, kBlockSize * 4, bars + s, policy);
-      bulk_copy_g2s(sc + kBlockSize, p.v_scale + int64_t(tile) * kBlockSize, kBlockSize * 4,
+    for (int j = 0; j < BPS; ++j) {
+      if (tiles[j] < 0) continue;
+      const int row = tiles[j] * kBlockSize;
+#pragma unroll
+      for (int x = 0; x < C::kBoxes; ++x) {
+        tma_load_2d(st + j * C::kTileBytes + x * C::kBoxBytes, &tmap_k, x * C::kBoxCols, row,
                     bars + s, policy);
+        tma_load_2d(st + (BPS + j) * C::kTileBytes + x * C::kBoxBytes, &tmap_v, x * C::kBoxCols,
+                    row, bars + s, policy);
+      }
+      if constexpr (C::kQuant) {
+        bulk_copy_g2s(sc + j * kBlockSize, p.k_scale + int64_t(tiles[j]) * kBlockSize,
+                      kBlockSize * 4, bars + s, policy);
+        bulk_copy_g2s(sc + (BPS + j) * kBlockSize, p.v_scale + int64_t(tiles[j]) * kBlockSize,
+                      kBlockSize * 4, bars + s, policy);
+      }
     }
   };
   if (lane == 0) {
@@ -205,92 +227,133 @@ __global__ void __launch_bounds__(NW * 32)
       if (lane == 0) set_error(p.err, kErrTimeout);
       break;
     }
-    const int ib = warp + k * NW;
-    const int phys = tbl[ib];
-    const bool valid = phys >= 0 && phys < p.num_blocks;
-    const int vt = valid ? min(kBlockSize, T - (blk0 + ib) * kBlockSize) : 0;
-    if (vt > 0) {
-      const unsigned char* st = ring + size_t(s) * C::kStageBytes;
-      const uint32_t ktile = smem_addr(st);
-      const uint32_t vtile = ktile + C::kTileBytes;
-
-      // ---- S = K q^T (fp32): sacc = {S[gi][2gj], S[gi][2gj+1], S[gi+8][2gj], S[gi+8][2gj+1]}
-      float sacc[4] = {0.0f, 0.0f, 0.0f, 0.0f};
-      if constexpr (!C::kQuant) {
+    const int ib0 = (warp + k * NW) * BPS;
+    const unsigned char* st = ring + size_t(s) * C::kStageBytes;
+    const float* sc_st = scl + s * (C::kScaleStage / 4);
+    int vt[BPS];
+    bool any = false;
 #pragma unroll
-        for (int s2 = 0; s2 < C::kKSteps; ++s2) {
-          uint32_t a[4];
-          ldmatrix_x4(a, swz(ktile, tok_k, 2 * s2 + ck));
-          mma_bf16_16816(sacc, a, qf[s2][0], qf[s2][1]);
-        }
-      } else {
-        // Lane (gi, gj) reads dims 32gj..32gj+31 of tokens gi and gi+8; k-step s2 pairs
-        // dims 32gj+4s2+{0,1} with k slots 2gj, 2gj+1 and +{2,3} with 2gj+8, 2gj+9.
-        const uint4 x0 = *reinterpret_cast<const uint4*>(st + gi * 128 + (((2 * gj) ^ gi) << 4));
-        const uint4 x1 = *reinterpret_cast<const uint4*>(st + gi * 128 + (((2 * gj + 1) ^ gi) << 4));
-        const uint4 y0 = *reinterpret_cast<const uint4*>(st + (gi + 8) * 128 + (((2 * gj) ^ gi) << 4));
-        const uint4 y1 = *reinterpret_cast<const uint4*>(st + (gi + 8) * 128 + (((2 * gj + 1) ^ gi) << 4));
-        const uint32_t wa[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
-        const uint32_t wb[8] = {y0.x, y0.y, y0.z, y0.w, y1.x, y1.y, y1.z, y1.w};
+    for (int j = 0; j < BPS; ++j) {
+      vt[j] = 0;
+      if (ib0 + j < nb_item) {
+        const int phys = tbl[ib0 + j];
+        if (phys >= 0 && phys < p.num_blocks) vt[j] = min(kBlockSize, T - (blk0 + ib0 + j) * kBlockSize);
+      }
+      any |= vt[j] > 0;
+    }
+    if (any) {
+      // ---- S_j = K_j q^T (fp32) per block j:
+      //      sacc[j] = {S[gi][2gj], S[gi][2gj+1], S[gi+8][2gj], S[gi+8][2gj+1]}
+      float sacc[BPS][4];
 #pragma unroll
-        for (int s2 = 0; s2 < 8; ++s2) {
-          const uint32_t ua = wa[s2] ^ 0x80808080u, ub = wb[s2] ^ 0x80808080u;
-          const uint32_t a[4] = {f16x2_from_flipped(ua, 0x4140u), f16x2_from_flipped(ub, 0x4140u),
-                                 f16x2_from_flipped(ua, 0x4342u), f16x2_from_flipped(ub, 0x4342u)};
-          mma_f16_16816(sacc, a, qf[s2][0], qf[s2][1]);
+      for (int j = 0; j < BPS; ++j) {
+        sacc[j][0] = sacc[j][1] = sacc[j][2] = sacc[j][3] = 0.0f;
+        if (vt[j] == 0) continue;
+        const unsigned char* kt = st + j * C::kTileBytes;
+        if constexpr (!C::kQuant) {
+          const uint32_t ktile = smem_addr(kt);
+#pragma unroll
+          for (int s2 = 0; s2 < C::kKSteps; ++s2) {
+            uint32_t a[4];
+            ldmatrix_x4(a, swz(ktile, tok_k, 2 * s2 + ck));
+            mma_bf16_16816(sacc[j], a, qf[s2][0], qf[s2][1]);
+          }
+        } else {
+          // Lane (gi, gj) reads dims 32gj..32gj+31 of tokens gi and gi+8; k-step s2 pairs
+          // dims 32gj+4s2+{0,1} with k slots 2gj, 2gj+1 and +{2,3} with 2gj+8, 2gj+9.
+          const uint4 x0 = *reinterpret_cast<const uint4*>(kt + gi * 128 + (((2 * gj) ^ gi) << 4));
+          const uint4 x1 = *reinterpret_cast<const uint4*>(kt + gi * 128 + (((2 * gj + 1) ^ gi) << 4));
+          const uint4 y0 = *reinterpret_cast<const uint4*>(kt + (gi + 8) * 128 + (((2 * gj) ^ gi) << 4));
+          const uint4 y1 = *reinterpret_cast<const uint4*>(kt + (gi + 8) * 128 + (((2 * gj + 1) ^ gi) << 4));
+          const uint32_t wa[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
+          const uint32_t wb[8] = {y0.x, y0.y, y0.z, y0.w, y1.x, y1.y, y1.z, y1.w};
+#pragma unroll
+          for (int s2 = 0; s2 < 8; ++s2) {
+            const uint32_t ua = wa[s2] ^ 0x80808080u, ub = wb[s2] ^ 0x80808080u;
+            const uint32_t a[4] = {f16x2_from_flipped(ua, 0x4140u), f16x2_from_flipped(ub, 0x4140u),
+                                   f16x2_from_flipped(ua, 0x4342u), f16x2_from_flipped(ub, 0x4342u)};
+            mma_f16_16816(sacc[j], a, qf[s2][0], qf[s2][1]);
+          }
         }
       }
 
-      // ---- logits in log2 units, masked past the context
-      float f0 = logit_factor, f1 = logit_factor;
-      if constexpr (C::kQuant) {
-        const float* ks = scl + s * (C::kScaleStage / 4);
-        f0 *= ks[gi];
-        f1 *= ks[gi + 8];
+      // ---- logits in log2 units, masked past the context (and for absent blocks)
+      float sc[BPS][4];
+      float bm0 = -INFINITY, bm1 = -INFINITY;
+#pragma unroll
+      for (int j = 0; j < BPS; ++j) {
+        float f0 = logit_factor, f1 = logit_factor;
+        if constexpr (C::kQuant) {
+          if (vt[j] > 0) {
+            f0 *= sc_st[j * kBlockSize + gi];
+            f1 *= sc_st[j * kBlockSize + gi + 8];
+          }
+        }
+        const bool v0 = gi < vt[j], v1 = gi + 8 < vt[j];
+        sc[j][0] = v0 ? sacc[j][0] * f0 : -INFINITY;
+        sc[j][1] = v0 ? sacc[j][1] * f0 : -INFINITY;
+        sc[j][2] = v1 ? sacc[j][2] * f1 : -INFINITY;
+        sc[j][3] = v1 ? sacc[j][3] * f1 : -INFINITY;
+        bm0 = fmaxf(bm0, fmaxf(sc[j][0], sc[j][2]));
+        bm1 = fmaxf(bm1, fmaxf(sc[j][1], sc[j][3]));
       }
-      const bool v0 = gi < vt, v1 = gi + 8 < vt;
-      const float sc0 = v0 ? sacc[0] * f0 : -INFINITY;
-      const float sc1 = v0 ? sacc[1] * f0 : -INFINITY;
-      const float sc2 = v1 ? sacc[2] * f1 : -INFINITY;
-      const float sc3 = v1 ? sacc[3] * f1 : -INFINITY;
 
-      // ---- online softmax for heads 2gj and 2gj+1
-      float bm0 = fmaxf(sc0, sc2), bm1 = fmaxf(sc1, sc3);
+      // ---- online softmax for heads 2gj and 2gj+1 over the stage's tokens
 #pragma unroll
       for (int ofs = 4; ofs < 32; ofs <<= 1) {
         bm0 = fmaxf(bm0, __shfl_xor_sync(kFull, bm0, ofs));
         bm1 = fmaxf(bm1, __shfl_xor_sync(kFull, bm1, ofs));
       }
       const float mn0 = fmaxf(m0, bm0), mn1 = fmaxf(m1, bm1);
-      float r0 = exp2f(m0 - mn0), r1 = exp2f(m1 - mn1);
+      float r0 = fast_exp2(m0 - mn0), r1 = fast_exp2(m1 - mn1);
       m0 = mn0;
       m1 = mn1;
-      const float p0 = exp2f(sc0 - mn0), p1 = exp2f(sc1 - mn1);
-      const float p2 = exp2f(sc2 - mn0), p3 = exp2f(sc3 - mn1);
-      l0 = fmaf(l0, r0, p0 + p2);
-      l1 = fmaf(l1, r1, p1 + p3);
+      float pr[BPS][4];
+      float ps0 = 0.0f, ps1 = 0.0f;
+#pragma unroll
+      for (int j = 0; j < BPS; ++j) {
+        pr[j][0] = fast_exp2(sc[j][0] - mn0);
+        pr[j][1] = fast_exp2(sc[j][1] - mn1);
+        pr[j][2] = fast_exp2(sc[j][2] - mn0);
+        pr[j][3] = fast_exp2(sc[j][3] - mn1);
+        ps0 += pr[j][0] + pr[j][2];
+        ps1 += pr[j][1] + pr[j][3];
+      }
+      l0 = fmaf(l0, r0, ps0);
+      l1 = fmaf(l1, r1, ps1);
 
-      uint32_t x01, x23;
+      uint32_t x01[BPS], x23[BPS];
       if constexpr (!C::kQuant) {
-        x01 = pack_bf16x2(p0, p1);
-        x23 = pack_bf16x2(p2, p3);
+#pragma unroll
+        for (int j = 0; j < BPS; ++j) {
+          x01[j] = pack_bf16x2(pr[j][0], pr[j][1]);
+          x23[j] = pack_bf16x2(pr[j][2], pr[j][3]);
+        }
       } else {
-        const float* vs = scl + s * (C::kScaleStage / 4) + kBlockSize;
-        const float sv0 = v0 ? vs[gi] : 0.0f, sv1 = v1 ? vs[gi + 8] : 0.0f;
-        float svm = fmaxf(sv0, sv1);
+        float sv[BPS][2];
+        float svm = 0.0f;
+#pragma unroll
+        for (int j = 0; j < BPS; ++j) {
+          sv[j][0] = gi < vt[j] ? sc_st[(BPS + j) * kBlockSize + gi] : 0.0f;
+          sv[j][1] = gi + 8 < vt[j] ? sc_st[(BPS + j) * kBlockSize + gi + 8] : 0.0f;
+          svm = fmaxf(svm, fmaxf(sv[j][0], sv[j][1]));
+        }
 #pragma unroll
         for (int ofs = 4; ofs < 32; ofs <<= 1) svm = fmaxf(svm, __shfl_xor_sync(kFull, svm, ofs));
-        const int eb = int((__float_as_uint(svm) >> 23) & 0xff) - 127;
-        const int e_new = e_run == INT_MIN ? eb : max(e_run, eb);
+        const int eb = int((__float_as_uint(svm) >> 23) & 0xff) - 127;  // floor(log2 svm)
+        const int e_new = min(126, e_run == INT_MIN ? eb : max(e_run, eb));
         if (e_run != INT_MIN && e_new != e_run) {
-          const float f = ldexpf(1.0f, e_run - e_new);
+          const float f = pow2i(max(-126, e_run - e_new));
           r0 *= f;
           r1 *= f;
         }
         e_run = e_new;
-        const float pe = ldexpf(1.0f, -e_new);
-        x01 = pack_f16x2(p0 * sv0 * pe, p1 * sv0 * pe);
-        x23 = pack_f16x2(p2 * sv1 * pe, p3 * sv1 * pe);
+        const float pe = pow2i(-e_new);  // P' = p * s_V * 2^-E lies in [0, 4)
+#pragma unroll
+        for (int j = 0; j < BPS; ++j) {
+          x01[j] = pack_f16x2(pr[j][0] * sv[j][0] * pe, pr[j][1] * sv[j][0] * pe);
+          x23[j] = pack_f16x2(pr[j][2] * sv[j][1] * pe, pr[j][3] * sv[j][1] * pe);
+        }
       }
       if (__any_sync(kFull, r0 != 1.0f || r1 != 1.0f)) {
 #pragma unroll
@@ -298,48 +361,53 @@ __global__ void __launch_bounds__(NW * 32)
           o[t][0] *= r0; o[t][1] *= r1; o[t][2] *= r0; o[t][3] *= r1;
         }
       }
-      // P as the B operand of O^T += V^T P: lane (gi, gj) needs P[tokens 2gj, 2gj+1][head gi].
-      const uint32_t pb0 = movmatrix_trans(x01);
-      const uint32_t pb1 = movmatrix_trans(x23);
 
-      // ---- O^T += V^T P
-      if constexpr (!C::kQuant) {
-        // Slots past the context in the last block may hold anything, NaN included, and
-        // 0 * NaN would poison the sum: zero those tokens' V.  Lane (gi, gj) holds tokens
-        // 2gj, 2gj+1 in A registers 0-1 and 2gj+8, 2gj+9 in registers 2-3 (low half first).
-        const bool tail = vt < kBlockSize;
-        const uint32_t mlo = (2 * gj < vt ? 0x0000ffffu : 0u) | (2 * gj + 1 < vt ? 0xffff0000u : 0u);
-        const uint32_t mhi = (2 * gj + 8 < vt ? 0x0000ffffu : 0u) | (2 * gj + 9 < vt ? 0xffff0000u : 0u);
+      // ---- O^T += V_j^T P_j.  P_j as the B operand: lane (gi, gj) needs
+      //      P_j[tokens 2gj, 2gj+1 (+8)][head gi], the transpose of what it holds.
 #pragma unroll
-        for (int t = 0; t < C::kMTiles; ++t) {
-          uint32_t a[4];
-          ldmatrix_x4_trans(a, swz(vtile, tok_v, 2 * t + cv));
-          if (tail) {
-            a[0] &= mlo; a[1] &= mlo; a[2] &= mhi; a[3] &= mhi;
+      for (int j = 0; j < BPS; ++j) {
+        if (vt[j] == 0) continue;
+        const uint32_t pb0 = movmatrix_trans(x01[j]);
+        const uint32_t pb1 = movmatrix_trans(x23[j]);
+        const unsigned char* vtp = st + (BPS + j) * C::kTileBytes;
+        if constexpr (!C::kQuant) {
+          // Slots past the context in the last block may hold anything, NaN included, and
+          // 0 * NaN would poison the sum: zero those tokens' V.  Lane (gi, gj) holds tokens
+          // 2gj, 2gj+1 in A registers 0-1 and 2gj+8, 2gj+9 in registers 2-3 (low half first).
+          const bool tail = vt[j] < kBlockSize;
+          const uint32_t mlo = (2 * gj < vt[j] ? 0x0000ffffu : 0u) | (2 * gj + 1 < vt[j] ? 0xffff0000u : 0u);
+          const uint32_t mhi = (2 * gj + 8 < vt[j] ? 0x0000ffffu : 0u) | (2 * gj + 9 < vt[j] ? 0xffff0000u : 0u);
+          const uint32_t vtile = smem_addr(vtp);
+#pragma unroll
+          for (int t = 0; t < C::kMTiles; ++t) {
+            uint32_t a[4];
+            ldmatrix_x4_trans(a, swz(vtile, tok_v, 2 * t + cv));
+            if (tail) {
+              a[0] &= mlo; a[1] &= mlo; a[2] &= mhi; a[3] &= mhi;
+            }
+            mma_bf16_16816(o[t], a, pb0, pb1);
           }
-          mma_bf16_16816(o[t], a, pb0, pb1);
-        }
-      } else {
-        // INT8 codes are always finite, and masked tokens have a zero weight in P.
-        // Lane (gi, gj) reads dims 16gi..16gi+15 of tokens 2gj, 2gj+1, 2gj+8, 2gj+9; m-tile t
-        // row gi is dim 16gi+2t and row gi+8 is dim 16gi+2t+1.
-        const unsigned char* vt8 = st + C::kTileBytes;
-        const uint4 va = *reinterpret_cast<const uint4*>(vt8 + (2 * gj) * 128 + ((gi ^ (2 * gj)) << 4));
-        const uint4 vb = *reinterpret_cast<const uint4*>(vt8 + (2 * gj + 1) * 128 + ((gi ^ (2 * gj + 1)) << 4));
-        const uint4 vc = *reinterpret_cast<const uint4*>(vt8 + (2 * gj + 8) * 128 + ((gi ^ (2 * gj)) << 4));
-        const uint4 vd = *reinterpret_cast<const uint4*>(vt8 + (2 * gj + 9) * 128 + ((gi ^ (2 * gj + 1)) << 4));
-        const uint32_t wa[4] = {va.x ^ 0x80808080u, va.y ^ 0x80808080u, va.z ^ 0x80808080u, va.w ^ 0x80808080u};
-        const uint32_t wb[4] = {vb.x ^ 0x80808080u, vb.y ^ 0x80808080u, vb.z ^ 0x80808080u, vb.w ^ 0x80808080u};
-        const uint32_t wc[4] = {vc.x ^ 0x80808080u, vc.y ^ 0x80808080u, vc.z ^ 0x80808080u, vc.w ^ 0x80808080u};
-        const uint32_t wd[4] = {vd.x ^ 0x80808080u, vd.y ^ 0x80808080u, vd.z ^ 0x80808080u, vd.w ^ 0x80808080u};
+        } else {
+          // INT8 codes are always finite, and masked tokens have a zero weight in P.
+          // Lane (gi, gj) reads dims 16gi..16gi+15 of tokens 2gj, 2gj+1, 2gj+8, 2gj+9; m-tile
+          // t row gi is dim 16gi+2t and row gi+8 is dim 16gi+2t+1.
+          const uint4 va = *reinterpret_cast<const uint4*>(vtp + (2 * gj) * 128 + ((gi ^ (2 * gj)) << 4));
+          const uint4 vb = *reinterpret_cast<const uint4*>(vtp + (2 * gj + 1) * 128 + ((gi ^ (2 * gj + 1)) << 4));
+          const uint4 vc = *reinterpret_cast<const uint4*>(vtp + (2 * gj + 8) * 128 + ((gi ^ (2 * gj)) << 4));
+          const uint4 vd = *reinterpret_cast<const uint4*>(vtp + (2 * gj + 9) * 128 + ((gi ^ (2 * gj + 1)) << 4));
+          const uint32_t wa[4] = {va.x ^ 0x80808080u, va.y ^ 0x80808080u, va.z ^ 0x80808080u, va.w ^ 0x80808080u};
+          const uint32_t wb[4] = {vb.x ^ 0x80808080u, vb.y ^ 0x80808080u, vb.z ^ 0x80808080u, vb.w ^ 0x80808080u};
+          const uint32_t wc[4] = {vc.x ^ 0x80808080u, vc.y ^ 0x80808080u, vc.z ^ 0x80808080u, vc.w ^ 0x80808080u};
+          const uint32_t wd[4] = {vd.x ^ 0x80808080u, vd.y ^ 0x80808080u, vd.z ^ 0x80808080u, vd.w ^ 0x80808080u};
 #pragma unroll
-        for (int t = 0; t < C::kMTiles; ++t) {
-          const uint32_t sel = (t & 1) ? 0x7362u : 0x5140u;  // interleave the two tokens' bytes
-          const uint32_t ab = __byte_perm(wa[t >> 1], wb[t >> 1], sel);
-          const uint32_t cd = __byte_perm(wc[t >> 1], wd[t >> 1], sel);
-          const uint32_t a[4] = {f16x2_from_flipped(ab, 0x4140u), f16x2_from_flipped(ab, 0x4342u),
-                                 f16x2_from_flipped(cd, 0x4140u), f16x2_from_flipped(cd, 0x4342u)};
-          mma_f16_16816(o[t], a, pb0, pb1);
+          for (int t = 0; t < C::kMTiles; ++t) {
+            const uint32_t sel = (t & 1) ? 0x7362u : 0x5140u;  // interleave the two tokens' bytes
+            const uint32_t ab = __byte_perm(wa[t >> 1], wb[t >> 1], sel);
+            const uint32_t cd = __byte_perm(wc[t >> 1], wd[t >> 1], sel);
+            const uint32_t a[4] = {f16x2_from_flipped(ab, 0x4140u), f16x2_from_flipped(ab, 0x4342u),
+                                   f16x2_from_flipped(cd, 0x4140u), f16x2_from_flipped(cd, 0x4342u)};
+            mma_f16_16816(o[t], a, pb0, pb1);
+          }
         }
       }
     }
@@ -366,7 +434,7 @@ __global__ void __launch_bounds__(NW * 32)
     l1 += __shfl_xor_sync(kFull, l1, ofs);
   }
   float oscale = 1.0f;
-  if constexpr (C::kQuant) oscale = e_run == INT_MIN ? 0.0f : ldexpf(1.0f, e_run);
+  if constexpr (C::kQuant) oscale = e_run == INT_MIN ? 0.0f : pow2i(max(-126, e_run));
   float* rec = reinterpret_cast<float*>(ring);
   const int h0 = 2 * gj, h1 = 2 * gj + 1;
   if (gi == 0) {
@@ -395,11 +463,11 @@ __global__ void __launch_bounds__(NW * 32)
   finish_items(p);
 }
 
-template <KvType KV, int D, int G, int NW, int S>
+template <KvType KV, int D, int G, int NW, int S, int BPS>
 cudaError_t launch_mma_variant(const DecodeParams& p, const CUtensorMap& tk, const CUtensorMap& tv,
                                cudaStream_t stream) {
-  using C = MmaCfg<KV, D, G, NW, S>;
-  auto kern = paged_decode_mma_kernel<KV, D, G, NW, S>;
+  using C = MmaCfg<KV, D, G, NW, S, BPS>;
+  auto kern = paged_decode_mma_kernel<KV, D, G, NW, S, BPS>;
   static bool attr_done[64] = {};
   int dev = 0;
   cudaGetDevice(&dev);
@@ -417,10 +485,10 @@ cudaError_t launch_mma_variant(const DecodeParams& p, const CUtensorMap& tk, con
   return cudaGetLastError();
 }
 
-template <KvType KV, int D, int G, int NW, int S>
+template <KvType KV, int D, int G, int NW, int S, int BPS>
 int mma_ctas_per_sm_variant() {
-  using C = MmaCfg<KV, D, G, NW, S>;
-  auto kern = paged_decode_mma_kernel<KV, D, G, NW, S>;
+  using C = MmaCfg<KV, D, G, NW, S, BPS>;
+  auto kern = paged_decode_mma_kernel<KV, D, G, NW, S, BPS>;
   cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                        static_cast<int>(C::smem_bytes(kMaxPartitionBlocks, kMaxSchedSeqs)));
   int n = 0;

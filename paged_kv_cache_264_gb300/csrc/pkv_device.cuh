@@ -45,14 +45,18 @@ __device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
   asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_addr(bar)) : "memory");
 }
 
-__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
+// Test the phase; while it is incomplete the thread may be suspended for up to
+// `suspend_ns` (it wakes as soon as the phase completes), so a waiting warp does not spin
+// on issue slots.
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity,
+                                              uint32_t suspend_ns = 1000000u) {
   uint32_t done;
   asm volatile(
       "{\n\t.reg .pred p;\n\t"
-      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
       "selp.u32 %0, 1, 0, p;\n\t}"
       : "=r"(done)
-      : "r"(smem_addr(bar)), "r"(parity)
+      : "r"(smem_addr(bar)), "r"(parity), "r"(suspend_ns)
       : "memory");
   return done != 0;
 }
@@ -74,6 +78,19 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity
     if ((it & 63u) == 63u && global_timer_ns() - t0 > kWaitTimeoutNs) return false;
   }
   return false;
+}
+
+// 2^x for the softmax (x <= 0 in practice): the hardware base-2 exponential, flushing
+// subnormal results to zero (weights below 2^-126 do not matter next to the largest, 1).
+__device__ __forceinline__ float fast_exp2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+// 2^e as an fp32 for an integer e in [-126, 127], built from its exponent bits.
+__device__ __forceinline__ float pow2i(int e) {
+  return __uint_as_float(static_cast<uint32_t>(e + 127) << 23);
 }
 
 // L2 policy for data read once per call (the K/V tiles): evict first.

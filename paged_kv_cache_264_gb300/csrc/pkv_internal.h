@@ -72,11 +72,12 @@ cudaError_t launch_lse_reduce(const DecodeParams& p, cudaStream_t stream);
 // Tensor-core decode (GQA groups 2/4/8): tk/tv are 2-D tensor maps of the K and V pools
 // (rows of head_dim elements, 128-byte boxes of 16 rows, 128-byte swizzle).
 bool mma_supported(KvType kv, int head_dim, int group);
-int mma_default_stages(KvType kv, int head_dim);
-bool mma_stages_built(KvType kv, int head_dim, int stages);
+// Ring shape (stages x blocks per stage) index for requested values (0 = default); -1 if
+// that shape is not built.
+int mma_ring_shape(KvType kv, int head_dim, int stages, int blocks_per_stage);
 cudaError_t launch_decode_mma(const DecodeParams& p, const CUtensorMap* tk, const CUtensorMap* tv,
-                              KvType kv, int group, int stages, cudaStream_t stream);
-int mma_ctas_per_sm(KvType kv, int head_dim, int group, int stages);
+                              KvType kv, int group, int shape, cudaStream_t stream);
+int mma_ctas_per_sm(KvType kv, int head_dim, int group, int shape);
 
 // Resident CTAs per SM of the CUDA-core decode kernel variant (0 if not built).
 int decode_ctas_per_sm(KvType kv, int head_dim, int group);

@@ -381,3 +381,25 @@ def test_large_batch_classic_grid(kernel):
     lens = torch.randint(1, 70, (4200,), generator=g)
     w = custom(lens, 8, 2, 64, "bf16", seed=92)
     check_all(w, "bf16", kernel=kernel, seqs=list(range(0, 4200, 97)))
+
+
+RING_SHAPES = [("bf16", 128, 2, 1), ("bf16", 128, 3, 1), ("bf16", 64, 3, 1), ("bf16", 64, 2, 2),
+               ("int8", 128, 3, 1), ("int8", 128, 2, 2), ("int8", 128, 3, 2)]
+
+
+@pytest.mark.parametrize("partition_blocks", [0, 3, 5])
+@pytest.mark.parametrize("shape", RING_SHAPES, ids=lambda s: f"{s[0]}_d{s[1]}_S{s[2]}_B{s[3]}")
+def test_tensor_core_ring_shapes(shape, partition_blocks):
+    """Every built ring shape of the tensor-core kernel, with odd block counts per item so
+    that a two-block stage is sometimes half empty."""
+    kv, d, stages, bps = shape
+    w = custom([1, 16, 17, 49, 95, 300, 613], 16, 4, d, kv, seed=101 + d)
+    pool = gpu_pool_from(w, kv)
+    out = pool.decode(w.q.cuda(), w.block_tables.cuda(), w.context_lens.cuda(), w.scale, w.max_context_len,
+                      partition_blocks=partition_blocks, kernel="tensor_core", stages=stages,
+                      blocks_per_stage=bps)
+    torch.cuda.synchronize()
+    assert pool.device_error() == 0
+    ref, _, _ = oracle_decode(w, kv)
+    compare(out, ref, f"ring {shape} P={partition_blocks}")
+    pool.close()
