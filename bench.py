@@ -47,14 +47,20 @@ TRAFFIC_FILE = os.path.join(ROOT, "profiles", "decode_traffic.txt")
 CSRC = os.path.join(ROOT, "paged_kv_cache_264_gb300", "csrc")
 
 
-def kernel_source_hash() -> str:
+KERNEL_SOURCES = {
+    # sources that define each decode kernel family (a capture stays valid while they are unchanged)
+    "cuda_core": ["pkv_device.cuh", "pkv_internal.h", "pkv_decode.cuh", "pkv_decode_bf16.cu",
+                  "pkv_decode_int8.cu"],
+    "tensor_core": ["pkv_device.cuh", "pkv_internal.h", "pkv_decode.cuh", "pkv_decode_mma.cuh",
+                    "pkv_decode_mma.cu"],
+}
+
+
+def kernel_source_hash(kernel: str = "cuda_core") -> str:
     h = hashlib.sha256()
-    for name in sorted(os.listdir(CSRC)):
-        if name.endswith((".cu", ".cuh", ".h")):
-            with open(os.path.join(CSRC, name), "rb") as f:
-                h.update(name.encode() + b"\0" + f.read())
-    with open(os.path.join(ROOT, "include", "pagedkv.h"), "rb") as f:
-        h.update(f.read())
+    for name in KERNEL_SOURCES[kernel]:
+        with open(os.path.join(CSRC, name), "rb") as f:
+            h.update(name.encode() + b"\0" + f.read())
     return h.hexdigest()[:16]
 
 
@@ -67,12 +73,12 @@ def measured_peaks():
     return FALLBACK_HBM_GBS, "fallback"
 
 
-def recorded_traffic(workload: str):
+def recorded_traffic(workload: str, kernel: str):
     """Per-launch DRAM bytes of the decode kernel from a committed ncu capture, if it was
-    taken on the current kernel sources."""
+    taken on the current sources of that kernel."""
     if not os.path.exists(TRAFFIC_FILE):
         return None
-    current = kernel_source_hash()
+    current = kernel_source_hash(kernel)
     with open(TRAFFIC_FILE) as f:
         for line in f:
             if line.startswith("#") or "=" not in line:
@@ -257,8 +263,9 @@ def run_ours(args, rank, world, local):
 
     peak, peak_kind = measured_peaks()
     achieved = sb.decode / (dec_ms * 1e-3) / 1e9
-    traffic = recorded_traffic(args.workload)
-    kernel = "paged_decode_kernel" + (" + lse_reduce_kernel" if plan["kernels_per_call"] == 2 else "")
+    traffic = recorded_traffic(args.workload, plan["kernel"])
+    kernel = ("paged_decode_mma_kernel" if plan["kernel"] == "tensor_core" else "paged_decode_kernel") + (
+        " + lse_reduce_kernel" if plan["kernels_per_call"] == 2 else "")
     line = {
         "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_step, 5),
