@@ -17,8 +17,9 @@
 //    The row (dims) of O^T that a lane holds and the column (head) of its softmax state
 //    coincide, so rescaling needs no data movement, and it is skipped whenever no head's
 //    running max moved in a block.
-//  * INT8: codes become fp16 exactly (see f16x2_from_flipped) and both products run in
-//    fp16.  q is scaled by a power of two into fp16 range (exact for bf16 values), the
+//  * INT8: codes become fp16 values 1152 + code exactly (see f16x2_biased) and both
+//    products run in fp16; the constant 1152 is taken out afterwards: from the logits as
+//    1152 * sum_d q_d per head, and from O^T as 1152 times the running sum of P per head.  q is scaled by a power of two into fp16 range (exact for bf16 values), the
 //    K scale multiplies the fp32 logits, and the V scale is folded into P together with a
 //    power-of-two block exponent that keeps P in [0, 2): O^T is kept in units of 2^E and E
 //    only grows, like the running max, so the rescale stays rare.  Within one k-step the
@@ -173,6 +174,7 @@ __global__ void __launch_bounds__(NW * 32)
   // ---- q as the B operand of S = K q^T: lane (gi, gj) holds head gi, k pairs 2gj, 2gj+8.
   uint32_t qf[C::kKSteps][2];
   float logit_factor = p.scale_log2;
+  float kbias0 = 0.0f, kbias1 = 0.0f;  // INT8: 1152 * sum_d q_d for heads 2gj, 2gj+1
   {
     const auto* qb = static_cast<const __nv_bfloat16*>(p.q) + qo_base;
     if constexpr (!C::kQuant) {
@@ -202,6 +204,19 @@ __global__ void __launch_bounds__(NW * 32)
           qf[s][0] = qf[s][1] = 0u;
         }
       }
+      // K codes enter the product as 1152 + code: S' = S + 1152 * sum_d q_d.  Sum the fp16
+      // values exactly as the MMA sees them, per head, and fold in the logit factor.
+      float qsum = 0.0f;
+#pragma unroll
+      for (int s = 0; s < C::kKSteps; ++s) {
+        const float2 a = __half22float2(*reinterpret_cast<const __half2*>(&qf[s][0]));
+        const float2 c = __half22float2(*reinterpret_cast<const __half2*>(&qf[s][1]));
+        qsum += (a.x + a.y) + (c.x + c.y);
+      }
+      qsum += __shfl_xor_sync(kFull, qsum, 1);
+      qsum += __shfl_xor_sync(kFull, qsum, 2);  // lanes of row gi now hold head gi's sum
+      kbias0 = 1152.0f * __shfl_sync(kFull, qsum, 4 * (2 * gj));
+      kbias1 = 1152.0f * __shfl_sync(kFull, qsum, 4 * (2 * gj + 1));
     }
   }
 
@@ -211,12 +226,18 @@ __global__ void __launch_bounds__(NW * 32)
   const int ck = mi >> 1;
   const int tok_v = (lane & 7) + (mi >> 1) * 8;  // V^T (A of O^T, transposed load)
   const int cv = mi & 1;
+  // INT8 tiles: this lane's 16-byte chunks in a swizzled tile (rows of 128 bytes).
+  const int koff[4] = {gi * 128 + (((2 * gj) ^ gi) << 4), gi * 128 + (((2 * gj + 1) ^ gi) << 4),
+                       (gi + 8) * 128 + (((2 * gj) ^ gi) << 4), (gi + 8) * 128 + (((2 * gj + 1) ^ gi) << 4)};
+  const int voff[4] = {(2 * gj) * 128 + ((gi ^ (2 * gj)) << 4), (2 * gj + 1) * 128 + ((gi ^ (2 * gj + 1)) << 4),
+                       (2 * gj + 8) * 128 + ((gi ^ (2 * gj)) << 4), (2 * gj + 9) * 128 + ((gi ^ (2 * gj + 1)) << 4)};
 
   float o[C::kMTiles][4];
 #pragma unroll
   for (int t = 0; t < C::kMTiles; ++t) o[t][0] = o[t][1] = o[t][2] = o[t][3] = 0.0f;
   float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.0f, l1 = 0.0f;
   int e_run = INT_MIN;  // INT8: O^T is kept in units of 2^e_run
+  float ptot0 = 0.0f, ptot1 = 0.0f;  // INT8: running sum of P' (same units), for the V bias
 
   int failed_at = -1;
   for (int k = 0; k < nw; ++k) {
@@ -250,31 +271,35 @@ __global__ void __launch_bounds__(NW * 32)
         sacc[j][0] = sacc[j][1] = sacc[j][2] = sacc[j][3] = 0.0f;
         if (vt[j] == 0) continue;
         const unsigned char* kt = st + j * C::kTileBytes;
+        // Two accumulators (even and odd k-steps) halve the dependent MMA chain.
+        float acc2[4] = {0.0f, 0.0f, 0.0f, 0.0f};
         if constexpr (!C::kQuant) {
           const uint32_t ktile = smem_addr(kt);
 #pragma unroll
           for (int s2 = 0; s2 < C::kKSteps; ++s2) {
             uint32_t a[4];
             ldmatrix_x4(a, swz(ktile, tok_k, 2 * s2 + ck));
-            mma_bf16_16816(sacc[j], a, qf[s2][0], qf[s2][1]);
+            mma_bf16_16816((s2 & 1) ? acc2 : sacc[j], a, qf[s2][0], qf[s2][1]);
           }
         } else {
           // Lane (gi, gj) reads dims 32gj..32gj+31 of tokens gi and gi+8; k-step s2 pairs
           // dims 32gj+4s2+{0,1} with k slots 2gj, 2gj+1 and +{2,3} with 2gj+8, 2gj+9.
-          const uint4 x0 = *reinterpret_cast<const uint4*>(kt + gi * 128 + (((2 * gj) ^ gi) << 4));
-          const uint4 x1 = *reinterpret_cast<const uint4*>(kt + gi * 128 + (((2 * gj + 1) ^ gi) << 4));
-          const uint4 y0 = *reinterpret_cast<const uint4*>(kt + (gi + 8) * 128 + (((2 * gj) ^ gi) << 4));
-          const uint4 y1 = *reinterpret_cast<const uint4*>(kt + (gi + 8) * 128 + (((2 * gj + 1) ^ gi) << 4));
+          const uint4 x0 = *reinterpret_cast<const uint4*>(kt + koff[0]);
+          const uint4 x1 = *reinterpret_cast<const uint4*>(kt + koff[1]);
+          const uint4 y0 = *reinterpret_cast<const uint4*>(kt + koff[2]);
+          const uint4 y1 = *reinterpret_cast<const uint4*>(kt + koff[3]);
           const uint32_t wa[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
           const uint32_t wb[8] = {y0.x, y0.y, y0.z, y0.w, y1.x, y1.y, y1.z, y1.w};
 #pragma unroll
           for (int s2 = 0; s2 < 8; ++s2) {
             const uint32_t ua = wa[s2] ^ 0x80808080u, ub = wb[s2] ^ 0x80808080u;
-            const uint32_t a[4] = {f16x2_from_flipped(ua, 0x4140u), f16x2_from_flipped(ub, 0x4140u),
-                                   f16x2_from_flipped(ua, 0x4342u), f16x2_from_flipped(ub, 0x4342u)};
-            mma_f16_16816(sacc[j], a, qf[s2][0], qf[s2][1]);
+            const uint32_t a[4] = {f16x2_biased(ua, 0x4140u), f16x2_biased(ub, 0x4140u),
+                                   f16x2_biased(ua, 0x4342u), f16x2_biased(ub, 0x4342u)};
+            mma_f16_16816((s2 & 1) ? acc2 : sacc[j], a, qf[s2][0], qf[s2][1]);
           }
         }
+#pragma unroll
+        for (int i = 0; i < 4; ++i) sacc[j][i] += acc2[i];
       }
 
       // ---- logits in log2 units, masked past the context (and for absent blocks)
@@ -290,10 +315,10 @@ __global__ void __launch_bounds__(NW * 32)
           }
         }
         const bool v0 = gi < vt[j], v1 = gi + 8 < vt[j];
-        sc[j][0] = v0 ? sacc[j][0] * f0 : -INFINITY;
-        sc[j][1] = v0 ? sacc[j][1] * f0 : -INFINITY;
-        sc[j][2] = v1 ? sacc[j][2] * f1 : -INFINITY;
-        sc[j][3] = v1 ? sacc[j][3] * f1 : -INFINITY;
+        sc[j][0] = v0 ? (sacc[j][0] - kbias0) * f0 : -INFINITY;
+        sc[j][1] = v0 ? (sacc[j][1] - kbias1) * f0 : -INFINITY;
+        sc[j][2] = v1 ? (sacc[j][2] - kbias0) * f1 : -INFINITY;
+        sc[j][3] = v1 ? (sacc[j][3] - kbias1) * f1 : -INFINITY;
         bm0 = fmaxf(bm0, fmaxf(sc[j][0], sc[j][2]));
         bm1 = fmaxf(bm1, fmaxf(sc[j][1], sc[j][3]));
       }
@@ -349,11 +374,18 @@ __global__ void __launch_bounds__(NW * 32)
         }
         e_run = e_new;
         const float pe = pow2i(-e_new);  // P' = p * s_V * 2^-E lies in [0, 4)
+        float q0 = 0.0f, q1 = 0.0f;  // this stage's sum of the fp16 P' for heads 2gj, 2gj+1
 #pragma unroll
         for (int j = 0; j < BPS; ++j) {
           x01[j] = pack_f16x2(pr[j][0] * sv[j][0] * pe, pr[j][1] * sv[j][0] * pe);
           x23[j] = pack_f16x2(pr[j][2] * sv[j][1] * pe, pr[j][3] * sv[j][1] * pe);
+          const float2 a = __half22float2(*reinterpret_cast<const __half2*>(&x01[j]));
+          const float2 c = __half22float2(*reinterpret_cast<const __half2*>(&x23[j]));
+          q0 += a.x + c.x;
+          q1 += a.y + c.y;
         }
+        ptot0 = fmaf(ptot0, r0, q0);
+        ptot1 = fmaf(ptot1, r1, q1);
       }
       if (__any_sync(kFull, r0 != 1.0f || r1 != 1.0f)) {
 #pragma unroll
@@ -391,10 +423,10 @@ __global__ void __launch_bounds__(NW * 32)
           // INT8 codes are always finite, and masked tokens have a zero weight in P.
           // Lane (gi, gj) reads dims 16gi..16gi+15 of tokens 2gj, 2gj+1, 2gj+8, 2gj+9; m-tile
           // t row gi is dim 16gi+2t and row gi+8 is dim 16gi+2t+1.
-          const uint4 va = *reinterpret_cast<const uint4*>(vtp + (2 * gj) * 128 + ((gi ^ (2 * gj)) << 4));
-          const uint4 vb = *reinterpret_cast<const uint4*>(vtp + (2 * gj + 1) * 128 + ((gi ^ (2 * gj + 1)) << 4));
-          const uint4 vc = *reinterpret_cast<const uint4*>(vtp + (2 * gj + 8) * 128 + ((gi ^ (2 * gj)) << 4));
-          const uint4 vd = *reinterpret_cast<const uint4*>(vtp + (2 * gj + 9) * 128 + ((gi ^ (2 * gj + 1)) << 4));
+          const uint4 va = *reinterpret_cast<const uint4*>(vtp + voff[0]);
+          const uint4 vb = *reinterpret_cast<const uint4*>(vtp + voff[1]);
+          const uint4 vc = *reinterpret_cast<const uint4*>(vtp + voff[2]);
+          const uint4 vd = *reinterpret_cast<const uint4*>(vtp + voff[3]);
           const uint32_t wa[4] = {va.x ^ 0x80808080u, va.y ^ 0x80808080u, va.z ^ 0x80808080u, va.w ^ 0x80808080u};
           const uint32_t wb[4] = {vb.x ^ 0x80808080u, vb.y ^ 0x80808080u, vb.z ^ 0x80808080u, vb.w ^ 0x80808080u};
           const uint32_t wc[4] = {vc.x ^ 0x80808080u, vc.y ^ 0x80808080u, vc.z ^ 0x80808080u, vc.w ^ 0x80808080u};
@@ -404,8 +436,8 @@ __global__ void __launch_bounds__(NW * 32)
             const uint32_t sel = (t & 1) ? 0x7362u : 0x5140u;  // interleave the two tokens' bytes
             const uint32_t ab = __byte_perm(wa[t >> 1], wb[t >> 1], sel);
             const uint32_t cd = __byte_perm(wc[t >> 1], wd[t >> 1], sel);
-            const uint32_t a[4] = {f16x2_from_flipped(ab, 0x4140u), f16x2_from_flipped(ab, 0x4342u),
-                                   f16x2_from_flipped(cd, 0x4140u), f16x2_from_flipped(cd, 0x4342u)};
+            const uint32_t a[4] = {f16x2_biased(ab, 0x4140u), f16x2_biased(ab, 0x4342u),
+                                   f16x2_biased(cd, 0x4140u), f16x2_biased(cd, 0x4342u)};
             mma_f16_16816(o[t], a, pb0, pb1);
           }
         }
@@ -434,7 +466,20 @@ __global__ void __launch_bounds__(NW * 32)
     l1 += __shfl_xor_sync(kFull, l1, ofs);
   }
   float oscale = 1.0f;
-  if constexpr (C::kQuant) oscale = e_run == INT_MIN ? 0.0f : pow2i(max(-126, e_run));
+  if constexpr (C::kQuant) {
+    oscale = e_run == INT_MIN ? 0.0f : pow2i(max(-126, e_run));
+    // V codes entered as 1152 + code: O'^T = O^T + 1152 * sum_t P'_t for every dim.
+#pragma unroll
+    for (int ofs = 4; ofs < 32; ofs <<= 1) {
+      ptot0 += __shfl_xor_sync(kFull, ptot0, ofs);
+      ptot1 += __shfl_xor_sync(kFull, ptot1, ofs);
+    }
+#pragma unroll
+    for (int t = 0; t < C::kMTiles; ++t) {
+      o[t][0] -= 1152.0f * ptot0; o[t][1] -= 1152.0f * ptot1;
+      o[t][2] -= 1152.0f * ptot0; o[t][3] -= 1152.0f * ptot1;
+    }
+  }
   float* rec = reinterpret_cast<float*>(ring);
   const int h0 = 2 * gj, h1 = 2 * gj + 1;
   if (gi == 0) {

@@ -176,15 +176,13 @@ __device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
   return *reinterpret_cast<const uint32_t*>(&v);
 }
 
-// Two int8 codes -> fp16x2 exactly.  `u` holds codes with their sign bits flipped
-// (u = x + 128); `sel` picks the two bytes (0x4140: bytes 0 and 1, 0x4342: bytes 2 and 3).
-// Placing u in the low mantissa byte of the fp16 1024 (0x6400) gives 1024 + u exactly (fp16
-// has 10 mantissa bits), and subtracting 1152 = 1024 + 128 leaves x.
-__device__ __forceinline__ uint32_t f16x2_from_flipped(uint32_t u, uint32_t sel) {
-  const uint32_t h = __byte_perm(u, 0x64646464u, sel);
-  const __half2 bias = __halves2half2(__ushort_as_half(0x6480), __ushort_as_half(0x6480));
-  const __half2 v = __hsub2(*reinterpret_cast<const __half2*>(&h), bias);
-  return *reinterpret_cast<const uint32_t*>(&v);
+// Two int8 codes -> fp16x2 holding 1152 + code, exactly.  `u` holds codes with their sign
+// bits flipped (u = x + 128); `sel` picks two bytes (0x4140: bytes 0 and 1, 0x4342: bytes 2
+// and 3).  Placing u in the low mantissa byte of the fp16 1024 (0x6400) gives 1024 + u
+// exactly (fp16 has 10 mantissa bits).  Callers remove the 1152 offset after the matrix
+// product.
+__device__ __forceinline__ uint32_t f16x2_biased(uint32_t u, uint32_t sel) {
+  return __byte_perm(u, 0x64646464u, sel);
 }
 
 __device__ __forceinline__ void set_error(uint32_t* err, uint32_t bits) {
