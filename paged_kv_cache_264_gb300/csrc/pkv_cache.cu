@@ -25,6 +25,8 @@ __global__ void __launch_bounds__(kCacheThreads)
                       uint4* __restrict__ v_cache, uint32_t* err, int64_t num_tokens,
                       int64_t num_slots, int kv_heads, int chunks_per_row) {
   // chunks_per_row = head_dim * 2 / 16 sixteen-byte vectors per (token, head) row.
+  griddep_wait();  // key/value/slots may come from the previous kernel in the stream
+  griddep_launch_dependents();
   const int64_t total = num_tokens * kv_heads * chunks_per_row;
   const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
   for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < total;
@@ -81,6 +83,8 @@ __global__ void __launch_bounds__(kCacheThreads)
                       int64_t num_slots, int kv_heads) {
   constexpr int DPV = D / 32;  // values per lane: 4 (D=128) or 2 (D=64)
   const int lane = threadIdx.x & 31;
+  griddep_wait();  // key/value/slots may come from the previous kernel in the stream
+  griddep_launch_dependents();
   const int64_t rows = num_tokens * kv_heads;
   const int64_t warps = static_cast<int64_t>(gridDim.x) * (blockDim.x / 32);
   for (int64_t row = static_cast<int64_t>(blockIdx.x) * (blockDim.x / 32) + (threadIdx.x >> 5);
@@ -142,11 +146,10 @@ int grid_for(int64_t work_items, int per_block) {
 cudaError_t launch_cache_bf16(const CacheParams& p, cudaStream_t stream) {
   const int chunks = p.head_dim * 2 / 16;
   const int64_t total = p.num_tokens * p.kv_heads * chunks;
-  cache_bf16_kernel<<<grid_for(total, kCacheThreads), kCacheThreads, 0, stream>>>(
-      static_cast<const uint4*>(p.key), static_cast<const uint4*>(p.value), p.slot_mapping,
-      static_cast<uint4*>(p.k_cache), static_cast<uint4*>(p.v_cache), p.err, p.num_tokens,
-      p.num_blocks * kBlockSize, p.kv_heads, chunks);
-  return cudaGetLastError();
+  return launch_pdl(cache_bf16_kernel, dim3(grid_for(total, kCacheThreads)), dim3(kCacheThreads), 0,
+                    stream, static_cast<const uint4*>(p.key), static_cast<const uint4*>(p.value),
+                    p.slot_mapping, static_cast<uint4*>(p.k_cache), static_cast<uint4*>(p.v_cache),
+                    p.err, p.num_tokens, p.num_blocks * kBlockSize, p.kv_heads, chunks);
 }
 
 cudaError_t launch_cache_int8(const CacheParams& p, cudaStream_t stream) {
@@ -156,18 +159,15 @@ cudaError_t launch_cache_int8(const CacheParams& p, cudaStream_t stream) {
   const auto* value = static_cast<const __nv_bfloat16*>(p.value);
   auto* kc = static_cast<int8_t*>(p.k_cache);
   auto* vc = static_cast<int8_t*>(p.v_cache);
-  if (p.head_dim == 128) {
-    cache_int8_kernel<128><<<grid, kCacheThreads, 0, stream>>>(
-        key, value, p.slot_mapping, kc, vc, p.k_scale, p.v_scale, p.err, p.num_tokens,
-        p.num_blocks * kBlockSize, p.kv_heads);
-  } else if (p.head_dim == 64) {
-    cache_int8_kernel<64><<<grid, kCacheThreads, 0, stream>>>(
-        key, value, p.slot_mapping, kc, vc, p.k_scale, p.v_scale, p.err, p.num_tokens,
-        p.num_blocks * kBlockSize, p.kv_heads);
-  } else {
-    return cudaErrorInvalidValue;
-  }
-  return cudaGetLastError();
+  if (p.head_dim == 128)
+    return launch_pdl(cache_int8_kernel<128>, dim3(grid), dim3(kCacheThreads), 0, stream, key, value,
+                      p.slot_mapping, kc, vc, p.k_scale, p.v_scale, p.err, p.num_tokens,
+                      p.num_blocks * kBlockSize, p.kv_heads);
+  if (p.head_dim == 64)
+    return launch_pdl(cache_int8_kernel<64>, dim3(grid), dim3(kCacheThreads), 0, stream, key, value,
+                      p.slot_mapping, kc, vc, p.k_scale, p.v_scale, p.err, p.num_tokens,
+                      p.num_blocks * kBlockSize, p.kv_heads);
+  return cudaErrorInvalidValue;
 }
 
 }  // namespace pkv

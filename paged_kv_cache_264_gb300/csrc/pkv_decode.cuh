@@ -336,6 +336,8 @@ __global__ void __launch_bounds__(NW * 32)
   using C = DecodeCfg<KV, D, G, NW, S>;
   constexpr uint32_t kFull = 0xffffffffu;
   extern __shared__ __align__(128) unsigned char smem[];
+  griddep_wait();  // inputs may come from the previous kernel in the stream
+  griddep_launch_dependents();
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -604,6 +606,7 @@ __global__ void __launch_bounds__(128) lse_reduce_kernel(const DecodeParams p) {
   constexpr int kDPV = D / 32;
   constexpr uint32_t kFull = 0xffffffffu;
   const int lane = threadIdx.x & 31;
+  griddep_wait();  // the partials come from the decode kernel just before
   const int gw = blockIdx.x * (blockDim.x / 32) + (threadIdx.x >> 5);
   if (gw >= p.num_seqs * p.num_q_heads) return;
   const int b = gw / p.num_q_heads;
@@ -663,8 +666,8 @@ cudaError_t launch_decode_variant(const DecodeParams& p, cudaStream_t stream) {
       p.persistent ? int64_t(p.grid) : int64_t(p.max_parts) * p.num_seqs * p.kv_heads;
   if (grid <= 0) return cudaSuccess;
   if (grid > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
-  kern<<<static_cast<unsigned>(grid), C::kThreads, C::smem_bytes(p.partition_blocks, p.persistent ? p.num_seqs : 0), stream>>>(p);
-  return cudaGetLastError();
+  return launch_pdl(kern, dim3(static_cast<unsigned>(grid)), dim3(C::kThreads),
+                    C::smem_bytes(p.partition_blocks, p.persistent ? p.num_seqs : 0), stream, p);
 }
 
 template <KvType KV, int D, int G, int NW, int S>

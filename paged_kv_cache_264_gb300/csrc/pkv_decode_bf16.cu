@@ -50,14 +50,11 @@ cudaError_t launch_lse_reduce(const DecodeParams& p, cudaStream_t stream) {
   const int64_t pairs = int64_t(p.num_seqs) * p.num_q_heads;
   const int64_t grid = (pairs + 3) / 4;
   if (grid <= 0) return cudaSuccess;
-  if (p.head_dim == 128) {
-    lse_reduce_kernel<128><<<static_cast<unsigned>(grid), 128, 0, stream>>>(p);
-  } else if (p.head_dim == 64) {
-    lse_reduce_kernel<64><<<static_cast<unsigned>(grid), 128, 0, stream>>>(p);
-  } else {
-    return cudaErrorInvalidValue;
-  }
-  return cudaGetLastError();
+  if (p.head_dim == 128)
+    return launch_pdl(lse_reduce_kernel<128>, dim3(static_cast<unsigned>(grid)), dim3(128), 0, stream, p);
+  if (p.head_dim == 64)
+    return launch_pdl(lse_reduce_kernel<64>, dim3(static_cast<unsigned>(grid)), dim3(128), 0, stream, p);
+  return cudaErrorInvalidValue;
 }
 
 }  // namespace pkv

@@ -75,6 +75,8 @@ __global__ void __launch_bounds__(NW * 32)
                             const __grid_constant__ CUtensorMap tmap_v, const DecodeParams p) {
   using C = MmaCfg<KV, D, G, NW, S, BPS>;
   constexpr uint32_t kFull = 0xffffffffu;
+  griddep_wait();  // inputs may come from the previous kernel in the stream
+  griddep_launch_dependents();
   extern __shared__ unsigned char smem_raw[];
   unsigned char* smem = reinterpret_cast<unsigned char*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -526,8 +528,8 @@ cudaError_t launch_mma_variant(const DecodeParams& p, const CUtensorMap& tk, con
       p.persistent ? int64_t(p.grid) : int64_t(p.max_parts) * p.num_seqs * p.kv_heads;
   if (grid <= 0) return cudaSuccess;
   if (grid > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
-  kern<<<static_cast<unsigned>(grid), C::kThreads, C::smem_bytes(p.partition_blocks, p.persistent ? p.num_seqs : 0), stream>>>(tk, tv, p);
-  return cudaGetLastError();
+  return launch_pdl(kern, dim3(static_cast<unsigned>(grid)), dim3(C::kThreads),
+                    C::smem_bytes(p.partition_blocks, p.persistent ? p.num_seqs : 0), stream, tk, tv, p);
 }
 
 template <KvType KV, int D, int G, int NW, int S, int BPS>

@@ -185,6 +185,18 @@ __device__ __forceinline__ uint32_t f16x2_biased(uint32_t u, uint32_t sel) {
   return __byte_perm(u, 0x64646464u, sel);
 }
 
+// Programmatic dependent launch.  A kernel launched with programmatic stream serialisation
+// may start while the previous kernel in the stream is still finishing; griddep_wait()
+// returns once that kernel has completed and its writes are visible, so it must precede
+// every read of data a previous kernel may have written.  griddep_launch_dependents()
+// lets the next kernel's launch begin; that kernel is only scheduled once every CTA of this
+// one has started, so it can never take resources this kernel still needs.  Both are no-ops
+// for ordinary launches.
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void griddep_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 __device__ __forceinline__ void set_error(uint32_t* err, uint32_t bits) {
   if (err) atomicOr(err, bits);
 }

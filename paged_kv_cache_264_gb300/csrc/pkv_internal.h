@@ -62,6 +62,24 @@ struct DecodeParams {
   float scale_log2;             // softmax scale * log2(e)
 };
 
+// Launch a kernel with programmatic stream serialisation (see griddep_wait in
+// pkv_device.cuh): its launch may overlap the tail of the previous kernel in the stream.
+template <typename... Params, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(Params...), dim3 grid, dim3 block, size_t smem,
+                       cudaStream_t stream, Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, static_cast<Args&&>(args)...);
+}
+
 // Kernel launchers (defined next to their kernels).  Each returns the launch status.
 cudaError_t launch_cache_bf16(const CacheParams& p, cudaStream_t stream);
 cudaError_t launch_cache_int8(const CacheParams& p, cudaStream_t stream);
