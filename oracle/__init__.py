@@ -20,6 +20,10 @@ What each function follows (page title, section):
 * ``quantize_rows`` / ``reshape_and_cache_int8`` -- INT8 symmetric quantisation
   ``round(x / s)``, ``s = max|x| / 127``, one scale per (token, kv head) row, fp32
   arithmetic, round half to even, codes in [-127, 127]; "Lesson 4", section 5.3.
+* ``e4m3_to_float`` / ``float_to_e4m3`` / ``quantize_rows_fp8`` / ``reshape_and_cache_fp8``
+  -- the FP8 (E4M3) KV cache read as the INT8 scheme with E4M3 codes: ``s = max|x| / 448``,
+  code = nearest E4M3 of ``x / s`` (ties to even, saturating); "Lesson 4", section 5.3
+  names FP8 KV caches without a scaling rule.
 * ``kv_cache_bytes`` -- the KV-cache size closed form
   ``2 * layers * n_kv * head_dim * seq_len * bytes``; "LLM/MLLM inference
   optimisation", section 2.2.
@@ -38,6 +42,7 @@ import numpy as np
 BLOCK_SIZE = 16
 KV_BF16 = 0
 KV_INT8 = 1
+KV_FP8 = 2
 
 _HERE = Path(__file__).resolve().parent
 SOURCE = _HERE / "oracle.c"
@@ -116,6 +121,15 @@ class Oracle:
         lib.oracle_quantize_rows_bf16.restype = i32
         lib.oracle_reshape_and_cache_int8.argtypes = [vp, vp, vp, i64, i32, i32, i64, vp, vp, vp, vp]
         lib.oracle_reshape_and_cache_int8.restype = i32
+        lib.oracle_e4m3_to_double.argtypes = [ctypes.c_uint8]
+        lib.oracle_e4m3_to_double.restype = ctypes.c_double
+        lib.oracle_float_to_e4m3.argtypes = [ctypes.c_float]
+        lib.oracle_float_to_e4m3.restype = ctypes.c_uint8
+        lib.oracle_quantize_row_fp8_f32.argtypes = [vp, i32, vp, vp]
+        lib.oracle_quantize_rows_fp8_bf16.argtypes = [vp, i64, i32, vp, vp]
+        lib.oracle_quantize_rows_fp8_bf16.restype = i32
+        lib.oracle_reshape_and_cache_fp8.argtypes = [vp, vp, vp, i64, i32, i32, i64, vp, vp, vp, vp]
+        lib.oracle_reshape_and_cache_fp8.restype = i32
         lib.oracle_paged_decode.argtypes = [
             vp, vp, vp, vp, vp, i32, i64, i32, i32, vp, i32, vp, i32, i32, ctypes.c_double, vp]
         lib.oracle_paged_decode.restype = i32
@@ -171,20 +185,56 @@ class Oracle:
             _ptr(key), _ptr(value), _ptr(slots), n, hkv, d, k_cache.shape[0],
             _ptr(k_cache), _ptr(v_cache), _ptr(k_scale), _ptr(v_scale)))
 
+    # -- FP8 (E4M3)
+    def e4m3_to_float(self, codes) -> np.ndarray:
+        codes = np.asarray(codes, np.uint8)
+        return np.array([self.lib.oracle_e4m3_to_double(int(c)) for c in codes.ravel()]).reshape(codes.shape)
+
+    def float_to_e4m3(self, y) -> np.ndarray:
+        y = np.asarray(y, np.float32)
+        return np.array([self.lib.oracle_float_to_e4m3(float(v)) for v in y.ravel()], np.uint8).reshape(y.shape)
+
+    def quantize_row_fp8_f32(self, x) -> tuple[np.ndarray, np.float32]:
+        x = _c(x, np.float32)
+        codes = np.zeros(x.shape[0], np.uint8)
+        scale = np.zeros(1, np.float32)
+        self.lib.oracle_quantize_row_fp8_f32(_ptr(x), x.shape[0], _ptr(codes), _ptr(scale))
+        return codes, scale[0]
+
+    def quantize_rows_fp8(self, x_bf16_bits) -> tuple[np.ndarray, np.ndarray]:
+        x = _c(x_bf16_bits, np.uint16)
+        d = x.shape[-1]
+        codes = np.zeros(x.shape, np.uint8)
+        scales = np.zeros(x.shape[:-1], np.float32)
+        _check(self.lib.oracle_quantize_rows_fp8_bf16(_ptr(x), x.size // d, d, _ptr(codes), _ptr(scales)))
+        return codes, scales
+
+    def reshape_and_cache_fp8(self, key, value, slot_mapping, k_cache, v_cache, k_scale, v_scale) -> None:
+        key, value = _c(key, np.uint16), _c(value, np.uint16)
+        slots = _c(slot_mapping, np.int32)
+        for a, dt in ((k_cache, np.uint8), (v_cache, np.uint8), (k_scale, np.float32), (v_scale, np.float32)):
+            assert a.dtype == dt and a.flags.c_contiguous
+        n, hkv, d = key.shape
+        _check(self.lib.oracle_reshape_and_cache_fp8(
+            _ptr(key), _ptr(value), _ptr(slots), n, hkv, d, k_cache.shape[0],
+            _ptr(k_cache), _ptr(v_cache), _ptr(k_scale), _ptr(v_scale)))
+
     # -- decode
     def paged_decode(self, q, k_cache, v_cache, block_tables, context_lens, scale,
                      k_scale=None, v_scale=None) -> np.ndarray:
         """fp64 [B, Hq, d] attention output.
 
-        q: uint16 bf16 bits [B, Hq, d]; k_cache/v_cache: uint16 (bf16) or int8
-        [num_blocks, Hkv, 16, d]; k_scale/v_scale: fp32 [num_blocks, Hkv, 16] for int8.
+        q: uint16 bf16 bits [B, Hq, d]; k_cache/v_cache: uint16 (bf16), int8 (INT8) or uint8
+        (FP8 E4M3 codes) [num_blocks, Hkv, 16, d]; k_scale/v_scale: fp32 [num_blocks, Hkv, 16]
+        for INT8 and FP8.
         """
         q = _c(q, np.uint16)
-        int8 = k_cache.dtype == np.int8
-        kv_dtype = KV_INT8 if int8 else KV_BF16
-        kdt = np.int8 if int8 else np.uint16
+        kdt = k_cache.dtype
+        kv_dtype = {np.dtype(np.int8): KV_INT8, np.dtype(np.uint8): KV_FP8}.get(np.dtype(kdt), KV_BF16)
+        if kv_dtype == KV_BF16:
+            kdt = np.uint16
         k_cache, v_cache = _c(k_cache, kdt), _c(v_cache, kdt)
-        if int8:
+        if kv_dtype != KV_BF16:
             k_scale, v_scale = _c(k_scale, np.float32), _c(v_scale, np.float32)
         bt = _c(block_tables, np.int32)
         cl = _c(context_lens, np.int32)

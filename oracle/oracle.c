@@ -28,6 +28,12 @@
  *    ("Lesson 4", section 5.3 "KV Cache Quantization").  One scale per
  *    (token, kv head) row of d values; fp32 arithmetic with IEEE round-to-nearest
  *    division, round-half-to-even to the integer code, codes clamped to [-127, 127].
+ *  - FP8 KV cache (same section names FP8 with its larger dynamic range, and that vLLM
+ *    supports an FP8 KV cache; it gives no scaling rule).  Read here as the INT8 scheme
+ *    with the E4M3 format in place of int8: s = max|x| / 448 per (token, kv head) row,
+ *    code = E4M3(x / s) rounded to nearest, ties to even, saturating at +-448.  E4M3 is
+ *    1 sign bit, 4 exponent bits (bias 7), 3 mantissa bits, no infinities; the largest
+ *    finite value is 448 and S.1111.111 is NaN.
  *
  * All floating point in the attention path is fp64.  bf16 values are widened exactly
  * (a bf16 is the top 16 bits of an fp32).  INT8 values are dequantised exactly in
@@ -52,7 +58,7 @@ enum {
   ORACLE_ERR_NOMEM = -5
 };
 
-enum { ORACLE_KV_BF16 = 0, ORACLE_KV_INT8 = 1 };
+enum { ORACLE_KV_BF16 = 0, ORACLE_KV_INT8 = 1, ORACLE_KV_FP8 = 2 };
 
 /* ---------------------------------------------------------------- threads */
 
@@ -201,6 +207,104 @@ int oracle_reshape_and_cache_int8(const uint16_t* key, const uint16_t* value,
   return ORACLE_OK;
 }
 
+/* ---------------------------------------------------------- FP8 (E4M3) */
+
+/* Value of an E4M3 byte: exponent field e (bits 6..3), mantissa m (bits 2..0).
+ * e == 0: subnormal m * 2^-9; e == 15 and m == 7: NaN; otherwise (1 + m/8) * 2^(e - 7). */
+double oracle_e4m3_to_double(uint8_t b) {
+  const int sign = (b >> 7) & 1;
+  const int e = (b >> 3) & 15;
+  const int m = b & 7;
+  double v;
+  if (e == 15 && m == 7) return NAN;
+  if (e == 0)
+    v = ldexp((double)m, -9);
+  else
+    v = ldexp(1.0 + m / 8.0, e - 7);
+  return sign ? -v : v;
+}
+
+/* Nearest E4M3 to a finite y, ties to the even mantissa, saturating at +-448.
+ * With |y| = f * 2^k, 1 <= f < 2: the grid spacing is 2^(k-3) for normal numbers
+ * (k >= -6) and 2^-9 below; q = round(|y| / spacing) is then an exact scaling by a power
+ * of two followed by one rounding, and code = (biased exponent) * 8 + q - 8 also covers a
+ * mantissa that rounds up into the next binade. */
+uint8_t oracle_float_to_e4m3(float y) {
+  const uint8_t sign = (y < 0.0f || (y == 0.0f && signbit(y))) ? 0x80 : 0x00;
+  double a = fabs((double)y);
+  if (a >= 448.0) return sign | 0x7E;
+  if (a == 0.0) return sign;
+  int k;
+  frexp(a, &k); /* a = f * 2^k with f in [0.5, 1): floor(log2 a) = k - 1 */
+  k -= 1;
+  int code;
+  if (k < -6) {
+    const double q = rint(ldexp(a, 9)); /* units of 2^-9 */
+    code = (int)q;                       /* q == 8 is the smallest normal, 0x08 */
+  } else {
+    const double q = rint(ldexp(a, 3 - k)); /* in [8, 16] */
+    code = (k + 7) * 8 + (int)q - 8;
+  }
+  if (code > 0x7E) code = 0x7E;
+  return sign | (uint8_t)code;
+}
+
+/* Quantise one row to E4M3 with its own fp32 scale s = max|x| / 448 (IEEE division);
+ * a zero row gets s = 0 and zero codes. */
+void oracle_quantize_row_fp8_f32(const float* x, int n, uint8_t* codes, float* scale_out) {
+  float amax = 0.0f;
+  for (int i = 0; i < n; ++i) {
+    float a = fabsf(x[i]);
+    if (a > amax) amax = a;
+  }
+  float s = amax / 448.0f;
+  *scale_out = s;
+  for (int i = 0; i < n; ++i) codes[i] = amax == 0.0f ? 0 : oracle_float_to_e4m3(x[i] / s);
+}
+
+int oracle_quantize_rows_fp8_bf16(const uint16_t* x, int64_t rows, int n, uint8_t* codes,
+                                  float* scales) {
+  if (rows < 0 || n < 1) return ORACLE_ERR_ARG;
+  float* tmp = (float*)malloc(sizeof(float) * (size_t)n);
+  if (!tmp) return ORACLE_ERR_NOMEM;
+  for (int64_t r = 0; r < rows; ++r) {
+    for (int i = 0; i < n; ++i) tmp[i] = oracle_bf16_to_float(x[r * n + i]);
+    oracle_quantize_row_fp8_f32(tmp, n, codes + r * n, scales + r);
+  }
+  free(tmp);
+  return ORACLE_OK;
+}
+
+/* FP8 cache write: the INT8 write's addressing with the E4M3 quantiser. */
+int oracle_reshape_and_cache_fp8(const uint16_t* key, const uint16_t* value,
+                                 const int32_t* slot_mapping, int64_t num_tokens, int kv_heads,
+                                 int head_dim, int64_t num_blocks, uint8_t* k_cache,
+                                 uint8_t* v_cache, float* k_scale, float* v_scale) {
+  if (num_tokens < 0 || kv_heads < 1 || head_dim < 1 || num_blocks < 1) return ORACLE_ERR_ARG;
+  int64_t t;
+  for (t = 0; t < num_tokens; ++t)
+    if ((int64_t)slot_mapping[t] >= num_blocks * ORACLE_BLOCK_SIZE) return ORACLE_ERR_SLOT;
+  float* row = (float*)malloc(sizeof(float) * (size_t)head_dim);
+  if (!row) return ORACLE_ERR_NOMEM;
+  for (t = 0; t < num_tokens; ++t) {
+    int64_t slot = slot_mapping[t];
+    if (slot < 0) continue;
+    int64_t block = slot / ORACLE_BLOCK_SIZE;
+    int64_t offset = slot % ORACLE_BLOCK_SIZE;
+    for (int h = 0; h < kv_heads; ++h) {
+      int64_t src = (t * kv_heads + h) * (int64_t)head_dim;
+      int64_t srow = (block * kv_heads + h) * ORACLE_BLOCK_SIZE + offset;
+      int64_t dst = srow * (int64_t)head_dim;
+      for (int c = 0; c < head_dim; ++c) row[c] = oracle_bf16_to_float(key[src + c]);
+      oracle_quantize_row_fp8_f32(row, head_dim, k_cache + dst, k_scale + srow);
+      for (int c = 0; c < head_dim; ++c) row[c] = oracle_bf16_to_float(value[src + c]);
+      oracle_quantize_row_fp8_f32(row, head_dim, v_cache + dst, v_scale + srow);
+    }
+  }
+  free(row);
+  return ORACLE_OK;
+}
+
 /* ------------------------------------------------------------ decode */
 
 /* Value of element c of the cached row (block, head, offset) as fp64. */
@@ -210,6 +314,10 @@ static double cache_value(const void* cache, const float* scales, int kv_dtype,
     const uint16_t* p = (const uint16_t*)cache;
     return (double)oracle_bf16_to_float(p[row * head_dim + c]);
   }
+  if (kv_dtype == ORACLE_KV_FP8) {
+    const uint8_t* p = (const uint8_t*)cache;
+    return (double)scales[row] * oracle_e4m3_to_double(p[row * head_dim + c]);
+  }
   const int8_t* p = (const int8_t*)cache;
   return (double)scales[row] * (double)p[row * head_dim + c];
 }
@@ -218,7 +326,8 @@ static double cache_value(const void* cache, const float* scales, int kv_dtype,
  * out[b][h][:] = sum_t softmax_t(scale * q[b][h] . k_t) v_t  over the T_b tokens of
  * sequence b, in logical order t = 0 .. T_b - 1.  Token t lives in logical block
  * j = t / 16 at offset i = t % 16; its physical block is block_tables[b][j]; its key
- * row is k_cache[phys][kvh][i][:] with kvh = h / (Hq / Hkv).
+ * row is k_cache[phys][kvh][i][:] with kvh = h / (Hq / Hkv).  INT8 and FP8 rows are
+ * dequantised as (double)scale * value(code).
  * The softmax is evaluated in two passes (find the largest logit, then exponentiate
  * the differences); this is the same value as exp(l_t) / sum exp(l_u).
  *
@@ -234,8 +343,9 @@ int oracle_paged_decode(const uint16_t* q, const void* k_cache, const void* v_ca
   if (num_seqs < 0 || kv_heads < 1 || head_dim < 1 || num_blocks < 1 || max_blocks_per_seq < 1)
     return ORACLE_ERR_ARG;
   if (num_q_heads < kv_heads || num_q_heads % kv_heads != 0) return ORACLE_ERR_ARG;
-  if (kv_dtype != ORACLE_KV_BF16 && kv_dtype != ORACLE_KV_INT8) return ORACLE_ERR_ARG;
-  if (kv_dtype == ORACLE_KV_INT8 && (!k_scale || !v_scale)) return ORACLE_ERR_ARG;
+  if (kv_dtype != ORACLE_KV_BF16 && kv_dtype != ORACLE_KV_INT8 && kv_dtype != ORACLE_KV_FP8)
+    return ORACLE_ERR_ARG;
+  if (kv_dtype != ORACLE_KV_BF16 && (!k_scale || !v_scale)) return ORACLE_ERR_ARG;
 
   /* Validate everything that will be read before any arithmetic. */
   for (int b = 0; b < num_seqs; ++b) {

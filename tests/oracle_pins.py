@@ -85,11 +85,13 @@ def paged_case(o, lens, hq, hkv, d, gen, *, num_blocks=None, perm=None, kv="bf16
         o.reshape_and_cache_bf16(bits(key), bits(value), slots, kc, vc)
         pool.update(k_cache=kc, v_cache=vc)
     else:
-        kc = np.zeros((num_blocks, hkv, BS, d), np.int8)
+        cdt = np.int8 if kv == "int8" else np.uint8
+        kc = np.zeros((num_blocks, hkv, BS, d), cdt)
         vc = kc.copy()
         ks = np.full((num_blocks, hkv, BS), np.nan if fill_nan else 0, np.float32)
         vs = ks.copy()
-        o.reshape_and_cache_int8(bits(key), bits(value), slots, kc, vc, ks, vs)
+        write = o.reshape_and_cache_int8 if kv == "int8" else o.reshape_and_cache_fp8
+        write(bits(key), bits(value), slots, kc, vc, ks, vs)
         pool.update(k_cache=kc, v_cache=vc, k_scale=ks, v_scale=vs)
     return bits(q), pool, tables, np.array(lens, np.int32), k, v
 
@@ -347,6 +349,80 @@ def pin_int8_cache_and_decode(o):
             assert np.array_equal(vs[blocks, h, offs], vscales[:, h])
         kd = torch.from_numpy(kcodes.astype(np.float64) * kscales.astype(np.float64)[..., None])
         vd = torch.from_numpy(vcodes.astype(np.float64) * vscales.astype(np.float64)[..., None])
+        g = hq // hkv
+        ref = sdpa_fp64(q[b], kd.repeat_interleave(g, 1), vd.repeat_interleave(g, 1), scale)
+        np.testing.assert_allclose(out[b], ref, rtol=1e-12, atol=1e-13)
+
+
+def pin_e4m3_decode_matches_torch(o):
+    """Every E4M3 byte decodes to torch's float8_e4m3fn value of the same bits (NaN codes
+    S.1111.111 included)."""
+    codes = np.arange(256, dtype=np.uint8)
+    mine = o.e4m3_to_float(codes)
+    ref = torch.from_numpy(codes).view(torch.float8_e4m3fn).double().numpy()
+    assert np.array_equal(np.isnan(mine), np.isnan(ref))
+    assert np.array_equal(mine[~np.isnan(ref)], ref[~np.isnan(ref)])
+
+
+def pin_e4m3_format_values(o):
+    """Values the E4M3 definition fixes (bias 7, 3 mantissa bits, no infinities): the
+    largest finite 448, 1.0, the smallest normal 2^-6 and subnormal 2^-9, ties to the even
+    mantissa, saturation of out-of-range values at +-448."""
+    cases = {448.0: 0x7E, 1.0: 0x38, 2.0 ** -6: 0x08, 2.0 ** -9: 0x01, -1.5: 0xBC, 0.0: 0x00,
+             1.0625: 0x38, 1.1875: 0x3A, 3.0 * 2.0 ** -10: 0x02, 500.0: 0x7E, -1e6: 0xFE,
+             464.0: 0x7E, 2.0 ** -11: 0x00}
+    for y, code in cases.items():
+        assert int(o.float_to_e4m3(np.float32(y))) == code, (y, hex(code))
+    assert o.e4m3_to_float(np.uint8(0x7E)) == 448.0 and np.isnan(o.e4m3_to_float(np.uint8(0x7F)))
+
+
+def pin_e4m3_encode_matches_torch(o):
+    """Nearest E4M3 (ties to even) agrees with torch's float8_e4m3fn cast on in-range
+    values spanning the subnormal and normal ranges, and on exact midpoints."""
+    gen = torch.Generator().manual_seed(25)
+    y = (torch.randn(20000, generator=gen) * torch.exp(torch.randn(20000, generator=gen) * 3)).clamp(-447.9, 447.9)
+    grid = torch.from_numpy(np.arange(0, 0x7E, dtype=np.uint8)).view(torch.float8_e4m3fn).float()
+    mids = (grid[1:] + grid[:-1]) / 2
+    y = torch.cat([y, mids, -mids]).float()
+    assert np.array_equal(o.float_to_e4m3(y.numpy()), y.to(torch.float8_e4m3fn).view(torch.uint8).numpy())
+
+
+def pin_fp8_quantiser(o):
+    """FP8 rows: s = max|x| / 448, the largest element maps to +-448, and every element is
+    within half an E4M3 spacing of s * value(code): 2^-4 relative for normals, s * 2^-10
+    absolute below the normal range."""
+    gen = torch.Generator().manual_seed(26)
+    for rows in (rand_bf16(gen, 300, 128), rand_bf16(gen, 100, 64, scale=1e-3)):
+        codes, scales = o.quantize_rows_fp8(bits(rows))
+        xf = rows.float().numpy().astype(np.float64)
+        s = scales.astype(np.float64)[:, None]
+        np.testing.assert_array_equal(scales, (np.abs(rows.float().numpy()).max(1) / np.float32(448)).astype(np.float32))
+        deq = s * o.e4m3_to_float(codes)
+        bound = np.maximum(np.abs(xf) * 2.0 ** -4, s * 2.0 ** -10) * (1 + 2.0 ** -10)
+        assert np.all(np.abs(xf - deq) <= bound)
+        arg = np.abs(xf).argmax(1)
+        assert np.all(np.abs(o.e4m3_to_float(codes[np.arange(len(arg)), arg])) == 448.0)
+
+
+def pin_fp8_cache_and_decode(o):
+    """The FP8 write stores each row's own codes and scale at its slot; the FP8 decode
+    equals fp64 SDPA over the dequantised values s * value(code)."""
+    gen = torch.Generator().manual_seed(27)
+    lens, hq, hkv, d = [9, 16, 40], 8, 2, 64
+    qb, pool, tab, ln, k, v = paged_case(o, lens, hq, hkv, d, gen, kv="fp8")
+    scale = 1.0 / math.sqrt(d)
+    out = decode(o, qb, pool, tab, ln, scale)
+    q = from_bits(qb)
+    for b, t_len in enumerate(lens):
+        kcodes, kscales = o.quantize_rows_fp8(bits(k[b]))
+        vcodes, vscales = o.quantize_rows_fp8(bits(v[b]))
+        blocks = tab[b, (np.arange(t_len) // BS)]
+        offs = np.arange(t_len) % BS
+        for h in range(hkv):
+            assert np.array_equal(pool["k_cache"][blocks, h, offs], kcodes[:, h])
+            assert np.array_equal(pool["v_scale"][blocks, h, offs], vscales[:, h])
+        kd = torch.from_numpy(o.e4m3_to_float(kcodes) * kscales.astype(np.float64)[..., None])
+        vd = torch.from_numpy(o.e4m3_to_float(vcodes) * vscales.astype(np.float64)[..., None])
         g = hq // hkv
         ref = sdpa_fp64(q[b], kd.repeat_interleave(g, 1), vd.repeat_interleave(g, 1), scale)
         np.testing.assert_allclose(out[b], ref, rtol=1e-12, atol=1e-13)

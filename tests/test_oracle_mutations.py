@@ -37,6 +37,12 @@ MUTANTS = [
      "int64_t dst = ((block * kv_heads + h) * ORACLE_BLOCK_SIZE + (ORACLE_BLOCK_SIZE - 1 - offset)) * (int64_t)head_dim;"),
     ("INT8 write ignores the head", "int64_t srow = (block * kv_heads + h) * ORACLE_BLOCK_SIZE + offset;",
      "int64_t srow = (block * kv_heads + 0) * ORACLE_BLOCK_SIZE + offset;"),
+    ("E4M3 decoded with exponent bias 8", "v = ldexp(1.0 + m / 8.0, e - 7);", "v = ldexp(1.0 + m / 8.0, e - 8);"),
+    ("E4M3 subnormals on the wrong grid", "v = ldexp((double)m, -9);", "v = ldexp((double)m, -10);"),
+    ("E4M3 encode rounds half away from zero", "const double q = rint(ldexp(a, 3 - k));",
+     "const double q = round(ldexp(a, 3 - k));"),
+    ("E4M3 encode does not saturate", "if (a >= 448.0) return sign | 0x7E;", "if (a >= 480.0) return sign | 0x7F;"),
+    ("FP8 scale uses the INT8 range", "float s = amax / 448.0f;", "float s = amax / 127.0f;"),
     ("query widened from the wrong head", "const uint16_t* qrow = q + bh * head_dim;",
      "const uint16_t* qrow = q + ((int64_t)b * num_q_heads + (num_q_heads - 1 - h)) * head_dim;"),
 ]
