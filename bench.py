@@ -270,7 +270,7 @@ def run_ours(args, rank, world, local):
         "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_step, 5),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-        "dtype": "bf16" if kv == "bf16" else "int8 KV, fp32 accumulate",
+        "dtype": {"bf16": "bf16", "int8": "int8 KV, fp32 accumulate", "fp8": "fp8 e4m3 KV, fp32 accumulate"}[kv],
         "data": "synthetic (seeded N(0,1) bf16 values; seeded lengths and shuffled block pool)",
         "config": {
             "workload": args.workload, "description": spec.description,

@@ -58,7 +58,13 @@ typedef enum pkv_kv_dtype {
   PKV_KV_BF16 = 0,
   /* K/V stored as int8 codes with one fp32 scale per (token, kv head) row, symmetric:
    * s = max|x| / 127, code = round(x / s) ("Lesson 4", 5.3 "KV Cache Quantization"). */
-  PKV_KV_INT8 = 1
+  PKV_KV_INT8 = 1,
+  /* K/V stored as FP8 E4M3 codes (1 sign, 4 exponent bits with bias 7, 3 mantissa bits, no
+   * infinities, largest finite 448) with one fp32 scale per (token, kv head) row:
+   * s = max|x| / 448, code = nearest E4M3 of x / s, ties to even, saturating at +-448.
+   * The same section names FP8 KV caches and their larger dynamic range; it gives no
+   * scaling rule, and this is the INT8 scheme with E4M3 codes. */
+  PKV_KV_FP8_E4M3 = 2
 } pkv_kv_dtype;
 
 /* Bits of the device error word. */
@@ -94,10 +100,11 @@ PKV_API pkv_status pkv_pool_bytes(int64_t num_blocks, int kv_heads, int head_dim
 /*
  * Describe a pool of physical KV blocks that the caller has allocated on the current
  * device ("Lesson 4", 4.2, global block pool).
- *   k_cache, v_cache (device): [num_blocks, kv_heads, 16, head_dim] of bf16 or int8,
- *                              each 16-byte aligned.
- *   k_scale, v_scale (device): [num_blocks, kv_heads, 16] fp32 for PKV_KV_INT8, 16-byte
- *                              aligned; must be NULL for PKV_KV_BF16.
+ *   k_cache, v_cache (device): [num_blocks, kv_heads, 16, head_dim] of bf16, int8 or E4M3
+ *                              bytes, each 16-byte aligned.
+ *   k_scale, v_scale (device): [num_blocks, kv_heads, 16] fp32 for PKV_KV_INT8 and
+ *                              PKV_KV_FP8_E4M3, 16-byte aligned; must be NULL for
+ *                              PKV_KV_BF16.
  *   block_size must be PKV_BLOCK_SIZE.
  * The library records the pointers and allocates a small device error word for the
  * pool on the current device (freed by pkv_pool_destroy).  The pool contents are not
@@ -123,6 +130,8 @@ PKV_API pkv_status pkv_pool_destroy(pkv_pool* pool);
  *   s = max_c |x_c| / 127 (fp32, IEEE division), code_c = round_half_even(x_c / s),
  *   clamped to [-127, 127]; a row of zeros stores s = 0 and zero codes;
  *   k_scale[block][h][offset] = s.
+ * An FP8 pool does the same with s = max_c |x_c| / 448 and code_c = nearest E4M3 of
+ * x_c / s (ties to even, saturating).
  *   key, value   (device): bf16 [num_tokens, kv_heads, head_dim], 16-byte aligned.
  *   slot_mapping (device): int32 [num_tokens]; a negative slot skips that token.
  * Slots must be distinct among the tokens of one call (two writes to one slot race).
@@ -139,7 +148,7 @@ PKV_API pkv_status pkv_reshape_and_cache(const pkv_pool* pool, const void* key, 
  *     one partition are combined by a log-sum-exp reduce.  0 = chosen from the batch
  *     shape and the device's SM count.
  *   kernel: which decode kernel family runs.  PKV_KERNEL_AUTO (0) picks the tensor-core
- *     kernel where it is built (GQA group 2, 4 or 8; bf16 head_dim 64/128 or INT8
+ *     kernel where it is built (GQA group 2, 4 or 8; bf16 head_dim 64/128, INT8 or FP8
  *     head_dim 128) and the CUDA-core kernel otherwise; PKV_KERNEL_CUDA_CORE (1) and
  *     PKV_KERNEL_TENSOR_CORE (2) force one (PKV_ERR_UNSUPPORTED if it is not built for
  *     the shape).  Both compute the same function.
@@ -195,8 +204,8 @@ PKV_API pkv_status pkv_decode_plan(const pkv_pool* pool, int num_seqs, int num_q
  *   out[b][h][:] = sum_{t < T_b} softmax_t(scale * q[b][h] . K_b[t]) V_b[t]
  * where token t of sequence b lives in physical block block_tables[b][t / 16] at offset
  * t % 16, T_b = context_lens[b], and query head h reads kv head h / (num_q_heads /
- * kv_heads) (contiguous GQA groups; "LLM/MLLM inference optimisation", 2.3).  For an
- * INT8 pool K and V are the dequantised values s * code.  Accumulation is fp32; out is
+ * kv_heads) (contiguous GQA groups; "LLM/MLLM inference optimisation", 2.3).  For INT8
+ * and FP8 pools K and V are the dequantised values s * value(code).  Accumulation is fp32; out is
  * rounded to bf16 (round to nearest even).
  *   q            (device): bf16 [num_seqs, num_q_heads, head_dim], 16-byte aligned.
  *   block_tables (device): int32 [num_seqs, max_blocks_per_seq]; entries past

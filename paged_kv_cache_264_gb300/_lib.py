@@ -19,6 +19,7 @@ PKV_ERR_WORKSPACE = 4
 
 PKV_KV_BF16 = 0
 PKV_KV_INT8 = 1
+PKV_KV_FP8_E4M3 = 2
 BLOCK_SIZE = 16
 
 DEVERR_BLOCK_ID = 0x1

@@ -13,9 +13,10 @@ import ctypes
 import torch
 
 from . import _lib
-from ._lib import BLOCK_SIZE, DecodeOptions, PKV_KV_BF16, PKV_KV_INT8, check
+from ._lib import BLOCK_SIZE, DecodeOptions, PKV_KV_BF16, PKV_KV_FP8_E4M3, PKV_KV_INT8, check
 
-_DTYPES = {"bf16": PKV_KV_BF16, "int8": PKV_KV_INT8}
+_DTYPES = {"bf16": PKV_KV_BF16, "int8": PKV_KV_INT8, "fp8": PKV_KV_FP8_E4M3}
+_CODE_DTYPES = {"bf16": torch.bfloat16, "int8": torch.int8, "fp8": torch.uint8}
 
 
 def _stream(stream) -> ctypes.c_void_p:
@@ -89,7 +90,8 @@ def pool_destroy(handle) -> None:
 
 class PagedKVPool:
     """A block pool ([num_blocks, kv_heads, 16, head_dim] K and V, plus fp32 scales for
-    INT8) allocated with torch on the current CUDA device, and its library descriptor."""
+    INT8 and FP8) allocated with torch on the current CUDA device, and its library
+    descriptor.  FP8 codes are held as uint8 (E4M3 bit patterns)."""
 
     def __init__(self, num_blocks: int, kv_heads: int, head_dim: int, dtype: str = "bf16",
                  device=None, fill=None):
@@ -98,11 +100,11 @@ class PagedKVPool:
         device = torch.device(device or "cuda")
         self.num_blocks, self.kv_heads, self.head_dim, self.dtype = num_blocks, kv_heads, head_dim, dtype
         shape = (num_blocks, kv_heads, BLOCK_SIZE, head_dim)
-        tdt = torch.bfloat16 if dtype == "bf16" else torch.int8
+        tdt = _CODE_DTYPES[dtype]
         self.k_cache = torch.empty(shape, dtype=tdt, device=device)
         self.v_cache = torch.empty(shape, dtype=tdt, device=device)
         self.k_scale = self.v_scale = None
-        if dtype == "int8":
+        if dtype != "bf16":
             self.k_scale = torch.empty(shape[:3], dtype=torch.float32, device=device)
             self.v_scale = torch.empty(shape[:3], dtype=torch.float32, device=device)
         if fill is not None:

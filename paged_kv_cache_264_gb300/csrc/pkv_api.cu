@@ -14,6 +14,7 @@
 namespace pkv {
 int ctas_per_sm_bf16(int head_dim, int group);
 int ctas_per_sm_int8(int head_dim, int group);
+int ctas_per_sm_fp8(int head_dim, int group);
 }  // namespace pkv
 
 struct pkv_pool {
@@ -45,6 +46,9 @@ pkv_status cuda_fail(cudaError_t e, const char* where) {
 }
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+bool valid_dtype(pkv_kv_dtype d) { return d == PKV_KV_BF16 || d == PKV_KV_INT8 || d == PKV_KV_FP8_E4M3; }
+bool scaled_dtype(pkv_kv_dtype d) { return d == PKV_KV_INT8 || d == PKV_KV_FP8_E4M3; }
 
 int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
 
@@ -150,7 +154,7 @@ PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
 // 128-byte spans, more than 2^31 rows, or no driver entry point).
 bool make_pool_tensor_map(CUtensorMap* map, void* base, pkv_kv_dtype dtype, int head_dim,
                           int64_t rows) {
-  const int esz = dtype == PKV_KV_INT8 ? 1 : 2;
+  const int esz = scaled_dtype(dtype) ? 1 : 2;
   if ((head_dim * esz) % 128 != 0 || rows >= (int64_t(1) << 31)) return false;
   auto encode = tensor_map_encoder();
   if (!encode) return false;
@@ -159,7 +163,7 @@ bool make_pool_tensor_map(CUtensorMap* map, void* base, pkv_kv_dtype dtype, int 
   const cuuint32_t box[2] = {cuuint32_t(128 / esz), cuuint32_t(pkv::kBlockSize)};
   const cuuint32_t elem_strides[2] = {1, 1};
   const CUresult r = encode(
-      map, dtype == PKV_KV_INT8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
+      map, scaled_dtype(dtype) ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
       2, base, dims, strides, box, elem_strides, CU_TENSOR_MAP_INTERLEAVE_NONE,
       CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
       CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
@@ -179,19 +183,21 @@ pkv_status check_decode_shape(const pkv_pool* pool, int num_seqs, int num_q_head
 
 namespace pkv {
 int decode_ctas_per_sm(KvType kv, int head_dim, int group) {
-  static int cache[2][2][9] = {};  // [dtype][head_dim 64/128][group]
+  static int cache[3][2][9] = {};  // [dtype][head_dim 64/128][group]
   const int di = head_dim == 128 ? 1 : 0;
-  const int ki = kv == KvType::kInt8 ? 1 : 0;
+  const int ki = static_cast<int>(kv);
   if (group < 1 || group > 8) return 0;
   int& slot = cache[ki][di][group];
   if (slot == 0)
-    slot = kv == KvType::kInt8 ? ctas_per_sm_int8(head_dim, group) : ctas_per_sm_bf16(head_dim, group);
+    slot = kv == KvType::kInt8  ? ctas_per_sm_int8(head_dim, group)
+           : kv == KvType::kFp8 ? ctas_per_sm_fp8(head_dim, group)
+                                : ctas_per_sm_bf16(head_dim, group);
   return slot;
 }
 
 int decode_block_bytes(KvType kv, int head_dim) {
-  const int esz = kv == KvType::kInt8 ? 1 : 2;
-  return 2 * kBlockSize * head_dim * esz + (kv == KvType::kInt8 ? 2 * kBlockSize * 4 : 0);
+  const bool scaled = kv != KvType::kBf16;
+  return 2 * kBlockSize * head_dim * (scaled ? 1 : 2) + (scaled ? 2 * kBlockSize * 4 : 0);
 }
 }  // namespace pkv
 
@@ -217,11 +223,11 @@ uint64_t pkv_launch_count(void) { return g_launches.load(std::memory_order_relax
 pkv_status pkv_pool_bytes(int64_t num_blocks, int kv_heads, int head_dim, pkv_kv_dtype dtype,
                           size_t* kv_bytes_each, size_t* scale_bytes_each) {
   if (num_blocks < 1 || kv_heads < 1 || head_dim < 1) return PKV_ERR_INVALID_ARG;
-  if (dtype != PKV_KV_BF16 && dtype != PKV_KV_INT8) return PKV_ERR_INVALID_ARG;
-  const size_t esz = dtype == PKV_KV_INT8 ? 1 : 2;
+  if (!valid_dtype(dtype)) return PKV_ERR_INVALID_ARG;
+  const size_t esz = scaled_dtype(dtype) ? 1 : 2;
   const size_t rows = size_t(num_blocks) * kv_heads * pkv::kBlockSize;
   if (kv_bytes_each) *kv_bytes_each = rows * head_dim * esz;
-  if (scale_bytes_each) *scale_bytes_each = dtype == PKV_KV_INT8 ? rows * sizeof(float) : 0;
+  if (scale_bytes_each) *scale_bytes_each = scaled_dtype(dtype) ? rows * sizeof(float) : 0;
   return PKV_OK;
 }
 
@@ -231,9 +237,9 @@ pkv_status pkv_pool_create(int64_t num_blocks, int kv_heads, int head_dim, int b
   if (!out) return PKV_ERR_INVALID_ARG;
   *out = nullptr;
   if (num_blocks < 1 || kv_heads < 1 || head_dim < 1) return PKV_ERR_INVALID_ARG;
-  if (dtype != PKV_KV_BF16 && dtype != PKV_KV_INT8) return PKV_ERR_INVALID_ARG;
+  if (!valid_dtype(dtype)) return PKV_ERR_INVALID_ARG;
   if (!k_cache || !v_cache || !aligned16(k_cache) || !aligned16(v_cache)) return PKV_ERR_INVALID_ARG;
-  if (dtype == PKV_KV_INT8) {
+  if (scaled_dtype(dtype)) {
     if (!k_scale || !v_scale || !aligned16(k_scale) || !aligned16(v_scale)) return PKV_ERR_INVALID_ARG;
   } else if (k_scale || v_scale) {
     return PKV_ERR_INVALID_ARG;
@@ -307,8 +313,9 @@ pkv_status pkv_reshape_and_cache(const pkv_pool* pool, const void* key, const vo
   p.kv_heads = pool->kv_heads;
   p.head_dim = pool->head_dim;
   auto s = static_cast<cudaStream_t>(stream);
-  cudaError_t e = pool->dtype == PKV_KV_INT8 ? pkv::launch_cache_int8(p, s)
-                                              : pkv::launch_cache_bf16(p, s);
+  cudaError_t e = pool->dtype == PKV_KV_INT8     ? pkv::launch_cache_int8(p, s)
+                   : pool->dtype == PKV_KV_FP8_E4M3 ? pkv::launch_cache_fp8(p, s)
+                                                    : pkv::launch_cache_bf16(p, s);
   if (e != cudaSuccess) return cuda_fail(e, "reshape_and_cache launch");
   g_launches.fetch_add(1, std::memory_order_relaxed);
   return PKV_OK;
@@ -404,8 +411,9 @@ pkv_status pkv_paged_attention_decode_ex(const pkv_pool* pool, const void* q,
     e = pkv::launch_decode_mma(p, &pool->tmap_k, &pool->tmap_v,
                                static_cast<pkv::KvType>(pool->dtype), group, plan.shape, s);
   else
-    e = pool->dtype == PKV_KV_INT8 ? pkv::launch_decode_int8(p, group, s)
-                                   : pkv::launch_decode_bf16(p, group, s);
+    e = pool->dtype == PKV_KV_INT8       ? pkv::launch_decode_int8(p, group, s)
+        : pool->dtype == PKV_KV_FP8_E4M3 ? pkv::launch_decode_fp8(p, group, s)
+                                         : pkv::launch_decode_bf16(p, group, s);
   if (e != cudaSuccess) return cuda_fail(e, "paged_attention_decode launch");
   g_launches.fetch_add(1, std::memory_order_relaxed);
   if (plan.max_parts > 1) {

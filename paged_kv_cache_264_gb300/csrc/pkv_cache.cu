@@ -10,6 +10,8 @@
 // s = max|x| / 127 with IEEE fp32 division, code = round-half-even(x / s), clamped to
 // [-127, 127]; the codes of one row are stored as one coalesced 32-lane write, and the
 // scale next to them in the [num_blocks, Hkv, 16] scale array.
+// FP8 pool (the same section names FP8 KV caches): the same with s = max|x| / 448 and the
+// code the nearest E4M3 of x / s (ties to even, saturating at +-448).
 #include <cuda_bf16.h>
 
 #include "pkv_device.cuh"
@@ -50,35 +52,41 @@ __global__ void __launch_bounds__(kCacheThreads)
 }
 
 // Quantise the D values of one row held by a warp (DPV = D / 32 per lane) and return the
-// lane's packed codes.  *scale receives s on every lane.
-template <int DPV>
+// lane's packed codes (INT8, or E4M3 when kFp8).  *scale receives s on every lane.
+template <int DPV, bool kFp8>
 __device__ __forceinline__ uint32_t quantise_row(const float (&x)[DPV], float* scale) {
   float amax = 0.0f;
 #pragma unroll
   for (int i = 0; i < DPV; ++i) amax = fmaxf(amax, fabsf(x[i]));
 #pragma unroll
   for (int o = 16; o >= 1; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
-  const float s = __fdiv_rn(amax, 127.0f);
+  const float s = __fdiv_rn(amax, kFp8 ? 448.0f : 127.0f);
   *scale = s;
-  uint32_t packed = 0;
+  if (amax == 0.0f) return 0u;
+  if constexpr (kFp8) {
+    uint32_t packed = 0;
 #pragma unroll
-  for (int i = 0; i < DPV; ++i) {
-    int code = 0;
-    if (amax != 0.0f) {
-      code = __float2int_rn(__fdiv_rn(x[i], s));
+    for (int i = 0; i < DPV; i += 2)
+      packed |= e4m3x2_from_f32(__fdiv_rn(x[i], s), __fdiv_rn(x[i + 1], s)) << (8 * i);
+    return packed;
+  } else {
+    uint32_t packed = 0;
+#pragma unroll
+    for (int i = 0; i < DPV; ++i) {
+      int code = __float2int_rn(__fdiv_rn(x[i], s));
       code = min(127, max(-127, code));
+      packed |= (static_cast<uint32_t>(code) & 0xffu) << (8 * i);
     }
-    packed |= (static_cast<uint32_t>(code) & 0xffu) << (8 * i);
+    return packed;
   }
-  return packed;
 }
 
-template <int D>
+template <int D, bool kFp8>
 __global__ void __launch_bounds__(kCacheThreads)
-    cache_int8_kernel(const __nv_bfloat16* __restrict__ key,
+    cache_quant_kernel(const __nv_bfloat16* __restrict__ key,
                       const __nv_bfloat16* __restrict__ value,
-                      const int32_t* __restrict__ slot_mapping, int8_t* __restrict__ k_cache,
-                      int8_t* __restrict__ v_cache, float* __restrict__ k_scale,
+                      const int32_t* __restrict__ slot_mapping, uint8_t* __restrict__ k_cache,
+                      uint8_t* __restrict__ v_cache, float* __restrict__ k_scale,
                       float* __restrict__ v_scale, uint32_t* err, int64_t num_tokens,
                       int64_t num_slots, int kv_heads) {
   constexpr int DPV = D / 32;  // values per lane: 4 (D=128) or 2 (D=64)
@@ -115,8 +123,8 @@ __global__ void __launch_bounds__(kCacheThreads)
       vx[0] = bf16lo(vw); vx[1] = bf16hi(vw);
     }
     float ks, vs;
-    const uint32_t kq = quantise_row<DPV>(kx, &ks);
-    const uint32_t vq = quantise_row<DPV>(vx, &vs);
+    const uint32_t kq = quantise_row<DPV, kFp8>(kx, &ks);
+    const uint32_t vq = quantise_row<DPV, kFp8>(vx, &vs);
     const int64_t dst = srow * D + lane * DPV;
     if constexpr (DPV == 4) {
       *reinterpret_cast<uint32_t*>(k_cache + dst) = kq;
@@ -152,22 +160,31 @@ cudaError_t launch_cache_bf16(const CacheParams& p, cudaStream_t stream) {
                     p.err, p.num_tokens, p.num_blocks * kBlockSize, p.kv_heads, chunks);
 }
 
-cudaError_t launch_cache_int8(const CacheParams& p, cudaStream_t stream) {
+template <bool kFp8>
+static cudaError_t launch_cache_quant(const CacheParams& p, cudaStream_t stream) {
   const int64_t rows = p.num_tokens * p.kv_heads;
   const int grid = grid_for(rows, kCacheThreads / 32);
   const auto* key = static_cast<const __nv_bfloat16*>(p.key);
   const auto* value = static_cast<const __nv_bfloat16*>(p.value);
-  auto* kc = static_cast<int8_t*>(p.k_cache);
-  auto* vc = static_cast<int8_t*>(p.v_cache);
+  auto* kc = static_cast<uint8_t*>(p.k_cache);
+  auto* vc = static_cast<uint8_t*>(p.v_cache);
   if (p.head_dim == 128)
-    return launch_pdl(cache_int8_kernel<128>, dim3(grid), dim3(kCacheThreads), 0, stream, key, value,
-                      p.slot_mapping, kc, vc, p.k_scale, p.v_scale, p.err, p.num_tokens,
+    return launch_pdl(cache_quant_kernel<128, kFp8>, dim3(grid), dim3(kCacheThreads), 0, stream, key,
+                      value, p.slot_mapping, kc, vc, p.k_scale, p.v_scale, p.err, p.num_tokens,
                       p.num_blocks * kBlockSize, p.kv_heads);
   if (p.head_dim == 64)
-    return launch_pdl(cache_int8_kernel<64>, dim3(grid), dim3(kCacheThreads), 0, stream, key, value,
-                      p.slot_mapping, kc, vc, p.k_scale, p.v_scale, p.err, p.num_tokens,
+    return launch_pdl(cache_quant_kernel<64, kFp8>, dim3(grid), dim3(kCacheThreads), 0, stream, key,
+                      value, p.slot_mapping, kc, vc, p.k_scale, p.v_scale, p.err, p.num_tokens,
                       p.num_blocks * kBlockSize, p.kv_heads);
   return cudaErrorInvalidValue;
+}
+
+cudaError_t launch_cache_int8(const CacheParams& p, cudaStream_t stream) {
+  return launch_cache_quant<false>(p, stream);
+}
+
+cudaError_t launch_cache_fp8(const CacheParams& p, cudaStream_t stream) {
+  return launch_cache_quant<true>(p, stream);
 }
 
 }  // namespace pkv

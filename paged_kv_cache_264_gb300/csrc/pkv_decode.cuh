@@ -31,6 +31,7 @@
 //
 // INT8 pools: logit = (scale * log2 e) * s_K[t] * sum_c q_c code_c, and the PV weight of
 // token t is p_t * s_V[t]; codes are widened to fp32 exactly (see i8_from_flipped).
+// FP8 (E4M3) pools work the same way with the hardware E4M3 -> fp16 conversion.
 //
 // Masking: tokens t >= T_b of the last block get logit -inf and are excluded from the
 // PV loop, so whatever bytes sit in unused slots are never used.  Block ids outside
@@ -58,6 +59,23 @@ struct KvTraits<KvType::kInt8> {
   static constexpr int kElemBytes = 1;
   static constexpr bool kQuant = true;
 };
+template <>
+struct KvTraits<KvType::kFp8> {
+  static constexpr int kElemBytes = 1;
+  static constexpr bool kQuant = true;
+};
+
+// Four 1-byte codes of a word -> fp32 values (INT8 or E4M3), exactly.
+template <KvType KV>
+__device__ __forceinline__ void dequant4(uint32_t w, float (&f)[4]) {
+  if constexpr (KV == KvType::kFp8) {
+    e4m3x4_to_f32(w, f);
+  } else {
+    const uint32_t u = w ^ 0x80808080u;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) f[i] = i8_from_flipped(u, i);
+  }
+}
 
 constexpr size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
@@ -142,15 +160,15 @@ __device__ __forceinline__ void fma_bf16x8(float (&part)[G], const float (&qr)[G
   }
 }
 
-template <int G, int NQ>
-__device__ __forceinline__ void fma_i8x4(float (&part)[G], const float (&qr)[G][NQ], int base,
-                                         uint32_t w) {
-  const uint32_t u = w ^ 0x80808080u;
+template <KvType KV, int G, int NQ>
+__device__ __forceinline__ void fma_code4(float (&part)[G], const float (&qr)[G][NQ], int base,
+                                          uint32_t w) {
+  float k[4];
+  dequant4<KV>(w, k);
 #pragma unroll
   for (int i = 0; i < 4; ++i) {
-    const float k = i8_from_flipped(u, i);
 #pragma unroll
-    for (int g = 0; g < G; ++g) part[g] = fmaf(qr[g][base + i], k, part[g]);
+    for (int g = 0; g < G; ++g) part[g] = fmaf(qr[g][base + i], k[i], part[g]);
   }
 }
 
@@ -474,14 +492,14 @@ __global__ void __launch_bounds__(NW * 32)
                                    *reinterpret_cast<const uint4*>(row + 16 * (h ^ sw)));
         } else if constexpr (C::kDPL == 16) {
           const uint4 w = *reinterpret_cast<const uint4*>(row);
-          fma_i8x4<G, C::kDPL>(part_g, qr, 0, w.x);
-          fma_i8x4<G, C::kDPL>(part_g, qr, 4, w.y);
-          fma_i8x4<G, C::kDPL>(part_g, qr, 8, w.z);
-          fma_i8x4<G, C::kDPL>(part_g, qr, 12, w.w);
+          fma_code4<KV, G, C::kDPL>(part_g, qr, 0, w.x);
+          fma_code4<KV, G, C::kDPL>(part_g, qr, 4, w.y);
+          fma_code4<KV, G, C::kDPL>(part_g, qr, 8, w.z);
+          fma_code4<KV, G, C::kDPL>(part_g, qr, 12, w.w);
         } else {
           const uint2 w = *reinterpret_cast<const uint2*>(row);
-          fma_i8x4<G, C::kDPL>(part_g, qr, 0, w.x);
-          fma_i8x4<G, C::kDPL>(part_g, qr, 4, w.y);
+          fma_code4<KV, G, C::kDPL>(part_g, qr, 0, w.x);
+          fma_code4<KV, G, C::kDPL>(part_g, qr, 4, w.y);
         }
         HeadReduce<G, C::kLPT / 2>::run(part_g, lane);
         float logit = part_g[0];
@@ -546,13 +564,12 @@ __global__ void __launch_bounds__(NW * 32)
           const uint32_t w = *reinterpret_cast<const uint32_t*>(vrow);
           vf[0] = bf16lo(w); vf[1] = bf16hi(w);
         } else if constexpr (C::kDPV == 4) {
-          const uint32_t u = *reinterpret_cast<const uint32_t*>(vrow) ^ 0x80808080u;
-#pragma unroll
-          for (int i = 0; i < 4; ++i) vf[i] = i8_from_flipped(u, i);
+          dequant4<KV>(*reinterpret_cast<const uint32_t*>(vrow), vf);
         } else {
-          const uint32_t u = uint32_t(*reinterpret_cast<const uint16_t*>(vrow)) ^ 0x8080u;
-          vf[0] = i8_from_flipped(u, 0);
-          vf[1] = i8_from_flipped(u, 1);
+          float v4[4];
+          dequant4<KV>(uint32_t(*reinterpret_cast<const uint16_t*>(vrow)), v4);
+          vf[0] = v4[0];
+          vf[1] = v4[1];
         }
 #pragma unroll
         for (int g = 0; g < G; ++g)

@@ -14,16 +14,16 @@ struct RingShape {
 
 static const RingShape kShapesBf16D128[] = {{2, 1}, {3, 1}};
 static const RingShape kShapesBf16D64[] = {{3, 1}, {2, 2}};
-static const RingShape kShapesInt8[] = {{3, 1}, {2, 2}, {3, 2}};
+static const RingShape kShapesInt8[] = {{3, 1}, {2, 2}, {3, 2}};  // INT8 and FP8
 
 bool mma_supported(KvType kv, int head_dim, int group) {
   if (group != 2 && group != 4 && group != 8) return false;
   if (kv == KvType::kBf16) return head_dim == 128 || head_dim == 64;
-  return head_dim == 128;
+  return head_dim == 128;  // INT8, FP8
 }
 
 static int shapes_of(KvType kv, int head_dim, const RingShape** out) {
-  if (kv == KvType::kInt8) { *out = kShapesInt8; return 3; }
+  if (kv != KvType::kBf16) { *out = kShapesInt8; return 3; }
   if (head_dim == 128) { *out = kShapesBf16D128; return 2; }
   *out = kShapesBf16D64;
   return 2;
@@ -59,6 +59,12 @@ cudaError_t launch_decode_mma(const DecodeParams& p, const CUtensorMap* tk, cons
       case 1: return dispatch_g<KvType::kInt8, 128, 2, 2>(p, *tk, *tv, group, stream);
       case 2: return dispatch_g<KvType::kInt8, 128, 3, 2>(p, *tk, *tv, group, stream);
     }
+  } else if (kv == KvType::kFp8) {
+    switch (shape) {
+      case 0: return dispatch_g<KvType::kFp8, 128, 3, 1>(p, *tk, *tv, group, stream);
+      case 1: return dispatch_g<KvType::kFp8, 128, 2, 2>(p, *tk, *tv, group, stream);
+      case 2: return dispatch_g<KvType::kFp8, 128, 3, 2>(p, *tk, *tv, group, stream);
+    }
   } else if (p.head_dim == 128) {
     switch (shape) {
       case 0: return dispatch_g<KvType::kBf16, 128, 2, 1>(p, *tk, *tv, group, stream);
@@ -85,8 +91,8 @@ static int occupancy(int group) {
 
 int mma_ctas_per_sm(KvType kv, int head_dim, int group, int shape) {
   if (!mma_supported(kv, head_dim, group) || shape < 0 || shape > 2) return 0;
-  static int cache[3][3][9] = {};  // [pool type][shape][group]
-  const int ti = kv == KvType::kInt8 ? 2 : (head_dim == 128 ? 0 : 1);
+  static int cache[4][3][9] = {};  // [pool type][shape][group]
+  const int ti = kv == KvType::kFp8 ? 3 : kv == KvType::kInt8 ? 2 : (head_dim == 128 ? 0 : 1);
   int& slot = cache[ti][shape][group];
   if (slot) return slot;
   int n = 0;
@@ -94,6 +100,10 @@ int mma_ctas_per_sm(KvType kv, int head_dim, int group, int shape) {
     n = shape == 0 ? occupancy<KvType::kInt8, 128, 3, 1>(group)
       : shape == 1 ? occupancy<KvType::kInt8, 128, 2, 2>(group)
                    : occupancy<KvType::kInt8, 128, 3, 2>(group);
+  } else if (kv == KvType::kFp8) {
+    n = shape == 0 ? occupancy<KvType::kFp8, 128, 3, 1>(group)
+      : shape == 1 ? occupancy<KvType::kFp8, 128, 2, 2>(group)
+                   : occupancy<KvType::kFp8, 128, 3, 2>(group);
   } else if (head_dim == 128) {
     n = shape == 0 ? occupancy<KvType::kBf16, 128, 2, 1>(group) : occupancy<KvType::kBf16, 128, 3, 1>(group);
   } else {

@@ -22,7 +22,8 @@
 //    1152 * sum_d q_d per head, and from O^T as 1152 times the running sum of P per head.  q is scaled by a power of two into fp16 range (exact for bf16 values), the
 //    K scale multiplies the fp32 logits, and the V scale is folded into P together with a
 //    power-of-two block exponent that keeps P in [0, 2): O^T is kept in units of 2^E and E
-//    only grows, like the running max, so the rescale stays rare.  Within one k-step the
+//    only grows, like the running max, so the rescale stays rare.  FP8 (E4M3) pools take
+//    the same path with the hardware E4M3 -> fp16 conversion and no offset.  Within one k-step the
 //    dims a lane handles are permuted (the same permutation on K and q), which lets each
 //    lane read its codes with 16-byte loads.
 #pragma once
@@ -37,6 +38,7 @@ template <KvType KV, int D, int G, int NW, int S, int BPS>
 struct MmaCfg {
   static constexpr int kEsz = KvTraits<KV>::kElemBytes;
   static constexpr bool kQuant = KvTraits<KV>::kQuant;
+  static constexpr bool kFp8 = KV == KvType::kFp8;     // E4M3 codes (else INT8 when kQuant)
   static constexpr int kRowBytes = D * kEsz;           // one token row of one tile
   static constexpr int kBoxCols = 128 / kEsz;          // elements in a 128-byte box row
   static constexpr int kBoxes = kRowBytes / 128;       // boxes per tile
@@ -57,7 +59,7 @@ struct MmaCfg {
   }
 
   static_assert(kRowBytes % 128 == 0, "rows must be whole 128-byte swizzle spans");
-  static_assert(!kQuant || D == 128, "INT8 tensor-core path is built for head_dim 128");
+  static_assert(!kQuant || D == 128, "INT8/FP8 tensor-core path is built for head_dim 128");
   static_assert(G == 2 || G == 4 || G == 8, "group of 2, 4 or 8 query heads");
   static_assert(BPS == 1 || BPS == 2, "one or two blocks per ring stage");
   static_assert(size_t(G) * (D + 2) * 4 <= size_t(S) * kStageBytes, "merge record fits the ring");
@@ -206,8 +208,8 @@ __global__ void __launch_bounds__(NW * 32)
           qf[s][0] = qf[s][1] = 0u;
         }
       }
-      // K codes enter the product as 1152 + code: S' = S + 1152 * sum_d q_d.  Sum the fp16
-      // values exactly as the MMA sees them, per head, and fold in the logit factor.
+      // INT8 K codes enter the product as 1152 + code: S' = S + 1152 * sum_d q_d.  Sum the
+      // fp16 values exactly as the MMA sees them, per head.
       float qsum = 0.0f;
 #pragma unroll
       for (int s = 0; s < C::kKSteps; ++s) {
@@ -217,8 +219,10 @@ __global__ void __launch_bounds__(NW * 32)
       }
       qsum += __shfl_xor_sync(kFull, qsum, 1);
       qsum += __shfl_xor_sync(kFull, qsum, 2);  // lanes of row gi now hold head gi's sum
-      kbias0 = 1152.0f * __shfl_sync(kFull, qsum, 4 * (2 * gj));
-      kbias1 = 1152.0f * __shfl_sync(kFull, qsum, 4 * (2 * gj + 1));
+      if constexpr (!C::kFp8) {
+        kbias0 = 1152.0f * __shfl_sync(kFull, qsum, 4 * (2 * gj));
+        kbias1 = 1152.0f * __shfl_sync(kFull, qsum, 4 * (2 * gj + 1));
+      }
     }
   }
 
@@ -294,9 +298,17 @@ __global__ void __launch_bounds__(NW * 32)
           const uint32_t wb[8] = {y0.x, y0.y, y0.z, y0.w, y1.x, y1.y, y1.z, y1.w};
 #pragma unroll
           for (int s2 = 0; s2 < 8; ++s2) {
-            const uint32_t ua = wa[s2] ^ 0x80808080u, ub = wb[s2] ^ 0x80808080u;
-            const uint32_t a[4] = {f16x2_biased(ua, 0x4140u), f16x2_biased(ub, 0x4140u),
-                                   f16x2_biased(ua, 0x4342u), f16x2_biased(ub, 0x4342u)};
+            uint32_t a[4];
+            if constexpr (C::kFp8) {
+              f16x2x2_from_e4m3x4(wa[s2], a[0], a[2]);
+              f16x2x2_from_e4m3x4(wb[s2], a[1], a[3]);
+            } else {
+              const uint32_t ua = wa[s2] ^ 0x80808080u, ub = wb[s2] ^ 0x80808080u;
+              a[0] = f16x2_biased(ua, 0x4140u);
+              a[1] = f16x2_biased(ub, 0x4140u);
+              a[2] = f16x2_biased(ua, 0x4342u);
+              a[3] = f16x2_biased(ub, 0x4342u);
+            }
             mma_f16_16816((s2 & 1) ? acc2 : sacc[j], a, qf[s2][0], qf[s2][1]);
           }
         }
@@ -422,24 +434,39 @@ __global__ void __launch_bounds__(NW * 32)
             mma_bf16_16816(o[t], a, pb0, pb1);
           }
         } else {
-          // INT8 codes are always finite, and masked tokens have a zero weight in P.
+          // INT8 codes are always finite and masked tokens have a zero weight in P; E4M3 has
+          // NaN codes, so an FP8 block's tail tokens are zeroed in the fragment as for bf16.
           // Lane (gi, gj) reads dims 16gi..16gi+15 of tokens 2gj, 2gj+1, 2gj+8, 2gj+9; m-tile
           // t row gi is dim 16gi+2t and row gi+8 is dim 16gi+2t+1.
           const uint4 va = *reinterpret_cast<const uint4*>(vtp + voff[0]);
           const uint4 vb = *reinterpret_cast<const uint4*>(vtp + voff[1]);
           const uint4 vc = *reinterpret_cast<const uint4*>(vtp + voff[2]);
           const uint4 vd = *reinterpret_cast<const uint4*>(vtp + voff[3]);
-          const uint32_t wa[4] = {va.x ^ 0x80808080u, va.y ^ 0x80808080u, va.z ^ 0x80808080u, va.w ^ 0x80808080u};
-          const uint32_t wb[4] = {vb.x ^ 0x80808080u, vb.y ^ 0x80808080u, vb.z ^ 0x80808080u, vb.w ^ 0x80808080u};
-          const uint32_t wc[4] = {vc.x ^ 0x80808080u, vc.y ^ 0x80808080u, vc.z ^ 0x80808080u, vc.w ^ 0x80808080u};
-          const uint32_t wd[4] = {vd.x ^ 0x80808080u, vd.y ^ 0x80808080u, vd.z ^ 0x80808080u, vd.w ^ 0x80808080u};
+          constexpr uint32_t kFlip = C::kFp8 ? 0u : 0x80808080u;
+          const uint32_t mlo8 = (2 * gj < vt[j] ? 0x0000ffffu : 0u) | (2 * gj + 1 < vt[j] ? 0xffff0000u : 0u);
+          const uint32_t mhi8 = (2 * gj + 8 < vt[j] ? 0x0000ffffu : 0u) | (2 * gj + 9 < vt[j] ? 0xffff0000u : 0u);
+          const uint32_t wa[4] = {va.x ^ kFlip, va.y ^ kFlip, va.z ^ kFlip, va.w ^ kFlip};
+          const uint32_t wb[4] = {vb.x ^ kFlip, vb.y ^ kFlip, vb.z ^ kFlip, vb.w ^ kFlip};
+          const uint32_t wc[4] = {vc.x ^ kFlip, vc.y ^ kFlip, vc.z ^ kFlip, vc.w ^ kFlip};
+          const uint32_t wd[4] = {vd.x ^ kFlip, vd.y ^ kFlip, vd.z ^ kFlip, vd.w ^ kFlip};
 #pragma unroll
           for (int t = 0; t < C::kMTiles; ++t) {
             const uint32_t sel = (t & 1) ? 0x7362u : 0x5140u;  // interleave the two tokens' bytes
             const uint32_t ab = __byte_perm(wa[t >> 1], wb[t >> 1], sel);
             const uint32_t cd = __byte_perm(wc[t >> 1], wd[t >> 1], sel);
-            const uint32_t a[4] = {f16x2_biased(ab, 0x4140u), f16x2_biased(ab, 0x4342u),
-                                   f16x2_biased(cd, 0x4140u), f16x2_biased(cd, 0x4342u)};
+            uint32_t a[4];
+            if constexpr (C::kFp8) {
+              f16x2x2_from_e4m3x4(ab, a[0], a[1]);
+              f16x2x2_from_e4m3x4(cd, a[2], a[3]);
+              if (vt[j] < kBlockSize) {
+                a[0] &= mlo8; a[1] &= mlo8; a[2] &= mhi8; a[3] &= mhi8;
+              }
+            } else {
+              a[0] = f16x2_biased(ab, 0x4140u);
+              a[1] = f16x2_biased(ab, 0x4342u);
+              a[2] = f16x2_biased(cd, 0x4140u);
+              a[3] = f16x2_biased(cd, 0x4342u);
+            }
             mma_f16_16816(o[t], a, pb0, pb1);
           }
         }
@@ -470,16 +497,18 @@ __global__ void __launch_bounds__(NW * 32)
   float oscale = 1.0f;
   if constexpr (C::kQuant) {
     oscale = e_run == INT_MIN ? 0.0f : pow2i(max(-126, e_run));
-    // V codes entered as 1152 + code: O'^T = O^T + 1152 * sum_t P'_t for every dim.
+    if constexpr (!C::kFp8) {
+      // INT8 V codes entered as 1152 + code: O'^T = O^T + 1152 * sum_t P'_t for every dim.
 #pragma unroll
-    for (int ofs = 4; ofs < 32; ofs <<= 1) {
-      ptot0 += __shfl_xor_sync(kFull, ptot0, ofs);
-      ptot1 += __shfl_xor_sync(kFull, ptot1, ofs);
-    }
+      for (int ofs = 4; ofs < 32; ofs <<= 1) {
+        ptot0 += __shfl_xor_sync(kFull, ptot0, ofs);
+        ptot1 += __shfl_xor_sync(kFull, ptot1, ofs);
+      }
 #pragma unroll
-    for (int t = 0; t < C::kMTiles; ++t) {
-      o[t][0] -= 1152.0f * ptot0; o[t][1] -= 1152.0f * ptot1;
-      o[t][2] -= 1152.0f * ptot0; o[t][3] -= 1152.0f * ptot1;
+      for (int t = 0; t < C::kMTiles; ++t) {
+        o[t][0] -= 1152.0f * ptot0; o[t][1] -= 1152.0f * ptot1;
+        o[t][2] -= 1152.0f * ptot0; o[t][3] -= 1152.0f * ptot1;
+      }
     }
   }
   float* rec = reinterpret_cast<float*>(ring);

@@ -18,7 +18,7 @@ constexpr uint32_t kErrContextLen = 0x2u;
 constexpr uint32_t kErrSlot = 0x4u;
 constexpr uint32_t kErrTimeout = 0x8u;
 
-enum class KvType : int { kBf16 = 0, kInt8 = 1 };
+enum class KvType : int { kBf16 = 0, kInt8 = 1, kFp8 = 2 };
 
 struct CacheParams {
   const void* key;              // bf16 [N, Hkv, D]
@@ -83,8 +83,10 @@ cudaError_t launch_pdl(void (*kernel)(Params...), dim3 grid, dim3 block, size_t 
 // Kernel launchers (defined next to their kernels).  Each returns the launch status.
 cudaError_t launch_cache_bf16(const CacheParams& p, cudaStream_t stream);
 cudaError_t launch_cache_int8(const CacheParams& p, cudaStream_t stream);
+cudaError_t launch_cache_fp8(const CacheParams& p, cudaStream_t stream);
 cudaError_t launch_decode_bf16(const DecodeParams& p, int group, cudaStream_t stream);
 cudaError_t launch_decode_int8(const DecodeParams& p, int group, cudaStream_t stream);
+cudaError_t launch_decode_fp8(const DecodeParams& p, int group, cudaStream_t stream);
 cudaError_t launch_lse_reduce(const DecodeParams& p, cudaStream_t stream);
 
 // Tensor-core decode (GQA groups 2/4/8): tk/tv are 2-D tensor maps of the K and V pools

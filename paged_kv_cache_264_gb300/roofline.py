@@ -42,7 +42,7 @@ def step_bytes(context_lens, num_q_heads: int, num_kv_heads: int, head_dim: int,
     sum_nb = int(((lens + BLOCK - 1) // BLOCK).sum())
     esz = 2 if kv_dtype == "bf16" else 1
     kv = 2 * sum_t * num_kv_heads * head_dim * esz
-    if kv_dtype == "int8":
+    if kv_dtype in ("int8", "fp8"):
         kv += 2 * sum_t * num_kv_heads * 4
     q_out = 2 * b * num_q_heads * head_dim * 2
     tables = 4 * (sum_nb + b)
@@ -50,7 +50,7 @@ def step_bytes(context_lens, num_q_heads: int, num_kv_heads: int, head_dim: int,
     if append:
         app = 2 * b * num_kv_heads * head_dim * 2          # new K and V rows (bf16) read
         app += 2 * b * num_kv_heads * head_dim * esz       # cached rows written
-        if kv_dtype == "int8":
+        if kv_dtype in ("int8", "fp8"):
             app += 2 * b * num_kv_heads * 4                # scales written
         app += 4 * b                                       # slot_mapping read
     flops = 4 * sum_t * num_q_heads * head_dim

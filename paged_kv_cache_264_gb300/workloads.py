@@ -19,11 +19,12 @@ llama3_8b_gqa    128   uniform [512, 8192]              32/8     128   bf16
 long_32k         8     32768 each                       32/32    128   bf16   1% key chans x8
 int8_cb          256   lognormal(ln 1024, 1) in         32/8     128   int8
                        [16, 16384]
+fp8_cb           256   as int8_cb                       32/8     128   fp8
 ===============  ====  ===============================  =======  ====  =====  ================
 
 Pools other than ``tiny`` hold ``ceil(1.25 * sum_b ceil(T_b / 16))`` blocks; the blocks
 that sequences use are drawn from a seeded permutation of the pool.  Everything is drawn
-from ``torch.Generator`` seeded with ``1000 + index`` of the workload (1 .. 5).  Values
+from ``torch.Generator`` seeded with ``1000 + index`` of the workload (1 .. 6).  Values
 are drawn per sequence from a generator seeded by (workload seed, sequence), so any
 subset of sequences can be regenerated alone.
 """
@@ -47,7 +48,7 @@ class Spec:
     num_q_heads: int
     num_kv_heads: int
     head_dim: int
-    kv_dtype: str  # "bf16" | "int8"
+    kv_dtype: str  # "bf16" | "int8" | "fp8"
     lens: tuple  # ("fixed", [..]) | ("uniform", lo, hi) | ("lognormal", median, sigma, lo, hi) | ("const", n)
     pool_blocks: int | None = None  # None: ceil(1.25 * blocks needed)
     outlier_key_channel_frac: float = 0.0
@@ -75,6 +76,9 @@ SPECS: dict[str, Spec] = {
         Spec("int8_cb", 5, "continuous-batching decode step with INT8 KV: 256 sequences, "
              "context_lens lognormal (median 1024, sigma 1) clipped to [16, 16384], 32/8 heads, "
              "head_dim 128", 256, 32, 8, 128, "int8", ("lognormal", 1024.0, 1.0, 16, 16384)),
+        Spec("fp8_cb", 6, "continuous-batching decode step with FP8 (E4M3) KV: the int8_cb batch "
+             "shape with E4M3 codes and per-(token, head) scales", 256, 32, 8, 128, "fp8",
+             ("lognormal", 1024.0, 1.0, 16, 16384)),
     )
 }
 

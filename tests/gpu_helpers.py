@@ -22,8 +22,9 @@ def fill_pool_garbage(pool: pkv.PagedKVPool) -> None:
         pool.k_cache.view(torch.int16).fill_(BF16_NAN)
         pool.v_cache.view(torch.int16).fill_(BF16_NAN)
     else:
-        pool.k_cache.fill_(127)
-        pool.v_cache.fill_(127)
+        code = 127 if pool.dtype == "int8" else 0x7F  # 0x7F is an E4M3 NaN
+        pool.k_cache.fill_(code)
+        pool.v_cache.fill_(code)
         pool.k_scale.fill_(float("nan"))
         pool.v_scale.fill_(float("nan"))
 
@@ -97,9 +98,11 @@ def oracle_decode(w: W.Workload, kv: str, seqs=None, o=None):
         out = o.paged_decode(c["q"], kc, vc, c["tables"], c["lens"], w.scale)
         pool = dict(k_cache=kc, v_cache=vc)
     else:
-        kc, vc = np.zeros(shape, np.int8), np.zeros(shape, np.int8)
+        cdt = np.int8 if kv == "int8" else np.uint8
+        kc, vc = np.zeros(shape, cdt), np.zeros(shape, cdt)
         ks, vs = np.zeros(shape[:3], np.float32), np.zeros(shape[:3], np.float32)
-        o.reshape_and_cache_int8(c["key"], c["value"], c["slots"], kc, vc, ks, vs)
+        write = o.reshape_and_cache_int8 if kv == "int8" else o.reshape_and_cache_fp8
+        write(c["key"], c["value"], c["slots"], kc, vc, ks, vs)
         out = o.paged_decode(c["q"], kc, vc, c["tables"], c["lens"], w.scale, ks, vs)
         pool = dict(k_cache=kc, v_cache=vc, k_scale=ks, v_scale=vs)
     return out, pool, c
@@ -118,7 +121,7 @@ def gpu_pool_blocks(pool: pkv.PagedKVPool, tables: np.ndarray, lens: np.ndarray)
         return t.view(torch.int16).numpy().view(np.uint16) if t.dtype == torch.bfloat16 else t.numpy()
 
     res = dict(k_cache=host(pool.k_cache), v_cache=host(pool.v_cache))
-    if pool.dtype == "int8":
+    if pool.dtype != "bf16":
         res.update(k_scale=host(pool.k_scale), v_scale=host(pool.v_scale))
     return res
 

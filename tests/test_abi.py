@@ -54,6 +54,8 @@ def test_pool_bytes(lib):
     assert kv.value == 10 * 8 * 16 * 128 * 2 and sc.value == 0
     assert lib.pkv_pool_bytes(10, 8, 128, _lib.PKV_KV_INT8, ctypes.byref(kv), ctypes.byref(sc)) == 0
     assert kv.value == 10 * 8 * 16 * 128 and sc.value == 10 * 8 * 16 * 4
+    assert lib.pkv_pool_bytes(10, 8, 128, _lib.PKV_KV_FP8_E4M3, ctypes.byref(kv), ctypes.byref(sc)) == 0
+    assert kv.value == 10 * 8 * 16 * 128 and sc.value == 10 * 8 * 16 * 4
     assert lib.pkv_pool_bytes(0, 8, 128, 0, None, None) == _lib.PKV_ERR_INVALID_ARG
     assert lib.pkv_pool_bytes(10, 8, 128, 7, None, None) == _lib.PKV_ERR_INVALID_ARG
 
@@ -68,6 +70,8 @@ ODD = ctypes.c_void_p(0x100008)
     ((4, 8, 128, 16, 0, ODD, FAKE, None, None), _lib.PKV_ERR_INVALID_ARG),    # misaligned K
     ((4, 8, 128, 16, 0, FAKE, FAKE, FAKE, FAKE), _lib.PKV_ERR_INVALID_ARG),   # scales on bf16
     ((4, 8, 128, 16, 1, FAKE, FAKE, None, None), _lib.PKV_ERR_INVALID_ARG),   # int8 without scales
+    ((4, 8, 128, 16, 2, FAKE, FAKE, None, None), _lib.PKV_ERR_INVALID_ARG),   # fp8 without scales
+    ((4, 8, 128, 16, 3, FAKE, FAKE, None, None), _lib.PKV_ERR_INVALID_ARG),   # unknown dtype
     ((4, 8, 96, 16, 0, FAKE, FAKE, None, None), _lib.PKV_ERR_UNSUPPORTED),    # head_dim 96
     ((4, 8, 128, 32, 0, FAKE, FAKE, None, None), _lib.PKV_ERR_UNSUPPORTED),   # block size 32
 ])

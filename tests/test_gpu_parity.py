@@ -68,7 +68,7 @@ def check_all(w, kv, partition_blocks=0, seqs=None, kernel=0, output_rounding=Fa
 
 # ------------------------------------------------------------ small shapes
 
-@pytest.mark.parametrize("kv", ["bf16", "int8"])
+@pytest.mark.parametrize("kv", ["bf16", "int8", "fp8"])
 def test_tiny_workload(kv):
     w = W.make("tiny")
     check_all(w, kv)
@@ -86,7 +86,7 @@ SHAPES = [
 ]
 
 
-@pytest.mark.parametrize("kv", ["bf16", "int8"])
+@pytest.mark.parametrize("kv", ["bf16", "int8", "fp8"])
 @pytest.mark.parametrize("shape", SHAPES, ids=lambda s: f"B{len(s[0])}_Hq{s[1]}_Hkv{s[2]}_d{s[3]}")
 def test_shapes_auto_plan(shape, kv):
     lens, hq, hkv, d = shape
@@ -94,7 +94,7 @@ def test_shapes_auto_plan(shape, kv):
 
 
 @pytest.mark.parametrize("kernel", KERNELS)
-@pytest.mark.parametrize("kv", ["bf16", "int8"])
+@pytest.mark.parametrize("kv", ["bf16", "int8", "fp8"])
 @pytest.mark.parametrize("shape", SHAPES, ids=lambda s: f"B{len(s[0])}_Hq{s[1]}_Hkv{s[2]}_d{s[3]}")
 def test_shapes_each_kernel(shape, kv, kernel):
     lens, hq, hkv, d = shape
@@ -102,7 +102,7 @@ def test_shapes_each_kernel(shape, kv, kernel):
 
 
 @pytest.mark.parametrize("kernel", KERNELS)
-@pytest.mark.parametrize("kv", ["bf16", "int8"])
+@pytest.mark.parametrize("kv", ["bf16", "int8", "fp8"])
 @pytest.mark.parametrize("partition_blocks", [1, 2, 3, 5, 8, 64])
 def test_partition_sweep(partition_blocks, kv, kernel):
     """Split-K: any partition size gives the oracle's result (log-sum-exp merge)."""
@@ -110,28 +110,30 @@ def test_partition_sweep(partition_blocks, kv, kernel):
     check_all(w, kv, partition_blocks, kernel=kernel)
 
 
+@pytest.mark.parametrize("kv", ["int8", "fp8"])
 @pytest.mark.parametrize("kernel", KERNELS)
 @pytest.mark.parametrize("qscale", [3e4, 1e-5])
-def test_int8_extreme_query_magnitudes(qscale, kernel):
+def test_int8_extreme_query_magnitudes(qscale, kernel, kv):
     """Very large and very small queries: the tensor-core path brings q into fp16 range
     with a power of two, which must not change the result.  Large queries make the
     softmax one-hot, so each output is a single O(1) value of V and its own bf16 rounding
     is counted in the mean bound."""
-    w = custom([40, 333], 16, 4, 128, "int8", seed=12)
+    w = custom([40, 333], 16, 4, 128, kv, seed=12)
     w.q = (w.q.float() * qscale).to(torch.bfloat16)
-    check_all(w, "int8", kernel=kernel, output_rounding=qscale > 1)
+    check_all(w, kv, kernel=kernel, output_rounding=qscale > 1)
 
 
+@pytest.mark.parametrize("kv", ["int8", "fp8"])
 @pytest.mark.parametrize("kernel", KERNELS)
-def test_int8_value_scales_spanning_binades(kernel):
+def test_int8_value_scales_spanning_binades(kernel, kv):
     """V rows whose scales differ by up to 2^14 across and within blocks (the tensor-core
     path keeps P in fp16 with a growing block exponent).  Values stay below 4x N(0,1) so
     that the absolute tolerance still applies to the bf16 output."""
-    w = custom([500, 70], 16, 4, 128, "int8", seed=13)
+    w = custom([500, 70], 16, 4, 128, kv, seed=13)
     g = torch.Generator().manual_seed(3)
     mult = torch.pow(2.0, torch.randint(-12, 3, (w.value.shape[0], 1, 1), generator=g).float())
     w.value = (w.value.float() * mult).to(torch.bfloat16)
-    check_all(w, "int8", kernel=kernel)
+    check_all(w, kv, kernel=kernel)
 
 
 def test_partitions_agree_with_each_other():
@@ -172,16 +174,18 @@ def test_long_single_sequence():
     check_all(w, "bf16")
 
 
-def test_int8_zero_rows():
+@pytest.mark.parametrize("kv", ["int8", "fp8"])
+def test_quantised_zero_rows(kv):
     """An all-zero row quantises to scale 0 and zero codes, and decodes without NaN."""
-    w = custom([20, 33], 8, 4, 64, "int8", seed=41)
+    w = custom([20, 33], 8, 4, 64, kv, seed=41)
     w.key[3].zero_()
     w.value[7].zero_()
     w.value[20:30].zero_()
-    check_all(w, "int8")
+    check_all(w, kv)
 
 
-def test_int8_quantiser_bit_exact_many_rows():
+@pytest.mark.parametrize("kv", ["int8", "fp8"])
+def test_quantiser_bit_exact_many_rows(kv):
     """Codes and scales of 64k token-head rows equal the oracle's bit for bit."""
     n, hkv, d = 8192, 8, 128
     gen = torch.Generator().manual_seed(5)
@@ -189,13 +193,14 @@ def test_int8_quantiser_bit_exact_many_rows():
     value = torch.randn(n, hkv, d, generator=gen).to(torch.bfloat16)
     nb = n // 16 + 3
     slots = torch.randperm(nb * 16, generator=gen)[:n].to(torch.int32)
-    pool = pkv.PagedKVPool(nb, hkv, d, "int8", fill=0)
+    pool = pkv.PagedKVPool(nb, hkv, d, kv, fill=0)
     pool.reshape_and_cache(key.cuda(), value.cuda(), slots.cuda())
     torch.cuda.synchronize()
     o = oracle.load()
-    kc = np.zeros((nb, hkv, 16, d), np.int8)
+    kc = np.zeros((nb, hkv, 16, d), np.int8 if kv == "int8" else np.uint8)
     vc, ks, vs = kc.copy(), np.zeros((nb, hkv, 16), np.float32), np.zeros((nb, hkv, 16), np.float32)
-    o.reshape_and_cache_int8(W.bf16_bits(key), W.bf16_bits(value), slots.numpy(), kc, vc, ks, vs)
+    write = o.reshape_and_cache_int8 if kv == "int8" else o.reshape_and_cache_fp8
+    write(W.bf16_bits(key), W.bf16_bits(value), slots.numpy(), kc, vc, ks, vs)
     assert np.array_equal(pool.k_cache.cpu().numpy(), kc)
     assert np.array_equal(pool.v_cache.cpu().numpy(), vc)
     assert np.array_equal(pool.k_scale.cpu().numpy().view(np.uint32), ks.view(np.uint32))
@@ -236,7 +241,7 @@ def _sample(w, k=6):
     return sorted(picks)
 
 
-@pytest.mark.parametrize("name", ["llama2_7b", "llama3_8b_gqa", "long_32k", "int8_cb"])
+@pytest.mark.parametrize("name", ["llama2_7b", "llama3_8b_gqa", "long_32k", "int8_cb", "fp8_cb"])
 def test_named_workload_full_size(name):
     """Full-size workloads in the launch configuration the benchmark times (automatic
     plan); the oracle checks sampled sequences (shortest, longest, median, random)."""
@@ -246,7 +251,7 @@ def test_named_workload_full_size(name):
     check_all(w, kv, 0, seqs)
 
 
-@pytest.mark.parametrize("name", ["llama3_8b_gqa", "int8_cb"])
+@pytest.mark.parametrize("name", ["llama3_8b_gqa", "int8_cb", "fp8_cb"])
 def test_named_workload_cuda_core_kernel(name):
     """The GQA workloads through the CUDA-core kernel too (auto picks the tensor cores)."""
     w = W.make(name, device="cuda")
@@ -384,7 +389,8 @@ def test_large_batch_classic_grid(kernel):
 
 
 RING_SHAPES = [("bf16", 128, 2, 1), ("bf16", 128, 3, 1), ("bf16", 64, 3, 1), ("bf16", 64, 2, 2),
-               ("int8", 128, 3, 1), ("int8", 128, 2, 2), ("int8", 128, 3, 2)]
+               ("int8", 128, 3, 1), ("int8", 128, 2, 2), ("int8", 128, 3, 2),
+               ("fp8", 128, 3, 1), ("fp8", 128, 2, 2), ("fp8", 128, 3, 2)]
 
 
 @pytest.mark.parametrize("partition_blocks", [0, 3, 5])
