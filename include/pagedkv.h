@@ -50,7 +50,8 @@ typedef enum pkv_status {
   PKV_ERR_INVALID_ARG = 1, /* a pointer, size or layout argument is invalid         */
   PKV_ERR_UNSUPPORTED = 2, /* valid but not built (head_dim, group size, ...)        */
   PKV_ERR_CUDA = 3,        /* a CUDA runtime call or kernel launch failed            */
-  PKV_ERR_WORKSPACE = 4    /* the workspace passed is smaller than the call needs    */
+  PKV_ERR_WORKSPACE = 4,   /* the workspace passed is smaller than the call needs    */
+  PKV_ERR_CAPACITY = 5     /* out of free blocks, sequence slots or table capacity   */
 } pkv_status;
 
 typedef enum pkv_kv_dtype {
@@ -140,6 +141,79 @@ PKV_API pkv_status pkv_pool_destroy(pkv_pool* pool);
  */
 PKV_API pkv_status pkv_reshape_and_cache(const pkv_pool* pool, const void* key, const void* value,
                                  const int32_t* slot_mapping, int64_t num_tokens, void* stream);
+
+/*
+ * Copy whole blocks inside the pool: for each pair (src, dst), every kv head's 16 K and V
+ * rows of block src (and their scales, for INT8/FP8) are copied to block dst.  This is the
+ * copy-on-write step of block sharing: when a sequence that shares a partly filled block
+ * with others appends a token, it first gets its own copy of that block
+ * ("Efficient AI Lecture 13: LLM Deployment Techniques", section "PagedAttention": shared
+ * prompt prefixes reuse physical blocks for parallel sampling and beam search).
+ *   pairs (device): int32 [num_pairs][2]; a dst must not appear twice or also as a src in
+ *                   the same call.  Out-of-range ids are skipped and set PKV_DEVERR_BLOCK_ID.
+ * num_pairs == 0 is a no-op.  Errors: PKV_ERR_INVALID_ARG (num_pairs > 65535), PKV_ERR_CUDA.
+ */
+PKV_API pkv_status pkv_copy_blocks(const pkv_pool* pool, const int32_t* pairs, int num_pairs,
+                                   void* stream);
+
+/*
+ * Host-side block manager (no device memory, no CUDA calls): the free list of a pool's
+ * num_blocks physical blocks, a reference count per block, and a page table per sequence
+ * ("Efficient AI Lecture 13", section "PagedAttention / How it works": allocate physical
+ * blocks on demand, translate logical blocks through a block table; "Lesson 4", 4.2: a
+ * pre-allocated pool with dynamic allocation and release).  Sequences are small integer
+ * handles in [0, max_seqs).  A manager serialises its own calls (one mutex).
+ */
+typedef struct pkv_block_manager pkv_block_manager;
+
+/* Errors: PKV_ERR_INVALID_ARG (sizes < 1, num_blocks > 2^31 - 1), PKV_ERR_CAPACITY (memory). */
+PKV_API pkv_status pkv_block_manager_create(int64_t num_blocks, int max_seqs,
+                                            int max_blocks_per_seq, pkv_block_manager** out);
+PKV_API pkv_status pkv_block_manager_destroy(pkv_block_manager* manager);
+
+/* A new empty sequence; *seq receives its handle.  PKV_ERR_CAPACITY when all handles are in use. */
+PKV_API pkv_status pkv_block_manager_add_sequence(pkv_block_manager* manager, int* seq);
+
+/*
+ * A new sequence that shares every block of `parent` (each block's count + 1) and has its
+ * length: prefix sharing for parallel sampling and beam search.
+ */
+PKV_API pkv_status pkv_block_manager_fork(pkv_block_manager* manager, int parent, int* child);
+
+/* Release a sequence: each of its blocks' count - 1; blocks reaching 0 return to the pool. */
+PKV_API pkv_status pkv_block_manager_free_sequence(pkv_block_manager* manager, int seq);
+
+/*
+ * Reserve cache slots for new tokens: sequence seqs[i] grows by num_new_tokens[i] tokens.
+ * slot_mapping (host, int32, sum of num_new_tokens) receives the slot of each new token in
+ * order (for pkv_reshape_and_cache).  A new block is taken whenever a token starts one.  If
+ * a sequence's last block is shared and partly filled, it is first replaced by a fresh
+ * block and the pair (old, new) is written to copy_pairs (host, int32 [max_copies][2]) for
+ * pkv_copy_blocks, which must run before the new tokens are written; *num_copies receives
+ * the number of pairs.  All or nothing: on error nothing changes.
+ * Errors: PKV_ERR_INVALID_ARG (unknown or repeated sequence, negative count, copy_pairs
+ * too small), PKV_ERR_CAPACITY (not enough free blocks, or a table would exceed
+ * max_blocks_per_seq).
+ */
+PKV_API pkv_status pkv_block_manager_append(pkv_block_manager* manager, const int* seqs,
+                                            const int* num_new_tokens, int n,
+                                            int32_t* slot_mapping, int32_t* copy_pairs,
+                                            int max_copies, int* num_copies);
+
+/*
+ * Page tables and lengths of sequences seqs[0..n): block_tables (host, int32
+ * [n][max_blocks_per_seq], -1 past each table) and context_lens (host, int32 [n]), the
+ * inputs of pkv_paged_attention_decode once copied to the device.
+ */
+PKV_API pkv_status pkv_block_manager_tables(const pkv_block_manager* manager, const int* seqs,
+                                            int n, int32_t* block_tables, int32_t* context_lens);
+
+/* Free blocks and live sequences (either pointer may be NULL). */
+PKV_API pkv_status pkv_block_manager_stats(const pkv_block_manager* manager, int64_t* free_blocks,
+                                           int* live_seqs);
+
+/* Reference count of a block (0 = free), or -1 for an id out of range. */
+PKV_API int32_t pkv_block_manager_refcount(const pkv_block_manager* manager, int32_t block);
 
 /*
  * Decode-plan knobs.  Zero-initialise and set what you need; zero means automatic.

@@ -5,7 +5,9 @@ The library is loaded on first use; importing the package does not need a GPU.
 """
 
 from .api import (  # noqa: F401
+    BlockManager,
     PagedKVPool,
+    copy_blocks,
     decode_plan,
     decode_workspace_bytes,
     get_device_error,

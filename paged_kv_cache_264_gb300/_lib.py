@@ -16,6 +16,7 @@ PKV_ERR_INVALID_ARG = 1
 PKV_ERR_UNSUPPORTED = 2
 PKV_ERR_CUDA = 3
 PKV_ERR_WORKSPACE = 4
+PKV_ERR_CAPACITY = 5
 
 PKV_KV_BF16 = 0
 PKV_KV_INT8 = 1
@@ -67,6 +68,16 @@ SIGNATURES = {
     "pkv_paged_attention_decode_static_scratch": (_i32, [_vp, _vp, _vp, _i32, _vp, _i32, _i32, _i32, _f32,
                                                          _vp, _vp]),
     "pkv_static_scratch_error": (ctypes.c_char_p, []),
+    "pkv_copy_blocks": (_i32, [_vp, _vp, _i32, _vp]),
+    "pkv_block_manager_create": (_i32, [_i64, _i32, _i32, ctypes.POINTER(_vp)]),
+    "pkv_block_manager_destroy": (_i32, [_vp]),
+    "pkv_block_manager_add_sequence": (_i32, [_vp, _pi32]),
+    "pkv_block_manager_fork": (_i32, [_vp, _i32, _pi32]),
+    "pkv_block_manager_free_sequence": (_i32, [_vp, _i32]),
+    "pkv_block_manager_append": (_i32, [_vp, _vp, _vp, _i32, _vp, _vp, _i32, _pi32]),
+    "pkv_block_manager_tables": (_i32, [_vp, _vp, _i32, _vp, _vp]),
+    "pkv_block_manager_stats": (_i32, [_vp, ctypes.POINTER(ctypes.c_int64), _pi32]),
+    "pkv_block_manager_refcount": (ctypes.c_int32, [_vp, ctypes.c_int32]),
 }
 
 STATIC_SCRATCH_BYTES = 16 << 20

@@ -243,3 +243,76 @@ def paged_attention_decode_static_scratch(pool: PagedKVPool, q: torch.Tensor, bl
                                 lib.pkv_static_scratch_error().decode() + ")")
     check(st, "paged_attention_decode_static_scratch")
     return out
+
+
+def copy_blocks(pool: PagedKVPool, pairs: torch.Tensor, stream=None) -> None:
+    """Copy whole blocks src -> dst for each row (src, dst) of int32 pairs [n, 2] (CUDA)."""
+    _need(pairs, torch.int32, "pairs", 2)
+    if pairs.shape[1] != 2:
+        raise ValueError("pairs must be [n, 2]")
+    check(_lib.load().pkv_copy_blocks(_handle(pool), _ptr(pairs), pairs.shape[0], _stream(stream)),
+          "copy_blocks")
+
+
+class BlockManager:
+    """Host-side free list, reference counts and page tables of a block pool (the C
+    ``pkv_block_manager``).  Sequences are small integer handles."""
+
+    def __init__(self, num_blocks: int, max_seqs: int, max_blocks_per_seq: int):
+        self.lib = _lib.load()
+        self.max_blocks_per_seq = max_blocks_per_seq
+        self.handle = ctypes.c_void_p()
+        check(self.lib.pkv_block_manager_create(num_blocks, max_seqs, max_blocks_per_seq,
+                                                ctypes.byref(self.handle)), "block_manager_create")
+
+    def close(self):
+        if getattr(self, "handle", None):
+            self.lib.pkv_block_manager_destroy(self.handle)
+            self.handle = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:  # noqa: BLE001 -- interpreter shutdown
+            pass
+
+    def add_sequence(self) -> int:
+        s = ctypes.c_int()
+        check(self.lib.pkv_block_manager_add_sequence(self.handle, ctypes.byref(s)), "add_sequence")
+        return s.value
+
+    def fork(self, parent: int) -> int:
+        c = ctypes.c_int()
+        check(self.lib.pkv_block_manager_fork(self.handle, parent, ctypes.byref(c)), "fork")
+        return c.value
+
+    def free_sequence(self, seq: int) -> None:
+        check(self.lib.pkv_block_manager_free_sequence(self.handle, seq), "free_sequence")
+
+    def append(self, seqs, num_new_tokens):
+        """Reserve slots: returns (slot_mapping int32 [sum], copy_pairs int32 [k, 2]) on the host."""
+        seqs = (ctypes.c_int * len(seqs))(*seqs)
+        counts = (ctypes.c_int * len(num_new_tokens))(*num_new_tokens)
+        total = sum(num_new_tokens)
+        slots = torch.empty(max(total, 1), dtype=torch.int32)
+        pairs = torch.empty(max(len(seqs), 1), 2, dtype=torch.int32)
+        k = ctypes.c_int()
+        check(self.lib.pkv_block_manager_append(self.handle, seqs, counts, len(seqs), _ptr(slots),
+                                                _ptr(pairs), pairs.shape[0], ctypes.byref(k)), "append")
+        return slots[:total], pairs[:k.value]
+
+    def tables(self, seqs):
+        """(block_tables int32 [n, max_blocks_per_seq] with -1 padding, context_lens int32 [n])."""
+        arr = (ctypes.c_int * len(seqs))(*seqs)
+        bt = torch.empty(max(len(seqs), 1), self.max_blocks_per_seq, dtype=torch.int32)
+        cl = torch.empty(max(len(seqs), 1), dtype=torch.int32)
+        check(self.lib.pkv_block_manager_tables(self.handle, arr, len(seqs), _ptr(bt), _ptr(cl)), "tables")
+        return bt[:len(seqs)], cl[:len(seqs)]
+
+    def stats(self) -> tuple[int, int]:
+        fb, ls = ctypes.c_int64(), ctypes.c_int()
+        check(self.lib.pkv_block_manager_stats(self.handle, ctypes.byref(fb), ctypes.byref(ls)), "stats")
+        return fb.value, ls.value
+
+    def refcount(self, block: int) -> int:
+        return int(self.lib.pkv_block_manager_refcount(self.handle, block))

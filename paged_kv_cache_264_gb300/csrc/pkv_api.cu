@@ -210,6 +210,7 @@ const char* pkv_status_string(pkv_status s) {
     case PKV_ERR_UNSUPPORTED: return "unsupported configuration";
     case PKV_ERR_CUDA: return "CUDA error";
     case PKV_ERR_WORKSPACE: return "workspace too small";
+    case PKV_ERR_CAPACITY: return "out of blocks, sequence slots or table capacity";
   }
   return "unknown status";
 }
@@ -317,6 +318,26 @@ pkv_status pkv_reshape_and_cache(const pkv_pool* pool, const void* key, const vo
                    : pool->dtype == PKV_KV_FP8_E4M3 ? pkv::launch_cache_fp8(p, s)
                                                     : pkv::launch_cache_bf16(p, s);
   if (e != cudaSuccess) return cuda_fail(e, "reshape_and_cache launch");
+  g_launches.fetch_add(1, std::memory_order_relaxed);
+  return PKV_OK;
+}
+
+pkv_status pkv_copy_blocks(const pkv_pool* pool, const int32_t* pairs, int num_pairs, void* stream) {
+  if (!pool || num_pairs < 0) return PKV_ERR_INVALID_ARG;
+  if (num_pairs == 0) return PKV_OK;
+  if (!pairs || num_pairs > 65535) return PKV_ERR_INVALID_ARG;
+  pkv::CacheParams p{};
+  p.k_cache = pool->k_cache;
+  p.v_cache = pool->v_cache;
+  p.k_scale = pool->k_scale;
+  p.v_scale = pool->v_scale;
+  p.err = pool->d_err;
+  p.num_blocks = pool->num_blocks;
+  p.kv_heads = pool->kv_heads;
+  p.head_dim = pool->head_dim;
+  cudaError_t e = pkv::launch_copy_blocks(p, pairs, num_pairs, scaled_dtype(pool->dtype) ? 1 : 2,
+                                          static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "copy_blocks launch");
   g_launches.fetch_add(1, std::memory_order_relaxed);
   return PKV_OK;
 }

@@ -140,6 +140,37 @@ __global__ void __launch_bounds__(kCacheThreads)
   }
 }
 
+// Copy whole blocks (every kv head's K and V rows, and INT8/FP8 scales) from src to dst:
+// the copy-on-write step of block sharing.  `pairs` is int32 [n][2] = (src, dst).  One CTA
+// per (pair, 16-byte chunk range); out-of-range ids are skipped and flagged.
+__global__ void __launch_bounds__(kCacheThreads)
+    copy_blocks_kernel(const int32_t* __restrict__ pairs, int n, uint4* __restrict__ k_cache,
+                       uint4* __restrict__ v_cache, uint4* __restrict__ k_scale,
+                       uint4* __restrict__ v_scale, uint32_t* err, int64_t num_blocks,
+                       int64_t chunks_per_block, int64_t scale_chunks_per_block) {
+  griddep_wait();  // the pairs and the source blocks may come from earlier kernels
+  griddep_launch_dependents();
+  const int pi = blockIdx.y;
+  if (pi >= n) return;
+  const int64_t src = __ldg(pairs + 2 * pi), dst = __ldg(pairs + 2 * pi + 1);
+  if (src < 0 || src >= num_blocks || dst < 0 || dst >= num_blocks) {
+    if (blockIdx.x == 0 && threadIdx.x == 0) set_error(err, kErrBlockId);
+    return;
+  }
+  for (int64_t c = int64_t(blockIdx.x) * blockDim.x + threadIdx.x; c < chunks_per_block;
+       c += int64_t(gridDim.x) * blockDim.x) {
+    k_cache[dst * chunks_per_block + c] = k_cache[src * chunks_per_block + c];
+    v_cache[dst * chunks_per_block + c] = v_cache[src * chunks_per_block + c];
+  }
+  if (k_scale) {
+    for (int64_t c = int64_t(blockIdx.x) * blockDim.x + threadIdx.x; c < scale_chunks_per_block;
+         c += int64_t(gridDim.x) * blockDim.x) {
+      k_scale[dst * scale_chunks_per_block + c] = k_scale[src * scale_chunks_per_block + c];
+      v_scale[dst * scale_chunks_per_block + c] = v_scale[src * scale_chunks_per_block + c];
+    }
+  }
+}
+
 int grid_for(int64_t work_items, int per_block) {
   int dev = 0, sms = 148;
   cudaGetDevice(&dev);
@@ -177,6 +208,18 @@ static cudaError_t launch_cache_quant(const CacheParams& p, cudaStream_t stream)
                       value, p.slot_mapping, kc, vc, p.k_scale, p.v_scale, p.err, p.num_tokens,
                       p.num_blocks * kBlockSize, p.kv_heads);
   return cudaErrorInvalidValue;
+}
+
+cudaError_t launch_copy_blocks(const CacheParams& p, const int32_t* pairs, int n, int elem_bytes,
+                               cudaStream_t stream) {
+  const int64_t chunks = int64_t(p.kv_heads) * kBlockSize * p.head_dim * elem_bytes / 16;
+  const int64_t scale_chunks = p.k_scale ? int64_t(p.kv_heads) * kBlockSize * 4 / 16 : 0;
+  const int xblocks = static_cast<int>((chunks + kCacheThreads - 1) / kCacheThreads);
+  if (n > 65535) return cudaErrorInvalidValue;
+  return launch_pdl(copy_blocks_kernel, dim3(xblocks, n), dim3(kCacheThreads), 0, stream, pairs, n,
+                    static_cast<uint4*>(p.k_cache), static_cast<uint4*>(p.v_cache),
+                    reinterpret_cast<uint4*>(p.k_scale), reinterpret_cast<uint4*>(p.v_scale), p.err,
+                    p.num_blocks, chunks, scale_chunks);
 }
 
 cudaError_t launch_cache_int8(const CacheParams& p, cudaStream_t stream) {

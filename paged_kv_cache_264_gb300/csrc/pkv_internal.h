@@ -84,6 +84,8 @@ cudaError_t launch_pdl(void (*kernel)(Params...), dim3 grid, dim3 block, size_t 
 cudaError_t launch_cache_bf16(const CacheParams& p, cudaStream_t stream);
 cudaError_t launch_cache_int8(const CacheParams& p, cudaStream_t stream);
 cudaError_t launch_cache_fp8(const CacheParams& p, cudaStream_t stream);
+cudaError_t launch_copy_blocks(const CacheParams& p, const int32_t* pairs, int n, int elem_bytes,
+                               cudaStream_t stream);
 cudaError_t launch_decode_bf16(const DecodeParams& p, int group, cudaStream_t stream);
 cudaError_t launch_decode_int8(const DecodeParams& p, int group, cudaStream_t stream);
 cudaError_t launch_decode_fp8(const DecodeParams& p, int group, cudaStream_t stream);
