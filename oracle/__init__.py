@@ -24,6 +24,9 @@ What each function follows (page title, section):
   -- the FP8 (E4M3) KV cache read as the INT8 scheme with E4M3 codes: ``s = max|x| / 448``,
   code = nearest E4M3 of ``x / s`` (ties to even, saturating); "Lesson 4", section 5.3
   names FP8 KV caches without a scaling rule.
+* ``paged_decode_multi`` -- k query tokens per sequence for speculative verification (the
+  target model checks k drafts in one pass; "Lesson 4", 5.2): the drafts are the last k
+  cached tokens, query i attends causally to tokens ``0 .. T - k + i``.
 * ``kv_cache_bytes`` -- the KV-cache size closed form
   ``2 * layers * n_kv * head_dim * seq_len * bytes``; "LLM/MLLM inference
   optimisation", section 2.2.
@@ -133,6 +136,9 @@ class Oracle:
         lib.oracle_paged_decode.argtypes = [
             vp, vp, vp, vp, vp, i32, i64, i32, i32, vp, i32, vp, i32, i32, ctypes.c_double, vp]
         lib.oracle_paged_decode.restype = i32
+        lib.oracle_paged_decode_multi.argtypes = [
+            vp, vp, vp, vp, vp, i32, i64, i32, i32, vp, i32, vp, i32, i32, i32, ctypes.c_double, vp]
+        lib.oracle_paged_decode_multi.restype = i32
         self.lib = lib
 
     # -- threads
@@ -245,6 +251,30 @@ class Oracle:
         _check(self.lib.oracle_paged_decode(
             _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(k_scale), _ptr(v_scale), kv_dtype,
             nb, hkv, d, _ptr(bt), bt.shape[1], _ptr(cl), b, hq, float(scale), _ptr(out)))
+        return out
+
+
+    def paged_decode_multi(self, q, k_cache, v_cache, block_tables, context_lens, scale,
+                           k_scale=None, v_scale=None) -> np.ndarray:
+        """fp64 [B, k, Hq, d]: q bf16 bits [B, k, Hq, d]; the k queries of sequence b are its
+        last k cached tokens, query i attending causally to tokens 0 .. T_b - k + i."""
+        q = _c(q, np.uint16)
+        kdt = k_cache.dtype
+        kv_dtype = {np.dtype(np.int8): KV_INT8, np.dtype(np.uint8): KV_FP8}.get(np.dtype(kdt), KV_BF16)
+        if kv_dtype == KV_BF16:
+            kdt = np.uint16
+        k_cache, v_cache = _c(k_cache, kdt), _c(v_cache, kdt)
+        if kv_dtype != KV_BF16:
+            k_scale, v_scale = _c(k_scale, np.float32), _c(v_scale, np.float32)
+        bt = _c(block_tables, np.int32)
+        cl = _c(context_lens, np.int32)
+        b, nq, hq, d = q.shape
+        nb, hkv, bs, d2 = k_cache.shape
+        assert bs == BLOCK_SIZE and d2 == d and bt.shape[0] == b and cl.shape[0] == b
+        out = np.zeros((b, nq, hq, d), np.float64)
+        _check(self.lib.oracle_paged_decode_multi(
+            _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(k_scale), _ptr(v_scale), kv_dtype,
+            nb, hkv, d, _ptr(bt), bt.shape[1], _ptr(cl), b, nq, hq, float(scale), _ptr(out)))
         return out
 
 

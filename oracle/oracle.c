@@ -28,6 +28,10 @@
  *    ("Lesson 4", section 5.3 "KV Cache Quantization").  One scale per
  *    (token, kv head) row of d values; fp32 arithmetic with IEEE round-to-nearest
  *    division, round-half-to-even to the integer code, codes clamped to [-127, 127].
+ *  - Multi-query decode for speculative verification: the target model checks k draft
+ *    tokens in one pass ("Lesson 4", 5.2 "Speculative Decoding", algorithm step 2; "LLM/MLLM
+ *    inference optimisation", 6.1).  The drafts are the last k tokens in the cache; query i
+ *    (position T - k + i) attends causally, to tokens 0 .. T - k + i.
  *  - FP8 KV cache (same section names FP8 with its larger dynamic range, and that vLLM
  *    supports an FP8 KV cache; it gives no scaling rule).  Read here as the INT8 scheme
  *    with the E4M3 format in place of int8: s = max|x| / 448 per (token, kv head) row,
@@ -334,13 +338,14 @@ static double cache_value(const void* cache, const float* scales, int kv_dtype,
  * q: bf16 bits [B, Hq, d]; block_tables: [B, max_blocks_per_seq]; context_lens: [B];
  * out: fp64 [B, Hq, d].  Entries of block_tables past the last used block are never read.
  */
-int oracle_paged_decode(const uint16_t* q, const void* k_cache, const void* v_cache,
-                        const float* k_scale, const float* v_scale, int kv_dtype,
-                        int64_t num_blocks, int kv_heads, int head_dim,
-                        const int32_t* block_tables, int max_blocks_per_seq,
-                        const int32_t* context_lens, int num_seqs, int num_q_heads,
-                        double scale, double* out) {
-  if (num_seqs < 0 || kv_heads < 1 || head_dim < 1 || num_blocks < 1 || max_blocks_per_seq < 1)
+int oracle_paged_decode_multi(const uint16_t* q, const void* k_cache, const void* v_cache,
+                              const float* k_scale, const float* v_scale, int kv_dtype,
+                              int64_t num_blocks, int kv_heads, int head_dim,
+                              const int32_t* block_tables, int max_blocks_per_seq,
+                              const int32_t* context_lens, int num_seqs, int num_queries,
+                              int num_q_heads, double scale, double* out) {
+  if (num_seqs < 0 || kv_heads < 1 || head_dim < 1 || num_blocks < 1 || max_blocks_per_seq < 1 ||
+      num_queries < 1)
     return ORACLE_ERR_ARG;
   if (num_q_heads < kv_heads || num_q_heads % kv_heads != 0) return ORACLE_ERR_ARG;
   if (kv_dtype != ORACLE_KV_BF16 && kv_dtype != ORACLE_KV_INT8 && kv_dtype != ORACLE_KV_FP8)
@@ -350,7 +355,7 @@ int oracle_paged_decode(const uint16_t* q, const void* k_cache, const void* v_ca
   /* Validate everything that will be read before any arithmetic. */
   for (int b = 0; b < num_seqs; ++b) {
     int T = context_lens[b];
-    if (T < 1 || (int64_t)T > (int64_t)max_blocks_per_seq * ORACLE_BLOCK_SIZE)
+    if (T < num_queries || (int64_t)T > (int64_t)max_blocks_per_seq * ORACLE_BLOCK_SIZE)
       return ORACLE_ERR_CONTEXT;
     int nblk = (T + ORACLE_BLOCK_SIZE - 1) / ORACLE_BLOCK_SIZE;
     for (int j = 0; j < nblk; ++j) {
@@ -360,15 +365,17 @@ int oracle_paged_decode(const uint16_t* q, const void* k_cache, const void* v_ca
   }
 
   const int group = num_q_heads / kv_heads;
-  const int64_t pairs = (int64_t)num_seqs * num_q_heads;
+  const int64_t pairs = (int64_t)num_seqs * num_queries * num_q_heads;  /* (b, query, head) */
   int err = ORACLE_OK;
 
 #pragma omp parallel for schedule(dynamic, 1)
   for (int64_t bh = 0; bh < pairs; ++bh) {
-    const int b = (int)(bh / num_q_heads);
+    const int b = (int)(bh / ((int64_t)num_queries * num_q_heads));
+    const int qi = (int)((bh / num_q_heads) % num_queries);
     const int h = (int)(bh % num_q_heads);
     const int kvh = h / group;
-    const int T = context_lens[b];
+    /* query qi sits at position T - num_queries + qi and sees tokens up to and including it */
+    const int T = context_lens[b] - (num_queries - 1 - qi);
     const uint16_t* qrow = q + bh * head_dim;
     double* orow = out + bh * head_dim;
 
@@ -417,4 +424,16 @@ int oracle_paged_decode(const uint16_t* q, const void* k_cache, const void* v_ca
     free(qd);
   }
   return err;
+}
+
+/* One query token per sequence (the newest): the multi-query decode with k = 1. */
+int oracle_paged_decode(const uint16_t* q, const void* k_cache, const void* v_cache,
+                        const float* k_scale, const float* v_scale, int kv_dtype,
+                        int64_t num_blocks, int kv_heads, int head_dim,
+                        const int32_t* block_tables, int max_blocks_per_seq,
+                        const int32_t* context_lens, int num_seqs, int num_q_heads,
+                        double scale, double* out) {
+  return oracle_paged_decode_multi(q, k_cache, v_cache, k_scale, v_scale, kv_dtype, num_blocks,
+                                   kv_heads, head_dim, block_tables, max_blocks_per_seq,
+                                   context_lens, num_seqs, 1, num_q_heads, scale, out);
 }

@@ -13,6 +13,8 @@ Sources (page title, section):
     the absmax worked example (fixture tests/golden/absmax_worked_example.json).
   * "LLM/MLLM inference optimisation", 2.2 -- KV size closed form (fixture
     tests/golden/kv_cache_sizes.json); 2.3 -- MQA/GQA head sharing.
+  * "Lesson 4", 5.2 "Speculative Decoding" -- the target model verifies k draft tokens in
+    one pass: k queries per sequence, each causal over the prefix up to itself.
 """
 
 from __future__ import annotations
@@ -426,6 +428,68 @@ def pin_fp8_cache_and_decode(o):
         g = hq // hkv
         ref = sdpa_fp64(q[b], kd.repeat_interleave(g, 1), vd.repeat_interleave(g, 1), scale)
         np.testing.assert_allclose(out[b], ref, rtol=1e-12, atol=1e-13)
+
+
+def sdpa_causal_fp64(q, k, v, scale):
+    """torch's fp64 scaled_dot_product_attention for the last n positions of a sequence:
+    q [n, H, d]; k, v [T, H, d]; query i (position T - n + i) may attend to t <= T - n + i,
+    given to torch as an explicit boolean mask."""
+    n, t_len = q.shape[0], k.shape[0]
+    allowed = torch.arange(t_len)[None, :] <= (t_len - n + torch.arange(n))[:, None]
+    qq = q.to(torch.float64).permute(1, 0, 2)[None]      # [1, H, n, d]
+    kk = k.to(torch.float64).permute(1, 0, 2)[None]      # [1, H, T, d]
+    vv = v.to(torch.float64).permute(1, 0, 2)[None]
+    out = torch.nn.functional.scaled_dot_product_attention(qq, kk, vv, attn_mask=allowed, scale=scale)
+    return out[0].permute(1, 0, 2).numpy()                # [n, H, d]
+
+
+def pin_multi_query_causal_sdpa(o):
+    """Verifying k draft tokens in one pass ("Lesson 4", 5.2): each of the k queries of a
+    sequence equals torch's fp64 SDPA under the causal mask over the sequence's last k
+    positions, for bf16, INT8 (over s * code) and MHA/GQA."""
+    gen = torch.Generator().manual_seed(31)
+    for lens, nq, hq, hkv, d, kv in (([4, 17, 33, 48], 4, 4, 2, 32, "bf16"), ([5, 16], 5, 3, 3, 16, "bf16"),
+                                     ([40], 1, 2, 1, 8, "bf16"), ([8, 19, 36], 3, 8, 2, 64, "int8")):
+        _, pool, tab, ln, k, v = paged_case(o, lens, hq, hkv, d, gen, kv=kv)
+        q = rand_bf16(gen, len(lens), nq, hq, d)
+        scale = 1.0 / math.sqrt(d)
+        out = o.paged_decode_multi(bits(q), pool["k_cache"], pool["v_cache"], tab, ln, scale,
+                                   pool.get("k_scale"), pool.get("v_scale"))
+        g = hq // hkv
+        for b in range(len(lens)):
+            kb, vb = k[b].double(), v[b].double()
+            if kv == "int8":
+                kcodes, kscales = o.quantize_rows(bits(k[b]))
+                vcodes, vscales = o.quantize_rows(bits(v[b]))
+                kb = torch.from_numpy(kcodes.astype(np.float64) * kscales.astype(np.float64)[..., None])
+                vb = torch.from_numpy(vcodes.astype(np.float64) * vscales.astype(np.float64)[..., None])
+            ref = sdpa_causal_fp64(q[b], kb.repeat_interleave(g, 1), vb.repeat_interleave(g, 1), scale)
+            np.testing.assert_allclose(out[b], ref, rtol=1e-12, atol=1e-13)
+
+
+def pin_multi_query_first_draft(o):
+    """With T == k the first query sees only token 0 (its output is v_0 exactly, in every
+    head of the group) and the second sees tokens 0 and 1: a two-term softmax written out."""
+    gen = torch.Generator().manual_seed(32)
+    nq, hq, hkv, d = 3, 4, 2, 16
+    _, pool, tab, ln, k, v = paged_case(o, [nq], hq, hkv, d, gen)
+    q = rand_bf16(gen, 1, nq, hq, d)
+    out = o.paged_decode_multi(bits(q), pool["k_cache"], pool["v_cache"], tab, ln, 0.5)
+    kk, vv, qq = k[0].double(), v[0].double(), q[0].double()
+    for h in range(hq):
+        kvh = h // (hq // hkv)
+        assert np.array_equal(out[0, 0, h], vv[0, kvh].numpy())
+        l0 = 0.5 * float(qq[1, h] @ kk[0, kvh])
+        l1 = 0.5 * float(qq[1, h] @ kk[1, kvh])
+        w1 = 1.0 / (1.0 + math.exp(l0 - l1))
+        np.testing.assert_allclose(out[0, 1, h], (1 - w1) * vv[0, kvh].numpy() + w1 * vv[1, kvh].numpy(),
+                                   rtol=1e-12, atol=1e-14)
+    try:
+        o.paged_decode_multi(bits(rand_bf16(gen, 1, nq + 1, hq, d)), pool["k_cache"], pool["v_cache"],
+                             tab, ln, 0.5)
+    except oracle_mod.OracleError:
+        return
+    raise AssertionError("more queries than cached tokens accepted")
 
 
 def pin_kv_cache_size_closed_forms(o):

@@ -43,6 +43,11 @@ MUTANTS = [
      "const double q = round(ldexp(a, 3 - k));"),
     ("E4M3 encode does not saturate", "if (a >= 448.0) return sign | 0x7E;", "if (a >= 480.0) return sign | 0x7F;"),
     ("FP8 scale uses the INT8 range", "float s = amax / 448.0f;", "float s = amax / 127.0f;"),
+    ("causal limit off by one (query sees its successor)",
+     "const int T = context_lens[b] - (num_queries - 1 - qi);",
+     "const int T = context_lens[b] - (num_queries - 2 - qi) - (qi == num_queries - 1);"),
+    ("queries in reverse order", "const int T = context_lens[b] - (num_queries - 1 - qi);",
+     "const int T = context_lens[b] - qi;"),
     ("query widened from the wrong head", "const uint16_t* qrow = q + bh * head_dim;",
      "const uint16_t* qrow = q + ((int64_t)b * num_q_heads + (num_q_heads - 1 - h)) * head_dim;"),
 ]
