@@ -10,6 +10,10 @@ Printed: one JSON line (rank 0).  `value` is KV-read GB/s over the whole step
 inputs resident in HBM.  Inputs are larger than L2 (the pool is >1 GB), so no L2 flush
 is done between steps.
 
+The ``*_verify4`` workloads time a speculative-decoding verification step instead: 4
+draft tokens per sequence are appended, then one multi-query call attends each draft
+causally over the cache.
+
 Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
                        [--workload NAME]
 For N > 1 run under torch.distributed.run: each rank runs its own independent batch of
@@ -210,9 +214,10 @@ def run_ours(args, rank, world, local):
     lens = w.context_lens.to(dev)
     out = torch.empty_like(q)
     max_ctx = w.max_context_len
-    ws_n = pkv.decode_workspace_bytes(pool, w.num_seqs, w.num_q_heads, max_ctx)
+    nq = w.num_queries
+    ws_n = pkv.decode_workspace_bytes(pool, w.num_seqs, w.num_q_heads, max_ctx, num_queries=nq)
     ws = torch.empty(max(ws_n, 16), dtype=torch.uint8, device=dev)
-    plan = pkv.decode_plan(pool, w.num_seqs, w.num_q_heads, max_ctx)
+    plan = pkv.decode_plan(pool, w.num_seqs, w.num_q_heads, max_ctx, num_queries=nq)
     torch.cuda.synchronize(dev)
     assert pool.device_error() == 0
 
@@ -251,7 +256,8 @@ def run_ours(args, rank, world, local):
     dec_ms = sum(a.elapsed_time(b) for a, b in ev) / args.steps
     assert pool.device_error() == 0
 
-    sb = roofline.step_bytes(w.context_lens, w.num_q_heads, w.num_kv_heads, w.head_dim, kv)
+    sb = roofline.step_bytes(w.context_lens, w.num_q_heads, w.num_kv_heads, w.head_dim, kv,
+                             num_queries=nq)
     ms_step = ms_total / args.steps
     total_bytes = sum_over_ranks(float(sb.step) * args.steps, world, dev)
     value = total_bytes / (ms_total * 1e-3) / 1e9
@@ -277,7 +283,10 @@ def run_ours(args, rank, world, local):
             "num_seqs": w.num_seqs, "num_q_heads": w.num_q_heads, "num_kv_heads": w.num_kv_heads,
             "head_dim": w.head_dim, "kv_dtype": kv, "sum_context_tokens": int(w.context_lens.sum()),
             "max_context_len": max_ctx, "num_blocks": w.num_blocks,
-            "step": "reshape_and_cache of one new token per sequence + paged_attention_decode",
+            "step": ("reshape_and_cache of one new token per sequence + paged_attention_decode" if nq == 1 else
+                     f"reshape_and_cache of {nq} draft tokens per sequence + one multi-query "
+                     f"paged_attention_decode verifying them (causal over the last {nq} positions)"),
+            "num_queries": nq,
             "plan": plan, "l2": "inputs larger than L2 (pool %.2f GB > 129 MB); no flush" % (
                 2 * pool.k_cache.numel() * pool.k_cache.element_size() / 1e9),
             "parallelism": f"{world} independent replicas" if world > 1 else "single GPU",
@@ -380,24 +389,29 @@ def oracle_sample(workload: str, target_s: float):
             pool = dict(k_cache=np.zeros(shape, np.uint16), v_cache=np.zeros(shape, np.uint16))
             o.reshape_and_cache_bf16(key[hist], value[hist], slots[hist], pool["k_cache"], pool["v_cache"])
         else:
-            pool = dict(k_cache=np.zeros(shape, np.int8), v_cache=np.zeros(shape, np.int8),
+            cdt = np.int8 if spec.kv_dtype == "int8" else np.uint8
+            pool = dict(k_cache=np.zeros(shape, cdt), v_cache=np.zeros(shape, cdt),
                         k_scale=np.zeros(shape[:3], np.float32), v_scale=np.zeros(shape[:3], np.float32))
-            o.reshape_and_cache_int8(key[hist], value[hist], slots[hist], pool["k_cache"], pool["v_cache"],
-                                     pool["k_scale"], pool["v_scale"])
+            write_q(key[hist], value[hist], slots[hist], pool["k_cache"], pool["v_cache"],
+                    pool["k_scale"], pool["v_scale"])
         args = dict(q=W.bf16_bits(w.q), key=key[last], value=value[last], slots=slots[last], tab=tab,
                     lens=lens, scale=w.scale)
-        sb = roofline.step_bytes(w.context_lens, w.num_q_heads, w.num_kv_heads, w.head_dim, spec.kv_dtype)
+        sb = roofline.step_bytes(w.context_lens, w.num_q_heads, w.num_kv_heads, w.head_dim, spec.kv_dtype,
+                                 num_queries=spec.num_queries)
         return pool, args, sb
+
+    write_q = o.reshape_and_cache_int8 if spec.kv_dtype == "int8" else o.reshape_and_cache_fp8
+    decode = o.paged_decode_multi if spec.num_queries > 1 else o.paged_decode
 
     def run(pool, a):
         if spec.kv_dtype == "bf16":
             o.reshape_and_cache_bf16(a["key"], a["value"], a["slots"], pool["k_cache"], pool["v_cache"])
-            o.paged_decode(a["q"], pool["k_cache"], pool["v_cache"], a["tab"], a["lens"], a["scale"])
+            decode(a["q"], pool["k_cache"], pool["v_cache"], a["tab"], a["lens"], a["scale"])
         else:
-            o.reshape_and_cache_int8(a["key"], a["value"], a["slots"], pool["k_cache"], pool["v_cache"],
-                                     pool["k_scale"], pool["v_scale"])
-            o.paged_decode(a["q"], pool["k_cache"], pool["v_cache"], a["tab"], a["lens"], a["scale"],
-                           pool["k_scale"], pool["v_scale"])
+            write_q(a["key"], a["value"], a["slots"], pool["k_cache"], pool["v_cache"],
+                    pool["k_scale"], pool["v_scale"])
+            decode(a["q"], pool["k_cache"], pool["v_cache"], a["tab"], a["lens"], a["scale"],
+                   pool["k_scale"], pool["v_scale"])
 
     # calibrate on one sequence, then size the sample to about target_s per step
     pool, a, sb = build(1)

@@ -201,6 +201,16 @@ PKV_API pkv_status pkv_block_manager_append(pkv_block_manager* manager, const in
                                             int max_copies, int* num_copies);
 
 /*
+ * Shorten a sequence to its first num_tokens tokens (0 <= num_tokens <= its length): the
+ * blocks past ceil(num_tokens / 16) are released (count - 1).  Speculative decoding uses it
+ * to drop the draft tokens the target model rejected ("Lesson 4", 5.2: only the accepted
+ * prefix is kept).  The slots past num_tokens in the last kept block are reused by the
+ * next append, with a copy first if that block is shared.
+ * Errors: PKV_ERR_INVALID_ARG (unknown sequence, num_tokens out of range).
+ */
+PKV_API pkv_status pkv_block_manager_truncate(pkv_block_manager* manager, int seq, int num_tokens);
+
+/*
  * Page tables and lengths of sequences seqs[0..n): block_tables (host, int32
  * [n][max_blocks_per_seq], -1 past each table) and context_lens (host, int32 [n]), the
  * inputs of pkv_paged_attention_decode once copied to the device.
@@ -221,9 +231,11 @@ PKV_API int32_t pkv_block_manager_refcount(const pkv_block_manager* manager, int
  *     (sequence, kv head, partition) becomes one work item, and sequences longer than
  *     one partition are combined by a log-sum-exp reduce.  0 = chosen from the batch
  *     shape and the device's SM count.
- *   kernel: which decode kernel family runs.  PKV_KERNEL_AUTO (0) picks the tensor-core
- *     kernel where it is built (GQA group 2, 4 or 8; bf16 head_dim 64/128, INT8 or FP8
- *     head_dim 128) and the CUDA-core kernel otherwise; PKV_KERNEL_CUDA_CORE (1) and
+ *   kernel: which decode kernel family runs.  Both serve, per (sequence, kv head), a tile
+ *     of group * num_queries query columns.  PKV_KERNEL_AUTO (0) picks the tensor-core
+ *     kernel where it is built (2 to 16 columns; bf16 head_dim 64/128, INT8 or FP8
+ *     head_dim 128) and the CUDA-core kernel otherwise (1 to 8 columns; the choice for a
+ *     single column, i.e. MHA with one query); PKV_KERNEL_CUDA_CORE (1) and
  *     PKV_KERNEL_TENSOR_CORE (2) force one (PKV_ERR_UNSUPPORTED if it is not built for
  *     the shape).  Both compute the same function.
  *   schedule: how CTAs map to work items.  PKV_SCHEDULE_AUTO (0) picks;
@@ -235,6 +247,14 @@ PKV_API int32_t pkv_block_manager_refcount(const pkv_block_manager* manager, int
  *     kernel (0 = automatic; otherwise a built shape, PKV_ERR_UNSUPPORTED for others).
  *     Shallower rings fit more CTAs on an SM; two blocks per stage run the softmax once
  *     per 32 tokens.
+ *   num_queries: query tokens per sequence, k (0 = 1).  With k > 1 the call verifies k
+ *     draft tokens in one pass ("Lesson 4", 5.2 "Speculative Decoding"; the target model
+ *     scores all drafts at once): the k queries are the sequence's last k cached
+ *     positions, appended beforehand by pkv_reshape_and_cache, and query i attends
+ *     causally, to tokens t < T_b - (k - 1 - i).  q and out are then
+ *     [num_seqs, k, num_q_heads, head_dim]; each K/V block is still read once per kv
+ *     head.  1 <= k <= 16, group * k <= 16 (<= 8 where only the CUDA-core kernel is built),
+ *     max_context_len >= k, and a sequence with T_b < k counts as out of range.
  */
 #define PKV_KERNEL_AUTO 0
 #define PKV_KERNEL_CUDA_CORE 1
@@ -248,7 +268,8 @@ typedef struct pkv_decode_options {
   int schedule;
   int stages;
   int blocks_per_stage;
-  int reserved[3];
+  int num_queries;
+  int reserved[2];
 } pkv_decode_options;
 
 /*
@@ -305,7 +326,10 @@ PKV_API pkv_status pkv_paged_attention_decode(const pkv_pool* pool, const void* 
                                       int max_context_len, float scale, void* out,
                                       void* workspace, size_t workspace_bytes, void* stream);
 
-/* pkv_paged_attention_decode with explicit plan options (NULL = automatic). */
+/*
+ * pkv_paged_attention_decode with explicit plan options (NULL = automatic), including
+ * options->num_queries for multi-query (draft verification) calls.
+ */
 PKV_API pkv_status pkv_paged_attention_decode_ex(const pkv_pool* pool, const void* q,
                                          const int32_t* block_tables, int max_blocks_per_seq,
                                          const int32_t* context_lens, int num_seqs,

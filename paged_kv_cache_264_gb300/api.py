@@ -47,8 +47,9 @@ _SCHEDULES = {0: 0, "auto": 0, 1: 1, "grid": 1, 2: 2, "persistent": 2}
 
 
 def _options(partition_blocks: int = 0, kernel=0, schedule=0, stages=0,
-             blocks_per_stage=0) -> ctypes.POINTER(DecodeOptions) | None:
-    if not (partition_blocks or _KERNELS[kernel] or _SCHEDULES[schedule] or stages or blocks_per_stage):
+             blocks_per_stage=0, num_queries=1) -> ctypes.POINTER(DecodeOptions) | None:
+    if not (partition_blocks or _KERNELS[kernel] or _SCHEDULES[schedule] or stages or blocks_per_stage
+            or num_queries != 1):
         return None
     o = DecodeOptions()
     o.partition_blocks = int(partition_blocks)
@@ -56,6 +57,7 @@ def _options(partition_blocks: int = 0, kernel=0, schedule=0, stages=0,
     o.schedule = _SCHEDULES[schedule]
     o.stages = int(stages)
     o.blocks_per_stage = int(blocks_per_stage)
+    o.num_queries = int(num_queries)
     return ctypes.pointer(o)
 
 
@@ -161,19 +163,21 @@ def reshape_and_cache(pool: PagedKVPool, key: torch.Tensor, value: torch.Tensor,
 
 
 def decode_workspace_bytes(pool: PagedKVPool, num_seqs: int, num_q_heads: int, max_context_len: int,
-                           partition_blocks: int = 0, kernel=0) -> int:
+                           partition_blocks: int = 0, kernel=0, num_queries: int = 1) -> int:
     n = ctypes.c_size_t()
     check(_lib.load().pkv_decode_workspace_bytes(_handle(pool), num_seqs, num_q_heads, max_context_len,
-                                                 _options(partition_blocks, kernel), ctypes.byref(n)),
+                                                 _options(partition_blocks, kernel, num_queries=num_queries),
+                                                 ctypes.byref(n)),
           "decode_workspace_bytes")
     return n.value
 
 
 def decode_plan(pool: PagedKVPool, num_seqs: int, num_q_heads: int, max_context_len: int,
-                partition_blocks: int = 0, kernel=0) -> dict:
+                partition_blocks: int = 0, kernel=0, num_queries: int = 1) -> dict:
     pb, mp, kc, kf = ctypes.c_int(), ctypes.c_int(), ctypes.c_int(), ctypes.c_int()
     check(_lib.load().pkv_decode_plan(_handle(pool), num_seqs, num_q_heads, max_context_len,
-                                      _options(partition_blocks, kernel), ctypes.byref(pb), ctypes.byref(mp),
+                                      _options(partition_blocks, kernel, num_queries=num_queries),
+                                      ctypes.byref(pb), ctypes.byref(mp),
                                       ctypes.byref(kc), ctypes.byref(kf)), "decode_plan")
     return {"partition_blocks": pb.value, "max_partitions": mp.value, "kernels_per_call": kc.value,
             "kernel": {1: "cuda_core", 2: "tensor_core"}.get(kf.value, str(kf.value))}
@@ -186,27 +190,34 @@ def paged_attention_decode(pool: PagedKVPool, q: torch.Tensor, block_tables: tor
                            blocks_per_stage=0, stream=None) -> torch.Tensor:
     """Decode attention for q bf16 [B, Hq, d] over the pool; returns out bf16 [B, Hq, d].
 
+    A 4-D q [B, k, Hq, d] holds k query tokens per sequence -- its last k cached positions,
+    query i attending causally to tokens t < T_b - (k - 1 - i) -- for verifying k draft
+    tokens in one pass; out is then [B, k, Hq, d].
     ``workspace`` (a uint8 CUDA tensor) is allocated here when not given and needed."""
-    _need(q, torch.bfloat16, "q", 3)
+    if q.dim() == 4:
+        _need(q, torch.bfloat16, "q", 4)
+        b, nq, hq, d = q.shape
+    else:
+        _need(q, torch.bfloat16, "q", 3)
+        (b, hq, d), nq = q.shape, 1
     _need(block_tables, torch.int32, "block_tables", 2)
     _need(context_lens, torch.int32, "context_lens", 1)
-    b, hq, d = q.shape
     if d != pool.head_dim or block_tables.shape[0] != b or context_lens.shape[0] != b:
         raise ValueError("q, block_tables and context_lens disagree in shape")
     if out is None:
         out = torch.empty_like(q)
     else:
-        _need(out, torch.bfloat16, "out", 3)
+        _need(out, torch.bfloat16, "out", q.dim())
         if out.shape != q.shape:
             raise ValueError("out must have q's shape")
-    need = decode_workspace_bytes(pool, b, hq, max_context_len, partition_blocks, kernel) if b else 0
+    need = decode_workspace_bytes(pool, b, hq, max_context_len, partition_blocks, kernel, nq) if b else 0
     if need and workspace is None:
         workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
     ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
     check(_lib.load().pkv_paged_attention_decode_ex(
         _handle(pool), _ptr(q), _ptr(block_tables), block_tables.shape[1], _ptr(context_lens), b, hq,
         int(max_context_len), float(scale), _ptr(out), _ptr(workspace), ws_bytes,
-        _options(partition_blocks, kernel, schedule, stages, blocks_per_stage), _stream(stream)),
+        _options(partition_blocks, kernel, schedule, stages, blocks_per_stage, nq), _stream(stream)),
         "paged_attention_decode")
     return out
 
@@ -300,6 +311,10 @@ class BlockManager:
         check(self.lib.pkv_block_manager_append(self.handle, seqs, counts, len(seqs), _ptr(slots),
                                                 _ptr(pairs), pairs.shape[0], ctypes.byref(k)), "append")
         return slots[:total], pairs[:k.value]
+
+    def truncate(self, seq: int, num_tokens: int) -> None:
+        """Keep the first num_tokens tokens of a sequence (drop rejected draft tokens)."""
+        check(self.lib.pkv_block_manager_truncate(self.handle, seq, num_tokens), "truncate")
 
     def tables(self, seqs):
         """(block_tables int32 [n, max_blocks_per_seq] with -1 padding, context_lens int32 [n])."""

@@ -12,9 +12,9 @@
 #include "pkv_internal.h"
 
 namespace pkv {
-int ctas_per_sm_bf16(int head_dim, int group);
-int ctas_per_sm_int8(int head_dim, int group);
-int ctas_per_sm_fp8(int head_dim, int group);
+int ctas_per_sm_bf16(int head_dim, int cols);
+int ctas_per_sm_int8(int head_dim, int cols);
+int ctas_per_sm_fp8(int head_dim, int cols);
 }  // namespace pkv
 
 struct pkv_pool {
@@ -54,12 +54,29 @@ int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
 
 bool group_supported(int g) { return g == 1 || g == 2 || g == 4 || g == 8; }
 
+constexpr int kMaxQueries = 16;  // query tokens per sequence in one call
+
+// Query tokens per sequence that the options ask for (0 or absent: 1); -1 if invalid.
+int num_queries_of(const pkv_decode_options* opt) {
+  if (!opt || opt->num_queries == 0) return 1;
+  return opt->num_queries >= 1 && opt->num_queries <= kMaxQueries ? opt->num_queries : -1;
+}
+
+// Smallest power of two >= n (n >= 1).
+int pow2_at_least(int n) {
+  int c = 1;
+  while (c < n) c <<= 1;
+  return c;
+}
+
 constexpr int kMaxPartitionBlocks = 1024;
 constexpr int kItemBlocksCudaCore = 128;   // blocks per work item, before shrinking to fill the GPU
 constexpr int kItemBlocksTensorCore = 64;
 
 struct Plan {
   int kernel;  // PKV_KERNEL_CUDA_CORE or PKV_KERNEL_TENSOR_CORE
+  int cols;    // query-column slots of the kernel variant (>= group * num_queries)
+  int num_queries;
   int shape;   // tensor-core ring shape index
   int persistent;
   int ctas_per_sm;
@@ -74,14 +91,31 @@ pkv_status make_plan(const pkv_pool* pool, int num_seqs, int num_q_heads, int ma
                      const pkv_decode_options* opt, Plan* plan) {
   const int64_t max_nblk = ceil_div(max_context_len, pkv::kBlockSize);
   const int group = num_q_heads / pool->kv_heads;
+  const int nq = num_queries_of(opt);
+  if (nq < 1) return PKV_ERR_INVALID_ARG;
+  if (max_context_len < nq) return PKV_ERR_INVALID_ARG;
   const auto kv = static_cast<pkv::KvType>(pool->dtype);
-  const bool mma_ok = pool->has_tmaps && pkv::mma_supported(kv, pool->head_dim, group);
+  // Query columns per (sequence, kv head): the group's heads times the query tokens.  The
+  // tensor-core kernel holds 2 to 16 column slots, the CUDA-core kernel 1 to 8.
+  const int ncols = group * nq;
+  const int mma_cols = pow2_at_least(ncols < 2 ? 2 : ncols);
+  const int cc_cols = pow2_at_least(ncols);
+  const bool mma_ok = pool->has_tmaps && pkv::mma_supported(kv, pool->head_dim, mma_cols);
+  const bool cc_ok = cc_cols <= 8;
   const int want = opt ? opt->kernel : PKV_KERNEL_AUTO;
-  if (want == PKV_KERNEL_TENSOR_CORE && !mma_ok) return PKV_ERR_UNSUPPORTED;
   if (want != PKV_KERNEL_AUTO && want != PKV_KERNEL_CUDA_CORE && want != PKV_KERNEL_TENSOR_CORE)
     return PKV_ERR_INVALID_ARG;
-  plan->kernel = (want == PKV_KERNEL_CUDA_CORE || !mma_ok) ? PKV_KERNEL_CUDA_CORE
-                                                           : PKV_KERNEL_TENSOR_CORE;
+  if (want == PKV_KERNEL_TENSOR_CORE && !mma_ok) return PKV_ERR_UNSUPPORTED;
+  if (want == PKV_KERNEL_CUDA_CORE && !cc_ok) return PKV_ERR_UNSUPPORTED;
+  if (!mma_ok && !cc_ok) return PKV_ERR_UNSUPPORTED;
+  // Automatic choice: the tensor cores once there are two or more query columns (measured
+  // on GB300: a one-column tile leaves too much of the MMA idle to beat the FMA kernel).
+  if (want == PKV_KERNEL_TENSOR_CORE || (want == PKV_KERNEL_AUTO && mma_ok && (ncols >= 2 || !cc_ok)))
+    plan->kernel = PKV_KERNEL_TENSOR_CORE;
+  else
+    plan->kernel = PKV_KERNEL_CUDA_CORE;
+  plan->cols = plan->kernel == PKV_KERNEL_TENSOR_CORE ? mma_cols : cc_cols;
+  plan->num_queries = nq;
   const int sched = opt ? opt->schedule : PKV_SCHEDULE_AUTO;
   if (sched != PKV_SCHEDULE_AUTO && sched != PKV_SCHEDULE_GRID && sched != PKV_SCHEDULE_PERSISTENT)
     return PKV_ERR_INVALID_ARG;
@@ -96,8 +130,8 @@ pkv_status make_plan(const pkv_pool* pool, int num_seqs, int num_q_heads, int ma
     return PKV_ERR_UNSUPPORTED;
   }
   const int per_sm = plan->kernel == PKV_KERNEL_TENSOR_CORE
-                         ? pkv::mma_ctas_per_sm(kv, pool->head_dim, group, plan->shape)
-                         : pkv::decode_ctas_per_sm(kv, pool->head_dim, group);
+                         ? pkv::mma_ctas_per_sm(kv, pool->head_dim, plan->cols, plan->shape)
+                         : pkv::decode_ctas_per_sm(kv, pool->head_dim, plan->cols);
   plan->ctas_per_sm = per_sm > 0 ? per_sm : 1;
   int P;
   if (opt && opt->partition_blocks > 0) {
@@ -126,7 +160,7 @@ pkv_status make_plan(const pkv_pool* pool, int num_seqs, int num_q_heads, int ma
   plan->ws_bytes = 0;
   plan->ws_ml_offset = 0;
   if (plan->max_parts > 1) {
-    const size_t rows = size_t(num_seqs) * num_q_heads * plan->max_parts;
+    const size_t rows = size_t(num_seqs) * nq * num_q_heads * plan->max_parts;
     const size_t acc = rows * pool->head_dim * sizeof(float);
     plan->ws_ml_offset = (acc + 255) / 256 * 256;
     plan->ws_bytes = plan->ws_ml_offset + rows * 2 * sizeof(float);
@@ -182,16 +216,16 @@ pkv_status check_decode_shape(const pkv_pool* pool, int num_seqs, int num_q_head
 }  // namespace
 
 namespace pkv {
-int decode_ctas_per_sm(KvType kv, int head_dim, int group) {
-  static int cache[3][2][9] = {};  // [dtype][head_dim 64/128][group]
+int decode_ctas_per_sm(KvType kv, int head_dim, int cols) {
+  static int cache[3][2][9] = {};  // [dtype][head_dim 64/128][column slots]
   const int di = head_dim == 128 ? 1 : 0;
   const int ki = static_cast<int>(kv);
-  if (group < 1 || group > 8) return 0;
-  int& slot = cache[ki][di][group];
+  if (cols < 1 || cols > 8) return 0;
+  int& slot = cache[ki][di][cols];
   if (slot == 0)
-    slot = kv == KvType::kInt8  ? ctas_per_sm_int8(head_dim, group)
-           : kv == KvType::kFp8 ? ctas_per_sm_fp8(head_dim, group)
-                                : ctas_per_sm_bf16(head_dim, group);
+    slot = kv == KvType::kInt8  ? ctas_per_sm_int8(head_dim, cols)
+           : kv == KvType::kFp8 ? ctas_per_sm_fp8(head_dim, cols)
+                                : ctas_per_sm_bf16(head_dim, cols);
   return slot;
 }
 
@@ -419,22 +453,24 @@ pkv_status pkv_paged_attention_decode_ex(const pkv_pool* pool, const void* q,
   p.num_seqs = num_seqs;
   p.num_q_heads = num_q_heads;
   p.kv_heads = pool->kv_heads;
+  p.group = num_q_heads / pool->kv_heads;
+  p.group_log2 = p.group == 8 ? 3 : p.group == 4 ? 2 : p.group == 2 ? 1 : 0;
+  p.num_queries = plan.num_queries;
   p.head_dim = pool->head_dim;
   p.max_context_len = max_context_len;
   p.partition_blocks = plan.partition_blocks;
   p.max_parts = plan.max_parts;
   p.scale_log2 = scale * 1.4426950408889634f;
 
-  const int group = num_q_heads / pool->kv_heads;
   auto s = static_cast<cudaStream_t>(stream);
   cudaError_t e;
   if (plan.kernel == PKV_KERNEL_TENSOR_CORE)
     e = pkv::launch_decode_mma(p, &pool->tmap_k, &pool->tmap_v,
-                               static_cast<pkv::KvType>(pool->dtype), group, plan.shape, s);
+                               static_cast<pkv::KvType>(pool->dtype), plan.cols, plan.shape, s);
   else
-    e = pool->dtype == PKV_KV_INT8       ? pkv::launch_decode_int8(p, group, s)
-        : pool->dtype == PKV_KV_FP8_E4M3 ? pkv::launch_decode_fp8(p, group, s)
-                                         : pkv::launch_decode_bf16(p, group, s);
+    e = pool->dtype == PKV_KV_INT8       ? pkv::launch_decode_int8(p, plan.cols, s)
+        : pool->dtype == PKV_KV_FP8_E4M3 ? pkv::launch_decode_fp8(p, plan.cols, s)
+                                         : pkv::launch_decode_bf16(p, plan.cols, s);
   if (e != cudaSuccess) return cuda_fail(e, "paged_attention_decode launch");
   g_launches.fetch_add(1, std::memory_order_relaxed);
   if (plan.max_parts > 1) {

@@ -194,6 +194,21 @@ PKV_API pkv_status pkv_block_manager_append(pkv_block_manager* m, const int* seq
   return PKV_OK;
 }
 
+PKV_API pkv_status pkv_block_manager_truncate(pkv_block_manager* m, int seq, int num_tokens) {
+  if (!m) return PKV_ERR_INVALID_ARG;
+  std::lock_guard<std::mutex> lock(m->mu);
+  if (!seq_ok(m, seq)) return PKV_ERR_INVALID_ARG;
+  auto& q = m->seqs[size_t(seq)];
+  if (num_tokens < 0 || num_tokens > q.len) return PKV_ERR_INVALID_ARG;
+  const size_t keep = size_t((num_tokens + kBlock - 1) / kBlock);
+  while (q.blocks.size() > keep) {
+    drop_block(m, q.blocks.back());
+    q.blocks.pop_back();
+  }
+  q.len = num_tokens;
+  return PKV_OK;
+}
+
 PKV_API pkv_status pkv_block_manager_tables(const pkv_block_manager* m, const int* seqs, int n,
                                             int32_t* block_tables, int32_t* context_lens) {
   if (!m || n < 0 || (n > 0 && (!seqs || !block_tables || !context_lens))) return PKV_ERR_INVALID_ARG;

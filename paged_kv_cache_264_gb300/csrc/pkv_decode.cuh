@@ -33,6 +33,13 @@
 // token t is p_t * s_V[t]; codes are widened to fp32 exactly (see i8_from_flipped).
 // FP8 (E4M3) pools work the same way with the hardware E4M3 -> fp16 conversion.
 //
+// Several query tokens per sequence (verifying k draft tokens in one pass; "Lesson 4", 5.2
+// "Speculative Decoding"): the k queries are the sequence's last k positions and query i
+// sees tokens t < T_b - (k - 1 - i).  A CTA then serves group * k query columns of its kv
+// head -- column c is query c / group of head kvh * group + c % group -- so each K/V block
+// is still read once, and each column carries its own causal cut.  With k = 1 this is the
+// plain decode above.
+//
 // Masking: tokens t >= T_b of the last block get logit -inf and are excluded from the
 // PV loop, so whatever bytes sit in unused slots are never used.  Block ids outside
 // [0, num_blocks) are skipped (no copy) and flagged in the device error word.
@@ -202,7 +209,7 @@ __device__ __forceinline__ SchedSmem sched_smem(unsigned char* tail, int num_seq
 }
 
 __device__ __forceinline__ int seq_parts(const DecodeParams& p, int T) {
-  if (T < 1 || T > p.max_context_len) return 1;
+  if (T < p.num_queries || T > p.max_context_len) return 1;
   const int nblk = (T + kBlockSize - 1) / kBlockSize;
   return (nblk + p.partition_blocks - 1) / p.partition_blocks;
 }
@@ -295,32 +302,60 @@ __device__ __forceinline__ bool locate_item(const DecodeParams& p, const SchedSm
     it.kvh = rem - it.b * p.kv_heads;
   }
   it.T = __ldg(p.context_lens + it.b);
-  it.bad_len = it.T < 1 || it.T > p.max_context_len;
+  it.bad_len = it.T < p.num_queries || it.T > p.max_context_len;
   it.nparts = seq_parts(p, it.T);
   return it.part < it.nparts;
 }
 
+// Row of q / out (in units of head_dim elements) that query column c of (b, kvh) reads
+// and writes: query token c / group of head kvh * group + c % group (group is a power of
+// two, so this is shifts and masks).
+__device__ __forceinline__ size_t col_row(const DecodeParams& p, int b, int kvh, int c) {
+  const int qi = c >> p.group_log2;
+  const int g = c & (p.group - 1);
+  return (size_t(b) * p.num_queries + qi) * p.num_q_heads + size_t(kvh) * p.group + g;
+}
+
+// Tokens of the sequence hidden from column c by the causal cut: query qi sits k - 1 - qi
+// positions before the newest token.  Columns past group * k get 0 (never written).
+__device__ __forceinline__ int col_cut(const DecodeParams& p, int c) {
+  const int qi = c >> p.group_log2;
+  return qi < p.num_queries ? p.num_queries - 1 - qi : 0;
+}
+
+// Start value of a running max.  A finite floor rather than -inf: a query column can see
+// no token of a whole block (all behind its causal cut), and with a finite start its
+// rescale factor exp2(m_old - m_new) is 1 and its probabilities exp2(-inf - m) are 0
+// without a special case; once a real logit arrives exp2(kMaxFloor - m) underflows to 0.
+constexpr float kMaxFloor = -3.402823466e38f;
+
 // Zero output and an error bit for a sequence with an out-of-range context length.
-template <int G, int D, int NT>
-__device__ __forceinline__ void write_bad_len(const DecodeParams& p, const ItemInfo& it, size_t qo_base) {
+template <int NC, int D, int NT>
+__device__ __forceinline__ void write_bad_len(const DecodeParams& p, const ItemInfo& it) {
   if (it.part != 0) return;
   auto* out = static_cast<__nv_bfloat16*>(p.out);
-  for (int i = threadIdx.x; i < G * D; i += NT) out[qo_base + i] = __float2bfloat16_rn(0.0f);
+  const int ncols = p.group * p.num_queries;
+  for (int i = threadIdx.x; i < NC * D; i += NT) {
+    const int c = i / D;
+    if (c < ncols) out[col_row(p, it.b, it.kvh, c) * D + (i - c * D)] = __float2bfloat16_rn(0.0f);
+  }
   if (threadIdx.x == 0) set_error(p.err, kErrContextLen);
 }
 
 // Merge the NW per-warp states of one work item by log-sum-exp and write the bf16 output
 // (single-partition sequences) or the item's partial (m, l, acc) to the workspace.  Warp w's
-// record is [G][D + 2] floats (running max in log2 units, sum, accumulator) at
-// smem + w * warp_stride.
-template <int G, int D, int NW>
+// record is [NC][D + 2] floats (running max in log2 units, sum, accumulator) per query
+// column at smem + w * warp_stride.
+template <int NC, int D, int NW>
 __device__ __forceinline__ void merge_warp_records(const unsigned char* smem, size_t warp_stride,
                                                    const DecodeParams& p, int b, int kvh, int part,
-                                                   int nparts, size_t qo_base) {
+                                                   int nparts) {
   auto* out = static_cast<__nv_bfloat16*>(p.out);
-  for (int i = threadIdx.x; i < G * D; i += NW * 32) {
+  const int ncols = p.group * p.num_queries;
+  for (int i = threadIdx.x; i < NC * D; i += NW * 32) {
     const int g = i / D;
     const int d = i - g * D;
+    if (g >= ncols) break;  // columns only grow along i: the rest are inactive too
     float M = -INFINITY;
 #pragma unroll
     for (int w = 0; w < NW; ++w)
@@ -335,10 +370,11 @@ __device__ __forceinline__ void merge_warp_records(const unsigned char* smem, si
         A = fmaf(f, r[2 + d], A);
       }
     }
+    const size_t row = col_row(p, b, kvh, g);
     if (nparts == 1) {
-      out[qo_base + i] = __float2bfloat16_rn(L > 0.0f ? A / L : 0.0f);
+      out[row * D + d] = __float2bfloat16_rn(L > 0.0f ? A / L : 0.0f);
     } else {
-      const size_t pi = (size_t(b) * p.num_q_heads + size_t(kvh) * G + g) * p.max_parts + part;
+      const size_t pi = row * p.max_parts + part;
       p.ws_acc[pi * D + d] = A;
       if (d == 0) {
         p.ws_ml[2 * pi] = M;
@@ -379,9 +415,8 @@ __global__ void __launch_bounds__(NW * 32)
   ItemInfo it;
   if (locate_item(p, ss, item, it)) {
   const int b = it.b, kvh = it.kvh, part = it.part, nparts = it.nparts, T = it.T;
-  const size_t qo_base = (size_t(b) * p.num_q_heads + size_t(kvh) * G) * D;
   if (it.bad_len) {
-    write_bad_len<G, D, C::kThreads>(p, it, qo_base);
+    write_bad_len<G, D, C::kThreads>(p, it);
   } else {
   const int nblk = (T + kBlockSize - 1) / kBlockSize;
   const int blk0 = part * P;
@@ -423,19 +458,21 @@ __global__ void __launch_bounds__(NW * 32)
     for (int k = 0; k < S && k < nw; ++k) issue(k);
   }
 
-  // ---- q for this lane's dims of all G heads, pre-multiplied by scale * log2(e)
+  // ---- q for this lane's dims of all G query columns, pre-multiplied by scale * log2(e)
   const int tok = lane / C::kLPT;    // token within a pass
   const int chunk = lane % C::kLPT;  // which DPL-dim slice of the row
   const int sw = C::kSwapHalves ? ((lane >> 2) & 1) : 0;
+  const int ncols = p.group * p.num_queries;
   float qr[G][C::kDPL];
   {
-    const auto* qb = static_cast<const __nv_bfloat16*>(p.q) + qo_base;
 #pragma unroll
     for (int g = 0; g < G; ++g) {
-      const uint4* src = reinterpret_cast<const uint4*>(qb + size_t(g) * D + chunk * C::kDPL);
+      const auto* qrow = static_cast<const __nv_bfloat16*>(p.q) + col_row(p, b, kvh, g) * D;
+      const uint4* src = reinterpret_cast<const uint4*>(qrow + chunk * C::kDPL);
 #pragma unroll
       for (int h = 0; h < C::kDPL / 8; ++h) {
-        const uint4 w = __ldg(src + (h ^ sw));
+        uint4 w = make_uint4(0u, 0u, 0u, 0u);  // inactive columns: q = 0, never written out
+        if (g < ncols) w = __ldg(src + (h ^ sw));
         const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
@@ -446,9 +483,10 @@ __global__ void __launch_bounds__(NW * 32)
     }
   }
 
-  const int g_lane = (lane % C::kLPT) / C::kDup;  // head whose logit this lane ends with
+  const int g_lane = (lane % C::kLPT) / C::kDup;  // column whose logit this lane ends with
   const bool store_lane = (lane % C::kDup) == 0;
-  float m_run = -INFINITY;
+  const int cut = col_cut(p, g_lane);              // its causal cut (0 for a single query)
+  float m_run = kMaxFloor;
   float l_run = 0.0f;
   float acc[G][C::kDPV];
 #pragma unroll
@@ -470,6 +508,8 @@ __global__ void __launch_bounds__(NW * 32)
     const bool valid = phys >= 0 && phys < p.num_blocks;
     const int vt = valid ? min(kBlockSize, T - (blk0 + ib) * kBlockSize) : 0;
     if (vt > 0) {
+      // tokens of this block that column g_lane may see: t < lim
+      const int lim = T - (blk0 + ib) * kBlockSize - cut;
       const unsigned char* st = ring + size_t(s) * C::kStageBytes;
       const unsigned char* ktile = st;
       const unsigned char* vtile = st + C::kTileBytes;
@@ -504,7 +544,7 @@ __global__ void __launch_bounds__(NW * 32)
         HeadReduce<G, C::kLPT / 2>::run(part_g, lane);
         float logit = part_g[0];
         if constexpr (C::kQuant) logit *= kscale[t];
-        sc[ps] = (t < vt) ? logit : -INFINITY;
+        sc[ps] = (t < lim) ? logit : -INFINITY;
       }
 
       // ---- online softmax update for head g_lane
@@ -608,7 +648,7 @@ __global__ void __launch_bounds__(NW * 32)
     for (int i = 0; i < C::kDPV; ++i) rec[g * (D + 2) + 2 + lane * C::kDPV + i] = acc[g][i];
   __syncthreads();
 
-  merge_warp_records<G, D, NW>(smem, size_t(S) * C::kStageBytes, p, b, kvh, part, nparts, qo_base);
+  merge_warp_records<G, D, NW>(smem, size_t(S) * C::kStageBytes, p, b, kvh, part, nparts);
   }  // valid context length
   }  // item located
   item = next_item(p, ss, ticket);
@@ -617,18 +657,18 @@ __global__ void __launch_bounds__(NW * 32)
 }
 
 // Merge the partitions of every split sequence: M = max_p m_p, L = sum_p 2^(m_p - M) l_p,
-// out = sum_p 2^(m_p - M) acc_p / L.  One warp per (sequence, query head).
+// out = sum_p 2^(m_p - M) acc_p / L.  One warp per (sequence, query token, query head).
 template <int D>
 __global__ void __launch_bounds__(128) lse_reduce_kernel(const DecodeParams p) {
   constexpr int kDPV = D / 32;
   constexpr uint32_t kFull = 0xffffffffu;
   const int lane = threadIdx.x & 31;
   griddep_wait();  // the partials come from the decode kernel just before
-  const int gw = blockIdx.x * (blockDim.x / 32) + (threadIdx.x >> 5);
-  if (gw >= p.num_seqs * p.num_q_heads) return;
-  const int b = gw / p.num_q_heads;
+  const int gw = blockIdx.x * (blockDim.x / 32) + (threadIdx.x >> 5);  // row of [B, k, Hq]
+  if (gw >= p.num_seqs * p.num_queries * p.num_q_heads) return;
+  const int b = gw / (p.num_queries * p.num_q_heads);
   const int T = __ldg(p.context_lens + b);
-  if (T < 1 || T > p.max_context_len) return;  // the decode kernel wrote zeros
+  if (T < p.num_queries || T > p.max_context_len) return;  // the decode kernel wrote zeros
   const int nblk = (T + kBlockSize - 1) / kBlockSize;
   const int nparts = (nblk + p.partition_blocks - 1) / p.partition_blocks;
   if (nparts <= 1) return;  // written directly by the decode kernel

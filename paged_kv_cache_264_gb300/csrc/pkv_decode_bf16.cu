@@ -11,8 +11,8 @@ constexpr int kStagesBf16D128 = 3;
 constexpr int kStagesBf16D64 = 4;
 
 template <int D, int S>
-static cudaError_t dispatch_group(const DecodeParams& p, int group, cudaStream_t stream) {
-  switch (group) {
+static cudaError_t dispatch_cols(const DecodeParams& p, int cols, cudaStream_t stream) {
+  switch (cols) {
     case 1: return launch_decode_variant<KvType::kBf16, D, 1, kNwBf16, S>(p, stream);
     case 2: return launch_decode_variant<KvType::kBf16, D, 2, kNwBf16, S>(p, stream);
     case 4: return launch_decode_variant<KvType::kBf16, D, 4, kNwBf16, S>(p, stream);
@@ -21,22 +21,22 @@ static cudaError_t dispatch_group(const DecodeParams& p, int group, cudaStream_t
   }
 }
 
-cudaError_t launch_decode_bf16(const DecodeParams& p, int group, cudaStream_t stream) {
-  if (p.head_dim == 128) return dispatch_group<128, kStagesBf16D128>(p, group, stream);
-  if (p.head_dim == 64) return dispatch_group<64, kStagesBf16D64>(p, group, stream);
+cudaError_t launch_decode_bf16(const DecodeParams& p, int cols, cudaStream_t stream) {
+  if (p.head_dim == 128) return dispatch_cols<128, kStagesBf16D128>(p, cols, stream);
+  if (p.head_dim == 64) return dispatch_cols<64, kStagesBf16D64>(p, cols, stream);
   return cudaErrorInvalidValue;
 }
 
-int ctas_per_sm_bf16(int head_dim, int group) {
+int ctas_per_sm_bf16(int head_dim, int cols) {
   if (head_dim == 128) {
-    switch (group) {
+    switch (cols) {
       case 1: return ctas_per_sm_variant<KvType::kBf16, 128, 1, kNwBf16, kStagesBf16D128>();
       case 2: return ctas_per_sm_variant<KvType::kBf16, 128, 2, kNwBf16, kStagesBf16D128>();
       case 4: return ctas_per_sm_variant<KvType::kBf16, 128, 4, kNwBf16, kStagesBf16D128>();
       case 8: return ctas_per_sm_variant<KvType::kBf16, 128, 8, kNwBf16, kStagesBf16D128>();
     }
   } else if (head_dim == 64) {
-    switch (group) {
+    switch (cols) {
       case 1: return ctas_per_sm_variant<KvType::kBf16, 64, 1, kNwBf16, kStagesBf16D64>();
       case 2: return ctas_per_sm_variant<KvType::kBf16, 64, 2, kNwBf16, kStagesBf16D64>();
       case 4: return ctas_per_sm_variant<KvType::kBf16, 64, 4, kNwBf16, kStagesBf16D64>();
@@ -47,7 +47,7 @@ int ctas_per_sm_bf16(int head_dim, int group) {
 }
 
 cudaError_t launch_lse_reduce(const DecodeParams& p, cudaStream_t stream) {
-  const int64_t pairs = int64_t(p.num_seqs) * p.num_q_heads;
+  const int64_t pairs = int64_t(p.num_seqs) * p.num_queries * p.num_q_heads;
   const int64_t grid = (pairs + 3) / 4;
   if (grid <= 0) return cudaSuccess;
   if (p.head_dim == 128)

@@ -1,5 +1,6 @@
-// pkv_decode_mma.cuh -- PagedAttention decode on the tensor cores (mma.sync) for GQA
-// groups of 2, 4 or 8 query heads, head_dim 128 (bf16 or INT8 pools) or 64 (bf16).
+// pkv_decode_mma.cuh -- PagedAttention decode on the tensor cores (mma.sync) for tiles of
+// 2, 4, 8 or 16 query columns per kv head (GQA groups, times the query tokens of a
+// multi-query call), head_dim 128 (bf16, INT8 or FP8 pools) or 64 (bf16).
 //
 // Same work decomposition and result as paged_decode_kernel (pkv_decode.cuh): one CTA
 // per (sequence, kv head, context partition), NW warps taking the item's blocks in turn,
@@ -9,8 +10,11 @@
 //  * Tiles arrive by TMA tensor copies (cp.async.bulk.tensor.2d) through a tensor map of
 //    the pool viewed as rows of head_dim elements, in 128-byte boxes with the 128-byte
 //    swizzle, so that the shared-memory reads below are free of bank conflicts.
-//  * Logits for all heads of the group come from m16n8k16 MMAs with fp32 accumulation:
-//    S[16 tokens x 8 heads] = K[16 x d] q^T[d x 8] (heads past G are zero columns).
+//  * Logits for all query columns come from m16n8k16 MMAs with fp32 accumulation:
+//    S[16 tokens x 8 columns] = K[16 x d] q^T[d x 8] per n-tile of 8 columns (columns past
+//    the active ones are zero).  Each K fragment feeds every n-tile.  A column is one
+//    (query token, head of the group) pair and has its own causal cut, applied when the
+//    logits are masked.
 //  * The probabilities stay in registers: the accumulator fragment of S, packed to 16-bit
 //    pairs and transposed with movmatrix, is exactly the B operand of the PV product
 //    O^T[d x 8] += V^T[d x 16] P[16 x 8], whose A operand is V read transposed by ldmatrix.
@@ -34,8 +38,9 @@
 
 namespace pkv {
 
-template <KvType KV, int D, int G, int NW, int S, int BPS>
+template <KvType KV, int D, int NC, int NW, int S, int BPS>
 struct MmaCfg {
+  static constexpr int kNT = NC > 8 ? NC / 8 : 1;     // n-tiles of 8 query columns
   static constexpr int kEsz = KvTraits<KV>::kElemBytes;
   static constexpr bool kQuant = KvTraits<KV>::kQuant;
   static constexpr bool kFp8 = KV == KvType::kFp8;     // E4M3 codes (else INT8 when kQuant)
@@ -60,9 +65,9 @@ struct MmaCfg {
 
   static_assert(kRowBytes % 128 == 0, "rows must be whole 128-byte swizzle spans");
   static_assert(!kQuant || D == 128, "INT8/FP8 tensor-core path is built for head_dim 128");
-  static_assert(G == 2 || G == 4 || G == 8, "group of 2, 4 or 8 query heads");
+  static_assert(NC == 2 || NC == 4 || NC == 8 || NC == 16, "2, 4, 8 or 16 query columns");
   static_assert(BPS == 1 || BPS == 2, "one or two blocks per ring stage");
-  static_assert(size_t(G) * (D + 2) * 4 <= size_t(S) * kStageBytes, "merge record fits the ring");
+  static_assert(size_t(NC) * (D + 2) * 4 <= size_t(S) * kStageBytes, "merge record fits the ring");
 };
 
 // Shared-memory address of 16-byte chunk `c` of token row `t` in a tile whose 128-byte
@@ -71,11 +76,12 @@ __device__ __forceinline__ uint32_t swz(uint32_t tile, int t, int c) {
   return tile + (c >> 3) * 2048 + t * 128 + (((c & 7) ^ (t & 7)) << 4);
 }
 
-template <KvType KV, int D, int G, int NW, int S, int BPS>
+template <KvType KV, int D, int NC, int NW, int S, int BPS>
 __global__ void __launch_bounds__(NW * 32)
     paged_decode_mma_kernel(const __grid_constant__ CUtensorMap tmap_k,
                             const __grid_constant__ CUtensorMap tmap_v, const DecodeParams p) {
-  using C = MmaCfg<KV, D, G, NW, S, BPS>;
+  using C = MmaCfg<KV, D, NC, NW, S, BPS>;
+  constexpr int NT = C::kNT;
   constexpr uint32_t kFull = 0xffffffffu;
   griddep_wait();  // inputs may come from the previous kernel in the stream
   griddep_launch_dependents();
@@ -111,9 +117,8 @@ __global__ void __launch_bounds__(NW * 32)
   ItemInfo it;
   if (locate_item(p, ss, item, it)) {
   const int b = it.b, kvh = it.kvh, part = it.part, nparts = it.nparts, T = it.T;
-  const size_t qo_base = (size_t(b) * p.num_q_heads + size_t(kvh) * G) * D;
   if (it.bad_len) {
-    write_bad_len<G, D, C::kThreads>(p, it, qo_base);
+    write_bad_len<NC, D, C::kThreads>(p, it);
   } else {
   const int nblk = (T + kBlockSize - 1) / kBlockSize;
   const int blk0 = part * P;
@@ -175,55 +180,86 @@ __global__ void __launch_bounds__(NW * 32)
     for (int k = 0; k < S && k < nw; ++k) issue(k);
   }
 
-  // ---- q as the B operand of S = K q^T: lane (gi, gj) holds head gi, k pairs 2gj, 2gj+8.
-  uint32_t qf[C::kKSteps][2];
+  // ---- q as the B operand of S = K q^T: in n-tile nt, lane (gi, gj) holds column
+  //      8nt + gi, k pairs 2gj, 2gj+8.
+  const int ncols = p.group * p.num_queries;
+  const auto* qall = static_cast<const __nv_bfloat16*>(p.q);
+  uint32_t qf[C::kKSteps][NT][2];
   float logit_factor = p.scale_log2;
-  float kbias0 = 0.0f, kbias1 = 0.0f;  // INT8: 1152 * sum_d q_d for heads 2gj, 2gj+1
-  {
-    const auto* qb = static_cast<const __nv_bfloat16*>(p.q) + qo_base;
-    if constexpr (!C::kQuant) {
+  float kbias[NT][2];  // INT8: 1152 * sum_d q_d for columns 8nt + 2gj, 8nt + 2gj + 1
+#pragma unroll
+  for (int nt = 0; nt < NT; ++nt) kbias[nt][0] = kbias[nt][1] = 0.0f;
+  if constexpr (!C::kQuant) {
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) {
+      const int c = 8 * nt + gi;
+      const bool act = c < ncols;
+      const __nv_bfloat16* qb = qall + col_row(p, b, kvh, c) * D;  // read only when active
 #pragma unroll
       for (int s = 0; s < C::kKSteps; ++s) {
-        qf[s][0] = gi < G ? __ldg(reinterpret_cast<const uint32_t*>(qb + gi * D + 16 * s + 2 * gj)) : 0u;
-        qf[s][1] = gi < G ? __ldg(reinterpret_cast<const uint32_t*>(qb + gi * D + 16 * s + 2 * gj + 8)) : 0u;
-      }
-    } else {
-      // fp16 operands: bring q into fp16 range with a power of two (exact for bf16 values);
-      // its inverse goes into the logit factor.
-      float amax = 0.0f;
-      for (int i = lane; i < G * D; i += 32) amax = fmaxf(amax, fabsf(__bfloat162float(qb[i])));
-#pragma unroll
-      for (int o = 16; o >= 1; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(kFull, amax, o));
-      int e = 0;
-      if (amax > 0.0f) e = min(100, max(-100, int((__float_as_uint(amax) >> 23) & 0xff) - 127 - 14));
-      const float qs = __uint_as_float(uint32_t(127 - e) << 23);
-      logit_factor = p.scale_log2 * __uint_as_float(uint32_t(127 + e) << 23);
-#pragma unroll
-      for (int s = 0; s < C::kKSteps; ++s) {
-        if (gi < G) {
-          const __nv_bfloat16* r = qb + gi * D + 32 * gj + 4 * s;  // permuted dims, see K below
-          qf[s][0] = pack_f16x2(__bfloat162float(r[0]) * qs, __bfloat162float(r[1]) * qs);
-          qf[s][1] = pack_f16x2(__bfloat162float(r[2]) * qs, __bfloat162float(r[3]) * qs);
-        } else {
-          qf[s][0] = qf[s][1] = 0u;
+        qf[s][nt][0] = qf[s][nt][1] = 0u;
+        if (act) {
+          qf[s][nt][0] = __ldg(reinterpret_cast<const uint32_t*>(qb + 16 * s + 2 * gj));
+          qf[s][nt][1] = __ldg(reinterpret_cast<const uint32_t*>(qb + 16 * s + 2 * gj + 8));
         }
       }
+    }
+  } else {
+    // fp16 operands: bring q into fp16 range with a power of two (exact for bf16 values);
+    // its inverse goes into the logit factor.  Lane (gi, gj) loads dims 32gj .. 32gj+31 of
+    // column 8nt + gi (k-step s takes dims 32gj+4s .. +3, the permutation used for K
+    // below), so the warp holds every active column once and reduces max |q| from
+    // registers.
+    uint2 raw[NT][C::kKSteps];
+    float amax = 0.0f;
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) {
+      const int c = 8 * nt + gi;
+      const __nv_bfloat16* qb = qall + col_row(p, b, kvh, c) * D + 32 * gj;  // read only when active
+#pragma unroll
+      for (int s = 0; s < C::kKSteps; ++s) {
+        raw[nt][s] = make_uint2(0u, 0u);
+        if (c < ncols) raw[nt][s] = __ldg(reinterpret_cast<const uint2*>(qb + 4 * s));
+        amax = fmaxf(amax, fmaxf(fmaxf(fabsf(bf16lo(raw[nt][s].x)), fabsf(bf16hi(raw[nt][s].x))),
+                                 fmaxf(fabsf(bf16lo(raw[nt][s].y)), fabsf(bf16hi(raw[nt][s].y)))));
+      }
+    }
+#pragma unroll
+    for (int o = 16; o >= 1; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(kFull, amax, o));
+    int e = 0;
+    if (amax > 0.0f) e = min(100, max(-100, int((__float_as_uint(amax) >> 23) & 0xff) - 127 - 14));
+    const float qs = __uint_as_float(uint32_t(127 - e) << 23);
+    logit_factor = p.scale_log2 * __uint_as_float(uint32_t(127 + e) << 23);
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) {
+#pragma unroll
+      for (int s = 0; s < C::kKSteps; ++s) {
+        qf[s][nt][0] = pack_f16x2(bf16lo(raw[nt][s].x) * qs, bf16hi(raw[nt][s].x) * qs);
+        qf[s][nt][1] = pack_f16x2(bf16lo(raw[nt][s].y) * qs, bf16hi(raw[nt][s].y) * qs);
+      }
       // INT8 K codes enter the product as 1152 + code: S' = S + 1152 * sum_d q_d.  Sum the
-      // fp16 values exactly as the MMA sees them, per head.
+      // fp16 values exactly as the MMA sees them, per column.
       float qsum = 0.0f;
 #pragma unroll
       for (int s = 0; s < C::kKSteps; ++s) {
-        const float2 a = __half22float2(*reinterpret_cast<const __half2*>(&qf[s][0]));
-        const float2 c = __half22float2(*reinterpret_cast<const __half2*>(&qf[s][1]));
-        qsum += (a.x + a.y) + (c.x + c.y);
+        const float2 a = __half22float2(*reinterpret_cast<const __half2*>(&qf[s][nt][0]));
+        const float2 c2 = __half22float2(*reinterpret_cast<const __half2*>(&qf[s][nt][1]));
+        qsum += (a.x + a.y) + (c2.x + c2.y);
       }
       qsum += __shfl_xor_sync(kFull, qsum, 1);
-      qsum += __shfl_xor_sync(kFull, qsum, 2);  // lanes of row gi now hold head gi's sum
+      qsum += __shfl_xor_sync(kFull, qsum, 2);  // lanes of row gi now hold column 8nt+gi's sum
       if constexpr (!C::kFp8) {
-        kbias0 = 1152.0f * __shfl_sync(kFull, qsum, 4 * (2 * gj));
-        kbias1 = 1152.0f * __shfl_sync(kFull, qsum, 4 * (2 * gj + 1));
+        kbias[nt][0] = 1152.0f * __shfl_sync(kFull, qsum, 4 * (2 * gj));
+        kbias[nt][1] = 1152.0f * __shfl_sync(kFull, qsum, 4 * (2 * gj + 1));
       }
     }
+  }
+  // Causal cuts of the accumulator columns 8nt + 2gj and 8nt + 2gj + 1 (0 for one query).
+  int cut[NT][2];
+#pragma unroll
+  for (int nt = 0; nt < NT; ++nt) {
+    cut[nt][0] = col_cut(p, 8 * nt + 2 * gj);
+    cut[nt][1] = col_cut(p, 8 * nt + 2 * gj + 1);
   }
 
   // ldmatrix row assignment: lane gives the row address of matrix lane / 8.
@@ -238,12 +274,21 @@ __global__ void __launch_bounds__(NW * 32)
   const int voff[4] = {(2 * gj) * 128 + ((gi ^ (2 * gj)) << 4), (2 * gj + 1) * 128 + ((gi ^ (2 * gj + 1)) << 4),
                        (2 * gj + 8) * 128 + ((gi ^ (2 * gj)) << 4), (2 * gj + 9) * 128 + ((gi ^ (2 * gj + 1)) << 4)};
 
-  float o[C::kMTiles][4];
+  float o[C::kMTiles][NT][4];
 #pragma unroll
-  for (int t = 0; t < C::kMTiles; ++t) o[t][0] = o[t][1] = o[t][2] = o[t][3] = 0.0f;
-  float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.0f, l1 = 0.0f;
-  int e_run = INT_MIN;  // INT8: O^T is kept in units of 2^e_run
-  float ptot0 = 0.0f, ptot1 = 0.0f;  // INT8: running sum of P' (same units), for the V bias
+  for (int t = 0; t < C::kMTiles; ++t)
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) o[t][nt][0] = o[t][nt][1] = o[t][nt][2] = o[t][nt][3] = 0.0f;
+  // Softmax state of columns 8nt + 2gj ([nt][0]) and 8nt + 2gj + 1 ([nt][1]).
+  float m[NT][2], l[NT][2];
+  float ptot[NT][2];  // INT8: running sum of P' (units of 2^e_run), for the V bias
+#pragma unroll
+  for (int nt = 0; nt < NT; ++nt) {
+    m[nt][0] = m[nt][1] = kMaxFloor;
+    l[nt][0] = l[nt][1] = 0.0f;
+    ptot[nt][0] = ptot[nt][1] = 0.0f;
+  }
+  int e_run = INT_MIN;  // quantised pools: O^T is kept in units of 2^e_run
 
   int failed_at = -1;
   for (int k = 0; k < nw; ++k) {
@@ -257,35 +302,46 @@ __global__ void __launch_bounds__(NW * 32)
     const int ib0 = (warp + k * NW) * BPS;
     const unsigned char* st = ring + size_t(s) * C::kStageBytes;
     const float* sc_st = scl + s * (C::kScaleStage / 4);
-    int vt[BPS];
+    int vt[BPS];   // tokens of block j inside the context (0: absent block)
+    int rem[BPS];  // context tokens from block j's first token on (0: absent block)
     bool any = false;
 #pragma unroll
     for (int j = 0; j < BPS; ++j) {
       vt[j] = 0;
+      rem[j] = 0;
       if (ib0 + j < nb_item) {
         const int phys = tbl[ib0 + j];
-        if (phys >= 0 && phys < p.num_blocks) vt[j] = min(kBlockSize, T - (blk0 + ib0 + j) * kBlockSize);
+        if (phys >= 0 && phys < p.num_blocks) {
+          rem[j] = T - (blk0 + ib0 + j) * kBlockSize;
+          vt[j] = min(kBlockSize, rem[j]);
+        }
       }
       any |= vt[j] > 0;
     }
     if (any) {
-      // ---- S_j = K_j q^T (fp32) per block j:
-      //      sacc[j] = {S[gi][2gj], S[gi][2gj+1], S[gi+8][2gj], S[gi+8][2gj+1]}
-      float sacc[BPS][4];
+      // ---- S_j = K_j q^T (fp32) per block j and n-tile nt:
+      //      sacc[j][nt] = {S[gi][c0], S[gi][c1], S[gi+8][c0], S[gi+8][c1]},
+      //      c0 = 8nt + 2gj, c1 = c0 + 1
+      float sacc[BPS][NT][4];
 #pragma unroll
       for (int j = 0; j < BPS; ++j) {
-        sacc[j][0] = sacc[j][1] = sacc[j][2] = sacc[j][3] = 0.0f;
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) sacc[j][nt][0] = sacc[j][nt][1] = sacc[j][nt][2] = sacc[j][nt][3] = 0.0f;
         if (vt[j] == 0) continue;
         const unsigned char* kt = st + j * C::kTileBytes;
         // Two accumulators (even and odd k-steps) halve the dependent MMA chain.
-        float acc2[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+        float acc2[NT][4];
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) acc2[nt][0] = acc2[nt][1] = acc2[nt][2] = acc2[nt][3] = 0.0f;
         if constexpr (!C::kQuant) {
           const uint32_t ktile = smem_addr(kt);
 #pragma unroll
           for (int s2 = 0; s2 < C::kKSteps; ++s2) {
             uint32_t a[4];
             ldmatrix_x4(a, swz(ktile, tok_k, 2 * s2 + ck));
-            mma_bf16_16816((s2 & 1) ? acc2 : sacc[j], a, qf[s2][0], qf[s2][1]);
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt)
+              mma_bf16_16816((s2 & 1) ? acc2[nt] : sacc[j][nt], a, qf[s2][nt][0], qf[s2][nt][1]);
           }
         } else {
           // Lane (gi, gj) reads dims 32gj..32gj+31 of tokens gi and gi+8; k-step s2 pairs
@@ -309,16 +365,23 @@ __global__ void __launch_bounds__(NW * 32)
               a[2] = f16x2_biased(ua, 0x4342u);
               a[3] = f16x2_biased(ub, 0x4342u);
             }
-            mma_f16_16816((s2 & 1) ? acc2 : sacc[j], a, qf[s2][0], qf[s2][1]);
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt)
+              mma_f16_16816((s2 & 1) ? acc2[nt] : sacc[j][nt], a, qf[s2][nt][0], qf[s2][nt][1]);
           }
         }
 #pragma unroll
-        for (int i = 0; i < 4; ++i) sacc[j][i] += acc2[i];
+        for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+          for (int i = 0; i < 4; ++i) sacc[j][nt][i] += acc2[nt][i];
       }
 
-      // ---- logits in log2 units, masked past the context (and for absent blocks)
-      float sc[BPS][4];
-      float bm0 = -INFINITY, bm1 = -INFINITY;
+      // ---- logits in log2 units, masked past the context and each column's causal cut
+      //      (and for absent blocks, whose rem is 0)
+      float sc[BPS][NT][4];
+      float bm[NT][2];
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt) bm[nt][0] = bm[nt][1] = -INFINITY;
 #pragma unroll
       for (int j = 0; j < BPS; ++j) {
         float f0 = logit_factor, f1 = logit_factor;
@@ -328,46 +391,65 @@ __global__ void __launch_bounds__(NW * 32)
             f1 *= sc_st[j * kBlockSize + gi + 8];
           }
         }
-        const bool v0 = gi < vt[j], v1 = gi + 8 < vt[j];
-        sc[j][0] = v0 ? (sacc[j][0] - kbias0) * f0 : -INFINITY;
-        sc[j][1] = v0 ? (sacc[j][1] - kbias1) * f0 : -INFINITY;
-        sc[j][2] = v1 ? (sacc[j][2] - kbias0) * f1 : -INFINITY;
-        sc[j][3] = v1 ? (sacc[j][3] - kbias1) * f1 : -INFINITY;
-        bm0 = fmaxf(bm0, fmaxf(sc[j][0], sc[j][2]));
-        bm1 = fmaxf(bm1, fmaxf(sc[j][1], sc[j][3]));
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) {
+          const int lim0 = rem[j] - cut[nt][0], lim1 = rem[j] - cut[nt][1];
+          sc[j][nt][0] = gi < lim0 ? (sacc[j][nt][0] - kbias[nt][0]) * f0 : -INFINITY;
+          sc[j][nt][1] = gi < lim1 ? (sacc[j][nt][1] - kbias[nt][1]) * f0 : -INFINITY;
+          sc[j][nt][2] = gi + 8 < lim0 ? (sacc[j][nt][2] - kbias[nt][0]) * f1 : -INFINITY;
+          sc[j][nt][3] = gi + 8 < lim1 ? (sacc[j][nt][3] - kbias[nt][1]) * f1 : -INFINITY;
+          bm[nt][0] = fmaxf(bm[nt][0], fmaxf(sc[j][nt][0], sc[j][nt][2]));
+          bm[nt][1] = fmaxf(bm[nt][1], fmaxf(sc[j][nt][1], sc[j][nt][3]));
+        }
       }
 
-      // ---- online softmax for heads 2gj and 2gj+1 over the stage's tokens
+      // ---- online softmax for this lane's columns over the stage's tokens
 #pragma unroll
-      for (int ofs = 4; ofs < 32; ofs <<= 1) {
-        bm0 = fmaxf(bm0, __shfl_xor_sync(kFull, bm0, ofs));
-        bm1 = fmaxf(bm1, __shfl_xor_sync(kFull, bm1, ofs));
-      }
-      const float mn0 = fmaxf(m0, bm0), mn1 = fmaxf(m1, bm1);
-      float r0 = fast_exp2(m0 - mn0), r1 = fast_exp2(m1 - mn1);
-      m0 = mn0;
-      m1 = mn1;
-      float pr[BPS][4];
-      float ps0 = 0.0f, ps1 = 0.0f;
+      for (int ofs = 4; ofs < 32; ofs <<= 1)
 #pragma unroll
-      for (int j = 0; j < BPS; ++j) {
-        pr[j][0] = fast_exp2(sc[j][0] - mn0);
-        pr[j][1] = fast_exp2(sc[j][1] - mn1);
-        pr[j][2] = fast_exp2(sc[j][2] - mn0);
-        pr[j][3] = fast_exp2(sc[j][3] - mn1);
-        ps0 += pr[j][0] + pr[j][2];
-        ps1 += pr[j][1] + pr[j][3];
+        for (int nt = 0; nt < NT; ++nt) {
+          bm[nt][0] = fmaxf(bm[nt][0], __shfl_xor_sync(kFull, bm[nt][0], ofs));
+          bm[nt][1] = fmaxf(bm[nt][1], __shfl_xor_sync(kFull, bm[nt][1], ofs));
+        }
+      float r[NT][2], mu[NT][2];  // rescale factors; new running max (finite, see kMaxFloor)
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+        for (int c = 0; c < 2; ++c) {
+          mu[nt][c] = fmaxf(m[nt][c], bm[nt][c]);
+          r[nt][c] = fast_exp2(m[nt][c] - mu[nt][c]);
+          m[nt][c] = mu[nt][c];
+        }
+      float pr[BPS][NT][4];
+      float ps[NT][2];
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt) ps[nt][0] = ps[nt][1] = 0.0f;
+#pragma unroll
+      for (int j = 0; j < BPS; ++j)
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) {
+          pr[j][nt][0] = fast_exp2(sc[j][nt][0] - mu[nt][0]);
+          pr[j][nt][1] = fast_exp2(sc[j][nt][1] - mu[nt][1]);
+          pr[j][nt][2] = fast_exp2(sc[j][nt][2] - mu[nt][0]);
+          pr[j][nt][3] = fast_exp2(sc[j][nt][3] - mu[nt][1]);
+          ps[nt][0] += pr[j][nt][0] + pr[j][nt][2];
+          ps[nt][1] += pr[j][nt][1] + pr[j][nt][3];
+        }
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt) {
+        l[nt][0] = fmaf(l[nt][0], r[nt][0], ps[nt][0]);
+        l[nt][1] = fmaf(l[nt][1], r[nt][1], ps[nt][1]);
       }
-      l0 = fmaf(l0, r0, ps0);
-      l1 = fmaf(l1, r1, ps1);
 
-      uint32_t x01[BPS], x23[BPS];
+      uint32_t x01[BPS][NT], x23[BPS][NT];
       if constexpr (!C::kQuant) {
 #pragma unroll
-        for (int j = 0; j < BPS; ++j) {
-          x01[j] = pack_bf16x2(pr[j][0], pr[j][1]);
-          x23[j] = pack_bf16x2(pr[j][2], pr[j][3]);
-        }
+        for (int j = 0; j < BPS; ++j)
+#pragma unroll
+          for (int nt = 0; nt < NT; ++nt) {
+            x01[j][nt] = pack_bf16x2(pr[j][nt][0], pr[j][nt][1]);
+            x23[j][nt] = pack_bf16x2(pr[j][nt][2], pr[j][nt][3]);
+          }
       } else {
         float sv[BPS][2];
         float svm = 0.0f;
@@ -383,38 +465,56 @@ __global__ void __launch_bounds__(NW * 32)
         const int e_new = min(126, e_run == INT_MIN ? eb : max(e_run, eb));
         if (e_run != INT_MIN && e_new != e_run) {
           const float f = pow2i(max(-126, e_run - e_new));
-          r0 *= f;
-          r1 *= f;
+#pragma unroll
+          for (int nt = 0; nt < NT; ++nt) {
+            r[nt][0] *= f;
+            r[nt][1] *= f;
+          }
         }
         e_run = e_new;
         const float pe = pow2i(-e_new);  // P' = p * s_V * 2^-E lies in [0, 4)
-        float q0 = 0.0f, q1 = 0.0f;  // this stage's sum of the fp16 P' for heads 2gj, 2gj+1
+        float qp[NT][2];  // this stage's sum of the fp16 P' per column
 #pragma unroll
-        for (int j = 0; j < BPS; ++j) {
-          x01[j] = pack_f16x2(pr[j][0] * sv[j][0] * pe, pr[j][1] * sv[j][0] * pe);
-          x23[j] = pack_f16x2(pr[j][2] * sv[j][1] * pe, pr[j][3] * sv[j][1] * pe);
-          const float2 a = __half22float2(*reinterpret_cast<const __half2*>(&x01[j]));
-          const float2 c = __half22float2(*reinterpret_cast<const __half2*>(&x23[j]));
-          q0 += a.x + c.x;
-          q1 += a.y + c.y;
+        for (int nt = 0; nt < NT; ++nt) qp[nt][0] = qp[nt][1] = 0.0f;
+#pragma unroll
+        for (int j = 0; j < BPS; ++j)
+#pragma unroll
+          for (int nt = 0; nt < NT; ++nt) {
+            x01[j][nt] = pack_f16x2(pr[j][nt][0] * sv[j][0] * pe, pr[j][nt][1] * sv[j][0] * pe);
+            x23[j][nt] = pack_f16x2(pr[j][nt][2] * sv[j][1] * pe, pr[j][nt][3] * sv[j][1] * pe);
+            const float2 a = __half22float2(*reinterpret_cast<const __half2*>(&x01[j][nt]));
+            const float2 c2 = __half22float2(*reinterpret_cast<const __half2*>(&x23[j][nt]));
+            qp[nt][0] += a.x + c2.x;
+            qp[nt][1] += a.y + c2.y;
+          }
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) {
+          ptot[nt][0] = fmaf(ptot[nt][0], r[nt][0], qp[nt][0]);
+          ptot[nt][1] = fmaf(ptot[nt][1], r[nt][1], qp[nt][1]);
         }
-        ptot0 = fmaf(ptot0, r0, q0);
-        ptot1 = fmaf(ptot1, r1, q1);
       }
-      if (__any_sync(kFull, r0 != 1.0f || r1 != 1.0f)) {
 #pragma unroll
-        for (int t = 0; t < C::kMTiles; ++t) {
-          o[t][0] *= r0; o[t][1] *= r1; o[t][2] *= r0; o[t][3] *= r1;
+      for (int nt = 0; nt < NT; ++nt) {
+        if (__any_sync(kFull, r[nt][0] != 1.0f || r[nt][1] != 1.0f)) {
+#pragma unroll
+          for (int t = 0; t < C::kMTiles; ++t) {
+            o[t][nt][0] *= r[nt][0]; o[t][nt][1] *= r[nt][1];
+            o[t][nt][2] *= r[nt][0]; o[t][nt][3] *= r[nt][1];
+          }
         }
       }
 
-      // ---- O^T += V_j^T P_j.  P_j as the B operand: lane (gi, gj) needs
-      //      P_j[tokens 2gj, 2gj+1 (+8)][head gi], the transpose of what it holds.
+      // ---- O^T += V_j^T P_j.  P_j as the B operand: in n-tile nt lane (gi, gj) needs
+      //      P_j[tokens 2gj, 2gj+1 (+8)][column 8nt + gi], the transpose of what it holds.
 #pragma unroll
       for (int j = 0; j < BPS; ++j) {
         if (vt[j] == 0) continue;
-        const uint32_t pb0 = movmatrix_trans(x01[j]);
-        const uint32_t pb1 = movmatrix_trans(x23[j]);
+        uint32_t pb0[NT], pb1[NT];
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) {
+          pb0[nt] = movmatrix_trans(x01[j][nt]);
+          pb1[nt] = movmatrix_trans(x23[j][nt]);
+        }
         const unsigned char* vtp = st + (BPS + j) * C::kTileBytes;
         if constexpr (!C::kQuant) {
           // Slots past the context in the last block may hold anything, NaN included, and
@@ -431,7 +531,8 @@ __global__ void __launch_bounds__(NW * 32)
             if (tail) {
               a[0] &= mlo; a[1] &= mlo; a[2] &= mhi; a[3] &= mhi;
             }
-            mma_bf16_16816(o[t], a, pb0, pb1);
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt) mma_bf16_16816(o[t][nt], a, pb0[nt], pb1[nt]);
           }
         } else {
           // INT8 codes are always finite and masked tokens have a zero weight in P; E4M3 has
@@ -467,7 +568,8 @@ __global__ void __launch_bounds__(NW * 32)
               a[2] = f16x2_biased(cd, 0x4140u);
               a[3] = f16x2_biased(cd, 0x4342u);
             }
-            mma_f16_16816(o[t], a, pb0, pb1);
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt) mma_f16_16816(o[t][nt], a, pb0[nt], pb1[nt]);
           }
         }
       }
@@ -488,50 +590,59 @@ __global__ void __launch_bounds__(NW * 32)
   }
   kb += failed_at >= 0 ? min(nw, failed_at + S) : nw;
 
-  // ---- this warp's state -> merge record [G][D + 2] in its ring
+  // ---- this warp's state -> merge record [NC][D + 2] in its ring
 #pragma unroll
-  for (int ofs = 4; ofs < 32; ofs <<= 1) {
-    l0 += __shfl_xor_sync(kFull, l0, ofs);
-    l1 += __shfl_xor_sync(kFull, l1, ofs);
-  }
+  for (int ofs = 4; ofs < 32; ofs <<= 1)
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) {
+      l[nt][0] += __shfl_xor_sync(kFull, l[nt][0], ofs);
+      l[nt][1] += __shfl_xor_sync(kFull, l[nt][1], ofs);
+    }
   float oscale = 1.0f;
   if constexpr (C::kQuant) {
     oscale = e_run == INT_MIN ? 0.0f : pow2i(max(-126, e_run));
     if constexpr (!C::kFp8) {
       // INT8 V codes entered as 1152 + code: O'^T = O^T + 1152 * sum_t P'_t for every dim.
 #pragma unroll
-      for (int ofs = 4; ofs < 32; ofs <<= 1) {
-        ptot0 += __shfl_xor_sync(kFull, ptot0, ofs);
-        ptot1 += __shfl_xor_sync(kFull, ptot1, ofs);
-      }
+      for (int ofs = 4; ofs < 32; ofs <<= 1)
 #pragma unroll
-      for (int t = 0; t < C::kMTiles; ++t) {
-        o[t][0] -= 1152.0f * ptot0; o[t][1] -= 1152.0f * ptot1;
-        o[t][2] -= 1152.0f * ptot0; o[t][3] -= 1152.0f * ptot1;
-      }
+        for (int nt = 0; nt < NT; ++nt) {
+          ptot[nt][0] += __shfl_xor_sync(kFull, ptot[nt][0], ofs);
+          ptot[nt][1] += __shfl_xor_sync(kFull, ptot[nt][1], ofs);
+        }
+#pragma unroll
+      for (int t = 0; t < C::kMTiles; ++t)
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) {
+          o[t][nt][0] -= 1152.0f * ptot[nt][0]; o[t][nt][1] -= 1152.0f * ptot[nt][1];
+          o[t][nt][2] -= 1152.0f * ptot[nt][0]; o[t][nt][3] -= 1152.0f * ptot[nt][1];
+        }
     }
   }
   float* rec = reinterpret_cast<float*>(ring);
-  const int h0 = 2 * gj, h1 = 2 * gj + 1;
-  if (gi == 0) {
-    if (h0 < G) { rec[h0 * (D + 2)] = m0; rec[h0 * (D + 2) + 1] = l0; }
-    if (h1 < G) { rec[h1 * (D + 2)] = m1; rec[h1 * (D + 2) + 1] = l1; }
-  }
 #pragma unroll
-  for (int t = 0; t < C::kMTiles; ++t) {
-    const int d0 = C::kQuant ? 16 * gi + 2 * t : 16 * t + gi;
-    const int d1 = C::kQuant ? d0 + 1 : d0 + 8;
-    if (h0 < G) {
-      rec[h0 * (D + 2) + 2 + d0] = o[t][0] * oscale;
-      rec[h0 * (D + 2) + 2 + d1] = o[t][2] * oscale;
+  for (int nt = 0; nt < NT; ++nt) {
+    const int h0 = 8 * nt + 2 * gj, h1 = h0 + 1;
+    if (gi == 0) {
+      if (h0 < NC) { rec[h0 * (D + 2)] = m[nt][0]; rec[h0 * (D + 2) + 1] = l[nt][0]; }
+      if (h1 < NC) { rec[h1 * (D + 2)] = m[nt][1]; rec[h1 * (D + 2) + 1] = l[nt][1]; }
     }
-    if (h1 < G) {
-      rec[h1 * (D + 2) + 2 + d0] = o[t][1] * oscale;
-      rec[h1 * (D + 2) + 2 + d1] = o[t][3] * oscale;
+#pragma unroll
+    for (int t = 0; t < C::kMTiles; ++t) {
+      const int d0 = C::kQuant ? 16 * gi + 2 * t : 16 * t + gi;
+      const int d1 = C::kQuant ? d0 + 1 : d0 + 8;
+      if (h0 < NC) {
+        rec[h0 * (D + 2) + 2 + d0] = o[t][nt][0] * oscale;
+        rec[h0 * (D + 2) + 2 + d1] = o[t][nt][2] * oscale;
+      }
+      if (h1 < NC) {
+        rec[h1 * (D + 2) + 2 + d0] = o[t][nt][1] * oscale;
+        rec[h1 * (D + 2) + 2 + d1] = o[t][nt][3] * oscale;
+      }
     }
   }
   __syncthreads();
-  merge_warp_records<G, D, NW>(smem, size_t(S) * C::kStageBytes, p, b, kvh, part, nparts, qo_base);
+  merge_warp_records<NC, D, NW>(smem, size_t(S) * C::kStageBytes, p, b, kvh, part, nparts);
   }  // valid context length
   }  // item located
   item = next_item(p, ss, ticket);
@@ -539,11 +650,11 @@ __global__ void __launch_bounds__(NW * 32)
   finish_items(p);
 }
 
-template <KvType KV, int D, int G, int NW, int S, int BPS>
+template <KvType KV, int D, int NC, int NW, int S, int BPS>
 cudaError_t launch_mma_variant(const DecodeParams& p, const CUtensorMap& tk, const CUtensorMap& tv,
                                cudaStream_t stream) {
-  using C = MmaCfg<KV, D, G, NW, S, BPS>;
-  auto kern = paged_decode_mma_kernel<KV, D, G, NW, S, BPS>;
+  using C = MmaCfg<KV, D, NC, NW, S, BPS>;
+  auto kern = paged_decode_mma_kernel<KV, D, NC, NW, S, BPS>;
   static bool attr_done[64] = {};
   int dev = 0;
   cudaGetDevice(&dev);
@@ -561,10 +672,10 @@ cudaError_t launch_mma_variant(const DecodeParams& p, const CUtensorMap& tk, con
                     C::smem_bytes(p.partition_blocks, p.persistent ? p.num_seqs : 0), stream, tk, tv, p);
 }
 
-template <KvType KV, int D, int G, int NW, int S, int BPS>
+template <KvType KV, int D, int NC, int NW, int S, int BPS>
 int mma_ctas_per_sm_variant() {
-  using C = MmaCfg<KV, D, G, NW, S, BPS>;
-  auto kern = paged_decode_mma_kernel<KV, D, G, NW, S, BPS>;
+  using C = MmaCfg<KV, D, NC, NW, S, BPS>;
+  auto kern = paged_decode_mma_kernel<KV, D, NC, NW, S, BPS>;
   cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                        static_cast<int>(C::smem_bytes(kMaxPartitionBlocks, kMaxSchedSeqs)));
   int n = 0;

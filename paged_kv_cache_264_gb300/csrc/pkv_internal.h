@@ -36,16 +36,16 @@ struct CacheParams {
 };
 
 struct DecodeParams {
-  const void* q;                // bf16 [B, Hq, D]
+  const void* q;                // bf16 [B, k, Hq, D]  (k = num_queries)
   const void* k_cache;          // [NB, Hkv, 16, D]
   const void* v_cache;
   const float* k_scale;         // [NB, Hkv, 16] (int8 only)
   const float* v_scale;
   const int32_t* block_tables;  // [B, max_blocks_per_seq]
   const int32_t* context_lens;  // [B]
-  void* out;                    // bf16 [B, Hq, D]
-  float* ws_acc;                // [B, Hq, max_parts, D]   (split only)
-  float* ws_ml;                 // [B, Hq, max_parts, 2]   (split only): running max (log2 units), sum
+  void* out;                    // bf16 [B, k, Hq, D]
+  float* ws_acc;                // [B, k, Hq, max_parts, D]   (split only)
+  float* ws_ml;                 // [B, k, Hq, max_parts, 2]   (split only): running max (log2 units), sum
   uint32_t* err;
   unsigned* sched;              // [2] work ticket and finished-CTA counters (zero between calls)
   int persistent;               // 1: persistent grid taking items from the ticket counter
@@ -55,6 +55,9 @@ struct DecodeParams {
   int num_seqs;
   int num_q_heads;
   int kv_heads;
+  int group;                    // query heads per kv head (num_q_heads / kv_heads), 1/2/4/8
+  int group_log2;               // log2(group)
+  int num_queries;              // k >= 1 query tokens per sequence, the last k positions
   int head_dim;
   int max_context_len;
   int partition_blocks;         // P: blocks per work item
@@ -86,23 +89,26 @@ cudaError_t launch_cache_int8(const CacheParams& p, cudaStream_t stream);
 cudaError_t launch_cache_fp8(const CacheParams& p, cudaStream_t stream);
 cudaError_t launch_copy_blocks(const CacheParams& p, const int32_t* pairs, int n, int elem_bytes,
                                cudaStream_t stream);
-cudaError_t launch_decode_bf16(const DecodeParams& p, int group, cudaStream_t stream);
-cudaError_t launch_decode_int8(const DecodeParams& p, int group, cudaStream_t stream);
-cudaError_t launch_decode_fp8(const DecodeParams& p, int group, cudaStream_t stream);
+// The decode kernels serve, per (sequence, kv head), a tile of query columns: column c is
+// query token c / group of head kvh * group + c % group.  `cols` is the column slot count
+// of the variant to launch (a power of two >= group * num_queries).
+cudaError_t launch_decode_bf16(const DecodeParams& p, int cols, cudaStream_t stream);
+cudaError_t launch_decode_int8(const DecodeParams& p, int cols, cudaStream_t stream);
+cudaError_t launch_decode_fp8(const DecodeParams& p, int cols, cudaStream_t stream);
 cudaError_t launch_lse_reduce(const DecodeParams& p, cudaStream_t stream);
 
-// Tensor-core decode (GQA groups 2/4/8): tk/tv are 2-D tensor maps of the K and V pools
-// (rows of head_dim elements, 128-byte boxes of 16 rows, 128-byte swizzle).
-bool mma_supported(KvType kv, int head_dim, int group);
+// Tensor-core decode (2, 4, 8 or 16 column slots): tk/tv are 2-D tensor maps of the K and
+// V pools (rows of head_dim elements, 128-byte boxes of 16 rows, 128-byte swizzle).
+bool mma_supported(KvType kv, int head_dim, int cols);
 // Ring shape (stages x blocks per stage) index for requested values (0 = default); -1 if
 // that shape is not built.
 int mma_ring_shape(KvType kv, int head_dim, int stages, int blocks_per_stage);
 cudaError_t launch_decode_mma(const DecodeParams& p, const CUtensorMap* tk, const CUtensorMap* tv,
-                              KvType kv, int group, int shape, cudaStream_t stream);
-int mma_ctas_per_sm(KvType kv, int head_dim, int group, int shape);
+                              KvType kv, int cols, int shape, cudaStream_t stream);
+int mma_ctas_per_sm(KvType kv, int head_dim, int cols, int shape);
 
 // Resident CTAs per SM of the CUDA-core decode kernel variant (0 if not built).
-int decode_ctas_per_sm(KvType kv, int head_dim, int group);
+int decode_ctas_per_sm(KvType kv, int head_dim, int cols);
 // Bytes of K+V (+scales) one 16-token block brings in for one kv head.
 int decode_block_bytes(KvType kv, int head_dim);
 

@@ -6,6 +6,10 @@ seq_len x bytes per layer), plus q, the output and the page table.  Tokens actua
 attended are counted, not whole 16-token blocks.  A decode step also appends one new
 token per sequence (reads its bf16 K/V row, writes the cached row and, for INT8, the
 scales).
+
+A multi-query step (k draft tokens per sequence, verified in one call) reads the same
+cached K/V once, k times the q and output rows, and appends k tokens per sequence; its
+flops count each query over the tokens up to its own position.
 """
 
 from __future__ import annotations
@@ -23,7 +27,7 @@ class StepBytes:
     q_out: int          # q read + output written (bf16)
     tables: int         # block-table entries + context lengths read
     append: int         # the appended tokens: bf16 rows read, cached rows (+ scales) and slots
-    flops: int          # 4 * sum_b T_b * Hq * d  (QK and PV, multiply-add = 2)
+    flops: int          # 4 * (tokens attended, summed over queries) * Hq * d  (QK and PV)
 
     @property
     def decode(self) -> int:
@@ -35,7 +39,7 @@ class StepBytes:
 
 
 def step_bytes(context_lens, num_q_heads: int, num_kv_heads: int, head_dim: int, kv_dtype: str,
-               append: bool = True) -> StepBytes:
+               append: bool = True, num_queries: int = 1) -> StepBytes:
     lens = torch.as_tensor(context_lens, dtype=torch.int64)
     b = int(lens.numel())
     sum_t = int(lens.sum())
@@ -44,14 +48,17 @@ def step_bytes(context_lens, num_q_heads: int, num_kv_heads: int, head_dim: int,
     kv = 2 * sum_t * num_kv_heads * head_dim * esz
     if kv_dtype in ("int8", "fp8"):
         kv += 2 * sum_t * num_kv_heads * 4
-    q_out = 2 * b * num_q_heads * head_dim * 2
+    k = int(num_queries)
+    q_out = 2 * b * k * num_q_heads * head_dim * 2
     tables = 4 * (sum_nb + b)
     app = 0
     if append:
-        app = 2 * b * num_kv_heads * head_dim * 2          # new K and V rows (bf16) read
-        app += 2 * b * num_kv_heads * head_dim * esz       # cached rows written
+        n_new = b * k
+        app = 2 * n_new * num_kv_heads * head_dim * 2          # new K and V rows (bf16) read
+        app += 2 * n_new * num_kv_heads * head_dim * esz       # cached rows written
         if kv_dtype in ("int8", "fp8"):
-            app += 2 * b * num_kv_heads * 4                # scales written
-        app += 4 * b                                       # slot_mapping read
-    flops = 4 * sum_t * num_q_heads * head_dim
+            app += 2 * n_new * num_kv_heads * 4                # scales written
+        app += 4 * n_new                                       # slot_mapping read
+    attended = k * sum_t - b * k * (k - 1) // 2  # query i of k sees T_b - (k - 1 - i) tokens
+    flops = 4 * attended * num_q_heads * head_dim
     return StepBytes(kv, q_out, tables, app, flops)

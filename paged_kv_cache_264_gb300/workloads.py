@@ -20,7 +20,16 @@ long_32k         8     32768 each                       32/32    128   bf16   1%
 int8_cb          256   lognormal(ln 1024, 1) in         32/8     128   int8
                        [16, 16384]
 fp8_cb           256   as int8_cb                       32/8     128   fp8
+llama2_7b_       64    as llama2_7b                     32/32    128   bf16   k = 4 queries
+verify4
+llama3_8b_gqa_   128   as llama3_8b_gqa                 32/8     128   bf16   k = 4 queries
+verify4
 ===============  ====  ===============================  =======  ====  =====  ================
+
+The two ``verify4`` workloads are multi-query decode batches for speculative decoding
+("Lesson 4", 5.2: the target model checks k draft tokens in one pass): each sequence's
+last 4 cached tokens are the drafts, and q holds 4 query tokens per sequence
+([B, 4, Hq, d]), query i attending causally to the tokens up to its own position.
 
 Pools other than ``tiny`` hold ``ceil(1.25 * sum_b ceil(T_b / 16))`` blocks; the blocks
 that sequences use are drawn from a seeded permutation of the pool.  Everything is drawn
@@ -53,6 +62,7 @@ class Spec:
     pool_blocks: int | None = None  # None: ceil(1.25 * blocks needed)
     outlier_key_channel_frac: float = 0.0
     outlier_key_scale: float = 8.0
+    num_queries: int = 1  # query tokens per sequence (k > 1: draft verification)
 
     @property
     def seed(self) -> int:
@@ -79,6 +89,12 @@ SPECS: dict[str, Spec] = {
         Spec("fp8_cb", 6, "continuous-batching decode step with FP8 (E4M3) KV: the int8_cb batch "
              "shape with E4M3 codes and per-(token, head) scales", 256, 32, 8, 128, "fp8",
              ("lognormal", 1024.0, 1.0, 16, 16384)),
+        Spec("llama2_7b_verify4", 7, "LLaMA-2-7B-shaped draft verification: the llama2_7b batch "
+             "shape with 4 query tokens per sequence (the last 4 cached tokens, causal)", 64, 32, 32,
+             128, "bf16", ("uniform", 128, 2048), num_queries=4),
+        Spec("llama3_8b_gqa_verify4", 8, "Llama-3-8B-shaped GQA draft verification: the "
+             "llama3_8b_gqa batch shape with 4 query tokens per sequence (causal)", 128, 32, 8, 128,
+             "bf16", ("uniform", 512, 8192), num_queries=4),
     )
 }
 
@@ -103,12 +119,13 @@ class Workload:
     block_tables: torch.Tensor  # int32 [B, max_blocks_per_seq] (cpu), -1 past the end
     slot_mapping: torch.Tensor  # int32 [N] (cpu)
     seq_offsets: torch.Tensor  # int64 [B+1] (cpu)
-    q: torch.Tensor  # bf16 [B, Hq, d]
+    q: torch.Tensor  # bf16 [B, Hq, d], or [B, k, Hq, d] with k = num_queries > 1
     key: torch.Tensor  # bf16 [N, Hkv, d]
     value: torch.Tensor  # bf16 [N, Hkv, d]
     scale: float
     seed: int
     outlier_channels: list = field(default_factory=list)
+    num_queries: int = 1
 
     @property
     def max_blocks_per_seq(self) -> int:
@@ -123,11 +140,14 @@ class Workload:
         return int(self.seq_offsets[-1].item())
 
     def last_token_rows(self) -> torch.Tensor:
-        """Row index of each sequence's newest token (position T_b - 1)."""
-        return (self.seq_offsets[1:] - 1).to(torch.int64)
+        """Row indices of each sequence's newest k = num_queries tokens (the tokens a decode
+        step appends: one new token, or k drafts), sequence by sequence."""
+        k = self.num_queries
+        ends = self.seq_offsets[1:].to(torch.int64)
+        return (ends[:, None] - k + torch.arange(k, dtype=torch.int64)[None, :]).flatten()
 
     def history_rows(self) -> torch.Tensor:
-        """Row indices of every token except each sequence's newest."""
+        """Row indices of every token except each sequence's newest k."""
         keep = torch.ones(self.num_tokens, dtype=torch.bool)
         keep[self.last_token_rows()] = False
         return torch.nonzero(keep).flatten()
@@ -174,6 +194,7 @@ def build(
     outlier_key_scale: float = 8.0,
     device="cpu",
     seqs: list | None = None,
+    num_queries: int = 1,
 ) -> Workload:
     """Build a workload from explicit context lengths.
 
@@ -219,11 +240,14 @@ def build(
         phys = tables[b].to(torch.int64)[t // BLOCK_SIZE]
         slot_mapping[offsets[i]:offsets[i + 1]] = (phys * BLOCK_SIZE + t % BLOCK_SIZE).to(torch.int32)
 
-    q = torch.empty((len(sel), num_q_heads, head_dim), dtype=torch.bfloat16, device=device)
+    if num_queries > 1 and int(lens.min()) < num_queries:
+        raise ValueError("every context must hold the k query tokens")
+    qshape = (num_q_heads, head_dim) if num_queries == 1 else (num_queries, num_q_heads, head_dim)
+    q = torch.empty((len(sel),) + qshape, dtype=torch.bfloat16, device=device)
     key = torch.empty((n_tok, num_kv_heads, head_dim), dtype=torch.bfloat16, device=device)
     value = torch.empty_like(key)
     for i, b in enumerate(sel):
-        q[i] = torch.randn((num_q_heads, head_dim), generator=_value_gen(seed, 0, b, device),
+        q[i] = torch.randn(qshape, generator=_value_gen(seed, 0, b, device),
                            device=device, dtype=torch.float32).to(torch.bfloat16)
         lo, hi = int(offsets[i]), int(offsets[i + 1])
         kf = torch.randn((hi - lo, num_kv_heads, head_dim), generator=_value_gen(seed, 1, b, device),
@@ -242,6 +266,7 @@ def build(
         context_lens=sub_lens.to(torch.int32), block_tables=tables[sel].contiguous(),
         slot_mapping=slot_mapping, seq_offsets=offsets, q=q, key=key, value=value,
         scale=1.0 / math.sqrt(head_dim), seed=seed, outlier_channels=outlier,
+        num_queries=num_queries,
     )
 
 
@@ -261,6 +286,7 @@ def make(name: str, device="cpu", seqs: list | None = None) -> Workload:
         seed=spec.seed, num_blocks=spec.pool_blocks,
         outlier_key_channel_frac=spec.outlier_key_channel_frac,
         outlier_key_scale=spec.outlier_key_scale, device=device, seqs=seqs,
+        num_queries=spec.num_queries,
     )
 
 

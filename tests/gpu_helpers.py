@@ -86,16 +86,20 @@ def compact_for_oracle(w: W.Workload, seqs):
                 num_blocks=max(cursor, 1), orig_tables=tables)
 
 
-def oracle_decode(w: W.Workload, kv: str, seqs=None, o=None):
-    """fp64 oracle output [len(seqs), Hq, d] plus its own pool (compacted)."""
+def oracle_decode(w: W.Workload, kv: str, seqs=None, o=None, q=None):
+    """fp64 oracle output [len(seqs), Hq, d] (or [len(seqs), k, Hq, d] for a multi-query
+    workload or a 4-D ``q``) plus its own pool (compacted)."""
     o = o or oracle.load()
     seqs = list(range(w.num_seqs)) if seqs is None else list(seqs)
     c = compact_for_oracle(w, seqs)
+    if q is not None:
+        c["q"] = W.bf16_bits(q[torch.tensor(seqs, device=q.device)])
+    decode = o.paged_decode_multi if c["q"].ndim == 4 else o.paged_decode
     shape = (c["num_blocks"], w.num_kv_heads, 16, w.head_dim)
     if kv == "bf16":
         kc, vc = np.zeros(shape, np.uint16), np.zeros(shape, np.uint16)
         o.reshape_and_cache_bf16(c["key"], c["value"], c["slots"], kc, vc)
-        out = o.paged_decode(c["q"], kc, vc, c["tables"], c["lens"], w.scale)
+        out = decode(c["q"], kc, vc, c["tables"], c["lens"], w.scale)
         pool = dict(k_cache=kc, v_cache=vc)
     else:
         cdt = np.int8 if kv == "int8" else np.uint8
@@ -103,7 +107,7 @@ def oracle_decode(w: W.Workload, kv: str, seqs=None, o=None):
         ks, vs = np.zeros(shape[:3], np.float32), np.zeros(shape[:3], np.float32)
         write = o.reshape_and_cache_int8 if kv == "int8" else o.reshape_and_cache_fp8
         write(c["key"], c["value"], c["slots"], kc, vc, ks, vs)
-        out = o.paged_decode(c["q"], kc, vc, c["tables"], c["lens"], w.scale, ks, vs)
+        out = decode(c["q"], kc, vc, c["tables"], c["lens"], w.scale, ks, vs)
         pool = dict(k_cache=kc, v_cache=vc, k_scale=ks, v_scale=vs)
     return out, pool, c
 

@@ -78,6 +78,30 @@ def test_errors_change_nothing():
         m.free_sequence(7)
 
 
+def test_truncate_drops_rejected_drafts():
+    """Append k draft tokens, keep an accepted prefix: blocks past it return to the pool,
+    and the next append reuses the freed slots (copying first if the block is shared)."""
+    m = pkv.BlockManager(num_blocks=10, max_seqs=4, max_blocks_per_seq=4)
+    s = m.add_sequence()
+    m.append([s], [14])                        # block 0 holds 14 tokens
+    slots, _ = m.append([s], [5])              # 5 drafts: 2 in block 0, 3 in block 1
+    assert slots.tolist() == [14, 15, 16, 17, 18]
+    m.truncate(s, 15)                          # one draft accepted
+    assert m.tables([s])[1].tolist() == [15] and m.refcount(1) == 0 and m.stats()[0] == 9
+    slots, _ = m.append([s], [2])
+    assert slots.tolist() == [15, 16]          # block 1 comes back from the free list
+    c = m.fork(s)                              # both share blocks 0 and 1 (17 tokens)
+    m.truncate(c, 10)                          # child keeps block 0 only; block 1 stays with s
+    assert m.refcount(0) == 2 and m.refcount(1) == 1
+    slots, pairs = m.append([c], [1])          # block 0 is shared and partly filled: copy
+    assert pairs.tolist() == [[0, 2]] and slots.tolist() == [2 * BS + 10]
+    m.truncate(c, 0)
+    assert m.tables([c])[1].tolist() == [0] and m.refcount(2) == 0
+    for bad in (-1, 18):
+        with pytest.raises(pkv.PagedKVError, match="invalid"):
+            m.truncate(s, bad)
+
+
 class Model:
     """The same rules in plain Python."""
 
@@ -137,6 +161,15 @@ def test_random_operations_match_model():
             m.free_sequence(s)
             for b in model.seqs.pop(s)[0]:
                 model.drop(b)
+        elif op < 0.5 and live:
+            s = rng.choice(live)
+            blocks, length = model.seqs[s]
+            keep = rng.randint(0, length)
+            m.truncate(s, keep)
+            nkeep = -(-keep // BS)
+            for b in reversed(blocks[nkeep:]):
+                model.drop(b)
+            model.seqs[s] = (blocks[:nkeep], keep)
         elif live:
             s = rng.choice(live)
             k = rng.randint(0, 20)
