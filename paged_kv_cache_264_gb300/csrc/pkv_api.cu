@@ -108,9 +108,10 @@ pkv_status make_plan(const pkv_pool* pool, int num_seqs, int num_q_heads, int ma
   if (want == PKV_KERNEL_TENSOR_CORE && !mma_ok) return PKV_ERR_UNSUPPORTED;
   if (want == PKV_KERNEL_CUDA_CORE && !cc_ok) return PKV_ERR_UNSUPPORTED;
   if (!mma_ok && !cc_ok) return PKV_ERR_UNSUPPORTED;
-  // Automatic choice: the tensor cores once there are two or more query columns (measured
-  // on GB300: a one-column tile leaves too much of the MMA idle to beat the FMA kernel).
-  if (want == PKV_KERNEL_TENSOR_CORE || (want == PKV_KERNEL_AUTO && mma_ok && (ncols >= 2 || !cc_ok)))
+  // Automatic choice: the tensor-core kernel wherever it is built, one query column (MHA
+  // decode) included -- measured on GB300 it beats the FMA kernel there too (LLaMA-2-7B
+  // shape: 154 us against 161 us).
+  if (want == PKV_KERNEL_TENSOR_CORE || (want == PKV_KERNEL_AUTO && mma_ok))
     plan->kernel = PKV_KERNEL_TENSOR_CORE;
   else
     plan->kernel = PKV_KERNEL_CUDA_CORE;
@@ -139,7 +140,11 @@ pkv_status make_plan(const pkv_pool* pool, int num_seqs, int num_q_heads, int ma
   } else {
     // Measured on GB300: items of 128 blocks (CUDA-core kernel) or 64 blocks (tensor-core
     // kernel, which consumes a block faster) balance fewer partials against load balance.
+    // The tensor-core kernel takes 128-block items too when that leaves every sequence in
+    // one item (no partials, no reduce kernel) and for 16-column tiles (twice the work per
+    // block).
     P = plan->kernel == PKV_KERNEL_TENSOR_CORE ? kItemBlocksTensorCore : kItemBlocksCudaCore;
+    if (plan->kernel == PKV_KERNEL_TENSOR_CORE && (max_nblk <= 128 || plan->cols == 16)) P = 128;
     const int64_t resident = int64_t(pool->sm_count) * plan->ctas_per_sm;
     const int64_t units = int64_t(num_seqs) * pool->kv_heads;
     // Shrink the partition while the batch would not fill the GPU twice over.

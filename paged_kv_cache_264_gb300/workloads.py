@@ -29,7 +29,9 @@ verify4
 The two ``verify4`` workloads are multi-query decode batches for speculative decoding
 ("Lesson 4", 5.2: the target model checks k draft tokens in one pass): each sequence's
 last 4 cached tokens are the drafts, and q holds 4 query tokens per sequence
-([B, 4, Hq, d]), query i attending causally to the tokens up to its own position.
+([B, 4, Hq, d]), query i attending causally to the tokens up to its own position.  They
+reuse their base workload's context lengths and block pool (its seed), so a verify step
+and a decode step over the same cache compare directly.
 
 Pools other than ``tiny`` hold ``ceil(1.25 * sum_b ceil(T_b / 16))`` blocks; the blocks
 that sequences use are drawn from a seeded permutation of the pool.  Everything is drawn
@@ -63,10 +65,11 @@ class Spec:
     outlier_key_channel_frac: float = 0.0
     outlier_key_scale: float = 8.0
     num_queries: int = 1  # query tokens per sequence (k > 1: draft verification)
+    base_index: int | None = None  # draw lengths, pool and values as workload base_index does
 
     @property
     def seed(self) -> int:
-        return 1000 + self.index
+        return 1000 + (self.index if self.base_index is None else self.base_index)
 
 
 SPECS: dict[str, Spec] = {
@@ -91,10 +94,10 @@ SPECS: dict[str, Spec] = {
              ("lognormal", 1024.0, 1.0, 16, 16384)),
         Spec("llama2_7b_verify4", 7, "LLaMA-2-7B-shaped draft verification: the llama2_7b batch "
              "shape with 4 query tokens per sequence (the last 4 cached tokens, causal)", 64, 32, 32,
-             128, "bf16", ("uniform", 128, 2048), num_queries=4),
+             128, "bf16", ("uniform", 128, 2048), num_queries=4, base_index=2),
         Spec("llama3_8b_gqa_verify4", 8, "Llama-3-8B-shaped GQA draft verification: the "
              "llama3_8b_gqa batch shape with 4 query tokens per sequence (causal)", 128, 32, 8, 128,
-             "bf16", ("uniform", 512, 8192), num_queries=4),
+             "bf16", ("uniform", 512, 8192), num_queries=4, base_index=3),
     )
 }
 

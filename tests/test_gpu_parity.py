@@ -251,9 +251,10 @@ def test_named_workload_full_size(name):
     check_all(w, kv, 0, seqs)
 
 
-@pytest.mark.parametrize("name", ["llama3_8b_gqa", "int8_cb", "fp8_cb"])
+@pytest.mark.parametrize("name", ["llama2_7b", "llama3_8b_gqa", "long_32k", "int8_cb", "fp8_cb"])
 def test_named_workload_cuda_core_kernel(name):
-    """The GQA workloads through the CUDA-core kernel too (auto picks the tensor cores)."""
+    """The full-size workloads through the CUDA-core kernel too (auto picks the tensor
+    cores wherever they are built)."""
     w = W.make(name, device="cuda")
     check_all(w, W.SPECS[name].kv_dtype, 0, _sample(w, 3), kernel="cuda_core")
 

@@ -130,7 +130,8 @@ def test_plan_limits():
     pool = pkv.PagedKVPool(4, 8, 128, "bf16", fill=0)
     assert pkv.decode_plan(pool, 2, 32, 64, num_queries=4)["kernel"] == "tensor_core"   # 16 columns
     assert pkv.decode_plan(pool, 2, 8, 64, num_queries=4)["kernel"] == "tensor_core"    # MHA, 4 columns
-    assert pkv.decode_plan(pool, 2, 8, 64, num_queries=1)["kernel"] == "cuda_core"      # MHA decode
+    assert pkv.decode_plan(pool, 2, 8, 64, num_queries=1)["kernel"] == "tensor_core"    # MHA decode
+    assert pkv.decode_plan(pool, 2, 8, 64, kernel="cuda_core")["kernel"] == "cuda_core"
     with pytest.raises(pkv.PagedKVError, match="unsupported"):
         pkv.decode_plan(pool, 2, 64, 64, num_queries=4)                 # 32 columns
     with pytest.raises(pkv.PagedKVError, match="unsupported"):
