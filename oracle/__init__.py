@@ -27,6 +27,9 @@ What each function follows (page title, section):
 * ``paged_decode_multi`` -- k query tokens per sequence for speculative verification (the
   target model checks k drafts in one pass; "Lesson 4", 5.2): the drafts are the last k
   cached tokens, query i attends causally to tokens ``0 .. T - k + i``.
+* ``paged_decode_multi(..., window=W)`` -- a sliding window ("LLM/MLLM inference
+  optimisation", 2.3: keep only the most recent window of the cache): each query attends to
+  its last W tokens.
 * ``kv_cache_bytes`` -- the KV-cache size closed form
   ``2 * layers * n_kv * head_dim * seq_len * bytes``; "LLM/MLLM inference
   optimisation", section 2.2.
@@ -139,6 +142,9 @@ class Oracle:
         lib.oracle_paged_decode_multi.argtypes = [
             vp, vp, vp, vp, vp, i32, i64, i32, i32, vp, i32, vp, i32, i32, i32, ctypes.c_double, vp]
         lib.oracle_paged_decode_multi.restype = i32
+        lib.oracle_paged_decode_window.argtypes = [
+            vp, vp, vp, vp, vp, i32, i64, i32, i32, vp, i32, vp, i32, i32, i32, i32, ctypes.c_double, vp]
+        lib.oracle_paged_decode_window.restype = i32
         self.lib = lib
 
     # -- threads
@@ -255,9 +261,10 @@ class Oracle:
 
 
     def paged_decode_multi(self, q, k_cache, v_cache, block_tables, context_lens, scale,
-                           k_scale=None, v_scale=None) -> np.ndarray:
+                           k_scale=None, v_scale=None, window: int = 0) -> np.ndarray:
         """fp64 [B, k, Hq, d]: q bf16 bits [B, k, Hq, d]; the k queries of sequence b are its
-        last k cached tokens, query i attending causally to tokens 0 .. T_b - k + i."""
+        last k cached tokens, query i attending causally to tokens 0 .. T_b - k + i (with
+        ``window`` W > 0, only to its last W: T_b - k + i - W + 1 .. T_b - k + i)."""
         q = _c(q, np.uint16)
         kdt = k_cache.dtype
         kv_dtype = {np.dtype(np.int8): KV_INT8, np.dtype(np.uint8): KV_FP8}.get(np.dtype(kdt), KV_BF16)
@@ -272,9 +279,9 @@ class Oracle:
         nb, hkv, bs, d2 = k_cache.shape
         assert bs == BLOCK_SIZE and d2 == d and bt.shape[0] == b and cl.shape[0] == b
         out = np.zeros((b, nq, hq, d), np.float64)
-        _check(self.lib.oracle_paged_decode_multi(
+        _check(self.lib.oracle_paged_decode_window(
             _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(k_scale), _ptr(v_scale), kv_dtype,
-            nb, hkv, d, _ptr(bt), bt.shape[1], _ptr(cl), b, nq, hq, float(scale), _ptr(out)))
+            nb, hkv, d, _ptr(bt), bt.shape[1], _ptr(cl), b, nq, int(window), hq, float(scale), _ptr(out)))
         return out
 
 

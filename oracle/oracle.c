@@ -32,6 +32,9 @@
  *    tokens in one pass ("Lesson 4", 5.2 "Speculative Decoding", algorithm step 2; "LLM/MLLM
  *    inference optimisation", 6.1).  The drafts are the last k tokens in the cache; query i
  *    (position T - k + i) attends causally, to tokens 0 .. T - k + i.
+ *  - Sliding window ("LLM/MLLM inference optimisation", 2.3, KV-cache table: keep only the
+ *    most recent window of the cache, for a fixed memory footprint): with a window of W
+ *    tokens a query at position p attends to tokens p - W + 1 .. p (those that exist).
  *  - FP8 KV cache (same section names FP8 with its larger dynamic range, and that vLLM
  *    supports an FP8 KV cache; it gives no scaling rule).  Read here as the INT8 scheme
  *    with the E4M3 format in place of int8: s = max|x| / 448 per (token, kv head) row,
@@ -338,27 +341,31 @@ static double cache_value(const void* cache, const float* scales, int kv_dtype,
  * q: bf16 bits [B, Hq, d]; block_tables: [B, max_blocks_per_seq]; context_lens: [B];
  * out: fp64 [B, Hq, d].  Entries of block_tables past the last used block are never read.
  */
-int oracle_paged_decode_multi(const uint16_t* q, const void* k_cache, const void* v_cache,
-                              const float* k_scale, const float* v_scale, int kv_dtype,
-                              int64_t num_blocks, int kv_heads, int head_dim,
-                              const int32_t* block_tables, int max_blocks_per_seq,
-                              const int32_t* context_lens, int num_seqs, int num_queries,
-                              int num_q_heads, double scale, double* out) {
+int oracle_paged_decode_window(const uint16_t* q, const void* k_cache, const void* v_cache,
+                               const float* k_scale, const float* v_scale, int kv_dtype,
+                               int64_t num_blocks, int kv_heads, int head_dim,
+                               const int32_t* block_tables, int max_blocks_per_seq,
+                               const int32_t* context_lens, int num_seqs, int num_queries,
+                               int window, int num_q_heads, double scale, double* out) {
   if (num_seqs < 0 || kv_heads < 1 || head_dim < 1 || num_blocks < 1 || max_blocks_per_seq < 1 ||
-      num_queries < 1)
+      num_queries < 1 || window < 0)
     return ORACLE_ERR_ARG;
   if (num_q_heads < kv_heads || num_q_heads % kv_heads != 0) return ORACLE_ERR_ARG;
   if (kv_dtype != ORACLE_KV_BF16 && kv_dtype != ORACLE_KV_INT8 && kv_dtype != ORACLE_KV_FP8)
     return ORACLE_ERR_ARG;
   if (kv_dtype != ORACLE_KV_BF16 && (!k_scale || !v_scale)) return ORACLE_ERR_ARG;
 
-  /* Validate everything that will be read before any arithmetic. */
+  /* Validate everything that will be read before any arithmetic: the table entries of the
+   * blocks that hold a token some query sees (with a window, earlier entries are never
+   * read and may hold anything). */
   for (int b = 0; b < num_seqs; ++b) {
     int T = context_lens[b];
     if (T < num_queries || (int64_t)T > (int64_t)max_blocks_per_seq * ORACLE_BLOCK_SIZE)
       return ORACLE_ERR_CONTEXT;
+    int first = 0;  /* the first query's first visible token */
+    if (window > 0 && T - (num_queries - 1) - window > 0) first = T - (num_queries - 1) - window;
     int nblk = (T + ORACLE_BLOCK_SIZE - 1) / ORACLE_BLOCK_SIZE;
-    for (int j = 0; j < nblk; ++j) {
+    for (int j = first / ORACLE_BLOCK_SIZE; j < nblk; ++j) {
       int32_t phys = block_tables[(int64_t)b * max_blocks_per_seq + j];
       if (phys < 0 || (int64_t)phys >= num_blocks) return ORACLE_ERR_BLOCK_ID;
     }
@@ -374,12 +381,14 @@ int oracle_paged_decode_multi(const uint16_t* q, const void* k_cache, const void
     const int qi = (int)((bh / num_q_heads) % num_queries);
     const int h = (int)(bh % num_q_heads);
     const int kvh = h / group;
-    /* query qi sits at position T - num_queries + qi and sees tokens up to and including it */
+    /* query qi sits at position T - num_queries + qi and sees tokens up to and including it,
+     * and with a window only the last `window` of those */
     const int T = context_lens[b] - (num_queries - 1 - qi);
+    const int lo = (window > 0 && T > window) ? T - window : 0;
     const uint16_t* qrow = q + bh * head_dim;
     double* orow = out + bh * head_dim;
 
-    double* logits = (double*)malloc(sizeof(double) * (size_t)T);
+    double* logits = (double*)malloc(sizeof(double) * (size_t)(T - lo));
     double* qd = (double*)malloc(sizeof(double) * (size_t)head_dim);
     if (!logits || !qd) {
       free(logits);
@@ -392,7 +401,7 @@ int oracle_paged_decode_multi(const uint16_t* q, const void* k_cache, const void
 
     /* Pass 1: the logits, walking the page table in logical order. */
     double lmax = -INFINITY;
-    for (int t = 0; t < T; ++t) {
+    for (int t = lo; t < T; ++t) {
       int j = t / ORACLE_BLOCK_SIZE;
       int i = t % ORACLE_BLOCK_SIZE;
       int64_t phys = block_tables[(int64_t)b * max_blocks_per_seq + j];
@@ -400,23 +409,23 @@ int oracle_paged_decode_multi(const uint16_t* q, const void* k_cache, const void
       double dot = 0.0;
       for (int c = 0; c < head_dim; ++c)
         dot += qd[c] * cache_value(k_cache, k_scale, kv_dtype, row, head_dim, c);
-      logits[t] = scale * dot;
-      if (logits[t] > lmax) lmax = logits[t];
+      logits[t - lo] = scale * dot;
+      if (logits[t - lo] > lmax) lmax = logits[t - lo];
     }
 
     /* Pass 2: softmax weights and the weighted sum of the value rows. */
     double denom = 0.0;
-    for (int t = 0; t < T; ++t) {
-      logits[t] = exp(logits[t] - lmax);
-      denom += logits[t];
+    for (int t = lo; t < T; ++t) {
+      logits[t - lo] = exp(logits[t - lo] - lmax);
+      denom += logits[t - lo];
     }
     for (int c = 0; c < head_dim; ++c) orow[c] = 0.0;
-    for (int t = 0; t < T; ++t) {
+    for (int t = lo; t < T; ++t) {
       int j = t / ORACLE_BLOCK_SIZE;
       int i = t % ORACLE_BLOCK_SIZE;
       int64_t phys = block_tables[(int64_t)b * max_blocks_per_seq + j];
       int64_t row = (phys * kv_heads + kvh) * ORACLE_BLOCK_SIZE + i;
-      double w = logits[t] / denom;
+      double w = logits[t - lo] / denom;
       for (int c = 0; c < head_dim; ++c)
         orow[c] += w * cache_value(v_cache, v_scale, kv_dtype, row, head_dim, c);
     }
@@ -424,6 +433,18 @@ int oracle_paged_decode_multi(const uint16_t* q, const void* k_cache, const void
     free(qd);
   }
   return err;
+}
+
+/* Every query over its whole causal prefix: the windowed decode with no window. */
+int oracle_paged_decode_multi(const uint16_t* q, const void* k_cache, const void* v_cache,
+                              const float* k_scale, const float* v_scale, int kv_dtype,
+                              int64_t num_blocks, int kv_heads, int head_dim,
+                              const int32_t* block_tables, int max_blocks_per_seq,
+                              const int32_t* context_lens, int num_seqs, int num_queries,
+                              int num_q_heads, double scale, double* out) {
+  return oracle_paged_decode_window(q, k_cache, v_cache, k_scale, v_scale, kv_dtype, num_blocks,
+                                    kv_heads, head_dim, block_tables, max_blocks_per_seq,
+                                    context_lens, num_seqs, num_queries, 0, num_q_heads, scale, out);
 }
 
 /* One query token per sequence (the newest): the multi-query decode with k = 1. */

@@ -15,6 +15,8 @@ Sources (page title, section):
     tests/golden/kv_cache_sizes.json); 2.3 -- MQA/GQA head sharing.
   * "Lesson 4", 5.2 "Speculative Decoding" -- the target model verifies k draft tokens in
     one pass: k queries per sequence, each causal over the prefix up to itself.
+  * "LLM/MLLM inference optimisation", 2.3 (KV-cache table) -- a sliding window keeps only
+    the most recent tokens: each query attends to its last W tokens.
 """
 
 from __future__ import annotations
@@ -490,6 +492,74 @@ def pin_multi_query_first_draft(o):
     except oracle_mod.OracleError:
         return
     raise AssertionError("more queries than cached tokens accepted")
+
+
+def sdpa_band_fp64(q, k, v, scale, window):
+    """torch fp64 SDPA for the last n positions of a sequence under an explicit boolean
+    band mask: query i at position p_i = T - n + i may attend to p_i - W < t <= p_i."""
+    n, t_len = q.shape[0], k.shape[0]
+    pos = (t_len - n + torch.arange(n))[:, None]
+    t = torch.arange(t_len)[None, :]
+    allowed = (t <= pos) & (t > pos - window)
+    qq = q.to(torch.float64).permute(1, 0, 2)[None]
+    kk = k.to(torch.float64).permute(1, 0, 2)[None]
+    vv = v.to(torch.float64).permute(1, 0, 2)[None]
+    out = torch.nn.functional.scaled_dot_product_attention(qq, kk, vv, attn_mask=allowed, scale=scale)
+    return out[0].permute(1, 0, 2).numpy()
+
+
+def pin_sliding_window_band_sdpa(o):
+    """A sliding window of W tokens ("LLM/MLLM inference optimisation", 2.3) equals torch's
+    fp64 SDPA under a band mask, for one and several queries per sequence, windows inside a
+    block, on block boundaries and longer than the context, bf16 and INT8."""
+    gen = torch.Generator().manual_seed(33)
+    cases = (([1, 16, 17, 40, 70], 1, 4, 2, 32, 5, "bf16"), ([3, 20, 48, 90], 3, 4, 4, 16, 16, "bf16"),
+             ([5, 33, 64], 4, 8, 2, 64, 17, "int8"), ([9, 30], 2, 2, 1, 8, 1, "bf16"),
+             ([12, 50], 3, 3, 3, 16, 200, "bf16"))
+    for lens, nq, hq, hkv, d, win, kv in cases:
+        _, pool, tab, ln, k, v = paged_case(o, lens, hq, hkv, d, gen, kv=kv)
+        q = rand_bf16(gen, len(lens), nq, hq, d)
+        scale = 1.0 / math.sqrt(d)
+        out = o.paged_decode_multi(bits(q), pool["k_cache"], pool["v_cache"], tab, ln, scale,
+                                   pool.get("k_scale"), pool.get("v_scale"), window=win)
+        g = hq // hkv
+        for b in range(len(lens)):
+            kb, vb = k[b].double(), v[b].double()
+            if kv == "int8":
+                kcodes, kscales = o.quantize_rows(bits(k[b]))
+                vcodes, vscales = o.quantize_rows(bits(v[b]))
+                kb = torch.from_numpy(kcodes.astype(np.float64) * kscales.astype(np.float64)[..., None])
+                vb = torch.from_numpy(vcodes.astype(np.float64) * vscales.astype(np.float64)[..., None])
+            ref = sdpa_band_fp64(q[b], kb.repeat_interleave(g, 1), vb.repeat_interleave(g, 1), scale, win)
+            np.testing.assert_allclose(out[b], ref, rtol=1e-12, atol=1e-13)
+
+
+def pin_sliding_window_special_cases(o):
+    """W = 1: each query returns its own token's V exactly.  W >= T: the full result, bit
+    for bit.  Blocks wholly before the window may be released: their table entries (-1) and
+    contents (NaN) are never read."""
+    gen = torch.Generator().manual_seed(34)
+    lens, nq, hq, hkv, d = [3, 18, 35, 64], 3, 4, 2, 16
+    _, pool, tab, ln, k, v = paged_case(o, lens, hq, hkv, d, gen)
+    q = rand_bf16(gen, len(lens), nq, hq, d)
+    run = lambda t, w: o.paged_decode_multi(bits(q), pool["k_cache"], pool["v_cache"], t, ln, 0.25, window=w)
+    one = run(tab, 1)
+    for b, t_len in enumerate(lens):
+        for i in range(nq):
+            own = v[b][t_len - nq + i].double().numpy()  # [Hkv, d]
+            assert np.array_equal(one[b, i], own.repeat(hq // hkv, axis=0))
+    assert np.array_equal(run(tab, 64), run(tab, 0))
+    win = 20
+    full = run(tab, win)
+    released = tab.copy()
+    kc = pool["k_cache"].copy()
+    for b, t_len in enumerate(lens):
+        first = max(0, t_len - (nq - 1) - win) // BS  # first block any query sees
+        for j in range(first):
+            kc[released[b, j]] = np.uint16(0x7FC0)
+            released[b, j] = -1
+    out = o.paged_decode_multi(bits(q), kc, pool["v_cache"], released, ln, 0.25, window=win)
+    assert np.array_equal(out, full)
 
 
 def pin_kv_cache_size_closed_forms(o):

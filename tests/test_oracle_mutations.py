@@ -12,19 +12,20 @@ import oracle_pins
 
 MUTANTS = [
     ("GQA maps head h to h % Hkv", "const int kvh = h / group;", "const int kvh = h % kv_heads;"),
-    ("softmax scale dropped", "logits[t] = scale * dot;", "logits[t] = dot;"),
+    ("softmax scale dropped", "logits[t - lo] = scale * dot;", "logits[t - lo] = dot;"),
     ("reversed offset inside the block when reading K",
      "int64_t row = (phys * kv_heads + kvh) * ORACLE_BLOCK_SIZE + i;\n      double dot",
      "int64_t row = (phys * kv_heads + kvh) * ORACLE_BLOCK_SIZE + (ORACLE_BLOCK_SIZE - 1 - i);\n      double dot"),
     ("pool index transposed (head-major)", "int64_t row = (phys * kv_heads + kvh)",
      "int64_t row = (kvh * num_blocks + phys)"),
     ("first softmax term left unexponentiated",
-     "for (int t = 0; t < T; ++t) {\n      logits[t] = exp(", "for (int t = 1; t < T; ++t) {\n      logits[t] = exp("),
+     "for (int t = lo; t < T; ++t) {\n      logits[t - lo] = exp(", "for (int t = lo + 1; t < T; ++t) {\n      logits[t - lo] = exp("),
     ("last token dropped from the value sum",
-     "for (int t = 0; t < T; ++t) {\n      int j = t / ORACLE_BLOCK_SIZE;\n      int i = t % ORACLE_BLOCK_SIZE;\n      int64_t phys = block_tables[(int64_t)b * max_blocks_per_seq + j];\n      int64_t row = (phys * kv_heads + kvh) * ORACLE_BLOCK_SIZE + i;\n      double w",
-     "for (int t = 0; t < T - 1; ++t) {\n      int j = t / ORACLE_BLOCK_SIZE;\n      int i = t % ORACLE_BLOCK_SIZE;\n      int64_t phys = block_tables[(int64_t)b * max_blocks_per_seq + j];\n      int64_t row = (phys * kv_heads + kvh) * ORACLE_BLOCK_SIZE + i;\n      double w"),
-    ("weights not normalised", "double w = logits[t] / denom;", "double w = logits[t];"),
-    ("no max shift (overflows on large logits)", "logits[t] = exp(logits[t] - lmax);", "logits[t] = exp(logits[t]);"),
+     "for (int t = lo; t < T; ++t) {\n      int j = t / ORACLE_BLOCK_SIZE;\n      int i = t % ORACLE_BLOCK_SIZE;\n      int64_t phys = block_tables[(int64_t)b * max_blocks_per_seq + j];\n      int64_t row = (phys * kv_heads + kvh) * ORACLE_BLOCK_SIZE + i;\n      double w",
+     "for (int t = lo; t < T - 1; ++t) {\n      int j = t / ORACLE_BLOCK_SIZE;\n      int i = t % ORACLE_BLOCK_SIZE;\n      int64_t phys = block_tables[(int64_t)b * max_blocks_per_seq + j];\n      int64_t row = (phys * kv_heads + kvh) * ORACLE_BLOCK_SIZE + i;\n      double w"),
+    ("weights not normalised", "double w = logits[t - lo] / denom;", "double w = logits[t - lo];"),
+    ("no max shift (overflows on large logits)", "logits[t - lo] = exp(logits[t - lo] - lmax);",
+     "logits[t - lo] = exp(logits[t - lo]);"),
     ("bf16 widened with the wrong shift", "((uint32_t)bits) << 16", "((uint32_t)bits) << 15"),
     ("quantiser divides by 128", "float s = amax / 127.0f;", "float s = amax / 128.0f;"),
     ("quantiser rounds half away from zero", "float r = rintf(y);", "float r = roundf(y);"),
@@ -48,6 +49,10 @@ MUTANTS = [
      "const int T = context_lens[b] - (num_queries - 2 - qi) - (qi == num_queries - 1);"),
     ("queries in reverse order", "const int T = context_lens[b] - (num_queries - 1 - qi);",
      "const int T = context_lens[b] - qi;"),
+    ("window one token too wide", "const int lo = (window > 0 && T > window) ? T - window : 0;",
+     "const int lo = (window > 0 && T > window) ? T - window - 1 : 0;"),
+    ("window ends at the newest token, not at the query", "const int lo = (window > 0 && T > window) ? T - window : 0;",
+     "const int lo = (window > 0 && T > window) ? (context_lens[b] - window > 0 ? context_lens[b] - window : 0) : 0;"),
     ("query widened from the wrong head", "const uint16_t* qrow = q + bh * head_dim;",
      "const uint16_t* qrow = q + ((int64_t)b * num_q_heads + (num_q_heads - 1 - h)) * head_dim;"),
 ]
