@@ -12,7 +12,8 @@ is done between steps.
 
 The ``*_verify4`` workloads time a speculative-decoding verification step instead: 4
 draft tokens per sequence are appended, then one multi-query call attends each draft
-causally over the cache.
+causally over the cache.  ``long_32k_window4k`` decodes the long_32k cache with a 4096-token
+sliding window (bytes count the tokens each sequence's window covers).
 
 Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
                        [--workload NAME]
@@ -56,7 +57,8 @@ KERNEL_SOURCES = {
     "cuda_core": ["pkv_device.cuh", "pkv_internal.h", "pkv_decode.cuh", "pkv_decode_bf16.cu",
                   "pkv_decode_int8.cu"],
     "tensor_core": ["pkv_device.cuh", "pkv_internal.h", "pkv_decode.cuh", "pkv_decode_mma.cuh",
-                    "pkv_decode_mma.cu"],
+                    "pkv_decode_mma.cu", "pkv_decode_mma_bf16.cu", "pkv_decode_mma_int8.cu",
+                    "pkv_decode_mma_fp8.cu"],
 }
 
 
@@ -214,17 +216,17 @@ def run_ours(args, rank, world, local):
     lens = w.context_lens.to(dev)
     out = torch.empty_like(q)
     max_ctx = w.max_context_len
-    nq = w.num_queries
-    ws_n = pkv.decode_workspace_bytes(pool, w.num_seqs, w.num_q_heads, max_ctx, num_queries=nq)
+    nq, win = w.num_queries, spec.window
+    ws_n = pkv.decode_workspace_bytes(pool, w.num_seqs, w.num_q_heads, max_ctx, num_queries=nq, window=win)
     ws = torch.empty(max(ws_n, 16), dtype=torch.uint8, device=dev)
-    plan = pkv.decode_plan(pool, w.num_seqs, w.num_q_heads, max_ctx, num_queries=nq)
+    plan = pkv.decode_plan(pool, w.num_seqs, w.num_q_heads, max_ctx, num_queries=nq, window=win)
     torch.cuda.synchronize(dev)
     assert pool.device_error() == 0
 
     def step():
         pkv.reshape_and_cache(pool, new_k, new_v, new_slots, stream)
         pkv.paged_attention_decode(pool, q, tables, lens, w.scale, max_ctx, out=out, workspace=ws,
-                                   stream=stream)
+                                   window=win, stream=stream)
 
     for _ in range(args.warmup):
         step()
@@ -244,7 +246,7 @@ def run_ours(args, rank, world, local):
         pkv.reshape_and_cache(pool, new_k, new_v, new_slots, stream)
         ev[i][0].record(stream)
         pkv.paged_attention_decode(pool, q, tables, lens, w.scale, max_ctx, out=out, workspace=ws,
-                                   stream=stream)
+                                   window=win, stream=stream)
         ev[i][1].record(stream)
     t1.record(stream)
     torch.cuda.synchronize(dev)
@@ -257,7 +259,7 @@ def run_ours(args, rank, world, local):
     assert pool.device_error() == 0
 
     sb = roofline.step_bytes(w.context_lens, w.num_q_heads, w.num_kv_heads, w.head_dim, kv,
-                             num_queries=nq)
+                             num_queries=nq, window=win)
     ms_step = ms_total / args.steps
     total_bytes = sum_over_ranks(float(sb.step) * args.steps, world, dev)
     value = total_bytes / (ms_total * 1e-3) / 1e9
@@ -265,7 +267,7 @@ def run_ours(args, rank, world, local):
 
     # ---- end to end through the public API with host buffers
     e2e = run_e2e(args, pkv, pool, w, new_k, new_v, new_slots, q, tables, lens, max_ctx, ws, sb,
-                  stream, dev, world)
+                  stream, dev, world, win)
 
     peak, peak_kind = measured_peaks()
     achieved = sb.decode / (dec_ms * 1e-3) / 1e9
@@ -286,7 +288,7 @@ def run_ours(args, rank, world, local):
             "step": ("reshape_and_cache of one new token per sequence + paged_attention_decode" if nq == 1 else
                      f"reshape_and_cache of {nq} draft tokens per sequence + one multi-query "
                      f"paged_attention_decode verifying them (causal over the last {nq} positions)"),
-            "num_queries": nq,
+            "num_queries": nq, "window": win or None,
             "plan": plan, "l2": "inputs larger than L2 (pool %.2f GB > 129 MB); no flush" % (
                 2 * pool.k_cache.numel() * pool.k_cache.element_size() / 1e9),
             "parallelism": f"{world} independent replicas" if world > 1 else "single GPU",
@@ -311,7 +313,7 @@ def run_ours(args, rank, world, local):
 
 
 def run_e2e(args, pkv, pool, w, new_k, new_v, new_slots, q, tables, lens, max_ctx, ws, sb, stream,
-            dev, world):
+            dev, world, win=0):
     """Same step through the public API, but every step copies its inputs from pinned
     host memory and reads the output back."""
     host = {
@@ -330,7 +332,7 @@ def run_e2e(args, pkv, pool, w, new_k, new_v, new_slots, q, tables, lens, max_ct
             dbuf[k].copy_(host[k], non_blocking=True)
         pkv.reshape_and_cache(pool, dbuf["k"], dbuf["v"], dbuf["slots"], stream)
         pkv.paged_attention_decode(pool, dbuf["q"], dbuf["tables"], dbuf["lens"], w.scale, max_ctx,
-                                   out=out_d, workspace=ws, stream=stream)
+                                   out=out_d, workspace=ws, window=win, stream=stream)
         out_h.copy_(out_d, non_blocking=True)
 
     for _ in range(max(3, args.warmup)):
@@ -397,11 +399,16 @@ def oracle_sample(workload: str, target_s: float):
         args = dict(q=W.bf16_bits(w.q), key=key[last], value=value[last], slots=slots[last], tab=tab,
                     lens=lens, scale=w.scale)
         sb = roofline.step_bytes(w.context_lens, w.num_q_heads, w.num_kv_heads, w.head_dim, spec.kv_dtype,
-                                 num_queries=spec.num_queries)
+                                 num_queries=spec.num_queries, window=spec.window)
+        if spec.num_queries == 1 and spec.window:
+            args["q"] = args["q"][:, None]  # one query token, through the windowed decode
         return pool, args, sb
 
     write_q = o.reshape_and_cache_int8 if spec.kv_dtype == "int8" else o.reshape_and_cache_fp8
-    decode = o.paged_decode_multi if spec.num_queries > 1 else o.paged_decode
+    if spec.window:
+        decode = lambda *a: o.paged_decode_multi(*a, window=spec.window)
+    else:
+        decode = o.paged_decode_multi if spec.num_queries > 1 else o.paged_decode
 
     def run(pool, a):
         if spec.kv_dtype == "bf16":

@@ -201,7 +201,8 @@ PKV_API pkv_status pkv_block_manager_append(pkv_block_manager* manager, const in
                                             int max_copies, int* num_copies);
 
 /*
- * Shorten a sequence to its first num_tokens tokens (0 <= num_tokens <= its length): the
+ * Shorten a sequence to its first num_tokens tokens (0 <= num_tokens <= its length, and not
+ * below its released blocks, see pkv_block_manager_release_before): the
  * blocks past ceil(num_tokens / 16) are released (count - 1).  Speculative decoding uses it
  * to drop the draft tokens the target model rejected ("Lesson 4", 5.2: only the accepted
  * prefix is kept).  The slots past num_tokens in the last kept block are reused by the
@@ -209,6 +210,19 @@ PKV_API pkv_status pkv_block_manager_append(pkv_block_manager* manager, const in
  * Errors: PKV_ERR_INVALID_ARG (unknown sequence, num_tokens out of range).
  */
 PKV_API pkv_status pkv_block_manager_truncate(pkv_block_manager* manager, int seq, int num_tokens);
+
+/*
+ * Sliding window ("LLM/MLLM inference optimisation", 2.3: keep only the most recent window
+ * of the cache, for a fixed memory footprint): release the sequence's blocks that hold only
+ * tokens before position `token` (block j when 16 (j + 1) <= token).  Their table entries
+ * become -1 and each block's count drops by one; the sequence's length and the positions of
+ * its later tokens do not change.  A decode with window W and k query tokens reads from
+ * token T - (k - 1) - W on, so token = T + n - (k - 1) - W keeps every block a decode after
+ * n more appended tokens needs.  Releasing already released blocks is a no-op; truncate
+ * below a released block is refused.
+ * Errors: PKV_ERR_INVALID_ARG (unknown sequence, token < 0 or past the length).
+ */
+PKV_API pkv_status pkv_block_manager_release_before(pkv_block_manager* manager, int seq, int token);
 
 /*
  * Page tables and lengths of sequences seqs[0..n): block_tables (host, int32
@@ -255,6 +269,13 @@ PKV_API int32_t pkv_block_manager_refcount(const pkv_block_manager* manager, int
  *     [num_seqs, k, num_q_heads, head_dim]; each K/V block is still read once per kv
  *     head.  1 <= k <= 16, group * k <= 16 (<= 8 where only the CUDA-core kernel is built),
  *     max_context_len >= k, and a sequence with T_b < k counts as out of range.
+ *   window: sliding-window attention ("LLM/MLLM inference optimisation", 2.3: keep only the
+ *     most recent window of the KV cache), 0 = none.  With window W > 0 a query at
+ *     position p attends to tokens p - W + 1 .. p only.  The blocks before the first one
+ *     any query sees are never read, so their block_tables entries may be -1 (see
+ *     pkv_block_manager_release_before); slots before the window in that first block may
+ *     hold anything.  Fewer blocks are read, and the plan sizes partitions and the
+ *     workspace for the window.
  */
 #define PKV_KERNEL_AUTO 0
 #define PKV_KERNEL_CUDA_CORE 1
@@ -269,7 +290,8 @@ typedef struct pkv_decode_options {
   int stages;
   int blocks_per_stage;
   int num_queries;
-  int reserved[2];
+  int window;
+  int reserved[1];
 } pkv_decode_options;
 
 /*

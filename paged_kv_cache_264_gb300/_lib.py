@@ -47,7 +47,7 @@ SCHEDULE_PERSISTENT = 2
 class DecodeOptions(ctypes.Structure):
     _fields_ = [("partition_blocks", ctypes.c_int), ("kernel", ctypes.c_int), ("schedule", ctypes.c_int),
                 ("stages", ctypes.c_int), ("blocks_per_stage", ctypes.c_int), ("num_queries", ctypes.c_int),
-                ("reserved", ctypes.c_int * 2)]
+                ("window", ctypes.c_int), ("reserved", ctypes.c_int * 1)]
 
 
 SIGNATURES = {
@@ -77,6 +77,7 @@ SIGNATURES = {
     "pkv_block_manager_free_sequence": (_i32, [_vp, _i32]),
     "pkv_block_manager_append": (_i32, [_vp, _vp, _vp, _i32, _vp, _vp, _i32, _pi32]),
     "pkv_block_manager_truncate": (_i32, [_vp, _i32, _i32]),
+    "pkv_block_manager_release_before": (_i32, [_vp, _i32, _i32]),
     "pkv_block_manager_tables": (_i32, [_vp, _vp, _i32, _vp, _vp]),
     "pkv_block_manager_stats": (_i32, [_vp, ctypes.POINTER(ctypes.c_int64), _pi32]),
     "pkv_block_manager_refcount": (ctypes.c_int32, [_vp, ctypes.c_int32]),

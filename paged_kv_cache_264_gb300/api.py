@@ -47,9 +47,9 @@ _SCHEDULES = {0: 0, "auto": 0, 1: 1, "grid": 1, 2: 2, "persistent": 2}
 
 
 def _options(partition_blocks: int = 0, kernel=0, schedule=0, stages=0,
-             blocks_per_stage=0, num_queries=1) -> ctypes.POINTER(DecodeOptions) | None:
+             blocks_per_stage=0, num_queries=1, window=0) -> ctypes.POINTER(DecodeOptions) | None:
     if not (partition_blocks or _KERNELS[kernel] or _SCHEDULES[schedule] or stages or blocks_per_stage
-            or num_queries != 1):
+            or num_queries != 1 or window):
         return None
     o = DecodeOptions()
     o.partition_blocks = int(partition_blocks)
@@ -58,6 +58,7 @@ def _options(partition_blocks: int = 0, kernel=0, schedule=0, stages=0,
     o.stages = int(stages)
     o.blocks_per_stage = int(blocks_per_stage)
     o.num_queries = int(num_queries)
+    o.window = int(window)
     return ctypes.pointer(o)
 
 
@@ -134,11 +135,11 @@ class PagedKVPool:
 
     def decode(self, q, block_tables, context_lens, scale, max_context_len, out=None,
                workspace=None, partition_blocks=0, kernel=0, schedule=0, stages=0,
-               blocks_per_stage=0, stream=None):
+               blocks_per_stage=0, window=0, stream=None):
         return paged_attention_decode(self, q, block_tables, context_lens, scale, max_context_len,
                                       out=out, workspace=workspace, partition_blocks=partition_blocks,
                                       kernel=kernel, schedule=schedule, stages=stages,
-                                      blocks_per_stage=blocks_per_stage, stream=stream)
+                                      blocks_per_stage=blocks_per_stage, window=window, stream=stream)
 
     def device_error(self, stream=None) -> int:
         return get_device_error(self, stream)
@@ -163,20 +164,21 @@ def reshape_and_cache(pool: PagedKVPool, key: torch.Tensor, value: torch.Tensor,
 
 
 def decode_workspace_bytes(pool: PagedKVPool, num_seqs: int, num_q_heads: int, max_context_len: int,
-                           partition_blocks: int = 0, kernel=0, num_queries: int = 1) -> int:
+                           partition_blocks: int = 0, kernel=0, num_queries: int = 1, window: int = 0) -> int:
     n = ctypes.c_size_t()
     check(_lib.load().pkv_decode_workspace_bytes(_handle(pool), num_seqs, num_q_heads, max_context_len,
-                                                 _options(partition_blocks, kernel, num_queries=num_queries),
+                                                 _options(partition_blocks, kernel, num_queries=num_queries,
+                                                          window=window),
                                                  ctypes.byref(n)),
           "decode_workspace_bytes")
     return n.value
 
 
 def decode_plan(pool: PagedKVPool, num_seqs: int, num_q_heads: int, max_context_len: int,
-                partition_blocks: int = 0, kernel=0, num_queries: int = 1) -> dict:
+                partition_blocks: int = 0, kernel=0, num_queries: int = 1, window: int = 0) -> dict:
     pb, mp, kc, kf = ctypes.c_int(), ctypes.c_int(), ctypes.c_int(), ctypes.c_int()
     check(_lib.load().pkv_decode_plan(_handle(pool), num_seqs, num_q_heads, max_context_len,
-                                      _options(partition_blocks, kernel, num_queries=num_queries),
+                                      _options(partition_blocks, kernel, num_queries=num_queries, window=window),
                                       ctypes.byref(pb), ctypes.byref(mp),
                                       ctypes.byref(kc), ctypes.byref(kf)), "decode_plan")
     return {"partition_blocks": pb.value, "max_partitions": mp.value, "kernels_per_call": kc.value,
@@ -187,8 +189,11 @@ def paged_attention_decode(pool: PagedKVPool, q: torch.Tensor, block_tables: tor
                            context_lens: torch.Tensor, scale: float, max_context_len: int,
                            out: torch.Tensor | None = None, workspace: torch.Tensor | None = None,
                            partition_blocks: int = 0, kernel=0, schedule=0, stages=0,
-                           blocks_per_stage=0, stream=None) -> torch.Tensor:
+                           blocks_per_stage=0, window: int = 0, stream=None) -> torch.Tensor:
     """Decode attention for q bf16 [B, Hq, d] over the pool; returns out bf16 [B, Hq, d].
+
+    ``window`` W > 0: sliding window, each query attends to its last W tokens only (table
+    entries of blocks before the first one any query sees are not read and may be -1).
 
     A 4-D q [B, k, Hq, d] holds k query tokens per sequence -- its last k cached positions,
     query i attending causally to tokens t < T_b - (k - 1 - i) -- for verifying k draft
@@ -210,14 +215,14 @@ def paged_attention_decode(pool: PagedKVPool, q: torch.Tensor, block_tables: tor
         _need(out, torch.bfloat16, "out", q.dim())
         if out.shape != q.shape:
             raise ValueError("out must have q's shape")
-    need = decode_workspace_bytes(pool, b, hq, max_context_len, partition_blocks, kernel, nq) if b else 0
+    need = decode_workspace_bytes(pool, b, hq, max_context_len, partition_blocks, kernel, nq, window) if b else 0
     if need and workspace is None:
         workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
     ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
     check(_lib.load().pkv_paged_attention_decode_ex(
         _handle(pool), _ptr(q), _ptr(block_tables), block_tables.shape[1], _ptr(context_lens), b, hq,
         int(max_context_len), float(scale), _ptr(out), _ptr(workspace), ws_bytes,
-        _options(partition_blocks, kernel, schedule, stages, blocks_per_stage, nq), _stream(stream)),
+        _options(partition_blocks, kernel, schedule, stages, blocks_per_stage, nq, window), _stream(stream)),
         "paged_attention_decode")
     return out
 
@@ -315,6 +320,11 @@ class BlockManager:
     def truncate(self, seq: int, num_tokens: int) -> None:
         """Keep the first num_tokens tokens of a sequence (drop rejected draft tokens)."""
         check(self.lib.pkv_block_manager_truncate(self.handle, seq, num_tokens), "truncate")
+
+    def release_before(self, seq: int, token: int) -> None:
+        """Give back the blocks holding only tokens before position ``token`` (sliding
+        window); their table entries become -1."""
+        check(self.lib.pkv_block_manager_release_before(self.handle, seq, token), "release_before")
 
     def tables(self, seqs):
         """(block_tables int32 [n, max_blocks_per_seq] with -1 padding, context_lens int32 [n])."""

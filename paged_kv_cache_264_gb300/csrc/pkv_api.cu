@@ -77,6 +77,7 @@ struct Plan {
   int kernel;  // PKV_KERNEL_CUDA_CORE or PKV_KERNEL_TENSOR_CORE
   int cols;    // query-column slots of the kernel variant (>= group * num_queries)
   int num_queries;
+  int window;  // tokens each query sees back from its own position (pkv::kNoWindow: all)
   int shape;   // tensor-core ring shape index
   int persistent;
   int ctas_per_sm;
@@ -89,11 +90,20 @@ struct Plan {
 
 pkv_status make_plan(const pkv_pool* pool, int num_seqs, int num_q_heads, int max_context_len,
                      const pkv_decode_options* opt, Plan* plan) {
-  const int64_t max_nblk = ceil_div(max_context_len, pkv::kBlockSize);
   const int group = num_q_heads / pool->kv_heads;
   const int nq = num_queries_of(opt);
   if (nq < 1) return PKV_ERR_INVALID_ARG;
   if (max_context_len < nq) return PKV_ERR_INVALID_ARG;
+  const int window = opt ? opt->window : 0;
+  if (window < 0) return PKV_ERR_INVALID_ARG;
+  plan->window = (window == 0 || window >= pkv::kNoWindow) ? pkv::kNoWindow : window;
+  // Blocks one sequence's work can span: the whole context, or with a window the blocks
+  // that hold the window of its first query up to its newest token.
+  int64_t max_nblk = ceil_div(max_context_len, pkv::kBlockSize);
+  if (plan->window != pkv::kNoWindow) {
+    const int64_t span = ceil_div(int64_t(plan->window) + nq - 1, pkv::kBlockSize) + 1;
+    if (span < max_nblk) max_nblk = span;
+  }
   const auto kv = static_cast<pkv::KvType>(pool->dtype);
   // Query columns per (sequence, kv head): the group's heads times the query tokens.  The
   // tensor-core kernel holds 2 to 16 column slots, the CUDA-core kernel 1 to 8.
@@ -131,7 +141,8 @@ pkv_status make_plan(const pkv_pool* pool, int num_seqs, int num_q_heads, int ma
     return PKV_ERR_UNSUPPORTED;
   }
   const int per_sm = plan->kernel == PKV_KERNEL_TENSOR_CORE
-                         ? pkv::mma_ctas_per_sm(kv, pool->head_dim, plan->cols, plan->shape)
+                         ? pkv::mma_ctas_per_sm(kv, pool->head_dim, plan->cols, plan->shape,
+                                                nq > 1 || plan->window != pkv::kNoWindow)
                          : pkv::decode_ctas_per_sm(kv, pool->head_dim, plan->cols);
   plan->ctas_per_sm = per_sm > 0 ? per_sm : 1;
   int P;
@@ -213,6 +224,7 @@ pkv_status check_decode_shape(const pkv_pool* pool, int num_seqs, int num_q_head
                               int max_context_len) {
   if (!pool) return PKV_ERR_INVALID_ARG;
   if (num_seqs < 0 || num_q_heads < 1 || max_context_len < 1) return PKV_ERR_INVALID_ARG;
+  if (max_context_len >= pkv::kNoWindow) return PKV_ERR_INVALID_ARG;
   if (num_q_heads % pool->kv_heads != 0) return PKV_ERR_INVALID_ARG;
   if (!group_supported(num_q_heads / pool->kv_heads)) return PKV_ERR_UNSUPPORTED;
   return PKV_OK;
@@ -461,6 +473,7 @@ pkv_status pkv_paged_attention_decode_ex(const pkv_pool* pool, const void* q,
   p.group = num_q_heads / pool->kv_heads;
   p.group_log2 = p.group == 8 ? 3 : p.group == 4 ? 2 : p.group == 2 ? 1 : 0;
   p.num_queries = plan.num_queries;
+  p.window = plan.window;
   p.head_dim = pool->head_dim;
   p.max_context_len = max_context_len;
   p.partition_blocks = plan.partition_blocks;

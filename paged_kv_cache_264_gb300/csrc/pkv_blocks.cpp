@@ -12,6 +12,11 @@
 // filled first copies that block (copy on write): the manager takes a fresh block,
 // reports the (source, destination) pair for pkv_copy_blocks, and moves its own reference.
 // Full shared blocks are never written again, so they stay shared.
+//
+// Sliding window ("LLM/MLLM inference optimisation", 2.3: keep only the most recent window
+// of the cache): release_before() gives back the blocks wholly behind a window; their
+// table entries become -1 while positions keep counting, so the memory a sequence holds
+// stays bounded by its window.
 #include <algorithm>
 #include <mutex>
 #include <new>
@@ -22,7 +27,8 @@
 struct pkv_block_manager {
   struct Seq {
     bool live = false;
-    int32_t len = 0;  // tokens in the cache
+    int32_t len = 0;       // tokens in the cache (positions, released ones included)
+    int32_t released = 0;  // leading blocks given back by release_before (entries -1)
     std::vector<int32_t> blocks;
   };
   int64_t num_blocks = 0;
@@ -52,6 +58,7 @@ int32_t take_block(pkv_block_manager* m) {
 }
 
 void drop_block(pkv_block_manager* m, int32_t b) {
+  if (b < 0) return;  // released entry
   if (--m->refcount[size_t(b)] == 0) m->free_blocks.push_back(b);
 }
 
@@ -100,6 +107,7 @@ PKV_API pkv_status pkv_block_manager_add_sequence(pkv_block_manager* m, int* seq
   auto& q = m->seqs[size_t(s)];
   q.live = true;
   q.len = 0;
+  q.released = 0;
   q.blocks.clear();
   ++m->live;
   *seq = s;
@@ -117,8 +125,10 @@ PKV_API pkv_status pkv_block_manager_fork(pkv_block_manager* m, int parent, int*
   auto& q = m->seqs[size_t(c)];
   q.live = true;
   q.len = p.len;
+  q.released = p.released;
   q.blocks = p.blocks;
-  for (int32_t b : q.blocks) ++m->refcount[size_t(b)];
+  for (int32_t b : q.blocks)
+    if (b >= 0) ++m->refcount[size_t(b)];
   ++m->live;
   *child = c;
   return PKV_OK;
@@ -132,6 +142,7 @@ PKV_API pkv_status pkv_block_manager_free_sequence(pkv_block_manager* m, int seq
   for (int32_t b : q.blocks) drop_block(m, b);
   q.blocks.clear();
   q.len = 0;
+  q.released = 0;
   q.live = false;
   m->free_seqs.push_back(seq);
   --m->live;
@@ -199,13 +210,29 @@ PKV_API pkv_status pkv_block_manager_truncate(pkv_block_manager* m, int seq, int
   std::lock_guard<std::mutex> lock(m->mu);
   if (!seq_ok(m, seq)) return PKV_ERR_INVALID_ARG;
   auto& q = m->seqs[size_t(seq)];
-  if (num_tokens < 0 || num_tokens > q.len) return PKV_ERR_INVALID_ARG;
+  if (num_tokens < 0 || num_tokens > q.len || num_tokens < q.released * kBlock)
+    return PKV_ERR_INVALID_ARG;
   const size_t keep = size_t((num_tokens + kBlock - 1) / kBlock);
   while (q.blocks.size() > keep) {
     drop_block(m, q.blocks.back());
     q.blocks.pop_back();
   }
   q.len = num_tokens;
+  return PKV_OK;
+}
+
+PKV_API pkv_status pkv_block_manager_release_before(pkv_block_manager* m, int seq, int token) {
+  if (!m) return PKV_ERR_INVALID_ARG;
+  std::lock_guard<std::mutex> lock(m->mu);
+  if (!seq_ok(m, seq)) return PKV_ERR_INVALID_ARG;
+  auto& q = m->seqs[size_t(seq)];
+  if (token < 0 || token > q.len) return PKV_ERR_INVALID_ARG;
+  const int32_t upto = token / kBlock;  // blocks 0 .. upto-1 hold only tokens before `token`
+  for (int32_t j = q.released; j < upto; ++j) {
+    drop_block(m, q.blocks[size_t(j)]);
+    q.blocks[size_t(j)] = -1;
+  }
+  if (upto > q.released) q.released = upto;
   return PKV_OK;
 }
 

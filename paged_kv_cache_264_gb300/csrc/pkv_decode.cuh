@@ -40,6 +40,12 @@
 // is still read once, and each column carries its own causal cut.  With k = 1 this is the
 // plain decode above.
 //
+// Sliding window ("LLM/MLLM inference optimisation", 2.3: keep only the most recent window
+// of the cache): a query at position p sees tokens p - W + 1 .. p.  A sequence's work then
+// starts at the first block any of its queries sees; earlier blocks are never read (their
+// table entries may be -1), and tokens of that first block before the window are masked
+// and their V zeroed, since their slots may hold anything.
+//
 // Masking: tokens t >= T_b of the last block get logit -inf and are excluded from the
 // PV loop, so whatever bytes sit in unused slots are never used.  Block ids outside
 // [0, num_blocks) are skipped (no copy) and flagged in the device error word.
@@ -208,10 +214,23 @@ __device__ __forceinline__ SchedSmem sched_smem(unsigned char* tail, int num_seq
   return SchedSmem{base, base + num_seqs + 1, base + num_seqs + 3};
 }
 
+// First logical block of a T-token sequence that some query sees (0 without a window).
+__device__ __forceinline__ int first_block(const DecodeParams& p, int T) {
+  const int lo = T - (p.num_queries - 1) - p.window;  // first query's first visible token
+  return lo > 0 ? lo / kBlockSize : 0;
+}
+
 __device__ __forceinline__ int seq_parts(const DecodeParams& p, int T) {
   if (T < p.num_queries || T > p.max_context_len) return 1;
-  const int nblk = (T + kBlockSize - 1) / kBlockSize;
+  const int nblk = (T + kBlockSize - 1) / kBlockSize - first_block(p, T);
   return (nblk + p.partition_blocks - 1) / p.partition_blocks;
+}
+
+// Whether token t of a block is visible to a column: lim = the column's visible tokens
+// counted from the block's first token (context minus causal cut minus block start);
+// visible iff lim - W <= t < lim, one unsigned compare.
+__device__ __forceinline__ bool visible(int lim, int t, int window) {
+  return unsigned(lim - 1 - t) < unsigned(window);
 }
 
 // First item of this CTA, or -1.  Builds the prefix sum in persistent mode.  Ends with a
@@ -419,7 +438,7 @@ __global__ void __launch_bounds__(NW * 32)
     write_bad_len<G, D, C::kThreads>(p, it);
   } else {
   const int nblk = (T + kBlockSize - 1) / kBlockSize;
-  const int blk0 = part * P;
+  const int blk0 = first_block(p, T) + part * P;
   const int nb_item = min(nblk, blk0 + P) - blk0;
   const int32_t* trow = p.block_tables + size_t(b) * p.max_blocks_per_seq + blk0;
   for (int i = threadIdx.x; i < nb_item; i += C::kThreads) tbl[i] = __ldg(trow + i);
@@ -508,8 +527,11 @@ __global__ void __launch_bounds__(NW * 32)
     const bool valid = phys >= 0 && phys < p.num_blocks;
     const int vt = valid ? min(kBlockSize, T - (blk0 + ib) * kBlockSize) : 0;
     if (vt > 0) {
-      // tokens of this block that column g_lane may see: t < lim
-      const int lim = T - (blk0 + ib) * kBlockSize - cut;
+      // tokens of this block that column g_lane may see: lim - W <= t < lim; tokens before
+      // t_lo are seen by no column (window) and take no part in PV
+      const int rem = T - (blk0 + ib) * kBlockSize;
+      const int lim = rem - cut;
+      const int t_lo = max(0, rem - (p.num_queries - 1) - p.window);
       const unsigned char* st = ring + size_t(s) * C::kStageBytes;
       const unsigned char* ktile = st;
       const unsigned char* vtile = st + C::kTileBytes;
@@ -544,7 +566,7 @@ __global__ void __launch_bounds__(NW * 32)
         HeadReduce<G, C::kLPT / 2>::run(part_g, lane);
         float logit = part_g[0];
         if constexpr (C::kQuant) logit *= kscale[t];
-        sc[ps] = (t < lim) ? logit : -INFINITY;
+        sc[ps] = visible(lim, t, p.window) ? logit : -INFINITY;
       }
 
       // ---- online softmax update for head g_lane
@@ -564,7 +586,7 @@ __global__ void __launch_bounds__(NW * 32)
         psum += pr;
         if (store_lane) {
           float w = pr;
-          if constexpr (C::kQuant) w = (t < vt) ? pr * vscale[t] : 0.0f;
+          if constexpr (C::kQuant) w = (t < vt && t >= t_lo) ? pr * vscale[t] : 0.0f;
           prob[t * G + g_lane] = w;
         }
       }
@@ -581,7 +603,7 @@ __global__ void __launch_bounds__(NW * 32)
 #pragma unroll
         for (int i = 0; i < C::kDPV; ++i) acc[g][i] *= al[g];
 #pragma unroll 4
-      for (int t = 0; t < vt; ++t) {
+      for (int t = t_lo; t < vt; ++t) {
         float pv[G];
         if constexpr (G % 4 == 0) {
 #pragma unroll
@@ -669,8 +691,7 @@ __global__ void __launch_bounds__(128) lse_reduce_kernel(const DecodeParams p) {
   const int b = gw / (p.num_queries * p.num_q_heads);
   const int T = __ldg(p.context_lens + b);
   if (T < p.num_queries || T > p.max_context_len) return;  // the decode kernel wrote zeros
-  const int nblk = (T + kBlockSize - 1) / kBlockSize;
-  const int nparts = (nblk + p.partition_blocks - 1) / p.partition_blocks;
+  const int nparts = seq_parts(p, T);
   if (nparts <= 1) return;  // written directly by the decode kernel
   const float* ml = p.ws_ml + size_t(gw) * p.max_parts * 2;
   const float* acc = p.ws_acc + size_t(gw) * p.max_parts * D;

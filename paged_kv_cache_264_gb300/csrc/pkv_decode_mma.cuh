@@ -70,13 +70,39 @@ struct MmaCfg {
   static_assert(size_t(NC) * (D + 2) * 4 <= size_t(S) * kStageBytes, "merge record fits the ring");
 };
 
+// Warps per CTA and the built ring shapes: (stages S, blocks per stage BPS).  A block's K
+// and V tiles take 8 KiB (bf16, head_dim 128) or 4 KiB (bf16 64, INT8/FP8 128).  The first
+// shape listed for a pool type is its default.
+constexpr int kNwMma = 4;
+struct RingShape {
+  int stages, bps;
+};
+constexpr RingShape kShapesBf16D128[] = {{2, 1}, {3, 1}};
+constexpr RingShape kShapesBf16D64[] = {{3, 1}, {2, 2}};
+constexpr RingShape kShapesQuant[] = {{3, 1}, {2, 2}, {3, 2}};  // INT8 and FP8
+
+// Launch / occupancy of one pool type's variants (defined in pkv_decode_mma_<type>.cu):
+// cols = column slots (2, 4, 8, 16), shape = index into the type's shape list, gen = kGen.
+cudaError_t launch_mma_bf16(const DecodeParams& p, const CUtensorMap& tk, const CUtensorMap& tv,
+                            int cols, int shape, bool gen, cudaStream_t stream);
+cudaError_t launch_mma_int8(const DecodeParams& p, const CUtensorMap& tk, const CUtensorMap& tv,
+                            int cols, int shape, bool gen, cudaStream_t stream);
+cudaError_t launch_mma_fp8(const DecodeParams& p, const CUtensorMap& tk, const CUtensorMap& tv,
+                           int cols, int shape, bool gen, cudaStream_t stream);
+int occupancy_mma_bf16(int head_dim, int cols, int shape, bool gen);
+int occupancy_mma_int8(int cols, int shape, bool gen);
+int occupancy_mma_fp8(int cols, int shape, bool gen);
+
 // Shared-memory address of 16-byte chunk `c` of token row `t` in a tile whose 128-byte
 // boxes were written with the 128-byte swizzle (chunk index xor row index mod 8).
 __device__ __forceinline__ uint32_t swz(uint32_t tile, int t, int c) {
   return tile + (c >> 3) * 2048 + t * 128 + (((c & 7) ^ (t & 7)) << 4);
 }
 
-template <KvType KV, int D, int NC, int NW, int S, int BPS>
+// kGen: the general masks (causal cuts of several query tokens, a sliding window).  Without
+// it a column sees every context token, the only mask is the context end, and the kernel
+// carries none of that arithmetic (the INT8 and FP8 paths are instruction-bound).
+template <KvType KV, int D, int NC, int NW, int S, int BPS, bool kGen>
 __global__ void __launch_bounds__(NW * 32)
     paged_decode_mma_kernel(const __grid_constant__ CUtensorMap tmap_k,
                             const __grid_constant__ CUtensorMap tmap_v, const DecodeParams p) {
@@ -121,7 +147,7 @@ __global__ void __launch_bounds__(NW * 32)
     write_bad_len<NC, D, C::kThreads>(p, it);
   } else {
   const int nblk = (T + kBlockSize - 1) / kBlockSize;
-  const int blk0 = part * P;
+  const int blk0 = (kGen ? first_block(p, T) : 0) + part * P;
   const int nb_item = min(nblk, blk0 + P) - blk0;
   const int32_t* trow = p.block_tables + size_t(b) * p.max_blocks_per_seq + blk0;
   for (int i = threadIdx.x; i < nb_item; i += C::kThreads) tbl[i] = __ldg(trow + i);
@@ -254,12 +280,12 @@ __global__ void __launch_bounds__(NW * 32)
       }
     }
   }
-  // Causal cuts of the accumulator columns 8nt + 2gj and 8nt + 2gj + 1 (0 for one query).
+  // Causal cuts of the accumulator columns 8nt + 2gj and 8nt + 2gj + 1.
   int cut[NT][2];
 #pragma unroll
   for (int nt = 0; nt < NT; ++nt) {
-    cut[nt][0] = col_cut(p, 8 * nt + 2 * gj);
-    cut[nt][1] = col_cut(p, 8 * nt + 2 * gj + 1);
+    cut[nt][0] = kGen ? col_cut(p, 8 * nt + 2 * gj) : 0;
+    cut[nt][1] = kGen ? col_cut(p, 8 * nt + 2 * gj + 1) : 0;
   }
 
   // ldmatrix row assignment: lane gives the row address of matrix lane / 8.
@@ -304,6 +330,7 @@ __global__ void __launch_bounds__(NW * 32)
     const float* sc_st = scl + s * (C::kScaleStage / 4);
     int vt[BPS];   // tokens of block j inside the context (0: absent block)
     int rem[BPS];  // context tokens from block j's first token on (0: absent block)
+    int tlo[BPS];  // tokens of block j before every query's window (0 without kGen)
     bool any = false;
 #pragma unroll
     for (int j = 0; j < BPS; ++j) {
@@ -316,6 +343,7 @@ __global__ void __launch_bounds__(NW * 32)
           vt[j] = min(kBlockSize, rem[j]);
         }
       }
+      tlo[j] = kGen ? max(0, rem[j] - (p.num_queries - 1) - p.window) : 0;
       any |= vt[j] > 0;
     }
     if (any) {
@@ -376,8 +404,8 @@ __global__ void __launch_bounds__(NW * 32)
           for (int i = 0; i < 4; ++i) sacc[j][nt][i] += acc2[nt][i];
       }
 
-      // ---- logits in log2 units, masked past the context and each column's causal cut
-      //      (and for absent blocks, whose rem is 0)
+      // ---- logits in log2 units, masked past the context, each column's causal cut and
+      //      window (and for absent blocks, whose rem is 0)
       float sc[BPS][NT][4];
       float bm[NT][2];
 #pragma unroll
@@ -393,11 +421,21 @@ __global__ void __launch_bounds__(NW * 32)
         }
 #pragma unroll
         for (int nt = 0; nt < NT; ++nt) {
-          const int lim0 = rem[j] - cut[nt][0], lim1 = rem[j] - cut[nt][1];
-          sc[j][nt][0] = gi < lim0 ? (sacc[j][nt][0] - kbias[nt][0]) * f0 : -INFINITY;
-          sc[j][nt][1] = gi < lim1 ? (sacc[j][nt][1] - kbias[nt][1]) * f0 : -INFINITY;
-          sc[j][nt][2] = gi + 8 < lim0 ? (sacc[j][nt][2] - kbias[nt][0]) * f1 : -INFINITY;
-          sc[j][nt][3] = gi + 8 < lim1 ? (sacc[j][nt][3] - kbias[nt][1]) * f1 : -INFINITY;
+          bool v0, v1, v2, v3;  // (token gi | gi + 8) x (column 8nt + 2gj | + 1) visible
+          if constexpr (kGen) {
+            const int lim0 = rem[j] - cut[nt][0], lim1 = rem[j] - cut[nt][1];
+            v0 = visible(lim0, gi, p.window);
+            v1 = visible(lim1, gi, p.window);
+            v2 = visible(lim0, gi + 8, p.window);
+            v3 = visible(lim1, gi + 8, p.window);
+          } else {
+            v0 = v1 = gi < vt[j];
+            v2 = v3 = gi + 8 < vt[j];
+          }
+          sc[j][nt][0] = v0 ? (sacc[j][nt][0] - kbias[nt][0]) * f0 : -INFINITY;
+          sc[j][nt][1] = v1 ? (sacc[j][nt][1] - kbias[nt][1]) * f0 : -INFINITY;
+          sc[j][nt][2] = v2 ? (sacc[j][nt][2] - kbias[nt][0]) * f1 : -INFINITY;
+          sc[j][nt][3] = v3 ? (sacc[j][nt][3] - kbias[nt][1]) * f1 : -INFINITY;
           bm[nt][0] = fmaxf(bm[nt][0], fmaxf(sc[j][nt][0], sc[j][nt][2]));
           bm[nt][1] = fmaxf(bm[nt][1], fmaxf(sc[j][nt][1], sc[j][nt][3]));
         }
@@ -455,8 +493,10 @@ __global__ void __launch_bounds__(NW * 32)
         float svm = 0.0f;
 #pragma unroll
         for (int j = 0; j < BPS; ++j) {
-          sv[j][0] = gi < vt[j] ? sc_st[(BPS + j) * kBlockSize + gi] : 0.0f;
-          sv[j][1] = gi + 8 < vt[j] ? sc_st[(BPS + j) * kBlockSize + gi + 8] : 0.0f;
+          // scales of tokens outside [tlo, vt) may be anything: their weight is 0 anyway
+          const unsigned span = unsigned(vt[j] - tlo[j]);
+          sv[j][0] = unsigned(gi - tlo[j]) < span ? sc_st[(BPS + j) * kBlockSize + gi] : 0.0f;
+          sv[j][1] = unsigned(gi + 8 - tlo[j]) < span ? sc_st[(BPS + j) * kBlockSize + gi + 8] : 0.0f;
           svm = fmaxf(svm, fmaxf(sv[j][0], sv[j][1]));
         }
 #pragma unroll
@@ -517,12 +557,16 @@ __global__ void __launch_bounds__(NW * 32)
         }
         const unsigned char* vtp = st + (BPS + j) * C::kTileBytes;
         if constexpr (!C::kQuant) {
-          // Slots past the context in the last block may hold anything, NaN included, and
-          // 0 * NaN would poison the sum: zero those tokens' V.  Lane (gi, gj) holds tokens
-          // 2gj, 2gj+1 in A registers 0-1 and 2gj+8, 2gj+9 in registers 2-3 (low half first).
-          const bool tail = vt[j] < kBlockSize;
-          const uint32_t mlo = (2 * gj < vt[j] ? 0x0000ffffu : 0u) | (2 * gj + 1 < vt[j] ? 0xffff0000u : 0u);
-          const uint32_t mhi = (2 * gj + 8 < vt[j] ? 0x0000ffffu : 0u) | (2 * gj + 9 < vt[j] ? 0xffff0000u : 0u);
+          // Slots past the context in the last block, and before every query's window in
+          // the first, may hold anything, NaN included, and 0 * NaN would poison the sum:
+          // zero those tokens' V.  Lane (gi, gj) holds tokens 2gj, 2gj+1 in A registers 0-1
+          // and 2gj+8, 2gj+9 in registers 2-3 (low half first).
+          const bool tail = vt[j] < kBlockSize || tlo[j] > 0;
+          const unsigned span = unsigned(vt[j] - tlo[j]);
+          const uint32_t mlo = (unsigned(2 * gj - tlo[j]) < span ? 0x0000ffffu : 0u) |
+                               (unsigned(2 * gj + 1 - tlo[j]) < span ? 0xffff0000u : 0u);
+          const uint32_t mhi = (unsigned(2 * gj + 8 - tlo[j]) < span ? 0x0000ffffu : 0u) |
+                               (unsigned(2 * gj + 9 - tlo[j]) < span ? 0xffff0000u : 0u);
           const uint32_t vtile = smem_addr(vtp);
 #pragma unroll
           for (int t = 0; t < C::kMTiles; ++t) {
@@ -536,7 +580,8 @@ __global__ void __launch_bounds__(NW * 32)
           }
         } else {
           // INT8 codes are always finite and masked tokens have a zero weight in P; E4M3 has
-          // NaN codes, so an FP8 block's tail tokens are zeroed in the fragment as for bf16.
+          // NaN codes, so an FP8 block's tokens outside [tlo, vt) are zeroed in the fragment
+          // as for bf16.
           // Lane (gi, gj) reads dims 16gi..16gi+15 of tokens 2gj, 2gj+1, 2gj+8, 2gj+9; m-tile
           // t row gi is dim 16gi+2t and row gi+8 is dim 16gi+2t+1.
           const uint4 va = *reinterpret_cast<const uint4*>(vtp + voff[0]);
@@ -544,8 +589,11 @@ __global__ void __launch_bounds__(NW * 32)
           const uint4 vc = *reinterpret_cast<const uint4*>(vtp + voff[2]);
           const uint4 vd = *reinterpret_cast<const uint4*>(vtp + voff[3]);
           constexpr uint32_t kFlip = C::kFp8 ? 0u : 0x80808080u;
-          const uint32_t mlo8 = (2 * gj < vt[j] ? 0x0000ffffu : 0u) | (2 * gj + 1 < vt[j] ? 0xffff0000u : 0u);
-          const uint32_t mhi8 = (2 * gj + 8 < vt[j] ? 0x0000ffffu : 0u) | (2 * gj + 9 < vt[j] ? 0xffff0000u : 0u);
+          const unsigned span8 = unsigned(vt[j] - tlo[j]);
+          const uint32_t mlo8 = (unsigned(2 * gj - tlo[j]) < span8 ? 0x0000ffffu : 0u) |
+                                (unsigned(2 * gj + 1 - tlo[j]) < span8 ? 0xffff0000u : 0u);
+          const uint32_t mhi8 = (unsigned(2 * gj + 8 - tlo[j]) < span8 ? 0x0000ffffu : 0u) |
+                                (unsigned(2 * gj + 9 - tlo[j]) < span8 ? 0xffff0000u : 0u);
           const uint32_t wa[4] = {va.x ^ kFlip, va.y ^ kFlip, va.z ^ kFlip, va.w ^ kFlip};
           const uint32_t wb[4] = {vb.x ^ kFlip, vb.y ^ kFlip, vb.z ^ kFlip, vb.w ^ kFlip};
           const uint32_t wc[4] = {vc.x ^ kFlip, vc.y ^ kFlip, vc.z ^ kFlip, vc.w ^ kFlip};
@@ -559,7 +607,7 @@ __global__ void __launch_bounds__(NW * 32)
             if constexpr (C::kFp8) {
               f16x2x2_from_e4m3x4(ab, a[0], a[1]);
               f16x2x2_from_e4m3x4(cd, a[2], a[3]);
-              if (vt[j] < kBlockSize) {
+              if (vt[j] < kBlockSize || tlo[j] > 0) {
                 a[0] &= mlo8; a[1] &= mlo8; a[2] &= mhi8; a[3] &= mhi8;
               }
             } else {
@@ -650,11 +698,11 @@ __global__ void __launch_bounds__(NW * 32)
   finish_items(p);
 }
 
-template <KvType KV, int D, int NC, int NW, int S, int BPS>
+template <KvType KV, int D, int NC, int NW, int S, int BPS, bool kGen>
 cudaError_t launch_mma_variant(const DecodeParams& p, const CUtensorMap& tk, const CUtensorMap& tv,
                                cudaStream_t stream) {
   using C = MmaCfg<KV, D, NC, NW, S, BPS>;
-  auto kern = paged_decode_mma_kernel<KV, D, NC, NW, S, BPS>;
+  auto kern = paged_decode_mma_kernel<KV, D, NC, NW, S, BPS, kGen>;
   static bool attr_done[64] = {};
   int dev = 0;
   cudaGetDevice(&dev);
@@ -672,10 +720,10 @@ cudaError_t launch_mma_variant(const DecodeParams& p, const CUtensorMap& tk, con
                     C::smem_bytes(p.partition_blocks, p.persistent ? p.num_seqs : 0), stream, tk, tv, p);
 }
 
-template <KvType KV, int D, int NC, int NW, int S, int BPS>
+template <KvType KV, int D, int NC, int NW, int S, int BPS, bool kGen>
 int mma_ctas_per_sm_variant() {
   using C = MmaCfg<KV, D, NC, NW, S, BPS>;
-  auto kern = paged_decode_mma_kernel<KV, D, NC, NW, S, BPS>;
+  auto kern = paged_decode_mma_kernel<KV, D, NC, NW, S, BPS, kGen>;
   cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                        static_cast<int>(C::smem_bytes(kMaxPartitionBlocks, kMaxSchedSeqs)));
   int n = 0;
@@ -683,6 +731,47 @@ int mma_ctas_per_sm_variant() {
       cudaSuccess)
     return 0;
   return n;
+}
+
+// Column-slot dispatch for one (pool type, head_dim, ring shape, kGen).  Plain decode has
+// at most 8 columns (a GQA group), so 16 columns exist only with kGen.
+template <KvType KV, int D, int S, int BPS, bool kGen>
+cudaError_t launch_mma_cols(const DecodeParams& p, const CUtensorMap& tk, const CUtensorMap& tv,
+                            int cols, cudaStream_t stream) {
+  switch (cols) {
+    case 2: return launch_mma_variant<KV, D, 2, kNwMma, S, BPS, kGen>(p, tk, tv, stream);
+    case 4: return launch_mma_variant<KV, D, 4, kNwMma, S, BPS, kGen>(p, tk, tv, stream);
+    case 8: return launch_mma_variant<KV, D, 8, kNwMma, S, BPS, kGen>(p, tk, tv, stream);
+    case 16:
+      if constexpr (kGen) return launch_mma_variant<KV, D, 16, kNwMma, S, BPS, kGen>(p, tk, tv, stream);
+      return cudaErrorInvalidValue;
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+template <KvType KV, int D, int S, int BPS, bool kGen>
+int occupancy_mma_cols(int cols) {
+  switch (cols) {
+    case 2: return mma_ctas_per_sm_variant<KV, D, 2, kNwMma, S, BPS, kGen>();
+    case 4: return mma_ctas_per_sm_variant<KV, D, 4, kNwMma, S, BPS, kGen>();
+    case 8: return mma_ctas_per_sm_variant<KV, D, 8, kNwMma, S, BPS, kGen>();
+    case 16:
+      if constexpr (kGen) return mma_ctas_per_sm_variant<KV, D, 16, kNwMma, S, BPS, kGen>();
+      return 0;
+  }
+  return 0;
+}
+
+template <KvType KV, int D, int S, int BPS>
+cudaError_t launch_mma_gen(const DecodeParams& p, const CUtensorMap& tk, const CUtensorMap& tv,
+                           int cols, bool gen, cudaStream_t stream) {
+  return gen ? launch_mma_cols<KV, D, S, BPS, true>(p, tk, tv, cols, stream)
+             : launch_mma_cols<KV, D, S, BPS, false>(p, tk, tv, cols, stream);
+}
+
+template <KvType KV, int D, int S, int BPS>
+int occupancy_mma_gen(int cols, bool gen) {
+  return gen ? occupancy_mma_cols<KV, D, S, BPS, true>(cols) : occupancy_mma_cols<KV, D, S, BPS, false>(cols);
 }
 
 }  // namespace pkv

@@ -11,6 +11,7 @@ namespace pkv {
 constexpr int kBlockSize = 16;                      // tokens per physical block
 constexpr uint64_t kWaitTimeoutNs = 2000000000ull;  // bounded waits give up after 2 s
 constexpr int kMaxSchedSeqs = 4096;  // largest batch scheduled by the persistent grid
+constexpr int kNoWindow = 1 << 30;   // window value meaning "no window" (contexts are shorter)
 
 // Device error word bits (mirror PKV_DEVERR_* of the public header).
 constexpr uint32_t kErrBlockId = 0x1u;
@@ -58,6 +59,7 @@ struct DecodeParams {
   int group;                    // query heads per kv head (num_q_heads / kv_heads), 1/2/4/8
   int group_log2;               // log2(group)
   int num_queries;              // k >= 1 query tokens per sequence, the last k positions
+  int window;                   // each query sees its last `window` tokens (kNoWindow: all)
   int head_dim;
   int max_context_len;
   int partition_blocks;         // P: blocks per work item
@@ -105,7 +107,8 @@ bool mma_supported(KvType kv, int head_dim, int cols);
 int mma_ring_shape(KvType kv, int head_dim, int stages, int blocks_per_stage);
 cudaError_t launch_decode_mma(const DecodeParams& p, const CUtensorMap* tk, const CUtensorMap* tv,
                               KvType kv, int cols, int shape, cudaStream_t stream);
-int mma_ctas_per_sm(KvType kv, int head_dim, int cols, int shape);
+// gen: the variant with the general masks (several query tokens or a window).
+int mma_ctas_per_sm(KvType kv, int head_dim, int cols, int shape, bool gen);
 
 // Resident CTAs per SM of the CUDA-core decode kernel variant (0 if not built).
 int decode_ctas_per_sm(KvType kv, int head_dim, int cols);

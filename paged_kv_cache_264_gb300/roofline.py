@@ -9,7 +9,9 @@ scales).
 
 A multi-query step (k draft tokens per sequence, verified in one call) reads the same
 cached K/V once, k times the q and output rows, and appends k tokens per sequence; its
-flops count each query over the tokens up to its own position.
+flops count each query over the tokens up to its own position.  With a sliding window of W
+tokens a sequence's K/V read covers the union of its queries' windows, min(T, W + k - 1)
+tokens, and each query attends to min(its position + 1, W).
 """
 
 from __future__ import annotations
@@ -39,16 +41,22 @@ class StepBytes:
 
 
 def step_bytes(context_lens, num_q_heads: int, num_kv_heads: int, head_dim: int, kv_dtype: str,
-               append: bool = True, num_queries: int = 1) -> StepBytes:
+               append: bool = True, num_queries: int = 1, window: int = 0) -> StepBytes:
     lens = torch.as_tensor(context_lens, dtype=torch.int64)
     b = int(lens.numel())
-    sum_t = int(lens.sum())
-    sum_nb = int(((lens + BLOCK - 1) // BLOCK).sum())
+    k = int(num_queries)
+    if window > 0:
+        read = torch.minimum(lens, torch.full_like(lens, window + k - 1))
+        first_blk = torch.clamp(lens - (k - 1) - window, min=0) // BLOCK
+    else:
+        read = lens
+        first_blk = torch.zeros_like(lens)
+    sum_t = int(read.sum())
+    sum_nb = int(((lens + BLOCK - 1) // BLOCK - first_blk).sum())
     esz = 2 if kv_dtype == "bf16" else 1
     kv = 2 * sum_t * num_kv_heads * head_dim * esz
     if kv_dtype in ("int8", "fp8"):
         kv += 2 * sum_t * num_kv_heads * 4
-    k = int(num_queries)
     q_out = 2 * b * k * num_q_heads * head_dim * 2
     tables = 4 * (sum_nb + b)
     app = 0
@@ -59,6 +67,9 @@ def step_bytes(context_lens, num_q_heads: int, num_kv_heads: int, head_dim: int,
         if kv_dtype in ("int8", "fp8"):
             app += 2 * n_new * num_kv_heads * 4                # scales written
         app += 4 * n_new                                       # slot_mapping read
-    attended = k * sum_t - b * k * (k - 1) // 2  # query i of k sees T_b - (k - 1 - i) tokens
+    pos1 = lens[:, None] - (k - 1) + torch.arange(k)[None, :]  # query i sees pos_i + 1 tokens
+    if window > 0:
+        pos1 = torch.clamp(pos1, max=window)
+    attended = int(pos1.sum())
     flops = 4 * attended * num_q_heads * head_dim
     return StepBytes(kv, q_out, tables, app, flops)

@@ -24,6 +24,8 @@ llama2_7b_       64    as llama2_7b                     32/32    128   bf16   k 
 verify4
 llama3_8b_gqa_   128   as llama3_8b_gqa                 32/8     128   bf16   k = 4 queries
 verify4
+long_32k_       8     as long_32k                      32/32    128   bf16   window 4096
+window4k
 ===============  ====  ===============================  =======  ====  =====  ================
 
 The two ``verify4`` workloads are multi-query decode batches for speculative decoding
@@ -31,7 +33,10 @@ The two ``verify4`` workloads are multi-query decode batches for speculative dec
 last 4 cached tokens are the drafts, and q holds 4 query tokens per sequence
 ([B, 4, Hq, d]), query i attending causally to the tokens up to its own position.  They
 reuse their base workload's context lengths and block pool (its seed), so a verify step
-and a decode step over the same cache compare directly.
+and a decode step over the same cache compare directly.  ``long_32k_window4k`` is the
+long_32k cache decoded with a sliding window of 4096 tokens ("LLM/MLLM inference
+optimisation", 2.3: keep only the most recent window): each query reads its last 4096
+tokens.
 
 Pools other than ``tiny`` hold ``ceil(1.25 * sum_b ceil(T_b / 16))`` blocks; the blocks
 that sequences use are drawn from a seeded permutation of the pool.  Everything is drawn
@@ -66,6 +71,7 @@ class Spec:
     outlier_key_scale: float = 8.0
     num_queries: int = 1  # query tokens per sequence (k > 1: draft verification)
     base_index: int | None = None  # draw lengths, pool and values as workload base_index does
+    window: int = 0  # sliding window of the decode (0: none)
 
     @property
     def seed(self) -> int:
@@ -98,6 +104,9 @@ SPECS: dict[str, Spec] = {
         Spec("llama3_8b_gqa_verify4", 8, "Llama-3-8B-shaped GQA draft verification: the "
              "llama3_8b_gqa batch shape with 4 query tokens per sequence (causal)", 128, 32, 8, 128,
              "bf16", ("uniform", 512, 8192), num_queries=4, base_index=3),
+        Spec("long_32k_window4k", 9, "long-context sliding window: the long_32k cache (8 x 32768 "
+             "tokens, 32/32 heads, head_dim 128, bf16) decoded with a 4096-token window", 8, 32, 32, 128,
+             "bf16", ("const", 32768), outlier_key_channel_frac=0.01, base_index=4, window=4096),
     )
 }
 

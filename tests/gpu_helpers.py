@@ -86,15 +86,23 @@ def compact_for_oracle(w: W.Workload, seqs):
                 num_blocks=max(cursor, 1), orig_tables=tables)
 
 
-def oracle_decode(w: W.Workload, kv: str, seqs=None, o=None, q=None):
+def oracle_decode(w: W.Workload, kv: str, seqs=None, o=None, q=None, window=0):
     """fp64 oracle output [len(seqs), Hq, d] (or [len(seqs), k, Hq, d] for a multi-query
-    workload or a 4-D ``q``) plus its own pool (compacted)."""
+    workload or a 4-D ``q``) plus its own pool (compacted).  ``window`` > 0: sliding-window
+    attention over each query's last ``window`` tokens."""
     o = o or oracle.load()
     seqs = list(range(w.num_seqs)) if seqs is None else list(seqs)
     c = compact_for_oracle(w, seqs)
     if q is not None:
         c["q"] = W.bf16_bits(q[torch.tensor(seqs, device=q.device)])
-    decode = o.paged_decode_multi if c["q"].ndim == 4 else o.paged_decode
+    if window:
+        single = c["q"].ndim == 3
+
+        def decode(qb, *rest):
+            out = o.paged_decode_multi(qb[:, None] if single else qb, *rest, window=window)
+            return out[:, 0] if single else out
+    else:
+        decode = o.paged_decode_multi if c["q"].ndim == 4 else o.paged_decode
     shape = (c["num_blocks"], w.num_kv_heads, 16, w.head_dim)
     if kv == "bf16":
         kc, vc = np.zeros(shape, np.uint16), np.zeros(shape, np.uint16)

@@ -102,6 +102,35 @@ def test_truncate_drops_rejected_drafts():
             m.truncate(s, bad)
 
 
+def test_release_before_keeps_a_window():
+    """Sliding window: blocks wholly behind the window go back to the pool, their table
+    entries read -1, positions keep counting, and appends and forks carry on."""
+    m = pkv.BlockManager(num_blocks=8, max_seqs=4, max_blocks_per_seq=8)
+    s = m.add_sequence()
+    m.append([s], [40])                        # blocks 0, 1, 2 (8 tokens in block 2)
+    m.release_before(s, 35)                    # blocks 0 and 1 hold only tokens < 32 <= 35
+    bt, cl = m.tables([s])
+    assert bt[0, :3].tolist() == [-1, -1, 2] and cl.tolist() == [40]
+    assert m.refcount(0) == 0 and m.refcount(1) == 0 and m.stats()[0] == 7
+    m.release_before(s, 10)                    # nothing more to release
+    assert m.stats()[0] == 7
+    c = m.fork(s)                              # shares block 2 only
+    assert m.refcount(2) == 2
+    slots, pairs = m.append([c], [1])          # shared partial block: copy first
+    assert pairs.tolist() == [[2, 1]] and slots.tolist() == [1 * BS + 8]
+    with pytest.raises(pkv.PagedKVError, match="invalid"):
+        m.truncate(s, 20)                      # below the released blocks
+    m.truncate(s, 32)                          # every kept block released: next append takes a new one
+    slots, _ = m.append([s], [1])
+    assert slots.tolist() == [2 * BS] and m.tables([s])[0][0, :3].tolist() == [-1, -1, 2]  # block 2 came back
+    for bad in (-1, 42):                       # c holds 41 tokens
+        with pytest.raises(pkv.PagedKVError, match="invalid"):
+            m.release_before(c, bad)
+    m.free_sequence(s)
+    m.free_sequence(c)
+    assert m.stats() == (8, 0)
+
+
 class Model:
     """The same rules in plain Python."""
 
@@ -121,7 +150,7 @@ class Model:
             self.free.append(b)
 
     def append(self, s, k):
-        blocks, length = self.seqs[s]
+        blocks, length, released = self.seqs[s]
         slots, pairs = [], []
         for _ in range(k):
             j, off = divmod(length, BS)
@@ -134,7 +163,7 @@ class Model:
                 pairs.append([src, dst])
             slots.append(blocks[j] * BS + off)
             length += 1
-        self.seqs[s] = (blocks, length)
+        self.seqs[s] = (blocks, length, released)
         return slots, pairs
 
 
@@ -148,32 +177,50 @@ def test_random_operations_match_model():
         live = list(model.seqs)
         if op < 0.15 and len(live) < 16:
             s = m.add_sequence()
-            model.seqs[s] = ([], 0)
+            model.seqs[s] = ([], 0, 0)
         elif op < 0.3 and live and len(live) < 16:
             p = rng.choice(live)
             c = m.fork(p)
-            blocks, length = model.seqs[p]
+            blocks, length, released = model.seqs[p]
             for b in blocks:
-                model.ref[b] += 1
-            model.seqs[c] = (list(blocks), length)
+                if b >= 0:
+                    model.ref[b] += 1
+            model.seqs[c] = (list(blocks), length, released)
         elif op < 0.4 and live:
             s = rng.choice(live)
             m.free_sequence(s)
             for b in model.seqs.pop(s)[0]:
-                model.drop(b)
+                if b >= 0:
+                    model.drop(b)
         elif op < 0.5 and live:
             s = rng.choice(live)
-            blocks, length = model.seqs[s]
+            blocks, length, released = model.seqs[s]
             keep = rng.randint(0, length)
+            if keep < released * BS:
+                with pytest.raises(pkv.PagedKVError):
+                    m.truncate(s, keep)
+                continue
             m.truncate(s, keep)
             nkeep = -(-keep // BS)
             for b in reversed(blocks[nkeep:]):
-                model.drop(b)
-            model.seqs[s] = (blocks[:nkeep], keep)
+                if b >= 0:
+                    model.drop(b)
+            model.seqs[s] = (blocks[:nkeep], keep, released)
+        elif op < 0.58 and live:
+            s = rng.choice(live)
+            blocks, length, released = model.seqs[s]
+            token = rng.randint(0, length)
+            m.release_before(s, token)
+            upto = token // BS
+            for j in range(released, upto):
+                if blocks[j] >= 0:
+                    model.drop(blocks[j])
+                blocks[j] = -1
+            model.seqs[s] = (blocks, length, max(released, upto))
         elif live:
             s = rng.choice(live)
             k = rng.randint(0, 20)
-            blocks, length = model.seqs[s]
+            blocks, length, released = model.seqs[s]
             need = -(-(length + k) // BS) - len(blocks) + (1 if length % BS and k and model.ref[blocks[-1]] > 1 else 0)
             if need > len(model.free) or -(-(length + k) // BS) > 32:
                 with pytest.raises(pkv.PagedKVError):
@@ -189,5 +236,5 @@ def test_random_operations_match_model():
             seqs = sorted(model.seqs)
             bt, cl = m.tables(seqs)
             for i, s in enumerate(seqs):
-                blocks, length = model.seqs[s]
+                blocks, length, _ = model.seqs[s]
                 assert cl[i] == length and bt[i, :len(blocks)].tolist() == blocks
