@@ -381,12 +381,40 @@ def test_repeated_calls_identical(kernel):
 
 
 @pytest.mark.parametrize("kernel", KERNELS)
-def test_large_batch_classic_grid(kernel):
-    """More sequences than the persistent scheduler holds (4096): one CTA per item slot."""
+@pytest.mark.parametrize("partition_blocks", [0, 2])
+def test_large_batch_classic_grid(kernel, partition_blocks):
+    """More sequences than the persistent scheduler holds (4096): one CTA per item slot,
+    with and without split sequences."""
     g = torch.Generator().manual_seed(91)
     lens = torch.randint(1, 70, (4200,), generator=g)
     w = custom(lens, 8, 2, 64, "bf16", seed=92)
-    check_all(w, "bf16", kernel=kernel, seqs=list(range(0, 4200, 97)))
+    if partition_blocks:
+        pool = pkv.PagedKVPool(1, 2, 64, "bf16", fill=0)
+        assert pkv.decode_plan(pool, 4200, 8, int(lens.max()), partition_blocks)["kernels_per_call"] == 2
+        pool.close()
+    check_all(w, "bf16", partition_blocks, kernel=kernel, seqs=list(range(0, 4200, 97)))
+
+
+@pytest.mark.parametrize("kv", ["bf16", "int8"])
+def test_scheduler_counters_reset_between_calls(kv):
+    """The persistent scheduler's counters live in the pool's device memory and reset
+    themselves: alternating batches of different shapes and partition sizes on one pool
+    give the oracle's result every time."""
+    wa = custom([1, 40, 300, 613, 17], 16, 4, 128, kv, seed=95)
+    wb = custom([700, 5, 129, 64, 33, 250, 90, 1000], 16, 4, 128, kv, seed=96)
+    ref_a, _, _ = oracle_decode(wa, kv)
+    ref_b, _, _ = oracle_decode(wb, kv)
+    pa, pb = gpu_pool_from(wa, kv), gpu_pool_from(wb, kv)
+    for rep in range(3):
+        for w, pool, ref in ((wa, pa, ref_a), (wb, pb, ref_b)):
+            for P in (1, 3, 0):
+                out = pool.decode(w.q.cuda(), w.block_tables.cuda(), w.context_lens.cuda(), w.scale,
+                                  w.max_context_len, partition_blocks=P)
+                torch.cuda.synchronize()
+                compare(out, ref, f"merge counters rep {rep} P={P}")
+    assert pa.device_error() == 0 and pb.device_error() == 0
+    pa.close()
+    pb.close()
 
 
 RING_SHAPES = [("bf16", 128, 2, 1), ("bf16", 128, 3, 1), ("bf16", 64, 3, 1), ("bf16", 64, 2, 2),
