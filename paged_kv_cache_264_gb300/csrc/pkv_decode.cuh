@@ -693,11 +693,16 @@ __global__ void __launch_bounds__(128) lse_reduce_kernel(const DecodeParams p) {
   if (T < p.num_queries || T > p.max_context_len) return;  // the decode kernel wrote zeros
   const int nparts = seq_parts(p, T);
   if (nparts <= 1) return;  // written directly by the decode kernel
-  const float* ml = p.ws_ml + size_t(gw) * p.max_parts * 2;
+  const float2* ml = reinterpret_cast<const float2*>(p.ws_ml) + size_t(gw) * p.max_parts;
   const float* acc = p.ws_acc + size_t(gw) * p.max_parts * D;
 
+  // One pass over (m, l): lane i holds partitions i, i + 32, ...  Weights 2^(m_p - M) of a
+  // lane's first partition stay in a register for the accumulator pass.
   float M = -INFINITY;
-  for (int i = lane; i < nparts; i += 32) M = fmaxf(M, ml[2 * i]);
+  float2 mine = make_float2(-INFINITY, 0.0f);
+  if (lane < nparts) mine = ml[lane];
+  M = mine.x;
+  for (int i = lane + 32; i < nparts; i += 32) M = fmaxf(M, ml[i].x);
 #pragma unroll
   for (int o = 16; o >= 1; o >>= 1) M = fmaxf(M, __shfl_xor_sync(kFull, M, o));
   float L = 0.0f;
@@ -705,20 +710,40 @@ __global__ void __launch_bounds__(128) lse_reduce_kernel(const DecodeParams p) {
 #pragma unroll
   for (int i = 0; i < kDPV; ++i) a[i] = 0.0f;
   if (M != -INFINITY) {
-    for (int i = lane; i < nparts; i += 32) L += exp2f(ml[2 * i] - M) * ml[2 * i + 1];
+    const float f_mine = lane < nparts ? exp2f(mine.x - M) : 0.0f;
+    L = f_mine * mine.y;
+    for (int i = lane + 32; i < nparts; i += 32) {
+      const float2 v = ml[i];
+      L = fmaf(exp2f(v.x - M), v.y, L);
+    }
 #pragma unroll
     for (int o = 16; o >= 1; o >>= 1) L += __shfl_xor_sync(kFull, L, o);
-    for (int i = 0; i < nparts; ++i) {
-      const float f = exp2f(ml[2 * i] - M);
-      const float* src = acc + size_t(i) * D + lane * kDPV;
-      if constexpr (kDPV == 4) {
-        const float4 v = *reinterpret_cast<const float4*>(src);
-        a[0] = fmaf(f, v.x, a[0]); a[1] = fmaf(f, v.y, a[1]);
-        a[2] = fmaf(f, v.z, a[2]); a[3] = fmaf(f, v.w, a[3]);
-      } else {
-        const float2 v = *reinterpret_cast<const float2*>(src);
-        a[0] = fmaf(f, v.x, a[0]); a[1] = fmaf(f, v.y, a[1]);
+    const float* src = acc + lane * kDPV;
+    int i = 0;
+    for (; i + 4 <= nparts; i += 4) {  // four partitions' loads in flight
+      float f[4];
+      float v[4][kDPV];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const int pi = i + u;
+        f[u] = pi < 32 ? __shfl_sync(kFull, f_mine, pi) : exp2f(ml[pi].x - M);
+        if constexpr (kDPV == 4) {
+          const float4 x = *reinterpret_cast<const float4*>(src + size_t(pi) * D);
+          v[u][0] = x.x; v[u][1] = x.y; v[u][2] = x.z; v[u][3] = x.w;
+        } else {
+          const float2 x = *reinterpret_cast<const float2*>(src + size_t(pi) * D);
+          v[u][0] = x.x; v[u][1] = x.y;
+        }
       }
+#pragma unroll
+      for (int u = 0; u < 4; ++u)
+#pragma unroll
+        for (int c = 0; c < kDPV; ++c) a[c] = fmaf(f[u], v[u][c], a[c]);
+    }
+    for (; i < nparts; ++i) {
+      const float f = i < 32 ? __shfl_sync(kFull, f_mine, i) : exp2f(ml[i].x - M);
+#pragma unroll
+      for (int c = 0; c < kDPV; ++c) a[c] = fmaf(f, src[size_t(i) * D + c], a[c]);
     }
   }
   auto* out = static_cast<__nv_bfloat16*>(p.out) + size_t(gw) * D + lane * kDPV;
