@@ -140,10 +140,19 @@ pkv_status make_plan(const pkv_pool* pool, int num_seqs, int num_q_heads, int ma
   } else if (want_stages || want_bps) {
     return PKV_ERR_UNSUPPORTED;
   }
-  const int per_sm = plan->kernel == PKV_KERNEL_TENSOR_CORE
-                         ? pkv::mma_ctas_per_sm(kv, pool->head_dim, plan->cols, plan->shape,
-                                                nq > 1 || plan->window != pkv::kNoWindow)
-                         : pkv::decode_ctas_per_sm(kv, pool->head_dim, plan->cols);
+  const bool gen = nq > 1 || plan->window != pkv::kNoWindow;
+  int per_sm = plan->kernel == PKV_KERNEL_TENSOR_CORE
+                   ? pkv::mma_ctas_per_sm(kv, pool->head_dim, plan->cols, plan->shape, gen)
+                   : pkv::decode_ctas_per_sm(kv, pool->head_dim, plan->cols);
+  if (plan->kernel == PKV_KERNEL_TENSOR_CORE && per_sm == 0 && !want_stages && !want_bps) {
+    // The default ring shape has no variant for this tile (a 16-column merge record needs
+    // a deeper ring): take the next built shape.
+    for (int sh = 1; sh < 4 && per_sm == 0; ++sh) {
+      per_sm = pkv::mma_ctas_per_sm(kv, pool->head_dim, plan->cols, sh, gen);
+      if (per_sm > 0) plan->shape = sh;
+    }
+  }
+  if (plan->kernel == PKV_KERNEL_TENSOR_CORE && per_sm == 0) return PKV_ERR_UNSUPPORTED;
   plan->ctas_per_sm = per_sm > 0 ? per_sm : 1;
   int P;
   if (opt && opt->partition_blocks > 0) {

@@ -46,8 +46,8 @@ cudaError_t launch_decode_mma(const DecodeParams& p, const CUtensorMap* tk, cons
 }
 
 int mma_ctas_per_sm(KvType kv, int head_dim, int cols, int shape, bool gen) {
-  if (!mma_supported(kv, head_dim, cols) || shape < 0 || shape > 2) return 0;
-  static int cache[4][3][17][2] = {};  // [pool type][shape][column slots][gen]
+  if (!mma_supported(kv, head_dim, cols) || shape < 0 || shape > 3) return 0;
+  static int cache[4][4][17][2] = {};  // [pool type][shape][column slots][gen]
   const int ti = kv == KvType::kFp8 ? 3 : kv == KvType::kInt8 ? 2 : (head_dim == 128 ? 0 : 1);
   int& slot = cache[ti][shape][cols][gen ? 1 : 0];
   if (slot) return slot;

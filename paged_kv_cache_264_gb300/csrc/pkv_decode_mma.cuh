@@ -79,7 +79,10 @@ struct RingShape {
 };
 constexpr RingShape kShapesBf16D128[] = {{2, 1}, {3, 1}};
 constexpr RingShape kShapesBf16D64[] = {{3, 1}, {2, 2}};
-constexpr RingShape kShapesQuant[] = {{3, 1}, {2, 2}, {3, 2}};  // INT8 and FP8
+// INT8 and FP8.  Measured on GB300 (int8_cb / fp8_cb, microseconds per call): 2x1 194 / 185,
+// 3x1 195 / 187, 2x2 203 / 192, 3x2 260 / 241.  Forcing more CTAs per SM through launch
+// bounds (fewer registers) never helped.
+constexpr RingShape kShapesQuant[] = {{2, 1}, {3, 1}, {2, 2}, {3, 2}};
 
 // Launch / occupancy of one pool type's variants (defined in pkv_decode_mma_<type>.cu):
 // cols = column slots (2, 4, 8, 16), shape = index into the type's shape list, gen = kGen.
@@ -734,7 +737,14 @@ int mma_ctas_per_sm_variant() {
 }
 
 // Column-slot dispatch for one (pool type, head_dim, ring shape, kGen).  Plain decode has
-// at most 8 columns (a GQA group), so 16 columns exist only with kGen.
+// at most 8 columns (a GQA group), so 16 columns exist only with kGen, and only where the
+// 16-column merge record fits a warp's ring.  Combinations not built report 0 CTAs per SM
+// (the plan turns that into "unsupported").
+template <KvType KV, int D, int S, int BPS>
+constexpr bool mma_record_fits(int nc) {
+  return size_t(nc) * (D + 2) * 4 <= size_t(S) * MmaCfg<KV, D, 2, kNwMma, S, BPS>::kStageBytes;
+}
+
 template <KvType KV, int D, int S, int BPS, bool kGen>
 cudaError_t launch_mma_cols(const DecodeParams& p, const CUtensorMap& tk, const CUtensorMap& tv,
                             int cols, cudaStream_t stream) {
@@ -743,7 +753,8 @@ cudaError_t launch_mma_cols(const DecodeParams& p, const CUtensorMap& tk, const 
     case 4: return launch_mma_variant<KV, D, 4, kNwMma, S, BPS, kGen>(p, tk, tv, stream);
     case 8: return launch_mma_variant<KV, D, 8, kNwMma, S, BPS, kGen>(p, tk, tv, stream);
     case 16:
-      if constexpr (kGen) return launch_mma_variant<KV, D, 16, kNwMma, S, BPS, kGen>(p, tk, tv, stream);
+      if constexpr (kGen && mma_record_fits<KV, D, S, BPS>(16))
+        return launch_mma_variant<KV, D, 16, kNwMma, S, BPS, kGen>(p, tk, tv, stream);
       return cudaErrorInvalidValue;
     default: return cudaErrorInvalidValue;
   }
@@ -756,7 +767,8 @@ int occupancy_mma_cols(int cols) {
     case 4: return mma_ctas_per_sm_variant<KV, D, 4, kNwMma, S, BPS, kGen>();
     case 8: return mma_ctas_per_sm_variant<KV, D, 8, kNwMma, S, BPS, kGen>();
     case 16:
-      if constexpr (kGen) return mma_ctas_per_sm_variant<KV, D, 16, kNwMma, S, BPS, kGen>();
+      if constexpr (kGen && mma_record_fits<KV, D, S, BPS>(16))
+        return mma_ctas_per_sm_variant<KV, D, 16, kNwMma, S, BPS, kGen>();
       return 0;
   }
   return 0;
