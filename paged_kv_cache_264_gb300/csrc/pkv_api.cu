@@ -255,10 +255,6 @@ int decode_ctas_per_sm(KvType kv, int head_dim, int cols) {
   return slot;
 }
 
-int decode_block_bytes(KvType kv, int head_dim) {
-  const bool scaled = kv != KvType::kBf16;
-  return 2 * kBlockSize * head_dim * (scaled ? 1 : 2) + (scaled ? 2 * kBlockSize * 4 : 0);
-}
 }  // namespace pkv
 
 extern "C" {

@@ -1,4 +1,7 @@
-// pkv_decode.cuh -- PagedAttention decode kernels for sm_103a.
+// pkv_decode.cuh -- PagedAttention decode on the CUDA cores (paged_decode_kernel), the
+// work scheduling and partition merge shared with the tensor-core kernel
+// (pkv_decode_mma.cuh), for sm_103a.  The tensor-core kernel is the automatic choice
+// wherever it is built; this one covers INT8 and FP8 pools at head_dim 64 and can be forced.
 //
 // What is computed ("Lesson 4: Model deployment and inference acceleration", 4.2,
 // attention-invariance equation): for sequence b and query head h,
@@ -9,22 +12,23 @@
 //
 // Work decomposition.  A work item is (sequence b, kv head, context partition p); the
 // partition covers P consecutive logical blocks.  One CTA of NW warps runs one item and
-// serves all G query heads of its kv head, so each K/V block is read from HBM once per
-// group.  Warp w takes the item's blocks w, w + NW, ...; each warp owns a ring of S
+// serves all query columns of its kv head (the G query heads of the group, times the query
+// tokens of a multi-query call; template parameter G counts column slots), so each K/V
+// block is read from HBM once per group.  Warp w takes the item's blocks w, w + NW, ...; each warp owns a ring of S
 // shared-memory stages, and its lane 0 fills a stage with one bulk asynchronous copy
 // per tile (the [phys][kvh] K tile and V tile are each one contiguous 16*D-element
 // run, so no tensor map is needed), completing on the stage's mbarrier.  The block
 // table slice of the item is staged in shared memory first.
 //
-// Per block a warp computes 16 tokens x G heads of logits with fp32 FMAs: lanes split
-// a token's D dims (DPL dims each) and hold q for all G heads in registers; a
+// Per block a warp computes 16 tokens x G columns of logits with fp32 FMAs: lanes split
+// a token's D dims (DPL dims each) and hold q for all G columns in registers; a
 // transposed butterfly reduces the G partial dot products across the lanes of a token
-// so that each lane ends with one head's logit.  The online softmax ("LLM/MLLM inference
+// so that each lane ends with one column's logit.  The online softmax ("LLM/MLLM inference
 // optimisation", 3.2: running max and running sum) rescales the running state by
 // exp(m_old - m_new) per block; logits are kept in log2 units (scale * log2 e is folded
 // into q) so that exp2 is the only exponential.  Probabilities go through a small
 // per-warp shared array to the PV layout, where each lane owns D/32 output dims of all
-// G heads.  At the end of the item the NW warp states merge in shared memory; a
+// G columns.  At the end of the item the NW warp states merge in shared memory; a
 // single-partition sequence writes bf16 output directly, otherwise the item writes its
 // partial (max, sum, accumulator) and a second kernel merges the partitions with the
 // same log-sum-exp algebra.
@@ -109,7 +113,7 @@ struct DecodeCfg {
   static constexpr int kLPT = D / kDPL;           // QK: lanes per token
   static constexpr int kTPP = 32 / kLPT;          // QK: tokens per pass
   static constexpr int kPasses = kBlockSize / kTPP;
-  static constexpr int kDup = kLPT / G;            // lanes holding the same (token, head) logit
+  static constexpr int kDup = kLPT / G;            // lanes holding the same (token, column) logit
   static constexpr int kDPV = D / 32;             // PV: dims per lane
   static constexpr int kThreads = NW * 32;
   static constexpr bool kSwapHalves = !kQuant && kDPL == 16;

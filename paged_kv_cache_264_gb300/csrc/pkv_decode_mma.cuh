@@ -473,25 +473,39 @@ __global__ void __launch_bounds__(NW * 32)
           pr[j][nt][1] = fast_exp2(sc[j][nt][1] - mu[nt][1]);
           pr[j][nt][2] = fast_exp2(sc[j][nt][2] - mu[nt][0]);
           pr[j][nt][3] = fast_exp2(sc[j][nt][3] - mu[nt][1]);
-          ps[nt][0] += pr[j][nt][0] + pr[j][nt][2];
-          ps[nt][1] += pr[j][nt][1] + pr[j][nt][3];
         }
-#pragma unroll
-      for (int nt = 0; nt < NT; ++nt) {
-        l[nt][0] = fmaf(l[nt][0], r[nt][0], ps[nt][0]);
-        l[nt][1] = fmaf(l[nt][1], r[nt][1], ps[nt][1]);
-      }
 
       uint32_t x01[BPS][NT], x23[BPS][NT];
       if constexpr (!C::kQuant) {
+        // P enters the PV product as bf16 (8 significant bits); the softmax sum takes the
+        // same rounded weights, so that numerator and denominator agree (summing the fp32
+        // weights instead leaves a systematic relative error of up to 2^-9 in the output).
 #pragma unroll
         for (int j = 0; j < BPS; ++j)
 #pragma unroll
           for (int nt = 0; nt < NT; ++nt) {
             x01[j][nt] = pack_bf16x2(pr[j][nt][0], pr[j][nt][1]);
             x23[j][nt] = pack_bf16x2(pr[j][nt][2], pr[j][nt][3]);
+            ps[nt][0] += bf16lo(x01[j][nt]) + bf16lo(x23[j][nt]);
+            ps[nt][1] += bf16hi(x01[j][nt]) + bf16hi(x23[j][nt]);
           }
       } else {
+        // fp16 P' (11 significant bits) carries the V scale too; the sum stays on the fp32
+        // weights, whose rounding in P' is 4x finer than bf16's.
+#pragma unroll
+        for (int j = 0; j < BPS; ++j)
+#pragma unroll
+          for (int nt = 0; nt < NT; ++nt) {
+            ps[nt][0] += pr[j][nt][0] + pr[j][nt][2];
+            ps[nt][1] += pr[j][nt][1] + pr[j][nt][3];
+          }
+      }
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt) {
+        l[nt][0] = fmaf(l[nt][0], r[nt][0], ps[nt][0]);
+        l[nt][1] = fmaf(l[nt][1], r[nt][1], ps[nt][1]);
+      }
+      if constexpr (C::kQuant) {
         float sv[BPS][2];
         float svm = 0.0f;
 #pragma unroll

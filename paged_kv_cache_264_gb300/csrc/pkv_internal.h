@@ -112,7 +112,5 @@ int mma_ctas_per_sm(KvType kv, int head_dim, int cols, int shape, bool gen);
 
 // Resident CTAs per SM of the CUDA-core decode kernel variant (0 if not built).
 int decode_ctas_per_sm(KvType kv, int head_dim, int cols);
-// Bytes of K+V (+scales) one 16-token block brings in for one kv head.
-int decode_block_bytes(KvType kv, int head_dim);
 
 }  // namespace pkv
