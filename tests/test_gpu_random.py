@@ -15,7 +15,7 @@ from gpu_helpers import compare, gpu_pool_from, oracle_decode
 
 pytestmark = pytest.mark.gpu
 
-N_CASES = 120
+N_CASES = 400
 
 
 @pytest.fixture(scope="module", autouse=True)
@@ -71,5 +71,8 @@ def test_random_case(seed):
     torch.cuda.synchronize()
     assert pool.device_error() == 0, c
     ref, _, _ = oracle_decode(w, c["kv"], window=c["window"])
-    compare(out, ref, str(c), output_rounding=0 < c["window"] < 16)
+    # Queries that attend to only a few tokens return (nearly) single V values, whose own
+    # bf16 rounding is then counted in the mean bound, as for other single-value outputs.
+    fewest = min(min(t - c["k"] + 1, c["window"] or t) for t in c["lens"])
+    compare(out, ref, str(c), output_rounding=fewest < 16)
     pool.close()
