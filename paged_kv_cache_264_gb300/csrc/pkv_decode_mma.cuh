@@ -377,10 +377,11 @@ __global__ void __launch_bounds__(NW * 32)
         } else {
           // Lane (gi, gj) reads dims 32gj..32gj+31 of tokens gi and gi+8; k-step s2 pairs
           // dims 32gj+4s2+{0,1} with k slots 2gj, 2gj+1 and +{2,3} with 2gj+8, 2gj+9.
-          const uint4 x0 = *reinterpret_cast<const uint4*>(kt + koff[0]);
-          const uint4 x1 = *reinterpret_cast<const uint4*>(kt + koff[1]);
-          const uint4 y0 = *reinterpret_cast<const uint4*>(kt + koff[2]);
-          const uint4 y1 = *reinterpret_cast<const uint4*>(kt + koff[3]);
+          const uint32_t kts = smem_addr(kt);
+          const uint4 x0 = lds_v4(kts + koff[0]);
+          const uint4 x1 = lds_v4(kts + koff[1]);
+          const uint4 y0 = lds_v4(kts + koff[2]);
+          const uint4 y1 = lds_v4(kts + koff[3]);
           const uint32_t wa[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
           const uint32_t wb[8] = {y0.x, y0.y, y0.z, y0.w, y1.x, y1.y, y1.z, y1.w};
 #pragma unroll
@@ -418,8 +419,8 @@ __global__ void __launch_bounds__(NW * 32)
         float f0 = logit_factor, f1 = logit_factor;
         if constexpr (C::kQuant) {
           if (vt[j] > 0) {
-            f0 *= sc_st[j * kBlockSize + gi];
-            f1 *= sc_st[j * kBlockSize + gi + 8];
+            f0 *= lds_f32(smem_addr(sc_st + j * kBlockSize + gi));
+            f1 *= lds_f32(smem_addr(sc_st + j * kBlockSize + gi + 8));
           }
         }
 #pragma unroll
@@ -512,8 +513,10 @@ __global__ void __launch_bounds__(NW * 32)
         for (int j = 0; j < BPS; ++j) {
           // scales of tokens outside [tlo, vt) may be anything: their weight is 0 anyway
           const unsigned span = unsigned(vt[j] - tlo[j]);
-          sv[j][0] = unsigned(gi - tlo[j]) < span ? sc_st[(BPS + j) * kBlockSize + gi] : 0.0f;
-          sv[j][1] = unsigned(gi + 8 - tlo[j]) < span ? sc_st[(BPS + j) * kBlockSize + gi + 8] : 0.0f;
+          const float s0 = lds_f32(smem_addr(sc_st + (BPS + j) * kBlockSize + gi));
+          const float s1 = lds_f32(smem_addr(sc_st + (BPS + j) * kBlockSize + gi + 8));
+          sv[j][0] = unsigned(gi - tlo[j]) < span ? s0 : 0.0f;
+          sv[j][1] = unsigned(gi + 8 - tlo[j]) < span ? s1 : 0.0f;
           svm = fmaxf(svm, fmaxf(sv[j][0], sv[j][1]));
         }
 #pragma unroll
@@ -601,10 +604,11 @@ __global__ void __launch_bounds__(NW * 32)
           // as for bf16.
           // Lane (gi, gj) reads dims 16gi..16gi+15 of tokens 2gj, 2gj+1, 2gj+8, 2gj+9; m-tile
           // t row gi is dim 16gi+2t and row gi+8 is dim 16gi+2t+1.
-          const uint4 va = *reinterpret_cast<const uint4*>(vtp + voff[0]);
-          const uint4 vb = *reinterpret_cast<const uint4*>(vtp + voff[1]);
-          const uint4 vc = *reinterpret_cast<const uint4*>(vtp + voff[2]);
-          const uint4 vd = *reinterpret_cast<const uint4*>(vtp + voff[3]);
+          const uint32_t vts = smem_addr(vtp);
+          const uint4 va = lds_v4(vts + voff[0]);
+          const uint4 vb = lds_v4(vts + voff[1]);
+          const uint4 vc = lds_v4(vts + voff[2]);
+          const uint4 vd = lds_v4(vts + voff[3]);
           constexpr uint32_t kFlip = C::kFp8 ? 0u : 0x80808080u;
           const unsigned span8 = unsigned(vt[j] - tlo[j]);
           const uint32_t mlo8 = (unsigned(2 * gj - tlo[j]) < span8 ? 0x0000ffffu : 0u) |

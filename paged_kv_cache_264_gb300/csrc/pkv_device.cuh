@@ -80,6 +80,22 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity
   return false;
 }
 
+// Shared-memory loads by shared-window address (ld.shared rather than a generic load).
+// Volatile, so they stay after the mbarrier wait (also volatile asm) that publishes the data.
+__device__ __forceinline__ uint4 lds_v4(uint32_t addr) {
+  uint4 v;
+  asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "r"(addr));
+  return v;
+}
+
+__device__ __forceinline__ float lds_f32(uint32_t addr) {
+  float v;
+  asm volatile("ld.shared.f32 %0, [%1];" : "=f"(v) : "r"(addr));
+  return v;
+}
+
 // 2^x for the softmax (x <= 0 in practice): the hardware base-2 exponential, flushing
 // subnormal results to zero (weights below 2^-126 do not matter next to the largest, 1).
 __device__ __forceinline__ float fast_exp2(float x) {
