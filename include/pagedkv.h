@@ -391,6 +391,18 @@ PKV_API pkv_status pkv_paged_attention_decode_static_scratch(
     const int32_t* context_lens, int num_seqs, int num_q_heads, int max_context_len, float scale,
     void* out, void* stream);
 
+/*
+ * Failure-detection self-test (no counterpart on the pages; for tests of this library).
+ * Runs the decode kernels' bounded mbarrier wait, in a one-warp kernel on `stream`, on a
+ * barrier that nothing completes, with a limit of limit_ns (1e5 .. 2e9 ns; the decode
+ * kernels use 2e9).  The wait must give up: *flags receives PKV_DEVERR_TIMEOUT and
+ * *waited_ns the wall time the kernel waited (at least limit_ns, plus at most 64 polls of
+ * up to 1 ms).  The CUDA context stays usable.  Synchronises `stream`.
+ * Errors: PKV_ERR_INVALID_ARG, PKV_ERR_CUDA.
+ */
+PKV_API pkv_status pkv_selftest_bounded_wait(uint64_t limit_ns, uint32_t* flags, uint64_t* waited_ns,
+                                             void* stream);
+
 /* Text of the last static-scratch error in this thread (static per thread). */
 PKV_API const char* pkv_static_scratch_error(void);
 

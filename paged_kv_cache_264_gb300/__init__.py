@@ -17,6 +17,7 @@ from .api import (  # noqa: F401
     pool_create,
     pool_destroy,
     reshape_and_cache,
+    selftest_bounded_wait,
     version,
 )
 from ._lib import (  # noqa: F401

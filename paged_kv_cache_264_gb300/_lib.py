@@ -70,6 +70,7 @@ SIGNATURES = {
                                                          _vp, _vp]),
     "pkv_static_scratch_error": (ctypes.c_char_p, []),
     "pkv_copy_blocks": (_i32, [_vp, _vp, _i32, _vp]),
+    "pkv_selftest_bounded_wait": (_i32, [ctypes.c_uint64, _vp, _vp, _vp]),
     "pkv_block_manager_create": (_i32, [_i64, _i32, _i32, ctypes.POINTER(_vp)]),
     "pkv_block_manager_destroy": (_i32, [_vp]),
     "pkv_block_manager_add_sequence": (_i32, [_vp, _pi32]),

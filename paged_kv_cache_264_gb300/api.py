@@ -235,6 +235,15 @@ def get_device_error(pool: PagedKVPool, stream=None) -> int:
     return v.value
 
 
+def selftest_bounded_wait(limit_ns: int, stream=None) -> tuple[int, int]:
+    """Run the kernels' bounded wait on a barrier nothing completes: (flags, waited_ns).
+    The wait is expected to give up with DEVERR_TIMEOUT after about limit_ns."""
+    flags, waited = ctypes.c_uint32(), ctypes.c_uint64()
+    check(_lib.load().pkv_selftest_bounded_wait(int(limit_ns), ctypes.byref(flags), ctypes.byref(waited),
+                                                _stream(stream)), "selftest_bounded_wait")
+    return flags.value, waited.value
+
+
 def paged_attention_decode_static_scratch(pool: PagedKVPool, q: torch.Tensor, block_tables: torch.Tensor,
                                           context_lens: torch.Tensor, scale: float, max_context_len: int,
                                           out: torch.Tensor | None = None, stream=None) -> torch.Tensor:

@@ -68,14 +68,15 @@ __device__ __forceinline__ uint64_t global_timer_ns() {
 }
 
 // Wait for the barrier phase with the given parity to complete.  Gives up (returns
-// false) after kWaitTimeoutNs of wall time or 2^26 polls, whichever comes first, so that
-// a lost copy can never hang the GPU.
-__device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity) {
+// false) after limit_ns of wall time (kWaitTimeoutNs in the kernels) or 2^26 polls,
+// whichever comes first, so that a lost copy can never hang the GPU.
+__device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity,
+                                                  uint64_t limit_ns = kWaitTimeoutNs) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = global_timer_ns();
   for (uint32_t it = 0; it < (1u << 26); ++it) {
     if (mbar_try_wait(bar, parity)) return true;
-    if ((it & 63u) == 63u && global_timer_ns() - t0 > kWaitTimeoutNs) return false;
+    if ((it & 63u) == 63u && global_timer_ns() - t0 > limit_ns) return false;
   }
   return false;
 }
