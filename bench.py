@@ -323,21 +323,29 @@ def run_ours(args, rank, world, local):
 def run_e2e(args, pkv, pool, w, new_k, new_v, new_slots, q, tables, lens, max_ctx, ws, sb, stream,
             dev, world, win=0):
     """Same step through the public API, but every step copies its inputs from pinned
-    host memory and reads the output back."""
-    host = {
-        "q": q.cpu().pin_memory(), "k": new_k.cpu().pin_memory(), "v": new_v.cpu().pin_memory(),
-        "slots": new_slots.cpu().pin_memory(), "tables": tables.cpu().pin_memory(),
-        "lens": lens.cpu().pin_memory(),
-    }
-    dbuf = {k: torch.empty_like(v, device=dev) for k, v in host.items()}
+    host memory and reads the output back.  The step's inputs (q, the appended K/V rows,
+    their slots, the page tables and lengths) sit in one pinned staging buffer and go to
+    the device in one copy."""
+    parts = [("q", q), ("k", new_k), ("v", new_v), ("slots", new_slots), ("tables", tables), ("lens", lens)]
+    offs, size = {}, 0
+    for name, t in parts:
+        nbytes = t.numel() * t.element_size()
+        offs[name] = (size, nbytes)
+        size += (nbytes + 255) // 256 * 256  # 256-byte aligned views
+    host_buf = torch.empty(size, dtype=torch.uint8).pin_memory()
+    dev_buf = torch.empty(size, dtype=torch.uint8, device=dev)
+    dbuf = {}
+    for name, t in parts:
+        o, nbytes = offs[name]
+        host_buf[o:o + nbytes].copy_(t.contiguous().cpu().view(torch.uint8).reshape(-1))
+        dbuf[name] = dev_buf[o:o + nbytes].view(t.dtype).view(t.shape)
     out_d = torch.empty_like(q)
     out_h = torch.empty(q.shape, dtype=q.dtype).pin_memory()
-    h2d = sum(t.numel() * t.element_size() for t in host.values())
+    h2d = size
     d2h = out_h.numel() * out_h.element_size()
 
     def step():
-        for k in host:
-            dbuf[k].copy_(host[k], non_blocking=True)
+        dev_buf.copy_(host_buf, non_blocking=True)
         pkv.reshape_and_cache(pool, dbuf["k"], dbuf["v"], dbuf["slots"], stream)
         pkv.paged_attention_decode(pool, dbuf["q"], dbuf["tables"], dbuf["lens"], w.scale, max_ctx,
                                    out=out_d, workspace=ws, window=win, stream=stream)

@@ -173,6 +173,12 @@ pkv_status make_plan(const pkv_pool* pool, int num_seqs, int num_q_heads, int ma
   if (P > kMaxPartitionBlocks) P = kMaxPartitionBlocks;
   if (P > max_nblk) P = static_cast<int>(max_nblk);
   if (P < 1) P = 1;
+  if (!(opt && opt->partition_blocks > 0)) {
+    // Same number of partitions, equal sizes: the longest sequences split into items of
+    // equal work instead of full items and a short remainder (a 257-block window with
+    // 64-block items would leave a 1-block item).
+    P = static_cast<int>(ceil_div(max_nblk, ceil_div(max_nblk, P)));
+  }
   plan->partition_blocks = P;
   plan->max_parts = static_cast<int>(ceil_div(max_nblk, P));
   // Persistent CTAs pay off when the grid would hold idle slots, i.e. when sequences split
