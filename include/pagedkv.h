@@ -23,7 +23,7 @@
  *    pkv_get_device_error), and the offending access is skipped.
  *  - Layouts are row-major ("C order"); element sizes are those of the named types.
  *  - Calls on one pool must be ordered on one stream (or otherwise serialised): the
- *    pool's device error word is shared by its calls.
+ *    pool's device error word and its scheduler counters are shared by its calls.
  */
 #ifndef PAGEDKV_H_
 #define PAGEDKV_H_
@@ -70,7 +70,7 @@ typedef enum pkv_kv_dtype {
 
 /* Bits of the device error word. */
 #define PKV_DEVERR_BLOCK_ID 0x1u    /* a block-table entry read by decode was < 0 or >= num_blocks */
-#define PKV_DEVERR_CONTEXT_LEN 0x2u /* a context length was < 1 or > max_context_len            */
+#define PKV_DEVERR_CONTEXT_LEN 0x2u /* a context length was < k (1 for one query token) or > max_context_len */
 #define PKV_DEVERR_SLOT 0x4u        /* a slot_mapping entry was >= num_blocks * 16               */
 #define PKV_DEVERR_TIMEOUT 0x8u     /* an asynchronous copy did not arrive within the time limit */
 
@@ -247,11 +247,12 @@ PKV_API int32_t pkv_block_manager_refcount(const pkv_block_manager* manager, int
  *     shape and the device's SM count.
  *   kernel: which decode kernel family runs.  Both serve, per (sequence, kv head), a tile
  *     of group * num_queries query columns.  PKV_KERNEL_AUTO (0) picks the tensor-core
- *     kernel where it is built (2 to 16 columns; bf16 head_dim 64/128, INT8 or FP8
- *     head_dim 128) and the CUDA-core kernel otherwise (1 to 8 columns; the choice for a
- *     single column, i.e. MHA with one query); PKV_KERNEL_CUDA_CORE (1) and
- *     PKV_KERNEL_TENSOR_CORE (2) force one (PKV_ERR_UNSUPPORTED if it is not built for
- *     the shape).  Both compute the same function.
+ *     kernel wherever it is built (1 to 16 columns; bf16 head_dim 64/128, INT8 or FP8
+ *     head_dim 128; measured faster than the CUDA-core kernel on every such shape, MHA
+ *     included) and the CUDA-core kernel otherwise (1 to 8 columns: INT8 and FP8 at
+ *     head_dim 64); PKV_KERNEL_CUDA_CORE (1) and PKV_KERNEL_TENSOR_CORE (2) force one
+ *     (PKV_ERR_UNSUPPORTED if it is not built for the shape).  Both compute the same
+ *     function.
  *   schedule: how CTAs map to work items.  PKV_SCHEDULE_AUTO (0) picks;
  *     PKV_SCHEDULE_GRID (1) launches one CTA per (partition slot, sequence, kv head), slots
  *     past a sequence's partition count exiting at once; PKV_SCHEDULE_PERSISTENT (2)
@@ -327,7 +328,8 @@ PKV_API pkv_status pkv_decode_plan(const pkv_pool* pool, int num_seqs, int num_q
  *   q            (device): bf16 [num_seqs, num_q_heads, head_dim], 16-byte aligned.
  *   block_tables (device): int32 [num_seqs, max_blocks_per_seq]; entries past
  *                          ceil(T_b / 16) are never read.
- *   context_lens (device): int32 [num_seqs], 1 <= T_b <= max_context_len.
+ *   context_lens (device): int32 [num_seqs], 1 <= T_b <= max_context_len (k <= T_b with
+ *                          k query tokens per sequence).
  *   max_context_len (host int): an upper bound on every T_b; it sizes the plan and the
  *                          workspace and must be <= max_blocks_per_seq * 16.
  *   scale: softmax scale, usually 1 / sqrt(head_dim).
@@ -350,7 +352,8 @@ PKV_API pkv_status pkv_paged_attention_decode(const pkv_pool* pool, const void* 
 
 /*
  * pkv_paged_attention_decode with explicit plan options (NULL = automatic), including
- * options->num_queries for multi-query (draft verification) calls.
+ * options->num_queries for multi-query (draft verification) calls and options->window for
+ * sliding-window attention.
  */
 PKV_API pkv_status pkv_paged_attention_decode_ex(const pkv_pool* pool, const void* q,
                                          const int32_t* block_tables, int max_blocks_per_seq,
@@ -391,18 +394,6 @@ PKV_API pkv_status pkv_paged_attention_decode_static_scratch(
     const int32_t* context_lens, int num_seqs, int num_q_heads, int max_context_len, float scale,
     void* out, void* stream);
 
-/*
- * Failure-detection self-test (no counterpart on the pages; for tests of this library).
- * Runs the decode kernels' bounded mbarrier wait, in a one-warp kernel on `stream`, on a
- * barrier that nothing completes, with a limit of limit_ns (1e5 .. 2e9 ns; the decode
- * kernels use 2e9).  The wait must give up: *flags receives PKV_DEVERR_TIMEOUT and
- * *waited_ns the wall time the kernel waited (at least limit_ns, plus at most 64 polls of
- * up to 1 ms).  The CUDA context stays usable.  Synchronises `stream`.
- * Errors: PKV_ERR_INVALID_ARG, PKV_ERR_CUDA.
- */
-PKV_API pkv_status pkv_selftest_bounded_wait(uint64_t limit_ns, uint32_t* flags, uint64_t* waited_ns,
-                                             void* stream);
-
 /* Text of the last static-scratch error in this thread (static per thread). */
 PKV_API const char* pkv_static_scratch_error(void);
 
@@ -414,6 +405,18 @@ PKV_API pkv_status pkv_get_device_error(const pkv_pool* pool, uint32_t* flags, v
 
 /* Number of kernels this library has launched in this process (all threads). */
 PKV_API uint64_t pkv_launch_count(void);
+
+/*
+ * Failure-detection self-test (no counterpart on the pages; for tests of this library).
+ * Runs the decode kernels' bounded mbarrier wait, in a one-warp kernel on `stream`, on a
+ * barrier that nothing completes, with a limit of limit_ns (1e5 .. 2e9 ns; the decode
+ * kernels use 2e9).  The wait must give up: *flags receives PKV_DEVERR_TIMEOUT and
+ * *waited_ns the wall time the kernel waited (at least limit_ns, plus at most 64 polls of
+ * up to 1 ms).  The CUDA context stays usable.  Synchronises `stream`.
+ * Errors: PKV_ERR_INVALID_ARG, PKV_ERR_CUDA.
+ */
+PKV_API pkv_status pkv_selftest_bounded_wait(uint64_t limit_ns, uint32_t* flags, uint64_t* waited_ns,
+                                             void* stream);
 
 #ifdef __cplusplus
 }

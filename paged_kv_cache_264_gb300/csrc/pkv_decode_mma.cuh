@@ -1,6 +1,7 @@
 // pkv_decode_mma.cuh -- PagedAttention decode on the tensor cores (mma.sync) for tiles of
-// 2, 4, 8 or 16 query columns per kv head (GQA groups, times the query tokens of a
-// multi-query call), head_dim 128 (bf16, INT8 or FP8 pools) or 64 (bf16).
+// 2, 4, 8 or 16 query columns per kv head (the GQA group's heads times the query tokens of
+// a multi-query call; a single column, MHA decode, uses 2), head_dim 128 (bf16, INT8 or
+// FP8 pools) or 64 (bf16).
 //
 // Same work decomposition and result as paged_decode_kernel (pkv_decode.cuh): one CTA
 // per (sequence, kv head, context partition), NW warps taking the item's blocks in turn,
@@ -13,23 +14,26 @@
 //  * Logits for all query columns come from m16n8k16 MMAs with fp32 accumulation:
 //    S[16 tokens x 8 columns] = K[16 x d] q^T[d x 8] per n-tile of 8 columns (columns past
 //    the active ones are zero).  Each K fragment feeds every n-tile.  A column is one
-//    (query token, head of the group) pair and has its own causal cut, applied when the
+//    (query token, head of the group) pair; with several query tokens or a sliding window
+//    (the kGen variant) each column has its own causal cut and window, applied when the
 //    logits are masked.
 //  * The probabilities stay in registers: the accumulator fragment of S, packed to 16-bit
 //    pairs and transposed with movmatrix, is exactly the B operand of the PV product
 //    O^T[d x 8] += V^T[d x 16] P[16 x 8], whose A operand is V read transposed by ldmatrix.
-//    The row (dims) of O^T that a lane holds and the column (head) of its softmax state
-//    coincide, so rescaling needs no data movement, and it is skipped whenever no head's
-//    running max moved in a block.
+//    The row (dims) of O^T that a lane holds and the column of its softmax state
+//    coincide, so rescaling needs no data movement, and it is skipped whenever no
+//    column's running max moved in a block.  For bf16 pools P enters the product as bf16,
+//    and the softmax sum adds those same rounded weights.
 //  * INT8: codes become fp16 values 1152 + code exactly (see f16x2_biased) and both
 //    products run in fp16; the constant 1152 is taken out afterwards: from the logits as
-//    1152 * sum_d q_d per head, and from O^T as 1152 times the running sum of P per head.  q is scaled by a power of two into fp16 range (exact for bf16 values), the
+//    1152 * sum_d q_d per column, and from O^T as 1152 times the running sum of P per
+//    column.  q is scaled by a power of two into fp16 range (exact for bf16 values), the
 //    K scale multiplies the fp32 logits, and the V scale is folded into P together with a
-//    power-of-two block exponent that keeps P in [0, 2): O^T is kept in units of 2^E and E
+//    power-of-two block exponent that keeps P in [0, 4): O^T is kept in units of 2^E and E
 //    only grows, like the running max, so the rescale stays rare.  FP8 (E4M3) pools take
-//    the same path with the hardware E4M3 -> fp16 conversion and no offset.  Within one k-step the
-//    dims a lane handles are permuted (the same permutation on K and q), which lets each
-//    lane read its codes with 16-byte loads.
+//    the same path with the hardware E4M3 -> fp16 conversion and no offset.  Within one
+//    k-step the dims a lane handles are permuted (the same permutation on K and q), which
+//    lets each lane read its codes with 16-byte loads.
 #pragma once
 
 #include <limits.h>
