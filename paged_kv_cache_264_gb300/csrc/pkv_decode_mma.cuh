@@ -29,7 +29,7 @@
 //    1152 * sum_d q_d per column, and from O^T as 1152 times the running sum of P per
 //    column.  q is scaled by a power of two into fp16 range (exact for bf16 values), the
 //    K scale multiplies the fp32 logits, and the V scale is folded into P together with a
-//    power-of-two block exponent that keeps P in [0, 4): O^T is kept in units of 2^E and E
+//    power-of-two block exponent that keeps P in [0, 2): O^T is kept in units of 2^E and E
 //    only grows, like the running max, so the rescale stays rare.  FP8 (E4M3) pools take
 //    the same path with the hardware E4M3 -> fp16 conversion and no offset.  Within one
 //    k-step the dims a lane handles are permuted (the same permutation on K and q), which
@@ -536,7 +536,7 @@ __global__ void __launch_bounds__(NW * 32)
           }
         }
         e_run = e_new;
-        const float pe = pow2i(-e_new);  // P' = p * s_V * 2^-E lies in [0, 4)
+        const float pe = pow2i(-e_new);  // P' = p * s_V * 2^-E lies in [0, 2)
         float qp[NT][2];  // this stage's sum of the fp16 P' per column
 #pragma unroll
         for (int nt = 0; nt < NT; ++nt) qp[nt][0] = qp[nt][1] = 0.0f;
