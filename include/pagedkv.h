@@ -246,10 +246,11 @@ PKV_API int32_t pkv_block_manager_refcount(const pkv_block_manager* manager, int
  *     one partition are combined by a log-sum-exp reduce.  0 = chosen from the batch
  *     shape and the device's SM count.
  *   kernel: which decode kernel family runs.  Both serve, per (sequence, kv head), a tile
- *     of group * num_queries query columns.  PKV_KERNEL_AUTO (0) picks the tensor-core
- *     kernel wherever it is built (1 to 16 columns; bf16 head_dim 64/128, INT8 or FP8
- *     head_dim 128; measured faster than the CUDA-core kernel on every such shape, MHA
- *     included) and the CUDA-core kernel otherwise (1 to 8 columns: INT8 and FP8 at
+ *     of group * num_queries query columns, in chunks of up to 16 (tensor cores) or 8
+ *     (CUDA cores) columns, each chunk one work unit that reads the kv head's blocks.
+ *     PKV_KERNEL_AUTO (0) picks the tensor-core kernel wherever it is built (bf16 head_dim
+ *     64/128, INT8 or FP8 head_dim 128; measured faster than the CUDA-core kernel on every
+ *     such shape, MHA included) and the CUDA-core kernel otherwise (INT8 and FP8 at
  *     head_dim 64); PKV_KERNEL_CUDA_CORE (1) and PKV_KERNEL_TENSOR_CORE (2) force one
  *     (PKV_ERR_UNSUPPORTED if it is not built for the shape).  Both compute the same
  *     function.
@@ -267,8 +268,8 @@ PKV_API int32_t pkv_block_manager_refcount(const pkv_block_manager* manager, int
  *     scores all drafts at once): the k queries are the sequence's last k cached
  *     positions, appended beforehand by pkv_reshape_and_cache, and query i attends
  *     causally, to tokens t < T_b - (k - 1 - i).  q and out are then
- *     [num_seqs, k, num_q_heads, head_dim]; each K/V block is still read once per kv
- *     head.  1 <= k <= 16, group * k <= 16 (<= 8 where only the CUDA-core kernel is built),
+ *     [num_seqs, k, num_q_heads, head_dim]; each K/V block is read once per kv head and
+ *     column chunk (one chunk while group * k <= 16 on the tensor cores).  1 <= k <= 16,
  *     max_context_len >= k, and a sequence with T_b < k counts as out of range.
  *   window: sliding-window attention ("LLM/MLLM inference optimisation", 2.3: keep only the
  *     most recent window of the KV cache), 0 = none.  With window W > 0 a query at

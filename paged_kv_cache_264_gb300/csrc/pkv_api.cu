@@ -75,7 +75,8 @@ constexpr int kItemBlocksTensorCore = 64;
 
 struct Plan {
   int kernel;  // PKV_KERNEL_CUDA_CORE or PKV_KERNEL_TENSOR_CORE
-  int cols;    // query-column slots of the kernel variant (>= group * num_queries)
+  int cols;    // query-column slots of the kernel variant
+  int chunks;  // column chunks per kv head: cols * chunks >= group * num_queries
   int num_queries;
   int window;  // tokens each query sees back from its own position (pkv::kNoWindow: all)
   int shape;   // tensor-core ring shape index
@@ -106,18 +107,17 @@ pkv_status make_plan(const pkv_pool* pool, int num_seqs, int num_q_heads, int ma
   }
   const auto kv = static_cast<pkv::KvType>(pool->dtype);
   // Query columns per (sequence, kv head): the group's heads times the query tokens.  The
-  // tensor-core kernel holds 2 to 16 column slots, the CUDA-core kernel 1 to 8.
+  // tensor-core kernel holds 2 to 16 column slots, the CUDA-core kernel 1 to 8; wider tiles
+  // are served in chunks of the largest slot count, each chunk its own work unit (it reads
+  // the kv head's blocks again, mostly from L2 since the chunks of a head run together).
   const int ncols = group * nq;
-  const int mma_cols = pow2_at_least(ncols < 2 ? 2 : ncols);
-  const int cc_cols = pow2_at_least(ncols);
+  const int mma_cols = ncols > 16 ? 16 : pow2_at_least(ncols < 2 ? 2 : ncols);
+  const int cc_cols = ncols > 8 ? 8 : pow2_at_least(ncols);
   const bool mma_ok = pool->has_tmaps && pkv::mma_supported(kv, pool->head_dim, mma_cols);
-  const bool cc_ok = cc_cols <= 8;
   const int want = opt ? opt->kernel : PKV_KERNEL_AUTO;
   if (want != PKV_KERNEL_AUTO && want != PKV_KERNEL_CUDA_CORE && want != PKV_KERNEL_TENSOR_CORE)
     return PKV_ERR_INVALID_ARG;
   if (want == PKV_KERNEL_TENSOR_CORE && !mma_ok) return PKV_ERR_UNSUPPORTED;
-  if (want == PKV_KERNEL_CUDA_CORE && !cc_ok) return PKV_ERR_UNSUPPORTED;
-  if (!mma_ok && !cc_ok) return PKV_ERR_UNSUPPORTED;
   // Automatic choice: the tensor-core kernel wherever it is built, one query column (MHA
   // decode) included -- measured on GB300 it beats the FMA kernel there too (LLaMA-2-7B
   // shape: 154 us against 161 us).
@@ -126,6 +126,7 @@ pkv_status make_plan(const pkv_pool* pool, int num_seqs, int num_q_heads, int ma
   else
     plan->kernel = PKV_KERNEL_CUDA_CORE;
   plan->cols = plan->kernel == PKV_KERNEL_TENSOR_CORE ? mma_cols : cc_cols;
+  plan->chunks = static_cast<int>(ceil_div(ncols, plan->cols));
   plan->num_queries = nq;
   const int sched = opt ? opt->schedule : PKV_SCHEDULE_AUTO;
   if (sched != PKV_SCHEDULE_AUTO && sched != PKV_SCHEDULE_GRID && sched != PKV_SCHEDULE_PERSISTENT)
@@ -166,7 +167,7 @@ pkv_status make_plan(const pkv_pool* pool, int num_seqs, int num_q_heads, int ma
     P = plan->kernel == PKV_KERNEL_TENSOR_CORE ? kItemBlocksTensorCore : kItemBlocksCudaCore;
     if (plan->kernel == PKV_KERNEL_TENSOR_CORE && (max_nblk <= 128 || plan->cols == 16)) P = 128;
     const int64_t resident = int64_t(pool->sm_count) * plan->ctas_per_sm;
-    const int64_t units = int64_t(num_seqs) * pool->kv_heads;
+    const int64_t units = int64_t(num_seqs) * pool->kv_heads * plan->chunks;
     // Shrink the partition while the batch would not fill the GPU twice over.
     while (P > 4 && units * ceil_div(max_nblk, P) < 2 * resident) P /= 2;
   }
@@ -472,7 +473,7 @@ pkv_status pkv_paged_attention_decode_ex(const pkv_pool* pool, const void* q,
   p.sched = pool->d_err + 1;
   p.persistent = plan.persistent;
   {
-    const int64_t items = int64_t(plan.max_parts) * num_seqs * pool->kv_heads;
+    const int64_t items = int64_t(plan.max_parts) * num_seqs * pool->kv_heads * plan.chunks;
     const int64_t resident = int64_t(pool->sm_count) * plan.ctas_per_sm;
     p.grid = static_cast<int>(items < resident ? items : resident);
   }
@@ -485,6 +486,7 @@ pkv_status pkv_paged_attention_decode_ex(const pkv_pool* pool, const void* q,
   p.group_log2 = p.group == 8 ? 3 : p.group == 4 ? 2 : p.group == 2 ? 1 : 0;
   p.num_queries = plan.num_queries;
   p.window = plan.window;
+  p.chunks = plan.chunks;
   p.head_dim = pool->head_dim;
   p.max_context_len = max_context_len;
   p.partition_blocks = plan.partition_blocks;

@@ -202,7 +202,7 @@ __device__ __forceinline__ void fma_code4(float (&part)[G], const float (&qr)[G]
 // A sequence whose context length is out of range counts as one item that writes zeros.
 
 struct ItemInfo {
-  int b, kvh, part, nparts, T;
+  int b, kvh, chunk, part, nparts, T;  // chunk: which slice of the kv head's query columns
   bool bad_len;
 };
 
@@ -276,7 +276,7 @@ __device__ __forceinline__ int first_item(const DecodeParams& p, const SchedSmem
   }
   __syncthreads();
   const int item = ss.slot[0];
-  return item < ss.cum[B] * p.kv_heads ? item : -1;
+  return item < ss.cum[B] * (p.kv_heads * p.chunks) ? item : -1;
 }
 
 // Ticket for the item after this one (thread 0 fetches it now; its value is used at the
@@ -292,7 +292,7 @@ __device__ __forceinline__ int next_item(const DecodeParams& p, const SchedSmem&
   __syncthreads();
   const int item = ss.slot[0];
   if (ss.slot[1]) return -1;  // a bounded wait gave up: stop taking work
-  return item < ss.cum[p.num_seqs] * p.kv_heads ? item : -1;
+  return item < ss.cum[p.num_seqs] * (p.kv_heads * p.chunks) ? item : -1;
 }
 
 __device__ __forceinline__ void finish_items(const DecodeParams& p) {
@@ -304,12 +304,16 @@ __device__ __forceinline__ void finish_items(const DecodeParams& p) {
   }
 }
 
-// (b, kv head, partition) of an item; false for an idle classic-grid slot.
+// (b, kv head, column chunk, partition) of an item; false for an idle classic-grid slot.
+// A sequence has kv_heads * chunks work units; the chunks of one kv head are adjacent, so
+// they tend to run together and share the head's K/V blocks in L2.
 __device__ __forceinline__ bool locate_item(const DecodeParams& p, const SchedSmem& ss, int item,
                                             ItemInfo& it) {
+  const int ups = p.kv_heads * p.chunks;  // work units per sequence
+  int v;
   if (p.persistent) {
-    const int u = item / p.kv_heads;
-    it.kvh = item - u * p.kv_heads;
+    const int u = item / ups;
+    v = item - u * ups;
     int lo = 0, hi = p.num_seqs;  // cum[lo] <= u < cum[hi]
     while (hi - lo > 1) {
       const int mid = (lo + hi) >> 1;
@@ -318,12 +322,14 @@ __device__ __forceinline__ bool locate_item(const DecodeParams& p, const SchedSm
     it.b = lo;
     it.part = u - ss.cum[lo];
   } else {
-    const int units = p.num_seqs * p.kv_heads;
+    const int units = p.num_seqs * ups;
     it.part = item / units;
     const int rem = item - it.part * units;
-    it.b = rem / p.kv_heads;
-    it.kvh = rem - it.b * p.kv_heads;
+    it.b = rem / ups;
+    v = rem - it.b * ups;
   }
+  it.kvh = v / p.chunks;
+  it.chunk = v - it.kvh * p.chunks;
   it.T = __ldg(p.context_lens + it.b);
   it.bad_len = it.T < p.num_queries || it.T > p.max_context_len;
   it.nparts = seq_parts(p, it.T);
@@ -352,15 +358,21 @@ __device__ __forceinline__ int col_cut(const DecodeParams& p, int c) {
 // without a special case; once a real logit arrives exp2(kMaxFloor - m) underflows to 0.
 constexpr float kMaxFloor = -3.402823466e38f;
 
+// Query columns in the chunk that starts at column c0 (NC slots; the last chunk may be short).
+__device__ __forceinline__ int chunk_cols(const DecodeParams& p, int c0, int nc) {
+  return min(nc, p.group * p.num_queries - c0);
+}
+
 // Zero output and an error bit for a sequence with an out-of-range context length.
 template <int NC, int D, int NT>
 __device__ __forceinline__ void write_bad_len(const DecodeParams& p, const ItemInfo& it) {
   if (it.part != 0) return;
   auto* out = static_cast<__nv_bfloat16*>(p.out);
-  const int ncols = p.group * p.num_queries;
+  const int c0 = it.chunk * NC;
+  const int ncols = chunk_cols(p, c0, NC);
   for (int i = threadIdx.x; i < NC * D; i += NT) {
     const int c = i / D;
-    if (c < ncols) out[col_row(p, it.b, it.kvh, c) * D + (i - c * D)] = __float2bfloat16_rn(0.0f);
+    if (c < ncols) out[col_row(p, it.b, it.kvh, c0 + c) * D + (i - c * D)] = __float2bfloat16_rn(0.0f);
   }
   if (threadIdx.x == 0) set_error(p.err, kErrContextLen);
 }
@@ -368,13 +380,13 @@ __device__ __forceinline__ void write_bad_len(const DecodeParams& p, const ItemI
 // Merge the NW per-warp states of one work item by log-sum-exp and write the bf16 output
 // (single-partition sequences) or the item's partial (m, l, acc) to the workspace.  Warp w's
 // record is [NC][D + 2] floats (running max in log2 units, sum, accumulator) per query
-// column at smem + w * warp_stride.
+// column at smem + w * warp_stride; record column c is query column c0 + c.
 template <int NC, int D, int NW>
 __device__ __forceinline__ void merge_warp_records(const unsigned char* smem, size_t warp_stride,
-                                                   const DecodeParams& p, int b, int kvh, int part,
-                                                   int nparts) {
+                                                   const DecodeParams& p, int b, int kvh, int c0,
+                                                   int part, int nparts) {
   auto* out = static_cast<__nv_bfloat16*>(p.out);
-  const int ncols = p.group * p.num_queries;
+  const int ncols = chunk_cols(p, c0, NC);
   for (int i = threadIdx.x; i < NC * D; i += NW * 32) {
     const int g = i / D;
     const int d = i - g * D;
@@ -393,7 +405,7 @@ __device__ __forceinline__ void merge_warp_records(const unsigned char* smem, si
         A = fmaf(f, r[2 + d], A);
       }
     }
-    const size_t row = col_row(p, b, kvh, g);
+    const size_t row = col_row(p, b, kvh, c0 + g);
     if (nparts == 1) {
       out[row * D + d] = __float2bfloat16_rn(L > 0.0f ? A / L : 0.0f);
     } else {
@@ -485,12 +497,13 @@ __global__ void __launch_bounds__(NW * 32)
   const int tok = lane / C::kLPT;    // token within a pass
   const int chunk = lane % C::kLPT;  // which DPL-dim slice of the row
   const int sw = C::kSwapHalves ? ((lane >> 2) & 1) : 0;
-  const int ncols = p.group * p.num_queries;
+  const int c0 = it.chunk * G;  // first query column of this item's chunk
+  const int ncols = chunk_cols(p, c0, G);
   float qr[G][C::kDPL];
   {
 #pragma unroll
     for (int g = 0; g < G; ++g) {
-      const auto* qrow = static_cast<const __nv_bfloat16*>(p.q) + col_row(p, b, kvh, g) * D;
+      const auto* qrow = static_cast<const __nv_bfloat16*>(p.q) + col_row(p, b, kvh, c0 + g) * D;
       const uint4* src = reinterpret_cast<const uint4*>(qrow + chunk * C::kDPL);
 #pragma unroll
       for (int h = 0; h < C::kDPL / 8; ++h) {
@@ -508,7 +521,7 @@ __global__ void __launch_bounds__(NW * 32)
 
   const int g_lane = (lane % C::kLPT) / C::kDup;  // column whose logit this lane ends with
   const bool store_lane = (lane % C::kDup) == 0;
-  const int cut = col_cut(p, g_lane);              // its causal cut (0 for a single query)
+  const int cut = col_cut(p, c0 + g_lane);         // its causal cut (0 for a single query)
   float m_run = kMaxFloor;
   float l_run = 0.0f;
   float acc[G][C::kDPV];
@@ -674,7 +687,7 @@ __global__ void __launch_bounds__(NW * 32)
     for (int i = 0; i < C::kDPV; ++i) rec[g * (D + 2) + 2 + lane * C::kDPV + i] = acc[g][i];
   __syncthreads();
 
-  merge_warp_records<G, D, NW>(smem, size_t(S) * C::kStageBytes, p, b, kvh, part, nparts);
+  merge_warp_records<G, D, NW>(smem, size_t(S) * C::kStageBytes, p, b, kvh, c0, part, nparts);
   }  // valid context length
   }  // item located
   item = next_item(p, ss, ticket);
@@ -770,7 +783,7 @@ cudaError_t launch_decode_variant(const DecodeParams& p, cudaStream_t stream) {
     if (dev >= 0 && dev < 64) attr_done[dev] = true;
   }
   const int64_t grid =
-      p.persistent ? int64_t(p.grid) : int64_t(p.max_parts) * p.num_seqs * p.kv_heads;
+      p.persistent ? int64_t(p.grid) : int64_t(p.max_parts) * p.num_seqs * p.kv_heads * p.chunks;
   if (grid <= 0) return cudaSuccess;
   if (grid > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
   return launch_pdl(kern, dim3(static_cast<unsigned>(grid)), dim3(C::kThreads),

@@ -215,7 +215,8 @@ __global__ void __launch_bounds__(NW * 32)
 
   // ---- q as the B operand of S = K q^T: in n-tile nt, lane (gi, gj) holds column
   //      8nt + gi, k pairs 2gj, 2gj+8.
-  const int ncols = p.group * p.num_queries;
+  const int c0 = it.chunk * NC;  // first query column of this item's chunk
+  const int ncols = chunk_cols(p, c0, NC);
   const auto* qall = static_cast<const __nv_bfloat16*>(p.q);
   uint32_t qf[C::kKSteps][NT][2];
   float logit_factor = p.scale_log2;
@@ -227,7 +228,7 @@ __global__ void __launch_bounds__(NW * 32)
     for (int nt = 0; nt < NT; ++nt) {
       const int c = 8 * nt + gi;
       const bool act = c < ncols;
-      const __nv_bfloat16* qb = qall + col_row(p, b, kvh, c) * D;  // read only when active
+      const __nv_bfloat16* qb = qall + col_row(p, b, kvh, c0 + c) * D;  // read only when active
 #pragma unroll
       for (int s = 0; s < C::kKSteps; ++s) {
         qf[s][nt][0] = qf[s][nt][1] = 0u;
@@ -248,7 +249,7 @@ __global__ void __launch_bounds__(NW * 32)
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt) {
       const int c = 8 * nt + gi;
-      const __nv_bfloat16* qb = qall + col_row(p, b, kvh, c) * D + 32 * gj;  // read only when active
+      const __nv_bfloat16* qb = qall + col_row(p, b, kvh, c0 + c) * D + 32 * gj;  // read only when active
 #pragma unroll
       for (int s = 0; s < C::kKSteps; ++s) {
         raw[nt][s] = make_uint2(0u, 0u);
@@ -291,8 +292,8 @@ __global__ void __launch_bounds__(NW * 32)
   int cut[NT][2];
 #pragma unroll
   for (int nt = 0; nt < NT; ++nt) {
-    cut[nt][0] = kGen ? col_cut(p, 8 * nt + 2 * gj) : 0;
-    cut[nt][1] = kGen ? col_cut(p, 8 * nt + 2 * gj + 1) : 0;
+    cut[nt][0] = kGen ? col_cut(p, c0 + 8 * nt + 2 * gj) : 0;
+    cut[nt][1] = kGen ? col_cut(p, c0 + 8 * nt + 2 * gj + 1) : 0;
   }
 
   // ldmatrix row assignment: lane gives the row address of matrix lane / 8.
@@ -715,7 +716,7 @@ __global__ void __launch_bounds__(NW * 32)
     }
   }
   __syncthreads();
-  merge_warp_records<NC, D, NW>(smem, size_t(S) * C::kStageBytes, p, b, kvh, part, nparts);
+  merge_warp_records<NC, D, NW>(smem, size_t(S) * C::kStageBytes, p, b, kvh, c0, part, nparts);
   }  // valid context length
   }  // item located
   item = next_item(p, ss, ticket);
@@ -738,7 +739,7 @@ cudaError_t launch_mma_variant(const DecodeParams& p, const CUtensorMap& tk, con
     if (dev >= 0 && dev < 64) attr_done[dev] = true;
   }
   const int64_t grid =
-      p.persistent ? int64_t(p.grid) : int64_t(p.max_parts) * p.num_seqs * p.kv_heads;
+      p.persistent ? int64_t(p.grid) : int64_t(p.max_parts) * p.num_seqs * p.kv_heads * p.chunks;
   if (grid <= 0) return cudaSuccess;
   if (grid > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
   return launch_pdl(kern, dim3(static_cast<unsigned>(grid)), dim3(C::kThreads),

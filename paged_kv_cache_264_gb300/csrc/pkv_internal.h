@@ -59,6 +59,8 @@ struct DecodeParams {
   int group;                    // query heads per kv head (num_q_heads / kv_heads), 1/2/4/8
   int group_log2;               // log2(group)
   int num_queries;              // k >= 1 query tokens per sequence, the last k positions
+  int chunks;                   // column chunks per kv head: group * k columns are served in
+                                // chunks of the variant's column slots, one work unit each
   int window;                   // each query sees its last `window` tokens (kNoWindow: all)
   int head_dim;
   int max_context_len;

@@ -32,9 +32,7 @@ def draw(seed):
     kv = r.choice(["bf16", "int8", "fp8"])
     group = r.choice([1, 2, 4, 8])
     hkv = r.choice([1, 2, 4])
-    k = r.choice([1, 1, 2, 3, 4, 5, 8])
-    while group * k > 16:
-        k = max(1, k // 2)
+    k = r.choice([1, 1, 2, 3, 4, 5, 8, 16])
     window = r.choice([0, 0, 1, 7, 16, 17, 50, 300])
     kernel = r.choice(["auto", "cuda_core", "tensor_core"])
     pb = r.choice([0, 0, 1, 2, 3, 7])

@@ -70,6 +70,8 @@ VERIFY_SHAPES = [
     ([16, 33, 100], 4, 4, 64, 16),                # MHA: 16 columns, the most queries
     ([7, 20, 90], 8, 4, 128, 5),                  # GQA 2 x 5 = 10 columns (16 slots)
     ([2, 15, 16, 17, 32, 33], 4, 2, 128, 2),      # causal cut on block boundaries
+    ([4, 33, 150], 16, 2, 128, 4),                # GQA 8 x 4 = 32 columns: two chunks
+    ([16, 40, 200], 16, 2, 64, 16),               # GQA 8 x 16 = 128 columns: eight chunks
 ]
 SHAPE_IDS = [f"Hq{s[1]}_Hkv{s[2]}_d{s[3]}_k{s[4]}" for s in VERIFY_SHAPES]
 
@@ -132,10 +134,8 @@ def test_plan_limits():
     assert pkv.decode_plan(pool, 2, 8, 64, num_queries=4)["kernel"] == "tensor_core"    # MHA, 4 columns
     assert pkv.decode_plan(pool, 2, 8, 64, num_queries=1)["kernel"] == "tensor_core"    # MHA decode
     assert pkv.decode_plan(pool, 2, 8, 64, kernel="cuda_core")["kernel"] == "cuda_core"
-    with pytest.raises(pkv.PagedKVError, match="unsupported"):
-        pkv.decode_plan(pool, 2, 64, 64, num_queries=4)                 # 32 columns
-    with pytest.raises(pkv.PagedKVError, match="unsupported"):
-        pkv.decode_plan(pool, 2, 32, 64, num_queries=4, kernel="cuda_core")  # 16 > 8 columns
+    assert pkv.decode_plan(pool, 2, 64, 64, num_queries=4)["kernel"] == "tensor_core"   # 32 columns, 2 chunks
+    assert pkv.decode_plan(pool, 2, 32, 64, num_queries=4, kernel="cuda_core")["kernel"] == "cuda_core"
     for bad_k in (17, -1):
         with pytest.raises(pkv.PagedKVError, match="invalid"):
             pkv.decode_plan(pool, 2, 8, 64, num_queries=bad_k)
@@ -144,8 +144,9 @@ def test_plan_limits():
     pool.close()
     pool = pkv.PagedKVPool(4, 4, 64, "int8", fill=0)                   # no tensor-core INT8 at d=64
     assert pkv.decode_plan(pool, 2, 8, 64, num_queries=4)["kernel"] == "cuda_core"
+    assert pkv.decode_plan(pool, 2, 16, 64, num_queries=4)["kernel"] == "cuda_core"  # 16 columns, 2 chunks
     with pytest.raises(pkv.PagedKVError, match="unsupported"):
-        pkv.decode_plan(pool, 2, 16, 64, num_queries=4)
+        pkv.decode_plan(pool, 2, 16, 64, num_queries=4, kernel="tensor_core")
     pool.close()
 
 
