@@ -164,7 +164,9 @@ __global__ void __launch_bounds__(NW * 32)
   // w, w + NW, ... of the item.
   const int nst = (nb_item + BPS - 1) / BPS;
   const int nw = warp < nst ? (nst - 1 - warp) / NW + 1 : 0;
-  const uint64_t policy = l2_evict_first_policy();
+  // Tiles are read once, unless the kv head's columns are split into chunks: then the
+  // other chunks' CTAs read them again right away, so keep them in L2.
+  const uint64_t policy = p.chunks > 1 ? l2_evict_last_policy() : l2_evict_first_policy();
 
   auto issue = [&](int k) {  // lane 0 only: fetch the warp's k-th stage of the item
     const int s = (kb + k) % S;

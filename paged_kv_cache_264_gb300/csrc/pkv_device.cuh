@@ -117,6 +117,14 @@ __device__ __forceinline__ uint64_t l2_evict_first_policy() {
   return pol;
 }
 
+// L2 policy for data read again soon by another CTA (the K/V tiles of a kv head whose query
+// columns are split into chunks): evict last.
+__device__ __forceinline__ uint64_t l2_evict_last_policy() {
+  uint64_t pol;
+  asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(pol));
+  return pol;
+}
+
 // Bulk copy of `bytes` (multiple of 16) from global to this CTA's shared memory;
 // completion is signalled on `bar` through its transaction count.  Both addresses
 // must be 16-byte aligned.
