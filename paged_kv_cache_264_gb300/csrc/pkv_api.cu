@@ -250,16 +250,21 @@ pkv_status check_decode_shape(const pkv_pool* pool, int num_seqs, int num_q_head
 
 namespace pkv {
 int decode_ctas_per_sm(KvType kv, int head_dim, int cols) {
-  static int cache[3][2][9] = {};  // [dtype][head_dim 64/128][column slots]
+  // [dtype][head_dim 64/128][column slots]; 0 = not yet queried.  Threads may fill an entry
+  // concurrently; they store the same value.
+  static std::atomic<int> cache[3][2][9];
   const int di = head_dim == 128 ? 1 : 0;
   const int ki = static_cast<int>(kv);
   if (cols < 1 || cols > 8) return 0;
-  int& slot = cache[ki][di][cols];
-  if (slot == 0)
-    slot = kv == KvType::kInt8  ? ctas_per_sm_int8(head_dim, cols)
-           : kv == KvType::kFp8 ? ctas_per_sm_fp8(head_dim, cols)
-                                : ctas_per_sm_bf16(head_dim, cols);
-  return slot;
+  std::atomic<int>& slot = cache[ki][di][cols];
+  int n = slot.load(std::memory_order_relaxed);
+  if (n == 0) {
+    n = kv == KvType::kInt8  ? ctas_per_sm_int8(head_dim, cols)
+        : kv == KvType::kFp8 ? ctas_per_sm_fp8(head_dim, cols)
+                             : ctas_per_sm_bf16(head_dim, cols);
+    slot.store(n, std::memory_order_relaxed);
+  }
+  return n;
 }
 
 }  // namespace pkv

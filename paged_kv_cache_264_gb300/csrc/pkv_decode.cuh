@@ -58,6 +58,8 @@
 #include <cuda_bf16.h>
 #include <math.h>
 
+#include <atomic>
+
 #include "pkv_device.cuh"
 
 namespace pkv {
@@ -773,14 +775,14 @@ template <KvType KV, int D, int G, int NW, int S>
 cudaError_t launch_decode_variant(const DecodeParams& p, cudaStream_t stream) {
   using C = DecodeCfg<KV, D, G, NW, S>;
   auto kern = paged_decode_kernel<KV, D, G, NW, S>;
-  static bool attr_done[64] = {};
+  static std::atomic<bool> attr_done[64];  // per device: the shared-memory limit is raised
   int dev = 0;
   cudaGetDevice(&dev);
-  if (dev < 0 || dev >= 64 || !attr_done[dev]) {
+  if (dev < 0 || dev >= 64 || !attr_done[dev].load(std::memory_order_relaxed)) {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(C::smem_bytes(kMaxPartitionBlocks, kMaxSchedSeqs)));
     if (e != cudaSuccess) return e;
-    if (dev >= 0 && dev < 64) attr_done[dev] = true;
+    if (dev >= 0 && dev < 64) attr_done[dev].store(true, std::memory_order_relaxed);
   }
   const int64_t grid =
       p.persistent ? int64_t(p.grid) : int64_t(p.max_parts) * p.num_seqs * p.kv_heads * p.chunks;

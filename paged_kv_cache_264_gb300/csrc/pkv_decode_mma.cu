@@ -1,5 +1,7 @@
 // pkv_decode_mma.cu -- tensor-core decode: which variants exist and which one a call uses.
 // The instantiations live in pkv_decode_mma_{bf16,int8,fp8}.cu (compiled in parallel).
+#include <atomic>
+
 #include "pkv_decode_mma.cuh"
 
 namespace pkv {
@@ -47,14 +49,18 @@ cudaError_t launch_decode_mma(const DecodeParams& p, const CUtensorMap* tk, cons
 
 int mma_ctas_per_sm(KvType kv, int head_dim, int cols, int shape, bool gen) {
   if (!mma_supported(kv, head_dim, cols) || shape < 0 || shape > 3) return 0;
-  static int cache[4][4][17][2] = {};  // [pool type][shape][column slots][gen]
+  // [pool type][shape][column slots][gen]; 0 = not yet queried (or not built).  Threads may
+  // fill an entry concurrently; they store the same value.
+  static std::atomic<int> cache[4][4][17][2];
   const int ti = kv == KvType::kFp8 ? 3 : kv == KvType::kInt8 ? 2 : (head_dim == 128 ? 0 : 1);
-  int& slot = cache[ti][shape][cols][gen ? 1 : 0];
-  if (slot) return slot;
-  slot = kv == KvType::kInt8  ? occupancy_mma_int8(cols, shape, gen)
-         : kv == KvType::kFp8 ? occupancy_mma_fp8(cols, shape, gen)
-                              : occupancy_mma_bf16(head_dim, cols, shape, gen);
-  return slot;
+  std::atomic<int>& slot = cache[ti][shape][cols][gen ? 1 : 0];
+  int n = slot.load(std::memory_order_relaxed);
+  if (n) return n;
+  n = kv == KvType::kInt8  ? occupancy_mma_int8(cols, shape, gen)
+      : kv == KvType::kFp8 ? occupancy_mma_fp8(cols, shape, gen)
+                           : occupancy_mma_bf16(head_dim, cols, shape, gen);
+  slot.store(n, std::memory_order_relaxed);
+  return n;
 }
 
 }  // namespace pkv

@@ -731,14 +731,14 @@ cudaError_t launch_mma_variant(const DecodeParams& p, const CUtensorMap& tk, con
                                cudaStream_t stream) {
   using C = MmaCfg<KV, D, NC, NW, S, BPS>;
   auto kern = paged_decode_mma_kernel<KV, D, NC, NW, S, BPS, kGen>;
-  static bool attr_done[64] = {};
+  static std::atomic<bool> attr_done[64];  // per device: the shared-memory limit is raised
   int dev = 0;
   cudaGetDevice(&dev);
-  if (dev < 0 || dev >= 64 || !attr_done[dev]) {
+  if (dev < 0 || dev >= 64 || !attr_done[dev].load(std::memory_order_relaxed)) {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(C::smem_bytes(kMaxPartitionBlocks, kMaxSchedSeqs)));
     if (e != cudaSuccess) return e;
-    if (dev >= 0 && dev < 64) attr_done[dev] = true;
+    if (dev >= 0 && dev < 64) attr_done[dev].store(true, std::memory_order_relaxed);
   }
   const int64_t grid =
       p.persistent ? int64_t(p.grid) : int64_t(p.max_parts) * p.num_seqs * p.kv_heads * p.chunks;
