@@ -360,6 +360,10 @@ __device__ __forceinline__ int col_cut(const DecodeParams& p, int c) {
 // without a special case; once a real logit arrives exp2(kMaxFloor - m) underflows to 0.
 constexpr float kMaxFloor = -3.402823466e38f;
 
+// Headroom of a lazily updated running max, in log2 units: a kernel may keep its max while
+// new logits stay within kMaxSlack above it, so probabilities reach at most 2^kMaxSlack.
+constexpr float kMaxSlack = 8.0f;
+
 // Query columns in the chunk that starts at column c0 (NC slots; the last chunk may be short).
 __device__ __forceinline__ int chunk_cols(const DecodeParams& p, int c0, int nc) {
   return min(nc, p.group * p.num_queries - c0);

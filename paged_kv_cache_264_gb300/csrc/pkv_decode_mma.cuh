@@ -21,8 +21,9 @@
 //    pairs and transposed with movmatrix, is exactly the B operand of the PV product
 //    O^T[d x 8] += V^T[d x 16] P[16 x 8], whose A operand is V read transposed by ldmatrix.
 //    The row (dims) of O^T that a lane holds and the column of its softmax state
-//    coincide, so rescaling needs no data movement, and it is skipped whenever no
-//    column's running max moved in a block.  For bf16 pools P enters the product as bf16,
+//    coincide, so rescaling needs no data movement.  The running max is lazy: it moves
+//    only when a logit passes it by more than kMaxSlack, so most stages need neither the
+//    cross-lane max nor a rescale.  For bf16 pools P enters the product as bf16,
 //    and the softmax sum adds those same rounded weights.
 //  * INT8: codes become fp16 values 1152 + code exactly (see f16x2_biased) and both
 //    products run in fp16; the constant 1152 is taken out afterwards: from the logits as
@@ -33,7 +34,8 @@
 //    only grows, like the running max, so the rescale stays rare.  FP8 (E4M3) pools take
 //    the same path with the hardware E4M3 -> fp16 conversion and no offset.  Within one
 //    k-step the dims a lane handles are permuted (the same permutation on K and q), which
-//    lets each lane read its codes with 16-byte loads.
+//    lets each lane read its K codes with 16-byte loads; V codes come through ldmatrix.trans
+//    on byte pairs, which puts two tokens' codes of a dim in one register.
 #pragma once
 
 #include <limits.h>
@@ -300,15 +302,14 @@ __global__ void __launch_bounds__(NW * 32)
 
   // ldmatrix row assignment: lane gives the row address of matrix lane / 8.
   const int mi = lane >> 3;
-  const int tok_k = (lane & 7) + (mi & 1) * 8;   // K (A of S): matrices (rows 0-7|8-15) x (k lo|hi)
+  // K (A of S; and quantised V, read transposed): matrices (rows 0-7|8-15) x (chunk lo|hi)
+  const int tok_k = (lane & 7) + (mi & 1) * 8;
   const int ck = mi >> 1;
   const int tok_v = (lane & 7) + (mi >> 1) * 8;  // V^T (A of O^T, transposed load)
   const int cv = mi & 1;
-  // INT8 tiles: this lane's 16-byte chunks in a swizzled tile (rows of 128 bytes).
+  // Quantised K tiles: this lane's 16-byte chunks in a swizzled tile (rows of 128 bytes).
   const int koff[4] = {gi * 128 + (((2 * gj) ^ gi) << 4), gi * 128 + (((2 * gj + 1) ^ gi) << 4),
                        (gi + 8) * 128 + (((2 * gj) ^ gi) << 4), (gi + 8) * 128 + (((2 * gj + 1) ^ gi) << 4)};
-  const int voff[4] = {(2 * gj) * 128 + ((gi ^ (2 * gj)) << 4), (2 * gj + 1) * 128 + ((gi ^ (2 * gj + 1)) << 4),
-                       (2 * gj + 8) * 128 + ((gi ^ (2 * gj)) << 4), (2 * gj + 9) * 128 + ((gi ^ (2 * gj + 1)) << 4)};
 
   float o[C::kMTiles][NT][4];
 #pragma unroll
@@ -325,6 +326,8 @@ __global__ void __launch_bounds__(NW * 32)
     ptot[nt][0] = ptot[nt][1] = 0.0f;
   }
   int e_run = INT_MIN;  // quantised pools: O^T is kept in units of 2^e_run
+  float pe = 1.0f;       // 2^-e_run
+  float pe_next = 0.0f;  // 2^(e_run + 1): a V scale at or above it moves e_run
 
   int failed_at = -1;
   for (int k = 0; k < nw; ++k) {
@@ -452,23 +455,36 @@ __global__ void __launch_bounds__(NW * 32)
         }
       }
 
-      // ---- online softmax for this lane's columns over the stage's tokens
-#pragma unroll
-      for (int ofs = 4; ofs < 32; ofs <<= 1)
-#pragma unroll
-        for (int nt = 0; nt < NT; ++nt) {
-          bm[nt][0] = fmaxf(bm[nt][0], __shfl_xor_sync(kFull, bm[nt][0], ofs));
-          bm[nt][1] = fmaxf(bm[nt][1], __shfl_xor_sync(kFull, bm[nt][1], ofs));
-        }
-      float r[NT][2], mu[NT][2];  // rescale factors; new running max (finite, see kMaxFloor)
+      // ---- online softmax for this lane's columns over the stage's tokens.  The running
+      //      max moves only when a logit passes it by more than kMaxSlack (log2 units):
+      //      until then the probabilities are taken against the old max and may reach
+      //      2^kMaxSlack, which fp32 sums and the 16-bit P operand hold with their usual
+      //      relative precision.  Most stages thus skip the cross-lane max and the rescale.
+      bool grow = false;
 #pragma unroll
       for (int nt = 0; nt < NT; ++nt)
+        grow |= (bm[nt][0] > m[nt][0] + kMaxSlack) | (bm[nt][1] > m[nt][1] + kMaxSlack);
+      float r[NT][2];  // rescale factors of the running sums
 #pragma unroll
-        for (int c = 0; c < 2; ++c) {
-          mu[nt][c] = fmaxf(m[nt][c], bm[nt][c]);
-          r[nt][c] = fast_exp2(m[nt][c] - mu[nt][c]);
-          m[nt][c] = mu[nt][c];
-        }
+      for (int nt = 0; nt < NT; ++nt) r[nt][0] = r[nt][1] = 1.0f;
+      bool rescale = __any_sync(kFull, grow);
+      if (rescale) {
+#pragma unroll
+        for (int ofs = 4; ofs < 32; ofs <<= 1)
+#pragma unroll
+          for (int nt = 0; nt < NT; ++nt) {
+            bm[nt][0] = fmaxf(bm[nt][0], __shfl_xor_sync(kFull, bm[nt][0], ofs));
+            bm[nt][1] = fmaxf(bm[nt][1], __shfl_xor_sync(kFull, bm[nt][1], ofs));
+          }
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+          for (int c = 0; c < 2; ++c) {
+            const float mu = fmaxf(m[nt][c], bm[nt][c]);  // finite, see kMaxFloor
+            r[nt][c] = fast_exp2(m[nt][c] - mu);
+            m[nt][c] = mu;
+          }
+      }
       float pr[BPS][NT][4];
       float ps[NT][2];
 #pragma unroll
@@ -477,10 +493,10 @@ __global__ void __launch_bounds__(NW * 32)
       for (int j = 0; j < BPS; ++j)
 #pragma unroll
         for (int nt = 0; nt < NT; ++nt) {
-          pr[j][nt][0] = fast_exp2(sc[j][nt][0] - mu[nt][0]);
-          pr[j][nt][1] = fast_exp2(sc[j][nt][1] - mu[nt][1]);
-          pr[j][nt][2] = fast_exp2(sc[j][nt][2] - mu[nt][0]);
-          pr[j][nt][3] = fast_exp2(sc[j][nt][3] - mu[nt][1]);
+          pr[j][nt][0] = fast_exp2(sc[j][nt][0] - m[nt][0]);
+          pr[j][nt][1] = fast_exp2(sc[j][nt][1] - m[nt][1]);
+          pr[j][nt][2] = fast_exp2(sc[j][nt][2] - m[nt][0]);
+          pr[j][nt][3] = fast_exp2(sc[j][nt][3] - m[nt][1]);
         }
 
       uint32_t x01[BPS][NT], x23[BPS][NT];
@@ -526,20 +542,26 @@ __global__ void __launch_bounds__(NW * 32)
           sv[j][1] = unsigned(gi + 8 - tlo[j]) < span ? s1 : 0.0f;
           svm = fmaxf(svm, fmaxf(sv[j][0], sv[j][1]));
         }
+        // The exponent E only grows: it moves when some scale reaches 2^(E+1) (and at the
+        // first stage), and then to the exponent of the largest scale of the stage.
+        if (__any_sync(kFull, e_run == INT_MIN || svm >= pe_next)) {
 #pragma unroll
-        for (int ofs = 4; ofs < 32; ofs <<= 1) svm = fmaxf(svm, __shfl_xor_sync(kFull, svm, ofs));
-        const int eb = int((__float_as_uint(svm) >> 23) & 0xff) - 127;  // floor(log2 svm)
-        const int e_new = min(126, e_run == INT_MIN ? eb : max(e_run, eb));
-        if (e_run != INT_MIN && e_new != e_run) {
-          const float f = pow2i(max(-126, e_run - e_new));
+          for (int ofs = 4; ofs < 32; ofs <<= 1) svm = fmaxf(svm, __shfl_xor_sync(kFull, svm, ofs));
+          const int eb = int((__float_as_uint(svm) >> 23) & 0xff) - 127;  // floor(log2 svm)
+          const int e_new = min(126, e_run == INT_MIN ? eb : max(e_run, eb));
+          if (e_run != INT_MIN && e_new != e_run) {
+            const float f = pow2i(max(-126, e_run - e_new));
 #pragma unroll
-          for (int nt = 0; nt < NT; ++nt) {
-            r[nt][0] *= f;
-            r[nt][1] *= f;
+            for (int nt = 0; nt < NT; ++nt) {
+              r[nt][0] *= f;
+              r[nt][1] *= f;
+            }
+            rescale = true;
           }
+          e_run = e_new;
+          pe = pow2i(-e_new);
+          pe_next = e_new >= 126 ? INFINITY : pow2i(e_new + 1);
         }
-        e_run = e_new;
-        const float pe = pow2i(-e_new);  // P' = p * s_V * 2^-E lies in [0, 2)
         float qp[NT][2];  // this stage's sum of the fp16 P' per column
 #pragma unroll
         for (int nt = 0; nt < NT; ++nt) qp[nt][0] = qp[nt][1] = 0.0f;
@@ -560,15 +582,14 @@ __global__ void __launch_bounds__(NW * 32)
           ptot[nt][1] = fmaf(ptot[nt][1], r[nt][1], qp[nt][1]);
         }
       }
+      if (rescale) {
 #pragma unroll
-      for (int nt = 0; nt < NT; ++nt) {
-        if (__any_sync(kFull, r[nt][0] != 1.0f || r[nt][1] != 1.0f)) {
+        for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
           for (int t = 0; t < C::kMTiles; ++t) {
             o[t][nt][0] *= r[nt][0]; o[t][nt][1] *= r[nt][1];
             o[t][nt][2] *= r[nt][0]; o[t][nt][3] *= r[nt][1];
           }
-        }
       }
 
       // ---- O^T += V_j^T P_j.  P_j as the B operand: in n-tile nt lane (gi, gj) needs
@@ -609,43 +630,43 @@ __global__ void __launch_bounds__(NW * 32)
           // INT8 codes are always finite and masked tokens have a zero weight in P; E4M3 has
           // NaN codes, so an FP8 block's tokens outside [tlo, vt) are zeroed in the fragment
           // as for bf16.
-          // Lane (gi, gj) reads dims 16gi..16gi+15 of tokens 2gj, 2gj+1, 2gj+8, 2gj+9; m-tile
-          // t row gi is dim 16gi+2t and row gi+8 is dim 16gi+2t+1.
-          const uint32_t vts = smem_addr(vtp);
-          const uint4 va = lds_v4(vts + voff[0]);
-          const uint4 vb = lds_v4(vts + voff[1]);
-          const uint4 vc = lds_v4(vts + voff[2]);
-          const uint4 vd = lds_v4(vts + voff[3]);
-          constexpr uint32_t kFlip = C::kFp8 ? 0u : 0x80808080u;
+          // ldmatrix.trans on the tile seen as pairs of bytes: matrix (tokens 0-7 | 8-15) x
+          // 16-byte column 2x + (0 | 1) gives lane (gi, gj) the bytes [t d, t d+1, t' d,
+          // t' d+1] of tokens t = 2gj, t' = 2gj + 1 (+8 in the second matrix) and dims
+          // d = 16t + 2gi, d + 1 of m-tile t: row gi is dim 16t + 2gi, row gi + 8 is
+          // 16t + 2gi + 1.  One byte permutation per fp16 pair then builds the A operand.
+          const uint32_t vtile = smem_addr(vtp);
           const unsigned span8 = unsigned(vt[j] - tlo[j]);
           const uint32_t mlo8 = (unsigned(2 * gj - tlo[j]) < span8 ? 0x0000ffffu : 0u) |
                                 (unsigned(2 * gj + 1 - tlo[j]) < span8 ? 0xffff0000u : 0u);
           const uint32_t mhi8 = (unsigned(2 * gj + 8 - tlo[j]) < span8 ? 0x0000ffffu : 0u) |
                                 (unsigned(2 * gj + 9 - tlo[j]) < span8 ? 0xffff0000u : 0u);
-          const uint32_t wa[4] = {va.x ^ kFlip, va.y ^ kFlip, va.z ^ kFlip, va.w ^ kFlip};
-          const uint32_t wb[4] = {vb.x ^ kFlip, vb.y ^ kFlip, vb.z ^ kFlip, vb.w ^ kFlip};
-          const uint32_t wc[4] = {vc.x ^ kFlip, vc.y ^ kFlip, vc.z ^ kFlip, vc.w ^ kFlip};
-          const uint32_t wd[4] = {vd.x ^ kFlip, vd.y ^ kFlip, vd.z ^ kFlip, vd.w ^ kFlip};
 #pragma unroll
-          for (int t = 0; t < C::kMTiles; ++t) {
-            const uint32_t sel = (t & 1) ? 0x7362u : 0x5140u;  // interleave the two tokens' bytes
-            const uint32_t ab = __byte_perm(wa[t >> 1], wb[t >> 1], sel);
-            const uint32_t cd = __byte_perm(wc[t >> 1], wd[t >> 1], sel);
-            uint32_t a[4];
-            if constexpr (C::kFp8) {
-              f16x2x2_from_e4m3x4(ab, a[0], a[1]);
-              f16x2x2_from_e4m3x4(cd, a[2], a[3]);
-              if (vt[j] < kBlockSize || tlo[j] > 0) {
-                a[0] &= mlo8; a[1] &= mlo8; a[2] &= mhi8; a[3] &= mhi8;
+          for (int x = 0; x < C::kMTiles / 2; ++x) {
+            uint32_t w[4];
+            ldmatrix_x4_trans(w, swz(vtile, tok_k, 2 * x + ck));
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+              const int t = 2 * x + h;
+              uint32_t lo = w[2 * h], hi = w[2 * h + 1];  // tokens 2gj, 2gj+1 | 2gj+8, 2gj+9
+              uint32_t a[4];
+              if constexpr (C::kFp8) {
+                f16x2x2_from_e4m3x4(__byte_perm(lo, 0u, 0x3120u), a[0], a[1]);
+                f16x2x2_from_e4m3x4(__byte_perm(hi, 0u, 0x3120u), a[2], a[3]);
+                if (vt[j] < kBlockSize || tlo[j] > 0) {
+                  a[0] &= mlo8; a[1] &= mlo8; a[2] &= mhi8; a[3] &= mhi8;
+                }
+              } else {
+                lo ^= 0x80808080u;
+                hi ^= 0x80808080u;
+                a[0] = f16x2_biased(lo, 0x4240u);
+                a[1] = f16x2_biased(lo, 0x4341u);
+                a[2] = f16x2_biased(hi, 0x4240u);
+                a[3] = f16x2_biased(hi, 0x4341u);
               }
-            } else {
-              a[0] = f16x2_biased(ab, 0x4140u);
-              a[1] = f16x2_biased(ab, 0x4342u);
-              a[2] = f16x2_biased(cd, 0x4140u);
-              a[3] = f16x2_biased(cd, 0x4342u);
-            }
 #pragma unroll
-            for (int nt = 0; nt < NT; ++nt) mma_f16_16816(o[t][nt], a, pb0[nt], pb1[nt]);
+              for (int nt = 0; nt < NT; ++nt) mma_f16_16816(o[t][nt], a, pb0[nt], pb1[nt]);
+            }
           }
         }
       }
@@ -705,7 +726,7 @@ __global__ void __launch_bounds__(NW * 32)
     }
 #pragma unroll
     for (int t = 0; t < C::kMTiles; ++t) {
-      const int d0 = C::kQuant ? 16 * gi + 2 * t : 16 * t + gi;
+      const int d0 = C::kQuant ? 16 * t + 2 * gi : 16 * t + gi;
       const int d1 = C::kQuant ? d0 + 1 : d0 + 8;
       if (h0 < NC) {
         rec[h0 * (D + 2) + 2 + d0] = o[t][nt][0] * oscale;
