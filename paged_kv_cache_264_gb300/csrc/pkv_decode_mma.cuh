@@ -32,10 +32,12 @@
 //    K scale multiplies the fp32 logits, and the V scale is folded into P together with a
 //    power-of-two block exponent that keeps P in [0, 2): O^T is kept in units of 2^E and E
 //    only grows, like the running max, so the rescale stays rare.  FP8 (E4M3) pools take
-//    the same path with the hardware E4M3 -> fp16 conversion and no offset.  Within one
-//    k-step the dims a lane handles are permuted (the same permutation on K and q), which
-//    lets each lane read its K codes with 16-byte loads; V codes come through ldmatrix.trans
-//    on byte pairs, which puts two tokens' codes of a dim in one register.
+//    the same path with the hardware E4M3 -> fp16 conversion and no offset.  Codes come
+//    through ldmatrix on the tile seen as byte pairs: plain for K (four dims of a token per
+//    register, the dims of a k-step permuted alike in K and q) and transposed for V (two
+//    tokens' codes of two dims per register).
+//  * Without the general masks the block loop is unrolled over the S ring stages, so that
+//    a stage's shared-memory addresses are per-lane registers plus immediates.
 #pragma once
 
 #include <limits.h>
@@ -102,10 +104,27 @@ int occupancy_mma_bf16(int head_dim, int cols, int shape, bool gen);
 int occupancy_mma_int8(int cols, int shape, bool gen);
 int occupancy_mma_fp8(int cols, int shape, bool gen);
 
-// Shared-memory address of 16-byte chunk `c` of token row `t` in a tile whose 128-byte
-// boxes were written with the 128-byte swizzle (chunk index xor row index mod 8).
-__device__ __forceinline__ uint32_t swz(uint32_t tile, int t, int c) {
-  return tile + (c >> 3) * 2048 + t * 128 + (((c & 7) ^ (t & 7)) << 4);
+// Byte offset of 16-byte chunk `c` of token row `t` in a tile whose 128-byte boxes were
+// written with the 128-byte swizzle (chunk index xor row index mod 8).
+__device__ __forceinline__ int swz_off(int t, int c) {
+  return (c >> 3) * 2048 + t * 128 + (((c & 7) ^ (t & 7)) << 4);
+}
+
+// A ring stage known at compile time (the stage of an unrolled loop body), a loop over
+// 0..N-1 of them, and a stage known only at run time.
+template <int N>
+struct IntC {
+  static constexpr int value = N;
+};
+struct StageRt {
+  int value;
+};
+template <int N, int I = 0, typename F>
+__device__ __forceinline__ void static_for(F&& f) {
+  if constexpr (I < N) {
+    f(IntC<I>{});
+    static_for<N, I + 1>(f);
+  }
 }
 
 // kGen: the general masks (causal cuts of several query tokens, a sliding window).  Without
@@ -145,7 +164,28 @@ __global__ void __launch_bounds__(NW * 32)
     prefetch_tensor_map(&tmap_v);
   }
   const int P = p.partition_blocks;
-  uint32_t kb = 0;  // blocks this warp has consumed over all its items: stage and phase counter
+  // Blocks this warp has consumed over all its items: stage and phase counter.  Without
+  // the general masks it is a multiple of S whenever an item starts, so that the stage of
+  // each unrolled step of the block loop is a compile-time constant and every
+  // shared-memory address below is a per-lane register plus an immediate.
+  uint32_t kb = 0;
+
+  // ldmatrix row assignment: lane gives the row address of matrix lane / 8.
+  const int mi = lane >> 3;
+  // K (A of S) and quantised V: matrices (token rows 0-7 | 8-15) x (16-byte chunk lo | hi).
+  const int tok_k = (lane & 7) + (mi & 1) * 8;
+  const int ck = mi >> 1;
+  // bf16 V^T (A of O^T, transposed load): matrices (chunk lo | hi) x (token rows 0-7 | 8-15).
+  const int tok_v = (lane & 7) + (mi >> 1) * 8;
+  const int cv = mi & 1;
+  // Row addresses in stage 0 of the ring for the 16-byte chunk pair m of a 128-byte box
+  // row (chunks 2m, 2m+1 before the swizzle): the 128-byte swizzle puts chunk c of row t at
+  // c ^ (t & 7).  A stage, a tile and a later box add constants.
+  const uint32_t ring_a = smem_addr(ring);
+  uint32_t kaddr[4];
+#pragma unroll
+  for (int m2 = 0; m2 < 4; ++m2) kaddr[m2] = ring_a + tok_k * 128 + ((((2 * m2) | ck) ^ (tok_k & 7)) << 4);
+  const uint32_t scl_a = smem_addr(scl) + gi * 4;  // this lane's token row gi in the scales
 
   for (int item = first_item<C::kThreads>(p, ss); item >= 0;) {
   const int ticket = prefetch_ticket(p);
@@ -170,9 +210,9 @@ __global__ void __launch_bounds__(NW * 32)
   // other chunks' CTAs read them again right away, so keep them in L2.
   const uint64_t policy = p.chunks > 1 ? l2_evict_last_policy() : l2_evict_first_policy();
 
-  auto issue = [&](int k) {  // lane 0 only: fetch the warp's k-th stage of the item
-    const int s = (kb + k) % S;
-    unsigned char* st = ring + size_t(s) * C::kStageBytes;
+  auto issue = [&](auto s_c, int k) {  // lane 0 only: fetch the warp's k-th stage of the item
+    const int s = s_c.value;  // (kb + k) % S
+    unsigned char* st = ring + s * C::kStageBytes;
     float* sc = scl + s * (C::kScaleStage / 4);
     const int ib0 = (warp + k * NW) * BPS;
     int tiles[BPS];
@@ -214,7 +254,14 @@ __global__ void __launch_bounds__(NW * 32)
     }
   };
   if (lane == 0) {
-    for (int k = 0; k < S && k < nw; ++k) issue(k);
+    if constexpr (kGen) {
+      for (int k = 0; k < S && k < nw; ++k) issue(StageRt{int((kb + k) % S)}, k);
+    } else {
+      static_for<S>([&](auto s_c) {  // kb is a multiple of S: stage k for the k-th
+        constexpr int k = decltype(s_c)::value;
+        if (k < nw) issue(s_c, k);
+      });
+    }
   }
 
   // ---- q as the B operand of S = K q^T: in n-tile nt, lane (gi, gj) holds column
@@ -244,20 +291,19 @@ __global__ void __launch_bounds__(NW * 32)
     }
   } else {
     // fp16 operands: bring q into fp16 range with a power of two (exact for bf16 values);
-    // its inverse goes into the logit factor.  Lane (gi, gj) loads dims 32gj .. 32gj+31 of
-    // column 8nt + gi (k-step s takes dims 32gj+4s .. +3, the permutation used for K
-    // below), so the warp holds every active column once and reduces max |q| from
-    // registers.
+    // its inverse goes into the logit factor.  Lane (gi, gj) loads dims 16s + 4gj .. +3 of
+    // column 8nt + gi for k-step s (the permutation used for K below), so the warp holds
+    // every active column once and reduces max |q| from registers.
     uint2 raw[NT][C::kKSteps];
     float amax = 0.0f;
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt) {
       const int c = 8 * nt + gi;
-      const __nv_bfloat16* qb = qall + col_row(p, b, kvh, c0 + c) * D + 32 * gj;  // read only when active
+      const __nv_bfloat16* qb = qall + col_row(p, b, kvh, c0 + c) * D + 4 * gj;  // read only when active
 #pragma unroll
       for (int s = 0; s < C::kKSteps; ++s) {
         raw[nt][s] = make_uint2(0u, 0u);
-        if (c < ncols) raw[nt][s] = __ldg(reinterpret_cast<const uint2*>(qb + 4 * s));
+        if (c < ncols) raw[nt][s] = __ldg(reinterpret_cast<const uint2*>(qb + 16 * s));
         amax = fmaxf(amax, fmaxf(fmaxf(fabsf(bf16lo(raw[nt][s].x)), fabsf(bf16hi(raw[nt][s].x))),
                                  fmaxf(fabsf(bf16lo(raw[nt][s].y)), fabsf(bf16hi(raw[nt][s].y)))));
       }
@@ -300,17 +346,6 @@ __global__ void __launch_bounds__(NW * 32)
     cut[nt][1] = kGen ? col_cut(p, c0 + 8 * nt + 2 * gj + 1) : 0;
   }
 
-  // ldmatrix row assignment: lane gives the row address of matrix lane / 8.
-  const int mi = lane >> 3;
-  // K (A of S; and quantised V, read transposed): matrices (rows 0-7|8-15) x (chunk lo|hi)
-  const int tok_k = (lane & 7) + (mi & 1) * 8;
-  const int ck = mi >> 1;
-  const int tok_v = (lane & 7) + (mi >> 1) * 8;  // V^T (A of O^T, transposed load)
-  const int cv = mi & 1;
-  // Quantised K tiles: this lane's 16-byte chunks in a swizzled tile (rows of 128 bytes).
-  const int koff[4] = {gi * 128 + (((2 * gj) ^ gi) << 4), gi * 128 + (((2 * gj + 1) ^ gi) << 4),
-                       (gi + 8) * 128 + (((2 * gj) ^ gi) << 4), (gi + 8) * 128 + (((2 * gj + 1) ^ gi) << 4)};
-
   float o[C::kMTiles][NT][4];
 #pragma unroll
   for (int t = 0; t < C::kMTiles; ++t)
@@ -330,17 +365,19 @@ __global__ void __launch_bounds__(NW * 32)
   float pe_next = 0.0f;  // 2^(e_run + 1): a V scale at or above it moves e_run
 
   int failed_at = -1;
-  for (int k = 0; k < nw; ++k) {
-    const int s = (kb + k) % S;
-    const bool ok = __all_sync(kFull, mbar_wait_bounded(bars + s, ((kb + k) / S) & 1));
+  // One block-loop step: the warp's k-th stage of the item, in ring stage s = k % S, whose
+  // barrier phase has parity ph.
+  auto step = [&](auto s_c, int k, uint32_t ph) {
+    const int s = s_c.value;
+    const int kSt = s * C::kStageBytes;  // byte offset of the stage in the ring
+    const int kScl = s * C::kScaleStage;  // byte offset of its scales
+    const bool ok = __all_sync(kFull, mbar_wait_bounded(bars + s, ph));
     if (!ok) {
       failed_at = k;
       if (lane == 0) set_error(p.err, kErrTimeout);
-      break;
+      return;
     }
     const int ib0 = (warp + k * NW) * BPS;
-    const unsigned char* st = ring + size_t(s) * C::kStageBytes;
-    const float* sc_st = scl + s * (C::kScaleStage / 4);
     int vt[BPS];   // tokens of block j inside the context (0: absent block)
     int rem[BPS];  // context tokens from block j's first token on (0: absent block)
     int tlo[BPS];  // tokens of block j before every query's window (0 without kGen)
@@ -369,47 +406,48 @@ __global__ void __launch_bounds__(NW * 32)
 #pragma unroll
         for (int nt = 0; nt < NT; ++nt) sacc[j][nt][0] = sacc[j][nt][1] = sacc[j][nt][2] = sacc[j][nt][3] = 0.0f;
         if (vt[j] == 0) continue;
-        const unsigned char* kt = st + j * C::kTileBytes;
+        const int kKt = kSt + j * C::kTileBytes;  // K tile j
         // Two accumulators (even and odd k-steps) halve the dependent MMA chain.
         float acc2[NT][4];
 #pragma unroll
         for (int nt = 0; nt < NT; ++nt) acc2[nt][0] = acc2[nt][1] = acc2[nt][2] = acc2[nt][3] = 0.0f;
         if constexpr (!C::kQuant) {
-          const uint32_t ktile = smem_addr(kt);
 #pragma unroll
           for (int s2 = 0; s2 < C::kKSteps; ++s2) {
             uint32_t a[4];
-            ldmatrix_x4(a, swz(ktile, tok_k, 2 * s2 + ck));
+            ldmatrix_x4(a, kaddr[s2 & 3] + (kKt + (s2 >> 2) * 2048));
 #pragma unroll
             for (int nt = 0; nt < NT; ++nt)
               mma_bf16_16816((s2 & 1) ? acc2[nt] : sacc[j][nt], a, qf[s2][nt][0], qf[s2][nt][1]);
           }
         } else {
-          // Lane (gi, gj) reads dims 32gj..32gj+31 of tokens gi and gi+8; k-step s2 pairs
-          // dims 32gj+4s2+{0,1} with k slots 2gj, 2gj+1 and +{2,3} with 2gj+8, 2gj+9.
-          const uint32_t kts = smem_addr(kt);
-          const uint4 x0 = lds_v4(kts + koff[0]);
-          const uint4 x1 = lds_v4(kts + koff[1]);
-          const uint4 y0 = lds_v4(kts + koff[2]);
-          const uint4 y1 = lds_v4(kts + koff[3]);
-          const uint32_t wa[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
-          const uint32_t wb[8] = {y0.x, y0.y, y0.z, y0.w, y1.x, y1.y, y1.z, y1.w};
+          // ldmatrix on the tile seen as pairs of bytes: matrix (tokens 0-7 | 8-15) x
+          // 16-byte chunk 2x + (0 | 1) gives lane (gi, gj) the codes of dims 16c + 4gj .. +3
+          // (chunk c = 2x + h) of token gi (register 2h) and gi + 8 (register 2h + 1).
+          // K-step c pairs dims 16c + 4gj + {0,1} with k slots 2gj, 2gj+1 and + {2,3} with
+          // 2gj+8, 2gj+9.
 #pragma unroll
-          for (int s2 = 0; s2 < 8; ++s2) {
-            uint32_t a[4];
-            if constexpr (C::kFp8) {
-              f16x2x2_from_e4m3x4(wa[s2], a[0], a[2]);
-              f16x2x2_from_e4m3x4(wb[s2], a[1], a[3]);
-            } else {
-              const uint32_t ua = wa[s2] ^ 0x80808080u, ub = wb[s2] ^ 0x80808080u;
-              a[0] = f16x2_biased(ua, 0x4140u);
-              a[1] = f16x2_biased(ub, 0x4140u);
-              a[2] = f16x2_biased(ua, 0x4342u);
-              a[3] = f16x2_biased(ub, 0x4342u);
+          for (int x = 0; x < C::kKSteps / 2; ++x) {
+            uint32_t w[4];
+            ldmatrix_x4(w, kaddr[x] + kKt);
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+              const int s2 = 2 * x + h;
+              uint32_t a[4];
+              if constexpr (C::kFp8) {
+                f16x2x2_from_e4m3x4(w[2 * h], a[0], a[2]);
+                f16x2x2_from_e4m3x4(w[2 * h + 1], a[1], a[3]);
+              } else {
+                const uint32_t ua = w[2 * h] ^ 0x80808080u, ub = w[2 * h + 1] ^ 0x80808080u;
+                a[0] = f16x2_biased(ua, 0x4140u);
+                a[1] = f16x2_biased(ub, 0x4140u);
+                a[2] = f16x2_biased(ua, 0x4342u);
+                a[3] = f16x2_biased(ub, 0x4342u);
+              }
+#pragma unroll
+              for (int nt = 0; nt < NT; ++nt)
+                mma_f16_16816(h ? acc2[nt] : sacc[j][nt], a, qf[s2][nt][0], qf[s2][nt][1]);
             }
-#pragma unroll
-            for (int nt = 0; nt < NT; ++nt)
-              mma_f16_16816((s2 & 1) ? acc2[nt] : sacc[j][nt], a, qf[s2][nt][0], qf[s2][nt][1]);
           }
         }
 #pragma unroll
@@ -429,8 +467,8 @@ __global__ void __launch_bounds__(NW * 32)
         float f0 = logit_factor, f1 = logit_factor;
         if constexpr (C::kQuant) {
           if (vt[j] > 0) {
-            f0 *= lds_f32(smem_addr(sc_st + j * kBlockSize + gi));
-            f1 *= lds_f32(smem_addr(sc_st + j * kBlockSize + gi + 8));
+            f0 *= lds_f32(scl_a + (kScl + j * kBlockSize * 4));
+            f1 *= lds_f32(scl_a + (kScl + j * kBlockSize * 4 + 32));
           }
         }
 #pragma unroll
@@ -536,8 +574,8 @@ __global__ void __launch_bounds__(NW * 32)
         for (int j = 0; j < BPS; ++j) {
           // scales of tokens outside [tlo, vt) may be anything: their weight is 0 anyway
           const unsigned span = unsigned(vt[j] - tlo[j]);
-          const float s0 = lds_f32(smem_addr(sc_st + (BPS + j) * kBlockSize + gi));
-          const float s1 = lds_f32(smem_addr(sc_st + (BPS + j) * kBlockSize + gi + 8));
+          const float s0 = lds_f32(scl_a + (kScl + (BPS + j) * kBlockSize * 4));
+          const float s1 = lds_f32(scl_a + (kScl + (BPS + j) * kBlockSize * 4 + 32));
           sv[j][0] = unsigned(gi - tlo[j]) < span ? s0 : 0.0f;
           sv[j][1] = unsigned(gi + 8 - tlo[j]) < span ? s1 : 0.0f;
           svm = fmaxf(svm, fmaxf(sv[j][0], sv[j][1]));
@@ -603,7 +641,7 @@ __global__ void __launch_bounds__(NW * 32)
           pb0[nt] = movmatrix_trans(x01[j][nt]);
           pb1[nt] = movmatrix_trans(x23[j][nt]);
         }
-        const unsigned char* vtp = st + (BPS + j) * C::kTileBytes;
+        const int kVt = kSt + (BPS + j) * C::kTileBytes;  // V tile j
         if constexpr (!C::kQuant) {
           // Slots past the context in the last block, and before every query's window in
           // the first, may hold anything, NaN included, and 0 * NaN would poison the sum:
@@ -615,11 +653,10 @@ __global__ void __launch_bounds__(NW * 32)
                                (unsigned(2 * gj + 1 - tlo[j]) < span ? 0xffff0000u : 0u);
           const uint32_t mhi = (unsigned(2 * gj + 8 - tlo[j]) < span ? 0x0000ffffu : 0u) |
                                (unsigned(2 * gj + 9 - tlo[j]) < span ? 0xffff0000u : 0u);
-          const uint32_t vtile = smem_addr(vtp);
 #pragma unroll
           for (int t = 0; t < C::kMTiles; ++t) {
             uint32_t a[4];
-            ldmatrix_x4_trans(a, swz(vtile, tok_v, 2 * t + cv));
+            ldmatrix_x4_trans(a, ring_a + kVt + swz_off(tok_v, 2 * t + cv));
             if (tail) {
               a[0] &= mlo; a[1] &= mlo; a[2] &= mhi; a[3] &= mhi;
             }
@@ -635,7 +672,6 @@ __global__ void __launch_bounds__(NW * 32)
           // t' d+1] of tokens t = 2gj, t' = 2gj + 1 (+8 in the second matrix) and dims
           // d = 16t + 2gi, d + 1 of m-tile t: row gi is dim 16t + 2gi, row gi + 8 is
           // 16t + 2gi + 1.  One byte permutation per fp16 pair then builds the A operand.
-          const uint32_t vtile = smem_addr(vtp);
           const unsigned span8 = unsigned(vt[j] - tlo[j]);
           const uint32_t mlo8 = (unsigned(2 * gj - tlo[j]) < span8 ? 0x0000ffffu : 0u) |
                                 (unsigned(2 * gj + 1 - tlo[j]) < span8 ? 0xffff0000u : 0u);
@@ -644,7 +680,7 @@ __global__ void __launch_bounds__(NW * 32)
 #pragma unroll
           for (int x = 0; x < C::kMTiles / 2; ++x) {
             uint32_t w[4];
-            ldmatrix_x4_trans(w, swz(vtile, tok_k, 2 * x + ck));
+            ldmatrix_x4_trans(w, kaddr[x] + kVt);
 #pragma unroll
             for (int h = 0; h < 2; ++h) {
               const int t = 2 * x + h;
@@ -674,7 +710,21 @@ __global__ void __launch_bounds__(NW * 32)
     __syncwarp();
     if (lane == 0 && k + S < nw) {
       fence_proxy_async_smem();
-      issue(k + S);
+      issue(s_c, k + S);
+    }
+  };
+  if constexpr (kGen) {
+    // The general masks carry more per-block state: a rolled loop is faster here, and kb
+    // need not be a multiple of S.
+    for (int k = 0; k < nw && failed_at < 0; ++k) step(StageRt{int((kb + k) % S)}, k, ((kb + k) / S) & 1u);
+  } else {
+    uint32_t ph = (kb / S) & 1u;  // parity of the current round of S stages
+    for (int k0 = 0; k0 < nw && failed_at < 0; k0 += S) {
+      static_for<S>([&](auto s_c) {
+        constexpr int s = decltype(s_c)::value;
+        if (failed_at < 0 && k0 + s < nw) step(s_c, k0 + s, ph);
+      });
+      ph ^= 1u;
     }
   }
   if (failed_at >= 0) {
@@ -686,6 +736,14 @@ __global__ void __launch_bounds__(NW * 32)
     __syncwarp();
   }
   kb += failed_at >= 0 ? min(nw, failed_at + S) : nw;
+  if (!kGen && failed_at < 0) {
+    // Back to a multiple of S: complete the phases of the stages this item left unused.
+    for (; kb % S != 0; ++kb) {
+      if (lane == 0) mbar_arrive(bars + kb % S);
+      __syncwarp();
+      (void)mbar_wait_bounded(bars + kb % S, (kb / S) & 1);
+    }
+  }
 
   // ---- this warp's state -> merge record [NC][D + 2] in its ring
 #pragma unroll
