@@ -353,12 +353,15 @@ __global__ void __launch_bounds__(NW * 32)
     for (int nt = 0; nt < NT; ++nt) o[t][nt][0] = o[t][nt][1] = o[t][nt][2] = o[t][nt][3] = 0.0f;
   // Softmax state of columns 8nt + 2gj ([nt][0]) and 8nt + 2gj + 1 ([nt][1]).
   float m[NT][2], l[NT][2];
-  float ptot[NT][2];  // INT8: running sum of P' (units of 2^e_run), for the V bias
+  // INT8: running sum of P' per column (units of 2^e_run), for the V bias.  An MMA with an
+  // all-ones A operand forms it from the same fp16 P' as the PV product, in the layout
+  // of an O^T fragment (every row holds its column's sum).
+  float psum[NT][4];
 #pragma unroll
   for (int nt = 0; nt < NT; ++nt) {
     m[nt][0] = m[nt][1] = kMaxFloor;
     l[nt][0] = l[nt][1] = 0.0f;
-    ptot[nt][0] = ptot[nt][1] = 0.0f;
+    psum[nt][0] = psum[nt][1] = psum[nt][2] = psum[nt][3] = 0.0f;
   }
   int e_run = INT_MIN;  // quantised pools: O^T is kept in units of 2^e_run
   float pe = 1.0f;       // 2^-e_run
@@ -473,21 +476,30 @@ __global__ void __launch_bounds__(NW * 32)
         }
 #pragma unroll
         for (int nt = 0; nt < NT; ++nt) {
-          bool v0, v1, v2, v3;  // (token gi | gi + 8) x (column 8nt + 2gj | + 1) visible
-          if constexpr (kGen) {
+          sc[j][nt][0] = (sacc[j][nt][0] - kbias[nt][0]) * f0;
+          sc[j][nt][1] = (sacc[j][nt][1] - kbias[nt][1]) * f0;
+          sc[j][nt][2] = (sacc[j][nt][2] - kbias[nt][0]) * f1;
+          sc[j][nt][3] = (sacc[j][nt][3] - kbias[nt][1]) * f1;
+          if constexpr (kGen) {  // (token gi | gi + 8) x (column 8nt + 2gj | + 1) visible
             const int lim0 = rem[j] - cut[nt][0], lim1 = rem[j] - cut[nt][1];
-            v0 = visible(lim0, gi, p.window);
-            v1 = visible(lim1, gi, p.window);
-            v2 = visible(lim0, gi + 8, p.window);
-            v3 = visible(lim1, gi + 8, p.window);
-          } else {
-            v0 = v1 = gi < vt[j];
-            v2 = v3 = gi + 8 < vt[j];
+            if (!visible(lim0, gi, p.window)) sc[j][nt][0] = -INFINITY;
+            if (!visible(lim1, gi, p.window)) sc[j][nt][1] = -INFINITY;
+            if (!visible(lim0, gi + 8, p.window)) sc[j][nt][2] = -INFINITY;
+            if (!visible(lim1, gi + 8, p.window)) sc[j][nt][3] = -INFINITY;
           }
-          sc[j][nt][0] = v0 ? (sacc[j][nt][0] - kbias[nt][0]) * f0 : -INFINITY;
-          sc[j][nt][1] = v1 ? (sacc[j][nt][1] - kbias[nt][1]) * f0 : -INFINITY;
-          sc[j][nt][2] = v2 ? (sacc[j][nt][2] - kbias[nt][0]) * f1 : -INFINITY;
-          sc[j][nt][3] = v3 ? (sacc[j][nt][3] - kbias[nt][1]) * f1 : -INFINITY;
+        }
+        // Without the general masks only a block that the context ends in (the item's last;
+        // the test is the same for the whole warp) has tokens to mask.
+        if (!kGen && vt[j] < kBlockSize) {
+          const bool h0 = gi >= vt[j], h1 = gi + 8 >= vt[j];
+#pragma unroll
+          for (int nt = 0; nt < NT; ++nt) {
+            if (h0) sc[j][nt][0] = sc[j][nt][1] = -INFINITY;
+            if (h1) sc[j][nt][2] = sc[j][nt][3] = -INFINITY;
+          }
+        }
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) {
           bm[nt][0] = fmaxf(bm[nt][0], fmaxf(sc[j][nt][0], sc[j][nt][2]));
           bm[nt][1] = fmaxf(bm[nt][1], fmaxf(sc[j][nt][1], sc[j][nt][3]));
         }
@@ -573,11 +585,13 @@ __global__ void __launch_bounds__(NW * 32)
 #pragma unroll
         for (int j = 0; j < BPS; ++j) {
           // scales of tokens outside [tlo, vt) may be anything: their weight is 0 anyway
-          const unsigned span = unsigned(vt[j] - tlo[j]);
-          const float s0 = lds_f32(scl_a + (kScl + (BPS + j) * kBlockSize * 4));
-          const float s1 = lds_f32(scl_a + (kScl + (BPS + j) * kBlockSize * 4 + 32));
-          sv[j][0] = unsigned(gi - tlo[j]) < span ? s0 : 0.0f;
-          sv[j][1] = unsigned(gi + 8 - tlo[j]) < span ? s1 : 0.0f;
+          sv[j][0] = lds_f32(scl_a + (kScl + (BPS + j) * kBlockSize * 4));
+          sv[j][1] = lds_f32(scl_a + (kScl + (BPS + j) * kBlockSize * 4 + 32));
+          if (kGen || vt[j] < kBlockSize) {
+            const unsigned span = unsigned(vt[j] - tlo[j]);
+            if (unsigned(gi - tlo[j]) >= span) sv[j][0] = 0.0f;
+            if (unsigned(gi + 8 - tlo[j]) >= span) sv[j][1] = 0.0f;
+          }
           svm = fmaxf(svm, fmaxf(sv[j][0], sv[j][1]));
         }
         // The exponent E only grows: it moves when some scale reaches 2^(E+1) (and at the
@@ -600,34 +614,27 @@ __global__ void __launch_bounds__(NW * 32)
           pe = pow2i(-e_new);
           pe_next = e_new >= 126 ? INFINITY : pow2i(e_new + 1);
         }
-        float qp[NT][2];  // this stage's sum of the fp16 P' per column
 #pragma unroll
-        for (int nt = 0; nt < NT; ++nt) qp[nt][0] = qp[nt][1] = 0.0f;
-#pragma unroll
-        for (int j = 0; j < BPS; ++j)
+        for (int j = 0; j < BPS; ++j) {
+          const float w0 = sv[j][0] * pe, w1 = sv[j][1] * pe;
 #pragma unroll
           for (int nt = 0; nt < NT; ++nt) {
-            x01[j][nt] = pack_f16x2(pr[j][nt][0] * sv[j][0] * pe, pr[j][nt][1] * sv[j][0] * pe);
-            x23[j][nt] = pack_f16x2(pr[j][nt][2] * sv[j][1] * pe, pr[j][nt][3] * sv[j][1] * pe);
-            const float2 a = __half22float2(*reinterpret_cast<const __half2*>(&x01[j][nt]));
-            const float2 c2 = __half22float2(*reinterpret_cast<const __half2*>(&x23[j][nt]));
-            qp[nt][0] += a.x + c2.x;
-            qp[nt][1] += a.y + c2.y;
+            x01[j][nt] = pack_f16x2(pr[j][nt][0] * w0, pr[j][nt][1] * w0);
+            x23[j][nt] = pack_f16x2(pr[j][nt][2] * w1, pr[j][nt][3] * w1);
           }
-#pragma unroll
-        for (int nt = 0; nt < NT; ++nt) {
-          ptot[nt][0] = fmaf(ptot[nt][0], r[nt][0], qp[nt][0]);
-          ptot[nt][1] = fmaf(ptot[nt][1], r[nt][1], qp[nt][1]);
         }
       }
       if (rescale) {
 #pragma unroll
-        for (int nt = 0; nt < NT; ++nt)
+        for (int nt = 0; nt < NT; ++nt) {
 #pragma unroll
           for (int t = 0; t < C::kMTiles; ++t) {
             o[t][nt][0] *= r[nt][0]; o[t][nt][1] *= r[nt][1];
             o[t][nt][2] *= r[nt][0]; o[t][nt][3] *= r[nt][1];
           }
+          psum[nt][0] *= r[nt][0]; psum[nt][1] *= r[nt][1];
+          psum[nt][2] *= r[nt][0]; psum[nt][3] *= r[nt][1];
+        }
       }
 
       // ---- O^T += V_j^T P_j.  P_j as the B operand: in n-tile nt lane (gi, gj) needs
@@ -704,6 +711,11 @@ __global__ void __launch_bounds__(NW * 32)
               for (int nt = 0; nt < NT; ++nt) mma_f16_16816(o[t][nt], a, pb0[nt], pb1[nt]);
             }
           }
+          if constexpr (!C::kFp8) {
+            const uint32_t ones[4] = {0x3C003C00u, 0x3C003C00u, 0x3C003C00u, 0x3C003C00u};  // fp16 1.0
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt) mma_f16_16816(psum[nt], ones, pb0[nt], pb1[nt]);
+          }
         }
       }
     }
@@ -759,19 +771,11 @@ __global__ void __launch_bounds__(NW * 32)
     if constexpr (!C::kFp8) {
       // INT8 V codes entered as 1152 + code: O'^T = O^T + 1152 * sum_t P'_t for every dim.
 #pragma unroll
-      for (int ofs = 4; ofs < 32; ofs <<= 1)
-#pragma unroll
-        for (int nt = 0; nt < NT; ++nt) {
-          ptot[nt][0] += __shfl_xor_sync(kFull, ptot[nt][0], ofs);
-          ptot[nt][1] += __shfl_xor_sync(kFull, ptot[nt][1], ofs);
-        }
-#pragma unroll
       for (int t = 0; t < C::kMTiles; ++t)
 #pragma unroll
-        for (int nt = 0; nt < NT; ++nt) {
-          o[t][nt][0] -= 1152.0f * ptot[nt][0]; o[t][nt][1] -= 1152.0f * ptot[nt][1];
-          o[t][nt][2] -= 1152.0f * ptot[nt][0]; o[t][nt][3] -= 1152.0f * ptot[nt][1];
-        }
+        for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+          for (int i = 0; i < 4; ++i) o[t][nt][i] = fmaf(-1152.0f, psum[nt][i], o[t][nt][i]);
     }
   }
   float* rec = reinterpret_cast<float*>(ring);
