@@ -334,7 +334,7 @@ PKV_API pkv_status pkv_decode_plan(const pkv_pool* pool, int num_seqs, int num_q
  *   max_context_len (host int): an upper bound on every T_b; it sizes the plan and the
  *                          workspace and must be <= max_blocks_per_seq * 16.
  *   scale: softmax scale, usually 1 / sqrt(head_dim).
- *   out          (device): bf16 [num_seqs, num_q_heads, head_dim].
+ *   out          (device): bf16 [num_seqs, num_q_heads, head_dim], 16-byte aligned.
  *   workspace    (device): at least pkv_decode_workspace_bytes(...) bytes, 16-byte
  *                          aligned; may be NULL when that size is 0.  Its contents need no
  *                          initialisation and are overwritten.

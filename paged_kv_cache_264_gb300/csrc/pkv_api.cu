@@ -448,7 +448,8 @@ pkv_status pkv_paged_attention_decode_ex(const pkv_pool* pool, const void* q,
   pkv_status st = check_decode_shape(pool, num_seqs, num_q_heads, max_context_len);
   if (st != PKV_OK) return st;
   if (num_seqs == 0) return PKV_OK;
-  if (!q || !block_tables || !context_lens || !out || !aligned16(q)) return PKV_ERR_INVALID_ARG;
+  if (!q || !block_tables || !context_lens || !out || !aligned16(q) || !aligned16(out))
+    return PKV_ERR_INVALID_ARG;
   if (max_blocks_per_seq < 1) return PKV_ERR_INVALID_ARG;
   if (int64_t(max_context_len) > int64_t(max_blocks_per_seq) * pkv::kBlockSize)
     return PKV_ERR_INVALID_ARG;

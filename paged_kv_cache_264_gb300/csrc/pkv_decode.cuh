@@ -386,41 +386,86 @@ __device__ __forceinline__ void write_bad_len(const DecodeParams& p, const ItemI
 // Merge the NW per-warp states of one work item by log-sum-exp and write the bf16 output
 // (single-partition sequences) or the item's partial (m, l, acc) to the workspace.  Warp w's
 // record is [NC][D + 2] floats (running max in log2 units, sum, accumulator) per query
-// column at smem + w * warp_stride; record column c is query column c0 + c.
+// column at smem + w * warp_stride; record column c is query column c0 + c.  Each thread
+// takes kE consecutive dims of one column, so that the column's weights 2^(m_w - M) are
+// formed once per thread and the reads and writes are vectors (out and the workspace are
+// 16-byte aligned, and kE divides D).
 template <int NC, int D, int NW>
 __device__ __forceinline__ void merge_warp_records(const unsigned char* smem, size_t warp_stride,
                                                    const DecodeParams& p, int b, int kvh, int c0,
                                                    int part, int nparts) {
-  auto* out = static_cast<__nv_bfloat16*>(p.out);
-  const int ncols = chunk_cols(p, c0, NC);
-  for (int i = threadIdx.x; i < NC * D; i += NW * 32) {
-    const int g = i / D;
-    const int d = i - g * D;
-    if (g >= ncols) break;  // columns only grow along i: the rest are inactive too
-    float M = -INFINITY;
+  constexpr int kThreads = NW * 32;
+  constexpr int kE = NC * D > kThreads ? NC * D / kThreads : 1;  // dims per thread
+  constexpr int kTpc = D / kE;                                    // threads per column
+  static_assert(kE * kThreads >= NC * D && D % kE == 0 && (kE == 1 || kE % 2 == 0),
+                "merge layout");
+  const int g = threadIdx.x / kTpc;
+  const int d0 = (threadIdx.x - g * kTpc) * kE;
+  if (g >= chunk_cols(p, c0, NC)) return;  // an inactive column, or a thread past NC * D
+  float mw[NW];
+  float M = -INFINITY;
 #pragma unroll
-    for (int w = 0; w < NW; ++w)
-      M = fmaxf(M, reinterpret_cast<const float*>(smem + size_t(w) * warp_stride)[g * (D + 2)]);
-    float L = 0.0f, A = 0.0f;
-    if (M != -INFINITY) {
+  for (int w = 0; w < NW; ++w) {
+    mw[w] = reinterpret_cast<const float*>(smem + size_t(w) * warp_stride)[g * (D + 2)];
+    M = fmaxf(M, mw[w]);
+  }
+  float L = 0.0f;
+  float acc[kE];
 #pragma unroll
-      for (int w = 0; w < NW; ++w) {
-        const float* r = reinterpret_cast<const float*>(smem + size_t(w) * warp_stride) + g * (D + 2);
-        const float f = exp2f(r[0] - M);
-        L = fmaf(f, r[1], L);
-        A = fmaf(f, r[2 + d], A);
+  for (int e = 0; e < kE; ++e) acc[e] = 0.0f;
+  if (M != -INFINITY) {
+#pragma unroll
+    for (int w = 0; w < NW; ++w) {
+      const float* r = reinterpret_cast<const float*>(smem + size_t(w) * warp_stride) + g * (D + 2);
+      const float f = fast_exp2(mw[w] - M);
+      L = fmaf(f, r[1], L);
+      if constexpr (kE == 1) {
+        acc[0] = fmaf(f, r[2 + d0], acc[0]);
+      } else {
+#pragma unroll
+        for (int e = 0; e < kE; e += 2) {  // record columns start at an even float
+          const float2 v = *reinterpret_cast<const float2*>(r + 2 + d0 + e);
+          acc[e] = fmaf(f, v.x, acc[e]);
+          acc[e + 1] = fmaf(f, v.y, acc[e + 1]);
+        }
       }
     }
-    const size_t row = col_row(p, b, kvh, c0 + g);
-    if (nparts == 1) {
-      out[row * D + d] = __float2bfloat16_rn(L > 0.0f ? A / L : 0.0f);
+  }
+  const size_t row = col_row(p, b, kvh, c0 + g);
+  if (nparts == 1) {
+    auto* out = static_cast<__nv_bfloat16*>(p.out) + row * D + d0;
+    const float inv = L > 0.0f ? 1.0f / L : 0.0f;
+    if constexpr (kE == 1) {
+      out[0] = __float2bfloat16_rn(acc[0] * inv);
     } else {
-      const size_t pi = row * p.max_parts + part;
-      p.ws_acc[pi * D + d] = A;
-      if (d == 0) {
-        p.ws_ml[2 * pi] = M;
-        p.ws_ml[2 * pi + 1] = L;
+      uint32_t packed[kE / 2];
+#pragma unroll
+      for (int e = 0; e < kE; e += 2) packed[e / 2] = pack_bf16x2(acc[e] * inv, acc[e + 1] * inv);
+      if constexpr (kE % 8 == 0) {
+#pragma unroll
+        for (int e = 0; e < kE / 2; e += 4)
+          *reinterpret_cast<uint4*>(out + 2 * e) = make_uint4(packed[e], packed[e + 1], packed[e + 2], packed[e + 3]);
+      } else if constexpr (kE == 4) {
+        *reinterpret_cast<uint2*>(out) = make_uint2(packed[0], packed[1]);
+      } else {
+        *reinterpret_cast<uint32_t*>(out) = packed[0];
       }
+    }
+  } else {
+    const size_t pi = row * p.max_parts + part;
+    float* ws = p.ws_acc + pi * D + d0;
+    if constexpr (kE % 4 == 0) {
+#pragma unroll
+      for (int e = 0; e < kE; e += 4)
+        *reinterpret_cast<float4*>(ws + e) = make_float4(acc[e], acc[e + 1], acc[e + 2], acc[e + 3]);
+    } else if constexpr (kE == 2) {
+      *reinterpret_cast<float2*>(ws) = make_float2(acc[0], acc[1]);
+    } else {
+      ws[0] = acc[0];
+    }
+    if (d0 == 0) {
+      p.ws_ml[2 * pi] = M;
+      p.ws_ml[2 * pi + 1] = L;
     }
   }
 }

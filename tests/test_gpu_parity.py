@@ -438,3 +438,17 @@ def test_tensor_core_ring_shapes(shape, partition_blocks):
     ref, _, _ = oracle_decode(w, kv)
     compare(out, ref, f"ring {shape} P={partition_blocks}")
     pool.close()
+
+
+def test_misaligned_out_rejected():
+    """out must be 16-byte aligned (the merge writes vectors); a view 2 bytes into a buffer
+    is refused before any launch."""
+    w = custom([40, 17], 8, 2, 128, "bf16", seed=3)
+    pool = gpu_pool_from(w, "bf16")
+    buf = torch.empty(w.q.numel() + 8, dtype=torch.bfloat16, device="cuda")
+    out = buf[1:1 + w.q.numel()].view(w.q.shape)
+    with pytest.raises(pkv.PagedKVError):
+        pool.decode(w.q.cuda(), w.block_tables.cuda(), w.context_lens.cuda(), w.scale,
+                    w.max_context_len, out=out)
+    assert pool.device_error() == 0
+    pool.close()
