@@ -130,8 +130,11 @@ __device__ __forceinline__ void static_for(F&& f) {
 // kGen: the general masks (causal cuts of several query tokens, a sliding window).  Without
 // it a column sees every context token, the only mask is the context end, and the kernel
 // carries none of that arithmetic (the INT8 and FP8 paths are instruction-bound).
+// INT8/FP8 tiles of up to 8 columns with one block per stage are held to 128 registers
+// (4 CTAs per SM), the compiler's own choice for most of them, which the 8-column tiles
+// otherwise exceed (168); every other variant keeps the compiler's choice.
 template <KvType KV, int D, int NC, int NW, int S, int BPS, bool kGen>
-__global__ void __launch_bounds__(NW * 32)
+__global__ void __launch_bounds__(NW * 32, (KvTraits<KV>::kQuant && NC <= 8 && BPS == 1) ? 4 : 0)
     paged_decode_mma_kernel(const __grid_constant__ CUtensorMap tmap_k,
                             const __grid_constant__ CUtensorMap tmap_v, const DecodeParams p) {
   using C = MmaCfg<KV, D, NC, NW, S, BPS>;
