@@ -81,16 +81,8 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity
   return false;
 }
 
-// Shared-memory loads by shared-window address (ld.shared rather than a generic load).
-// Volatile, so they stay after the mbarrier wait (also volatile asm) that publishes the data.
-__device__ __forceinline__ uint4 lds_v4(uint32_t addr) {
-  uint4 v;
-  asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
-               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
-               : "r"(addr));
-  return v;
-}
-
+// Shared-memory load by shared-window address (ld.shared rather than a generic load).
+// Volatile, so it stays after the mbarrier wait (also volatile asm) that publishes the data.
 __device__ __forceinline__ float lds_f32(uint32_t addr) {
   float v;
   asm volatile("ld.shared.f32 %0, [%1];" : "=f"(v) : "r"(addr));
