@@ -141,15 +141,18 @@ def gpu_pool_blocks(pool: pkv.PagedKVPool, tables: np.ndarray, lens: np.ndarray)
 def compare(out_gpu: torch.Tensor, ref: np.ndarray, what="", output_rounding=False):
     """Element-wise comparison with the fp64 oracle.
 
-    ``output_rounding`` widens the mean-abs bound by the bf16 rounding of the output
-    itself (bf16 keeps 8 significant bits, so rounding moves x by at most 2^-8 |x|); it is
-    used where the outputs are single O(1) values rather than averages over many tokens."""
+    ``output_rounding`` widens both bounds by the bf16 rounding of the output itself (bf16
+    keeps 8 significant bits, so rounding moves x by at most 2^-8 |x|); it is used where
+    the outputs are single values of V rather than averages over many tokens.  Such a
+    value of magnitude 4 or more is 2^-5 apart from its bf16 neighbours, so even the
+    correctly rounded output can miss the exact one by more than the 1e-2 bound."""
     got = out_gpu.float().cpu().numpy().astype(np.float64)
     assert got.shape == ref.shape, (got.shape, ref.shape)
     assert np.all(np.isfinite(got)), f"{what}: non-finite output"
     err = np.abs(got - ref)
+    slack = 2.0 ** -8 * np.abs(ref) if output_rounding else 0.0
     mean_bound = MEAN_ABS + (2.0 ** -8 * np.abs(ref).mean() if output_rounding else 0.0)
-    assert err.max() <= MAX_ABS, f"{what}: max abs err {err.max():.3e}"
+    assert np.all(err <= MAX_ABS + slack), f"{what}: max abs err {err.max():.3e}"
     assert err.mean() <= mean_bound, f"{what}: mean abs err {err.mean():.3e} > {mean_bound:.3e}"
     return float(err.max()), float(err.mean())
 
