@@ -751,25 +751,44 @@ __global__ void __launch_bounds__(NW * 32)
 template <int D>
 __global__ void __launch_bounds__(128) lse_reduce_kernel(const DecodeParams p) {
   constexpr int kDPV = D / 32;
+  constexpr int kAhead = 4;  // partitions whose accumulators are loaded before T is known
   constexpr uint32_t kFull = 0xffffffffu;
   const int lane = threadIdx.x & 31;
   griddep_wait();  // the partials come from the decode kernel just before
   const int gw = blockIdx.x * (blockDim.x / 32) + (threadIdx.x >> 5);  // row of [B, k, Hq]
   if (gw >= p.num_seqs * p.num_queries * p.num_q_heads) return;
   const int b = gw / (p.num_queries * p.num_q_heads);
+  const float2* ml = reinterpret_cast<const float2*>(p.ws_ml) + size_t(gw) * p.max_parts;
+  const float* src = p.ws_acc + size_t(gw) * p.max_parts * D + lane * kDPV;
+
+  // The length, this lane's (m, l) and the first kAhead partitions' accumulators are all
+  // requested before any of them is used, so the row costs one global-memory round trip
+  // instead of three.  Slots past the row's partition count (the workspace has max_parts
+  // per row) hold stale values; they are loaded but never used.
   const int T = __ldg(p.context_lens + b);
+  float2 mine = make_float2(-INFINITY, 0.0f);
+  if (lane < p.max_parts) mine = ml[lane];
+  float v[kAhead][kDPV];
+#pragma unroll
+  for (int u = 0; u < kAhead; ++u) {
+    if (u < p.max_parts) {
+      if constexpr (kDPV == 4) {
+        const float4 x = *reinterpret_cast<const float4*>(src + size_t(u) * D);
+        v[u][0] = x.x; v[u][1] = x.y; v[u][2] = x.z; v[u][3] = x.w;
+      } else {
+        const float2 x = *reinterpret_cast<const float2*>(src + size_t(u) * D);
+        v[u][0] = x.x; v[u][1] = x.y;
+      }
+    }
+  }
   if (T < p.num_queries || T > p.max_context_len) return;  // the decode kernel wrote zeros
   const int nparts = seq_parts(p, T);
   if (nparts <= 1) return;  // written directly by the decode kernel
-  const float2* ml = reinterpret_cast<const float2*>(p.ws_ml) + size_t(gw) * p.max_parts;
-  const float* acc = p.ws_acc + size_t(gw) * p.max_parts * D;
+  if (lane >= nparts) mine = make_float2(-INFINITY, 0.0f);
 
-  // One pass over (m, l): lane i holds partitions i, i + 32, ...  Weights 2^(m_p - M) of a
-  // lane's first partition stay in a register for the accumulator pass.
-  float M = -INFINITY;
-  float2 mine = make_float2(-INFINITY, 0.0f);
-  if (lane < nparts) mine = ml[lane];
-  M = mine.x;
+  // Lane i holds partitions i, i + 32, ...; the weight 2^(m_p - M) of a lane's first
+  // partition stays in a register for the accumulator pass.
+  float M = mine.x;
   for (int i = lane + 32; i < nparts; i += 32) M = fmaxf(M, ml[i].x);
 #pragma unroll
   for (int o = 16; o >= 1; o >>= 1) M = fmaxf(M, __shfl_xor_sync(kFull, M, o));
@@ -781,32 +800,39 @@ __global__ void __launch_bounds__(128) lse_reduce_kernel(const DecodeParams p) {
     const float f_mine = lane < nparts ? exp2f(mine.x - M) : 0.0f;
     L = f_mine * mine.y;
     for (int i = lane + 32; i < nparts; i += 32) {
-      const float2 v = ml[i];
-      L = fmaf(exp2f(v.x - M), v.y, L);
+      const float2 w = ml[i];
+      L = fmaf(exp2f(w.x - M), w.y, L);
     }
 #pragma unroll
     for (int o = 16; o >= 1; o >>= 1) L += __shfl_xor_sync(kFull, L, o);
-    const float* src = acc + lane * kDPV;
-    int i = 0;
+#pragma unroll
+    for (int u = 0; u < kAhead; ++u) {
+      const float f = __shfl_sync(kFull, f_mine, u);
+      if (u < nparts) {
+#pragma unroll
+        for (int c = 0; c < kDPV; ++c) a[c] = fmaf(f, v[u][c], a[c]);
+      }
+    }
+    int i = kAhead;
     for (; i + 4 <= nparts; i += 4) {  // four partitions' loads in flight
       float f[4];
-      float v[4][kDPV];
+      float w[4][kDPV];
 #pragma unroll
       for (int u = 0; u < 4; ++u) {
         const int pi = i + u;
         f[u] = pi < 32 ? __shfl_sync(kFull, f_mine, pi) : exp2f(ml[pi].x - M);
         if constexpr (kDPV == 4) {
           const float4 x = *reinterpret_cast<const float4*>(src + size_t(pi) * D);
-          v[u][0] = x.x; v[u][1] = x.y; v[u][2] = x.z; v[u][3] = x.w;
+          w[u][0] = x.x; w[u][1] = x.y; w[u][2] = x.z; w[u][3] = x.w;
         } else {
           const float2 x = *reinterpret_cast<const float2*>(src + size_t(pi) * D);
-          v[u][0] = x.x; v[u][1] = x.y;
+          w[u][0] = x.x; w[u][1] = x.y;
         }
       }
 #pragma unroll
       for (int u = 0; u < 4; ++u)
 #pragma unroll
-        for (int c = 0; c < kDPV; ++c) a[c] = fmaf(f[u], v[u][c], a[c]);
+        for (int c = 0; c < kDPV; ++c) a[c] = fmaf(f[u], w[u][c], a[c]);
     }
     for (; i < nparts; ++i) {
       const float f = i < 32 ? __shfl_sync(kFull, f_mine, i) : exp2f(ml[i].x - M);
