@@ -94,3 +94,50 @@ def test_null_pool_rejected(lib):
 
 def test_launch_count_starts_at_zero_without_work(lib):
     assert lib.pkv_launch_count() == 0 or lib.pkv_launch_count() > 0  # a plain counter
+
+
+def test_ctypes_layout_and_constants_match_the_header(tmp_path):
+    """The binding's mirror of the header, checked by the C compiler: the options struct's
+    size and field offsets, and the status, pool-type, kernel, schedule and device-error
+    constants."""
+    import shutil
+    import subprocess
+
+    import paged_kv_cache_264_gb300 as pkv
+
+    cc = shutil.which("gcc") or shutil.which("cc")
+    if cc is None:
+        pytest.skip("no C compiler")
+    fields = [f[0] for f in _lib.DecodeOptions._fields_]
+    consts = ["PKV_OK", "PKV_ERR_INVALID_ARG", "PKV_ERR_UNSUPPORTED", "PKV_ERR_CUDA",
+              "PKV_ERR_WORKSPACE", "PKV_ERR_CAPACITY", "PKV_KV_BF16", "PKV_KV_INT8",
+              "PKV_KV_FP8_E4M3", "PKV_KERNEL_AUTO", "PKV_KERNEL_CUDA_CORE",
+              "PKV_KERNEL_TENSOR_CORE", "PKV_SCHEDULE_AUTO", "PKV_SCHEDULE_GRID",
+              "PKV_SCHEDULE_PERSISTENT", "PKV_DEVERR_BLOCK_ID", "PKV_DEVERR_CONTEXT_LEN",
+              "PKV_DEVERR_SLOT", "PKV_DEVERR_TIMEOUT", "PKV_BLOCK_SIZE"]
+    src = tmp_path / "layout.c"
+    body = ['printf("size %zu\\n", sizeof(pkv_decode_options));']
+    body += [f'printf("{f} %zu\\n", offsetof(pkv_decode_options, {f}));' for f in fields]
+    body += [f'printf("{c} %lld\\n", (long long)({c}));' for c in consts]
+    src.write_text("#include <stdio.h>\n#include <stddef.h>\n#include \"pagedkv.h\"\n"
+                   "int main(void) {\n" + "\n".join(body) + "\nreturn 0;\n}\n")
+    exe = tmp_path / "layout"
+    subprocess.run([cc, "-std=c11", "-I", os.path.join(ROOT, "include"), str(src), "-o", str(exe)],
+                   check=True, capture_output=True)
+    got = dict(line.split() for line in subprocess.run([str(exe)], capture_output=True, text=True,
+                                                      check=True).stdout.splitlines())
+    assert int(got["size"]) == ctypes.sizeof(_lib.DecodeOptions)
+    for f in fields:
+        assert int(got[f]) == getattr(_lib.DecodeOptions, f).offset, f
+    from paged_kv_cache_264_gb300 import api
+    py = {c: getattr(_lib, c) for c in consts[:9]}
+    py.update(PKV_KERNEL_AUTO=api._KERNELS["auto"], PKV_KERNEL_CUDA_CORE=api._KERNELS["cuda_core"],
+              PKV_KERNEL_TENSOR_CORE=api._KERNELS["tensor_core"],
+              PKV_SCHEDULE_AUTO=api._SCHEDULES["auto"], PKV_SCHEDULE_GRID=api._SCHEDULES["grid"],
+              PKV_SCHEDULE_PERSISTENT=api._SCHEDULES["persistent"],
+              PKV_DEVERR_BLOCK_ID=pkv.DEVERR_BLOCK_ID, PKV_DEVERR_CONTEXT_LEN=pkv.DEVERR_CONTEXT_LEN,
+              PKV_DEVERR_SLOT=pkv.DEVERR_SLOT, PKV_DEVERR_TIMEOUT=pkv.DEVERR_TIMEOUT,
+              PKV_BLOCK_SIZE=16)
+    assert set(py) == set(consts)
+    for c in consts:
+        assert int(got[c]) == int(py[c]), c
