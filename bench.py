@@ -2,8 +2,9 @@
 
 A step appends one new token per sequence to the paged KV cache (reshape_and_cache)
 and runs paged_attention_decode over every sequence's full context.  The default
-workload is the LLaMA-2-7B-shaped single layer (64 sequences, context lengths uniform
-in [128, 2048], 32/32 heads, head_dim 128, bf16 KV, shuffled 1.25x block pool).
+workload is the largest single-GPU one, the long-context split-K batch (8 sequences of
+32768 tokens, 32/32 heads, head_dim 128, bf16 KV with one key channel scaled x8,
+shuffled 1.25x block pool: 4.3 GB of K/V read per step); ``--workload`` names the others.
 
 Printed: one JSON line (rank 0).  `value` is KV-read GB/s over the whole step
 (algorithmic bytes: cached K/V actually attended + q + out + tables + the append),
@@ -16,7 +17,9 @@ causally over the cache.  ``long_32k_window4k`` decodes the long_32k cache with 
 sliding window (bytes count the tokens each sequence's window covers).
 
 Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                       [--workload NAME]
+                       [--workload NAME] [--seqs N]
+``--seqs N`` keeps only the first N sequences of the workload (a smaller case of the same
+shape, for profiler captures).
 For N > 1 run under torch.distributed.run: each rank runs its own independent batch of
 the same shape (weak scaling; the only collectives are the timing barrier and the
 max-over-ranks reduction).
@@ -47,7 +50,7 @@ from paged_kv_cache_264_gb300 import roofline, workloads as W  # noqa: E402
 
 METRIC = "paged decode attention: KV-read GB/s (% of HBM peak) and decode steps/s"
 UNIT = "GB/s"
-DEFAULT_WORKLOAD = "llama2_7b"
+DEFAULT_WORKLOAD = "long_32k"
 FALLBACK_HBM_GBS = 6800.0
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "decode_traffic.txt")
 CSRC = os.path.join(ROOT, "paged_kv_cache_264_gb300", "csrc")
@@ -195,6 +198,24 @@ class ClockSampler:
 
 # ------------------------------------------------------------------ our arm
 
+def make_workload(name: str, seqs: int, device):
+    """The named workload, or a batch of its first ``seqs`` sequences' lengths with the
+    same head shape, pool type and value distribution, in a shuffled pool sized 1.25x what
+    those sequences need (a smaller case of the same shape: device memory shrinks with it)."""
+    if not seqs:
+        return W.make(name, device=device)
+    spec = W.SPECS[name]
+    if not 1 <= seqs <= spec.num_seqs:
+        raise SystemExit(f"--seqs must be in 1..{spec.num_seqs}")
+    lens = W.context_lens_of(name)[:seqs]
+    return W.build(name=name, context_lens=lens, num_q_heads=spec.num_q_heads,
+                   num_kv_heads=spec.num_kv_heads, head_dim=spec.head_dim, kv_dtype=spec.kv_dtype,
+                   seed=spec.seed,
+                   outlier_key_channel_frac=spec.outlier_key_channel_frac,
+                   outlier_key_scale=spec.outlier_key_scale, device=device,
+                   num_queries=spec.num_queries)
+
+
 def run_ours(args, rank, world, local):
     import paged_kv_cache_264_gb300 as pkv
     from paged_kv_cache_264_gb300 import build as pkv_build
@@ -205,7 +226,7 @@ def run_ours(args, rank, world, local):
     dev = torch.device("cuda", local if world > 1 else 0)
     torch.cuda.set_device(dev)
     spec = W.SPECS[args.workload]
-    w = W.make(args.workload, device=dev)
+    w = make_workload(args.workload, args.seqs, dev)
     kv = spec.kv_dtype
     stream = torch.cuda.current_stream(dev)
 
@@ -263,7 +284,10 @@ def run_ours(args, rank, world, local):
     clk = clocks.stop()
     ms_total = t0.elapsed_time(t1)
     ms_total = max_over_ranks(ms_total, world, dev)
-    dec_ms = sum(a.elapsed_time(b) for a, b in ev) / args.steps
+    dec_all = sorted(a.elapsed_time(b) for a, b in ev)
+    dec_ms = sum(dec_all) / args.steps
+    dec_median = statistics.median(dec_all)
+    dec_p90 = dec_all[min(len(dec_all) - 1, math.ceil(0.9 * len(dec_all)) - 1)]
     assert pool.device_error() == 0
 
     sb = roofline.step_bytes(w.context_lens, w.num_q_heads, w.num_kv_heads, w.head_dim, kv,
@@ -279,7 +303,7 @@ def run_ours(args, rank, world, local):
 
     peak, peak_kind = measured_peaks()
     achieved = sb.decode / (dec_ms * 1e-3) / 1e9
-    traffic = recorded_traffic(args.workload, plan["kernel"])
+    traffic = None if args.seqs else recorded_traffic(args.workload, plan["kernel"])
     kernel = ("paged_decode_mma_kernel" if plan["kernel"] == "tensor_core" else "paged_decode_kernel") + (
         " + lse_reduce_kernel" if plan["kernels_per_call"] == 2 else "")
     line = {
@@ -290,6 +314,7 @@ def run_ours(args, rank, world, local):
         "data": "synthetic (seeded N(0,1) bf16 values; seeded lengths and shuffled block pool)",
         "config": {
             "workload": args.workload, "description": spec.description,
+            "subset": f"first {args.seqs} of {spec.num_seqs} sequences" if args.seqs else None,
             "num_seqs": w.num_seqs, "num_q_heads": w.num_q_heads, "num_kv_heads": w.num_kv_heads,
             "head_dim": w.head_dim, "kv_dtype": kv, "sum_context_tokens": int(w.context_lens.sum()),
             "max_context_len": max_ctx, "num_blocks": w.num_blocks,
@@ -309,6 +334,9 @@ def run_ours(args, rank, world, local):
             "peak": peak, "peak_kind": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)" if peak_kind == "measured" else "fallback",
             "unit": "GB/s", "frac": round(achieved / peak, 4), "traffic": traffic,
             "algorithmic_bytes_per_launch": sb.decode, "avg_launch_ms": round(dec_ms, 5),
+            "median_launch_ms": round(dec_median, 5), "p90_launch_ms": round(dec_p90, 5),
+            "frac_median": round(sb.decode / (dec_median * 1e-3) / 1e9 / peak, 4),
+            "launches_timed": len(dec_all),
         },
         "e2e": e2e,
         "gpu_launches": int(launches),
@@ -504,6 +532,8 @@ def main(argv=None):
     ap.add_argument("--cpu-seconds", type=float, default=12.0,
                     help="CPU work for the oracle baseline sample")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--seqs", type=int, default=0,
+                    help="keep only the first N sequences (a smaller case for profiler captures)")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
