@@ -48,7 +48,7 @@ extern "C" {
 typedef enum pkv_status {
   PKV_OK = 0,
   PKV_ERR_INVALID_ARG = 1, /* a pointer, size or layout argument is invalid         */
-  PKV_ERR_UNSUPPORTED = 2, /* valid but not built (head_dim, group size, ...)        */
+  PKV_ERR_UNSUPPORTED = 2, /* valid but not built (head_dim, forced kernel, ...)      */
   PKV_ERR_CUDA = 3,        /* a CUDA runtime call or kernel launch failed            */
   PKV_ERR_WORKSPACE = 4,   /* the workspace passed is smaller than the call needs    */
   PKV_ERR_CAPACITY = 5     /* out of free blocks, sequence slots or table capacity   */
@@ -341,9 +341,13 @@ PKV_API pkv_status pkv_decode_plan(const pkv_pool* pool, int num_seqs, int num_q
  * A sequence whose T_b is out of range gets a zero output and sets
  * PKV_DEVERR_CONTEXT_LEN; a block id out of range is skipped and sets
  * PKV_DEVERR_BLOCK_ID.  num_seqs == 0 is a no-op.
- * num_q_heads must be a multiple of kv_heads with a group size of 1, 2, 4 or 8
- * (else PKV_ERR_UNSUPPORTED).  Errors: PKV_ERR_INVALID_ARG, PKV_ERR_UNSUPPORTED,
- * PKV_ERR_WORKSPACE, PKV_ERR_CUDA.
+ * num_q_heads must be a multiple of kv_heads (else PKV_ERR_INVALID_ARG); any group size
+ * G = num_q_heads / kv_heads is served: MHA (G = 1), GQA (1 < G < num_q_heads, powers of
+ * two or not) and MQA (kv_heads = 1, G = num_q_heads) ("LLM/MLLM inference
+ * optimisation", 2.2 and the 2.3 table).  A group that is not a power of two fills the
+ * next power-of-two column tile with its unused slots idle; groups wider than a tile (16
+ * columns on the tensor cores, 8 on the CUDA cores) are served in column chunks.
+ * Errors: PKV_ERR_INVALID_ARG, PKV_ERR_UNSUPPORTED, PKV_ERR_WORKSPACE, PKV_ERR_CUDA.
  */
 PKV_API pkv_status pkv_paged_attention_decode(const pkv_pool* pool, const void* q,
                                       const int32_t* block_tables, int max_blocks_per_seq,
@@ -381,7 +385,7 @@ PKV_API pkv_status pkv_paged_attention_decode_ex(const pkv_pool* pool, const voi
  *  - Every GPU that loads the library holds that array until the process exits.
  *  - The first call on a device looks up the array's device address (with that device
  *    current) and caches it; make that first call before any stream capture.
- *  - Call it with the pool's device current.
+ *  - Call it with the pool's device current (else PKV_ERR_INVALID_ARG, nothing launched).
  *  - All calls on a device share the array, which keeps the last call's contents.
  *    Nothing in it needs to start at zero: each call writes every partial it reads.
  *    Calls whose work overlaps on the GPU (other streams, other host threads) race on
@@ -395,7 +399,11 @@ PKV_API pkv_status pkv_paged_attention_decode_static_scratch(
     const int32_t* context_lens, int num_seqs, int num_q_heads, int max_context_len, float scale,
     void* out, void* stream);
 
-/* Text of the last static-scratch error in this thread (static per thread). */
+/*
+ * Text of the last pkv_paged_attention_decode_static_scratch outcome in this thread
+ * ("no error" after a call that succeeded; static storage per thread).  For
+ * PKV_ERR_CUDA it names the status only; pkv_last_cuda_error() has the CUDA text.
+ */
 PKV_API const char* pkv_static_scratch_error(void);
 
 /*

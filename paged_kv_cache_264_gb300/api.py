@@ -185,6 +185,27 @@ def decode_plan(pool: PagedKVPool, num_seqs: int, num_q_heads: int, max_context_
             "kernel": {1: "cuda_core", 2: "tensor_core"}.get(kf.value, str(kf.value))}
 
 
+def check_decode_shapes(head_dim: int, q_shape, tables_shape, lens_shape, out_shape=None):
+    """Shape agreement of a decode call's tensors, checked on the host before anything is
+    launched: q [B, Hq, d] or [B, k, Hq, d] with d the pool's head_dim, block_tables
+    [B, max_blocks], context_lens [B], out (if given) q's shape.  Returns (B, k, Hq);
+    raises ValueError otherwise."""
+    q_shape = tuple(q_shape)
+    if len(q_shape) == 4:
+        b, nq, hq, d = q_shape
+    elif len(q_shape) == 3:
+        (b, hq, d), nq = q_shape, 1
+    else:
+        raise ValueError(f"q must be [B, Hq, d] or [B, k, Hq, d], got {q_shape}")
+    if d != head_dim:
+        raise ValueError(f"q's head_dim {d} is not the pool's {head_dim}")
+    if len(tables_shape) != 2 or tables_shape[0] != b or tuple(lens_shape) != (b,):
+        raise ValueError("q, block_tables and context_lens disagree in shape")
+    if out_shape is not None and tuple(out_shape) != q_shape:
+        raise ValueError("out must have q's shape")
+    return b, nq, hq
+
+
 def paged_attention_decode(pool: PagedKVPool, q: torch.Tensor, block_tables: torch.Tensor,
                            context_lens: torch.Tensor, scale: float, max_context_len: int,
                            out: torch.Tensor | None = None, workspace: torch.Tensor | None = None,
@@ -201,20 +222,16 @@ def paged_attention_decode(pool: PagedKVPool, q: torch.Tensor, block_tables: tor
     ``workspace`` (a uint8 CUDA tensor) is allocated here when not given and needed."""
     if q.dim() == 4:
         _need(q, torch.bfloat16, "q", 4)
-        b, nq, hq, d = q.shape
     else:
         _need(q, torch.bfloat16, "q", 3)
-        (b, hq, d), nq = q.shape, 1
     _need(block_tables, torch.int32, "block_tables", 2)
     _need(context_lens, torch.int32, "context_lens", 1)
-    if d != pool.head_dim or block_tables.shape[0] != b or context_lens.shape[0] != b:
-        raise ValueError("q, block_tables and context_lens disagree in shape")
+    if out is not None:
+        _need(out, torch.bfloat16, "out", q.dim())
+    b, nq, hq = check_decode_shapes(pool.head_dim, q.shape, block_tables.shape, context_lens.shape,
+                                    None if out is None else out.shape)
     if out is None:
         out = torch.empty_like(q)
-    else:
-        _need(out, torch.bfloat16, "out", q.dim())
-        if out.shape != q.shape:
-            raise ValueError("out must have q's shape")
     need = decode_workspace_bytes(pool, b, hq, max_context_len, partition_blocks, kernel, nq, window) if b else 0
     if need and workspace is None:
         workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
@@ -254,19 +271,20 @@ def paged_attention_decode_static_scratch(pool: PagedKVPool, q: torch.Tensor, bl
     _need(q, torch.bfloat16, "q", 3)
     _need(block_tables, torch.int32, "block_tables", 2)
     _need(context_lens, torch.int32, "context_lens", 1)
+    if out is not None:
+        _need(out, torch.bfloat16, "out", 3)
+    b, _, hq = check_decode_shapes(pool.head_dim, q.shape, block_tables.shape, context_lens.shape,
+                                   None if out is None else out.shape)
     if out is None:
         out = torch.empty_like(q)
-    else:
-        _need(out, torch.bfloat16, "out", 3)
-    b, hq, _ = q.shape
     lib = _lib.load()
-    st = lib.pkv_paged_attention_decode_static_scratch(
-        _handle(pool), _ptr(q), _ptr(block_tables), block_tables.shape[1], _ptr(context_lens), b, hq,
-        int(max_context_len), float(scale), _ptr(out), _stream(stream))
-    if st == _lib.PKV_ERR_WORKSPACE:
+    with torch.cuda.device(q.device):  # the library's scratch address is per device
+        st = lib.pkv_paged_attention_decode_static_scratch(
+            _handle(pool), _ptr(q), _ptr(block_tables), block_tables.shape[1], _ptr(context_lens), b, hq,
+            int(max_context_len), float(scale), _ptr(out), _stream(stream))
+    if st != 0:
         raise _lib.PagedKVError(st, "paged_attention_decode_static_scratch (" +
                                 lib.pkv_static_scratch_error().decode() + ")")
-    check(st, "paged_attention_decode_static_scratch")
     return out
 
 

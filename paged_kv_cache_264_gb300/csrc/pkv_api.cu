@@ -52,8 +52,6 @@ bool scaled_dtype(pkv_kv_dtype d) { return d == PKV_KV_INT8 || d == PKV_KV_FP8_E
 
 int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
 
-bool group_supported(int g) { return g == 1 || g == 2 || g == 4 || g == 8; }
-
 constexpr int kMaxQueries = 16;  // query tokens per sequence in one call
 
 // Query tokens per sequence that the options ask for (0 or absent: 1); -1 if invalid.
@@ -101,9 +99,15 @@ pkv_status make_plan(const pkv_pool* pool, int num_seqs, int num_q_heads, int ma
   // Blocks one sequence's work can span: the whole context, or with a window the blocks
   // that hold the window of its first query up to its newest token.
   int64_t max_nblk = ceil_div(max_context_len, pkv::kBlockSize);
+  // With a window shorter than the longest context, every sequence longer than the window
+  // spans this same bound (or one block less): the window, not the lengths, sets the work.
+  bool window_bound = false;
   if (plan->window != pkv::kNoWindow) {
     const int64_t span = ceil_div(int64_t(plan->window) + nq - 1, pkv::kBlockSize) + 1;
-    if (span < max_nblk) max_nblk = span;
+    if (span < max_nblk) {
+      max_nblk = span;
+      window_bound = true;
+    }
   }
   const auto kv = static_cast<pkv::KvType>(pool->dtype);
   // Query columns per (sequence, kv head): the group's heads times the query tokens.  The
@@ -141,7 +145,7 @@ pkv_status make_plan(const pkv_pool* pool, int num_seqs, int num_q_heads, int ma
   } else if (want_stages || want_bps) {
     return PKV_ERR_UNSUPPORTED;
   }
-  const bool gen = nq > 1 || plan->window != pkv::kNoWindow;
+  const bool gen = pkv::mma_needs_general(nq, plan->window, plan->cols);
   int per_sm = plan->kernel == PKV_KERNEL_TENSOR_CORE
                    ? pkv::mma_ctas_per_sm(kv, pool->head_dim, plan->cols, plan->shape, gen)
                    : pkv::decode_ctas_per_sm(kv, pool->head_dim, plan->cols);
@@ -156,8 +160,22 @@ pkv_status make_plan(const pkv_pool* pool, int num_seqs, int num_q_heads, int ma
   if (plan->kernel == PKV_KERNEL_TENSOR_CORE && per_sm == 0) return PKV_ERR_UNSUPPORTED;
   plan->ctas_per_sm = per_sm > 0 ? per_sm : 1;
   int P;
+  const int64_t resident = int64_t(pool->sm_count) * plan->ctas_per_sm;
+  const int64_t units = int64_t(num_seqs) * pool->kv_heads * plan->chunks;
+  bool one_wave = false;
   if (opt && opt->partition_blocks > 0) {
     P = opt->partition_blocks;
+  } else if (window_bound && units > 0 && units <= resident) {
+    // The window bounds every work unit to about the same number of blocks, and the units
+    // fit on the GPU at once: split each into as many equal items as still run in one
+    // wave, all concurrently, so that none starts late.  Measured on GB300 (8 sequences of
+    // 32768 tokens, 32 kv heads, 4096-token window, 256 units, 3 CTAs per SM): one item
+    // per unit on the grid 81.9 us; 2 items (512 CTAs, a second partial wave) 99.2 us;
+    // 3 items 84.9 us; the earlier plan (5 items of 52 blocks, persistent) 89.0 us.
+    int64_t parts = resident / units;
+    if (parts < ceil_div(max_nblk, kMaxPartitionBlocks)) parts = ceil_div(max_nblk, kMaxPartitionBlocks);
+    P = static_cast<int>(ceil_div(max_nblk, parts));
+    one_wave = true;
   } else {
     // Measured on GB300: items of 128 blocks (CUDA-core kernel) or 64 blocks (tensor-core
     // kernel, which consumes a block faster) balance fewer partials against load balance.
@@ -166,8 +184,6 @@ pkv_status make_plan(const pkv_pool* pool, int num_seqs, int num_q_heads, int ma
     // block).
     P = plan->kernel == PKV_KERNEL_TENSOR_CORE ? kItemBlocksTensorCore : kItemBlocksCudaCore;
     if (plan->kernel == PKV_KERNEL_TENSOR_CORE && (max_nblk <= 128 || plan->cols == 16)) P = 128;
-    const int64_t resident = int64_t(pool->sm_count) * plan->ctas_per_sm;
-    const int64_t units = int64_t(num_seqs) * pool->kv_heads * plan->chunks;
     // Shrink the partition while the batch would not fill the GPU twice over.
     while (P > 4 && units * ceil_div(max_nblk, P) < 2 * resident) P /= 2;
   }
@@ -183,10 +199,11 @@ pkv_status make_plan(const pkv_pool* pool, int num_seqs, int num_q_heads, int ma
   plan->partition_blocks = P;
   plan->max_parts = static_cast<int>(ceil_div(max_nblk, P));
   // Persistent CTAs pay off when the grid would hold idle slots, i.e. when sequences split
-  // into different numbers of partitions; with one partition each, the grid is exact.
+  // into different numbers of partitions; with one partition each, or one wave of equal
+  // items under a window bound, the grid is exact.
   if (num_seqs <= pkv::kMaxSchedSeqs) {
     if (sched == PKV_SCHEDULE_PERSISTENT) plan->persistent = 1;
-    else if (sched == PKV_SCHEDULE_AUTO) plan->persistent = plan->max_parts > 1;
+    else if (sched == PKV_SCHEDULE_AUTO) plan->persistent = plan->max_parts > 1 && !one_wave;
   }
   plan->kernels = plan->max_parts > 1 ? 2 : 1;
   plan->ws_bytes = 0;
@@ -242,13 +259,14 @@ pkv_status check_decode_shape(const pkv_pool* pool, int num_seqs, int num_q_head
   if (num_seqs < 0 || num_q_heads < 1 || max_context_len < 1) return PKV_ERR_INVALID_ARG;
   if (max_context_len >= pkv::kNoWindow) return PKV_ERR_INVALID_ARG;
   if (num_q_heads % pool->kv_heads != 0) return PKV_ERR_INVALID_ARG;
-  if (!group_supported(num_q_heads / pool->kv_heads)) return PKV_ERR_UNSUPPORTED;
   return PKV_OK;
 }
 
 }  // namespace
 
 namespace pkv {
+int pool_device(const pkv_pool* pool) { return pool ? pool->device : -1; }
+
 int decode_ctas_per_sm(KvType kv, int head_dim, int cols) {
   // [dtype][head_dim 64/128][column slots]; 0 = not yet queried.  Threads may fill an entry
   // concurrently; they store the same value.
@@ -489,7 +507,9 @@ pkv_status pkv_paged_attention_decode_ex(const pkv_pool* pool, const void* q,
   p.num_q_heads = num_q_heads;
   p.kv_heads = pool->kv_heads;
   p.group = num_q_heads / pool->kv_heads;
-  p.group_log2 = p.group == 8 ? 3 : p.group == 4 ? 2 : p.group == 2 ? 1 : 0;
+  p.group_log2 = -1;
+  for (int l = 0; l < 31; ++l)
+    if ((1 << l) == p.group) p.group_log2 = l;
   p.num_queries = plan.num_queries;
   p.window = plan.window;
   p.chunks = plan.chunks;

@@ -98,6 +98,12 @@ __device__ __forceinline__ void dequant4(uint32_t w, float (&f)[4]) {
 
 constexpr size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
+// Floats per query column in a warp's merge record: running max, sum, D accumulators and
+// two of padding.  With a stride of D + 4 (4 mod 16), the tensor-core kernel's transposed
+// record writes -- lane (gi, gj) writes column 2gj (+1), dims 16t + 2gi (+1) or 16t + gi
+// (+8) -- land in distinct banks (a stride of D + 2 put two to four lanes on one bank).
+constexpr int record_stride(int d) { return d + 4; }
+
 // Shared memory of the persistent-grid scheduler: the batch's partition prefix sum
 // (num_seqs + 1 ints), two control ints and one scan slot per thread.
 __host__ __device__ constexpr size_t sched_smem_bytes(int num_seqs, int threads) {
@@ -132,7 +138,7 @@ struct DecodeCfg {
   static_assert(D % 32 == 0 && (D == 64 || D == 128), "head_dim 64 or 128");
   static_assert(kLPT >= G && kLPT <= 32, "a token's lanes must cover the group");
   static_assert(kTPP * kPasses == kBlockSize, "passes must cover the block");
-  static_assert(size_t(G) * (D + 2) * 4 <= size_t(kStageBytes), "merge record fits a stage");
+  static_assert(size_t(G) * record_stride(D) * 4 <= size_t(kStageBytes), "merge record fits a stage");
   static_assert(kTileBytes % 16 == 0 && kStageBytes % 16 == 0, "bulk copies need 16 B");
 };
 
@@ -306,10 +312,10 @@ __device__ __forceinline__ void finish_items(const DecodeParams& p) {
   }
 }
 
-// (b, kv head, column chunk, partition) of an item; false for an idle classic-grid slot.
-// A sequence has kv_heads * chunks work units; the chunks of one kv head are adjacent, so
+// (b, kv head, column chunk, partition) of an item, which need no context length.  A
+// sequence has kv_heads * chunks work units; the chunks of one kv head are adjacent, so
 // they tend to run together and share the head's K/V blocks in L2.
-__device__ __forceinline__ bool locate_item(const DecodeParams& p, const SchedSmem& ss, int item,
+__device__ __forceinline__ void locate_unit(const DecodeParams& p, const SchedSmem& ss, int item,
                                             ItemInfo& it) {
   const int ups = p.kv_heads * p.chunks;  // work units per sequence
   int v;
@@ -332,25 +338,44 @@ __device__ __forceinline__ bool locate_item(const DecodeParams& p, const SchedSm
   }
   it.kvh = v / p.chunks;
   it.chunk = v - it.kvh * p.chunks;
-  it.T = __ldg(p.context_lens + it.b);
+}
+
+// The rest of an item once its sequence's context length T is known; false for an idle
+// classic-grid slot.
+__device__ __forceinline__ bool locate_len(const DecodeParams& p, int T, ItemInfo& it) {
+  it.T = T;
   it.bad_len = it.T < p.num_queries || it.T > p.max_context_len;
   it.nparts = seq_parts(p, it.T);
   return it.part < it.nparts;
 }
 
+__device__ __forceinline__ bool locate_item(const DecodeParams& p, const SchedSmem& ss, int item,
+                                            ItemInfo& it) {
+  locate_unit(p, ss, item, it);
+  return locate_len(p, __ldg(p.context_lens + it.b), it);
+}
+
+// Query token of column c and, in *g, its head within the group: c / group and c % group
+// (a shift and a mask when the group is a power of two).
+__device__ __forceinline__ int col_query(const DecodeParams& p, int c, int* g) {
+  const int qi = p.group_log2 >= 0 ? c >> p.group_log2 : c / p.group;
+  *g = c - qi * p.group;
+  return qi;
+}
+
 // Row of q / out (in units of head_dim elements) that query column c of (b, kvh) reads
-// and writes: query token c / group of head kvh * group + c % group (group is a power of
-// two, so this is shifts and masks).
+// and writes: query token c / group of head kvh * group + c % group.
 __device__ __forceinline__ size_t col_row(const DecodeParams& p, int b, int kvh, int c) {
-  const int qi = c >> p.group_log2;
-  const int g = c & (p.group - 1);
+  int g;
+  const int qi = col_query(p, c, &g);
   return (size_t(b) * p.num_queries + qi) * p.num_q_heads + size_t(kvh) * p.group + g;
 }
 
 // Tokens of the sequence hidden from column c by the causal cut: query qi sits k - 1 - qi
 // positions before the newest token.  Columns past group * k get 0 (never written).
 __device__ __forceinline__ int col_cut(const DecodeParams& p, int c) {
-  const int qi = c >> p.group_log2;
+  int g;
+  const int qi = col_query(p, c, &g);
   return qi < p.num_queries ? p.num_queries - 1 - qi : 0;
 }
 
@@ -385,7 +410,7 @@ __device__ __forceinline__ void write_bad_len(const DecodeParams& p, const ItemI
 
 // Merge the NW per-warp states of one work item by log-sum-exp and write the bf16 output
 // (single-partition sequences) or the item's partial (m, l, acc) to the workspace.  Warp w's
-// record is [NC][D + 2] floats (running max in log2 units, sum, accumulator) per query
+// record is [NC][record_stride(D)] floats (running max in log2 units, sum, accumulator) per query
 // column at smem + w * warp_stride; record column c is query column c0 + c.  Each thread
 // takes kE consecutive dims of one column, so that the column's weights 2^(m_w - M) are
 // formed once per thread and the reads and writes are vectors (out and the workspace are
@@ -406,7 +431,7 @@ __device__ __forceinline__ void merge_warp_records(const unsigned char* smem, si
   float M = -INFINITY;
 #pragma unroll
   for (int w = 0; w < NW; ++w) {
-    mw[w] = reinterpret_cast<const float*>(smem + size_t(w) * warp_stride)[g * (D + 2)];
+    mw[w] = reinterpret_cast<const float*>(smem + size_t(w) * warp_stride)[g * record_stride(D)];
     M = fmaxf(M, mw[w]);
   }
   float L = 0.0f;
@@ -416,7 +441,7 @@ __device__ __forceinline__ void merge_warp_records(const unsigned char* smem, si
   if (M != -INFINITY) {
 #pragma unroll
     for (int w = 0; w < NW; ++w) {
-      const float* r = reinterpret_cast<const float*>(smem + size_t(w) * warp_stride) + g * (D + 2);
+      const float* r = reinterpret_cast<const float*>(smem + size_t(w) * warp_stride) + g * record_stride(D);
       const float f = fast_exp2(mw[w] - M);
       L = fmaf(f, r[1], L);
       if constexpr (kE == 1) {
@@ -727,15 +752,16 @@ __global__ void __launch_bounds__(NW * 32)
   // ---- this warp's softmax sum per head, then its merge record in its ring stage 0
 #pragma unroll
   for (int o = C::kLPT; o < 32; o <<= 1) l_run += __shfl_xor_sync(kFull, l_run, o);
-  float* rec = reinterpret_cast<float*>(ring);  // [G][D + 2]: max, sum, accumulator
+  float* rec = reinterpret_cast<float*>(ring);  // [G][record_stride(D)]: max, sum, accumulator
+  constexpr int kRec = record_stride(D);
   if (lane < C::kLPT && store_lane) {
-    rec[g_lane * (D + 2)] = m_run;
-    rec[g_lane * (D + 2) + 1] = l_run;
+    rec[g_lane * kRec] = m_run;
+    rec[g_lane * kRec + 1] = l_run;
   }
 #pragma unroll
   for (int g = 0; g < G; ++g)
 #pragma unroll
-    for (int i = 0; i < C::kDPV; ++i) rec[g * (D + 2) + 2 + lane * C::kDPV + i] = acc[g][i];
+    for (int i = 0; i < C::kDPV; ++i) rec[g * kRec + 2 + lane * C::kDPV + i] = acc[g][i];
   __syncthreads();
 
   merge_warp_records<G, D, NW>(smem, size_t(S) * C::kStageBytes, p, b, kvh, c0, part, nparts);

@@ -35,13 +35,10 @@ int mma_ring_shape(KvType kv, int head_dim, int stages, int bps) {
   return -1;
 }
 
-// The general-mask variant runs only when some query has a causal cut or a window.
-static bool needs_general(const DecodeParams& p) { return p.num_queries > 1 || p.window != kNoWindow; }
-
 cudaError_t launch_decode_mma(const DecodeParams& p, const CUtensorMap* tk, const CUtensorMap* tv,
                               KvType kv, int cols, int shape, cudaStream_t stream) {
   if (!mma_supported(kv, p.head_dim, cols)) return cudaErrorInvalidValue;
-  const bool gen = needs_general(p);
+  const bool gen = mma_needs_general(p.num_queries, p.window, cols);
   if (kv == KvType::kInt8) return launch_mma_int8(p, *tk, *tv, cols, shape, gen, stream);
   if (kv == KvType::kFp8) return launch_mma_fp8(p, *tk, *tv, cols, shape, gen, stream);
   return launch_mma_bf16(p, *tk, *tv, cols, shape, gen, stream);

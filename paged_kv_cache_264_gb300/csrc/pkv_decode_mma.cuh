@@ -75,7 +75,7 @@ struct MmaCfg {
   static_assert(!kQuant || D == 128, "INT8/FP8 tensor-core path is built for head_dim 128");
   static_assert(NC == 2 || NC == 4 || NC == 8 || NC == 16, "2, 4, 8 or 16 query columns");
   static_assert(BPS == 1 || BPS == 2, "one or two blocks per ring stage");
-  static_assert(size_t(NC) * (D + 2) * 4 <= size_t(S) * kStageBytes, "merge record fits the ring");
+  static_assert(size_t(NC) * record_stride(D) * 4 <= size_t(S) * kStageBytes, "merge record fits the ring");
 };
 
 // Warps per CTA and the built ring shapes: (stages S, blocks per stage BPS).  A block's K
@@ -193,7 +193,15 @@ __global__ void __launch_bounds__(NW * 32, (KvTraits<KV>::kQuant && NC <= 8 && B
   for (int item = first_item<C::kThreads>(p, ss); item >= 0;) {
   const int ticket = prefetch_ticket(p);
   ItemInfo it;
-  if (locate_item(p, ss, item, it)) {
+  locate_unit(p, ss, item, it);
+  // Without a window the item's table slice starts at block part * P whatever the
+  // context length, so the length and the slice's first kThreads entries are requested
+  // together (one global-memory round trip instead of two).  Entries past the context
+  // still lie inside the table row (part * P < max_blocks_per_seq) and are never used.
+  const int32_t* trow0 = p.block_tables + size_t(it.b) * p.max_blocks_per_seq + it.part * P;
+  int tpre = 0;
+  if (!kGen && int(threadIdx.x) < min(P, p.max_blocks_per_seq - it.part * P)) tpre = __ldg(trow0 + threadIdx.x);
+  if (locate_len(p, __ldg(p.context_lens + it.b), it)) {
   const int b = it.b, kvh = it.kvh, part = it.part, nparts = it.nparts, T = it.T;
   if (it.bad_len) {
     write_bad_len<NC, D, C::kThreads>(p, it);
@@ -202,7 +210,12 @@ __global__ void __launch_bounds__(NW * 32, (KvTraits<KV>::kQuant && NC <= 8 && B
   const int blk0 = (kGen ? first_block(p, T) : 0) + part * P;
   const int nb_item = min(nblk, blk0 + P) - blk0;
   const int32_t* trow = p.block_tables + size_t(b) * p.max_blocks_per_seq + blk0;
-  for (int i = threadIdx.x; i < nb_item; i += C::kThreads) tbl[i] = __ldg(trow + i);
+  if constexpr (!kGen) {
+    if (int(threadIdx.x) < nb_item) tbl[threadIdx.x] = tpre;
+    for (int i = threadIdx.x + C::kThreads; i < nb_item; i += C::kThreads) tbl[i] = __ldg(trow + i);
+  } else {
+    for (int i = threadIdx.x; i < nb_item; i += C::kThreads) tbl[i] = __ldg(trow + i);
+  }
   __syncthreads();
 
   // The item's blocks are taken BPS at a time (one ring stage); warp w takes stages
@@ -760,7 +773,7 @@ __global__ void __launch_bounds__(NW * 32, (KvTraits<KV>::kQuant && NC <= 8 && B
     }
   }
 
-  // ---- this warp's state -> merge record [NC][D + 2] in its ring
+  // ---- this warp's state -> merge record [NC][record_stride(D)] in its ring
 #pragma unroll
   for (int ofs = 4; ofs < 32; ofs <<= 1)
 #pragma unroll
@@ -782,24 +795,36 @@ __global__ void __launch_bounds__(NW * 32, (KvTraits<KV>::kQuant && NC <= 8 && B
     }
   }
   float* rec = reinterpret_cast<float*>(ring);
+  constexpr int kRec = record_stride(D);
 #pragma unroll
   for (int nt = 0; nt < NT; ++nt) {
     const int h0 = 8 * nt + 2 * gj, h1 = h0 + 1;
     if (gi == 0) {
-      if (h0 < NC) { rec[h0 * (D + 2)] = m[nt][0]; rec[h0 * (D + 2) + 1] = l[nt][0]; }
-      if (h1 < NC) { rec[h1 * (D + 2)] = m[nt][1]; rec[h1 * (D + 2) + 1] = l[nt][1]; }
+      if (h0 < NC) { rec[h0 * kRec] = m[nt][0]; rec[h0 * kRec + 1] = l[nt][0]; }
+      if (h1 < NC) { rec[h1 * kRec] = m[nt][1]; rec[h1 * kRec + 1] = l[nt][1]; }
     }
 #pragma unroll
     for (int t = 0; t < C::kMTiles; ++t) {
-      const int d0 = C::kQuant ? 16 * t + 2 * gi : 16 * t + gi;
-      const int d1 = C::kQuant ? d0 + 1 : d0 + 8;
-      if (h0 < NC) {
-        rec[h0 * (D + 2) + 2 + d0] = o[t][nt][0] * oscale;
-        rec[h0 * (D + 2) + 2 + d1] = o[t][nt][2] * oscale;
-      }
-      if (h1 < NC) {
-        rec[h1 * (D + 2) + 2 + d0] = o[t][nt][1] * oscale;
-        rec[h1 * (D + 2) + 2 + d1] = o[t][nt][3] * oscale;
+      if constexpr (C::kQuant) {
+        // rows gi and gi + 8 of the O^T fragment are dims 16t + 2gi and 16t + 2gi + 1:
+        // one 8-byte store per column (the record's columns start at even floats)
+        const int d0 = 16 * t + 2 * gi;
+        if (h0 < NC)
+          *reinterpret_cast<float2*>(rec + h0 * kRec + 2 + d0) =
+              make_float2(o[t][nt][0] * oscale, o[t][nt][2] * oscale);
+        if (h1 < NC)
+          *reinterpret_cast<float2*>(rec + h1 * kRec + 2 + d0) =
+              make_float2(o[t][nt][1] * oscale, o[t][nt][3] * oscale);
+      } else {
+        const int d0 = 16 * t + gi, d1 = d0 + 8;
+        if (h0 < NC) {
+          rec[h0 * kRec + 2 + d0] = o[t][nt][0];
+          rec[h0 * kRec + 2 + d1] = o[t][nt][2];
+        }
+        if (h1 < NC) {
+          rec[h1 * kRec + 2 + d0] = o[t][nt][1];
+          rec[h1 * kRec + 2 + d1] = o[t][nt][3];
+        }
       }
     }
   }
@@ -853,7 +878,7 @@ int mma_ctas_per_sm_variant() {
 // (the plan turns that into "unsupported").
 template <KvType KV, int D, int S, int BPS>
 constexpr bool mma_record_fits(int nc) {
-  return size_t(nc) * (D + 2) * 4 <= size_t(S) * MmaCfg<KV, D, 2, kNwMma, S, BPS>::kStageBytes;
+  return size_t(nc) * record_stride(D) * 4 <= size_t(S) * MmaCfg<KV, D, 2, kNwMma, S, BPS>::kStageBytes;
 }
 
 template <KvType KV, int D, int S, int BPS, bool kGen>

@@ -6,6 +6,8 @@
 #include <stddef.h>
 #include <stdint.h>
 
+struct pkv_pool;  // the C ABI's opaque pool descriptor (include/pagedkv.h)
+
 namespace pkv {
 
 constexpr int kBlockSize = 16;                      // tokens per physical block
@@ -56,8 +58,8 @@ struct DecodeParams {
   int num_seqs;
   int num_q_heads;
   int kv_heads;
-  int group;                    // query heads per kv head (num_q_heads / kv_heads), 1/2/4/8
-  int group_log2;               // log2(group)
+  int group;                    // query heads per kv head (num_q_heads / kv_heads), any >= 1
+  int group_log2;               // log2(group) when group is a power of two, else -1
   int num_queries;              // k >= 1 query tokens per sequence, the last k positions
   int chunks;                   // column chunks per kv head: group * k columns are served in
                                 // chunks of the variant's column slots, one work unit each
@@ -95,7 +97,8 @@ cudaError_t launch_copy_blocks(const CacheParams& p, const int32_t* pairs, int n
                                cudaStream_t stream);
 // The decode kernels serve, per (sequence, kv head), a tile of query columns: column c is
 // query token c / group of head kvh * group + c % group.  `cols` is the column slot count
-// of the variant to launch (a power of two >= group * num_queries).
+// of the variant to launch: the smallest built power of two >= group * num_queries, or the
+// largest built one, the columns then served in chunks of that many.
 cudaError_t launch_decode_bf16(const DecodeParams& p, int cols, cudaStream_t stream);
 cudaError_t launch_decode_int8(const DecodeParams& p, int cols, cudaStream_t stream);
 cudaError_t launch_decode_fp8(const DecodeParams& p, int cols, cudaStream_t stream);
@@ -111,6 +114,15 @@ cudaError_t launch_decode_mma(const DecodeParams& p, const CUtensorMap* tk, cons
                               KvType kv, int cols, int shape, cudaStream_t stream);
 // gen: the variant with the general masks (several query tokens or a window).
 int mma_ctas_per_sm(KvType kv, int head_dim, int cols, int shape, bool gen);
+// Whether a tensor-core call takes the general-mask variant: some query has a causal cut
+// or a window, or the tile is 16 columns wide (plain decode of a group of more than 8
+// heads; the 16-column tiles are built with the general masks only).
+inline bool mma_needs_general(int num_queries, int window, int cols) {
+  return num_queries > 1 || window != kNoWindow || cols > 8;
+}
+
+// The CUDA device a pool was created on (-1 for NULL).
+int pool_device(const pkv_pool* pool);
 
 // Resident CTAs per SM of the CUDA-core decode kernel variant (0 if not built).
 int decode_ctas_per_sm(KvType kv, int head_dim, int cols);

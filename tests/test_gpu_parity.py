@@ -312,8 +312,8 @@ def test_empty_calls_are_noops():
 
 def test_host_validation_errors():
     pool = pkv.PagedKVPool(4, 2, 64, "bf16", fill=0)
-    q = torch.zeros(1, 6, 64, dtype=torch.bfloat16, device="cuda")  # group 3: unsupported
-    with pytest.raises(pkv.PagedKVError, match="unsupported"):
+    q = torch.zeros(1, 3, 64, dtype=torch.bfloat16, device="cuda")  # 3 heads over 2 kv heads
+    with pytest.raises(pkv.PagedKVError, match="invalid"):
         pool.decode(q, torch.zeros(1, 1, dtype=torch.int32, device="cuda"),
                     torch.ones(1, dtype=torch.int32, device="cuda"), 1.0, 16)
     q = torch.zeros(1, 2, 64, dtype=torch.bfloat16, device="cuda")
