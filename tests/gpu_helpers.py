@@ -145,16 +145,30 @@ def compare(out_gpu: torch.Tensor, ref: np.ndarray, what="", output_rounding=Fal
     keeps 8 significant bits, so rounding moves x by at most 2^-8 |x|); it is used where
     the outputs are single values of V rather than averages over many tokens.  Such a
     value of magnitude 4 or more is 2^-5 apart from its bf16 neighbours, so even the
-    correctly rounded output can miss the exact one by more than the 1e-2 bound."""
+    correctly rounded output can miss the exact one by more than the 1e-2 bound.  It is
+    either a bool (every element) or a boolean array broadcastable to ``ref`` that marks
+    the elements which get the slack; the mean bound then grows by the slack of the marked
+    elements only, averaged over all elements."""
     got = out_gpu.float().cpu().numpy().astype(np.float64)
     assert got.shape == ref.shape, (got.shape, ref.shape)
     assert np.all(np.isfinite(got)), f"{what}: non-finite output"
     err = np.abs(got - ref)
-    slack = 2.0 ** -8 * np.abs(ref) if output_rounding else 0.0
-    mean_bound = MEAN_ABS + (2.0 ** -8 * np.abs(ref).mean() if output_rounding else 0.0)
+    mask = np.broadcast_to(np.asarray(output_rounding, dtype=bool), ref.shape)
+    slack = np.where(mask, 2.0 ** -8 * np.abs(ref), 0.0)
+    mean_bound = MEAN_ABS + slack.mean()
     assert np.all(err <= MAX_ABS + slack), f"{what}: max abs err {err.max():.3e}"
     assert err.mean() <= mean_bound, f"{what}: mean abs err {err.mean():.3e} > {mean_bound:.3e}"
     return float(err.max()), float(err.mean())
+
+
+def few_token_queries(lens, num_queries: int, window: int = 0, fewer_than: int = 16) -> np.ndarray:
+    """Boolean [B, k]: query i of sequence b attends to fewer than ``fewer_than`` tokens
+    (its causal prefix T_b - (k - 1 - i), cut to the window)."""
+    lens = np.asarray(lens, dtype=np.int64)
+    seen = lens[:, None] - (num_queries - 1 - np.arange(num_queries))[None, :]
+    if window:
+        seen = np.minimum(seen, window)
+    return seen < fewer_than
 
 
 def valid_slot_bytes_equal(pool_gpu: dict, pool_ref: dict, lens: np.ndarray):
