@@ -62,7 +62,7 @@ KERNEL_SOURCES = {
                   "pkv_decode_int8.cu"],
     "tensor_core": ["pkv_device.cuh", "pkv_internal.h", "pkv_decode.cuh", "pkv_decode_mma.cuh",
                     "pkv_decode_mma.cu", "pkv_decode_mma_bf16.cu", "pkv_decode_mma_int8.cu",
-                    "pkv_decode_mma_fp8.cu"],
+                    "pkv_decode_mma_fp8.cu", "pkv_decode_mma_quant_d64.cu"],
 }
 
 
@@ -101,7 +101,8 @@ def recorded_traffic(workload: str, kernel: str):
             if line.startswith("#") or "=" not in line:
                 continue
             rec = dict(kv.split("=", 1) for kv in line.split())
-            if rec.get("workload") == workload and rec.get("source_hash") == current:
+            if (rec.get("workload") == workload and rec.get("kernel") == kernel
+                    and rec.get("source_hash") == current):
                 return int(rec["dram_bytes"])
     return None
 
@@ -246,16 +247,18 @@ def run_ours(args, rank, world, local):
     out = torch.empty_like(q)
     max_ctx = w.max_context_len
     nq, win = w.num_queries, spec.window
-    ws_n = pkv.decode_workspace_bytes(pool, w.num_seqs, w.num_q_heads, max_ctx, num_queries=nq, window=win)
+    kern = args.kernel
+    ws_n = pkv.decode_workspace_bytes(pool, w.num_seqs, w.num_q_heads, max_ctx, kernel=kern, num_queries=nq,
+                                      window=win)
     ws = torch.empty(max(ws_n, 16), dtype=torch.uint8, device=dev)
-    plan = pkv.decode_plan(pool, w.num_seqs, w.num_q_heads, max_ctx, num_queries=nq, window=win)
+    plan = pkv.decode_plan(pool, w.num_seqs, w.num_q_heads, max_ctx, kernel=kern, num_queries=nq, window=win)
     torch.cuda.synchronize(dev)
     assert pool.device_error() == 0
 
     def step():
         pkv.reshape_and_cache(pool, new_k, new_v, new_slots, stream)
         pkv.paged_attention_decode(pool, q, tables, lens, w.scale, max_ctx, out=out, workspace=ws,
-                                   window=win, stream=stream)
+                                   kernel=kern, window=win, stream=stream)
 
     for _ in range(args.warmup):
         step()
@@ -275,7 +278,7 @@ def run_ours(args, rank, world, local):
         pkv.reshape_and_cache(pool, new_k, new_v, new_slots, stream)
         ev[i][0].record(stream)
         pkv.paged_attention_decode(pool, q, tables, lens, w.scale, max_ctx, out=out, workspace=ws,
-                                   window=win, stream=stream)
+                                   kernel=kern, window=win, stream=stream)
         ev[i][1].record(stream)
     t1.record(stream)
     torch.cuda.synchronize(dev)
@@ -299,7 +302,7 @@ def run_ours(args, rank, world, local):
 
     # ---- end to end through the public API with host buffers
     e2e = run_e2e(args, pkv, pool, w, new_k, new_v, new_slots, q, tables, lens, max_ctx, ws, sb,
-                  stream, dev, world, win)
+                  stream, dev, world, win, kern)
 
     peak, peak_kind = measured_peaks()
     achieved = sb.decode / (dec_ms * 1e-3) / 1e9
@@ -321,7 +324,7 @@ def run_ours(args, rank, world, local):
             "step": ("reshape_and_cache of one new token per sequence + paged_attention_decode" if nq == 1 else
                      f"reshape_and_cache of {nq} draft tokens per sequence + one multi-query "
                      f"paged_attention_decode verifying them (causal over the last {nq} positions)"),
-            "num_queries": nq, "window": win or None,
+            "num_queries": nq, "window": win or None, "kernel_option": kern,
             "plan": plan, "l2": "inputs larger than L2 (pool %.2f GB > 129 MB); no flush" % (
                 2 * pool.k_cache.numel() * pool.k_cache.element_size() / 1e9),
             "parallelism": f"{world} independent replicas" if world > 1 else "single GPU",
@@ -349,7 +352,7 @@ def run_ours(args, rank, world, local):
 
 
 def run_e2e(args, pkv, pool, w, new_k, new_v, new_slots, q, tables, lens, max_ctx, ws, sb, stream,
-            dev, world, win=0):
+            dev, world, win=0, kern="auto"):
     """Same step through the public API, but every step copies its inputs from pinned
     host memory and reads the output back.  The step's inputs (q, the appended K/V rows,
     their slots, the page tables and lengths) sit in one pinned staging buffer and go to
@@ -376,7 +379,7 @@ def run_e2e(args, pkv, pool, w, new_k, new_v, new_slots, q, tables, lens, max_ct
         dev_buf.copy_(host_buf, non_blocking=True)
         pkv.reshape_and_cache(pool, dbuf["k"], dbuf["v"], dbuf["slots"], stream)
         pkv.paged_attention_decode(pool, dbuf["q"], dbuf["tables"], dbuf["lens"], w.scale, max_ctx,
-                                   out=out_d, workspace=ws, window=win, stream=stream)
+                                   out=out_d, workspace=ws, kernel=kern, window=win, stream=stream)
         out_h.copy_(out_d, non_blocking=True)
 
     for _ in range(max(3, args.warmup)):
@@ -532,6 +535,8 @@ def main(argv=None):
     ap.add_argument("--cpu-seconds", type=float, default=12.0,
                     help="CPU work for the oracle baseline sample")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--kernel", choices=["auto", "cuda_core", "tensor_core"], default="auto",
+                    help="decode kernel family (auto: the plan's choice)")
     ap.add_argument("--seqs", type=int, default=0,
                     help="keep only the first N sequences (a smaller case for profiler captures)")
     args = ap.parse_args(argv)

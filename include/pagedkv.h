@@ -248,11 +248,10 @@ PKV_API int32_t pkv_block_manager_refcount(const pkv_block_manager* manager, int
  *   kernel: which decode kernel family runs.  Both serve, per (sequence, kv head), a tile
  *     of group * num_queries query columns, in chunks of up to 16 (tensor cores) or 8
  *     (CUDA cores) columns, each chunk one work unit that reads the kv head's blocks.
- *     PKV_KERNEL_AUTO (0) picks the tensor-core kernel wherever it is built (bf16 head_dim
- *     64/128, INT8 or FP8 head_dim 128; measured faster than the CUDA-core kernel on every
- *     such shape, MHA included) and the CUDA-core kernel otherwise (INT8 and FP8 at
- *     head_dim 64); PKV_KERNEL_CUDA_CORE (1) and PKV_KERNEL_TENSOR_CORE (2) force one
- *     (PKV_ERR_UNSUPPORTED if it is not built for the shape).  Both compute the same
+ *     PKV_KERNEL_AUTO (0) picks the tensor-core kernel, which is built for every pool type
+ *     at head_dim 64 and 128 and measured faster than the CUDA-core kernel on every such
+ *     shape, MHA included; PKV_KERNEL_CUDA_CORE (1) and PKV_KERNEL_TENSOR_CORE (2) force
+ *     one (PKV_ERR_UNSUPPORTED if it is not built for the shape).  Both compute the same
  *     function.
  *   schedule: how CTAs map to work items.  PKV_SCHEDULE_AUTO (0) picks;
  *     PKV_SCHEDULE_GRID (1) launches one CTA per (partition slot, sequence, kv head), slots

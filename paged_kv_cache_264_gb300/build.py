@@ -19,7 +19,7 @@ INCLUDE = ROOT / "include"
 ARCH_FLAGS = ["-gencode", "arch=compute_103a,code=sm_103a"]
 SOURCES = ["pkv_api.cu", "pkv_cache.cu", "pkv_decode_bf16.cu", "pkv_decode_int8.cu",
            "pkv_decode_fp8.cu", "pkv_decode_mma.cu", "pkv_decode_mma_bf16.cu", "pkv_decode_mma_int8.cu",
-           "pkv_decode_mma_fp8.cu", "pkv_static_scratch.cu", "pkv_selftest.cu", "pkv_blocks.cpp"]
+           "pkv_decode_mma_fp8.cu", "pkv_decode_mma_quant_d64.cu", "pkv_static_scratch.cu", "pkv_selftest.cu", "pkv_blocks.cpp"]
 
 
 def build_dir() -> Path:

@@ -233,17 +233,23 @@ PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
 }
 
 // A 2-D tensor map over a [rows, head_dim] pool: 128-byte boxes of 16 rows, 128-byte
-// swizzle.  Returns false when the layout does not qualify (rows not a whole number of
-// 128-byte spans, more than 2^31 rows, or no driver entry point).
+// swizzle.  Token rows of 64 bytes (INT8/FP8 at head_dim 64) are mapped two to a 128-byte
+// row: the pool seen as [rows / 2, 128 bytes], boxes of 8 such rows (one 16-token tile).
+// Returns false when the layout does not qualify (rows neither whole 128-byte spans nor
+// 64 bytes, more than 2^31 rows, or no driver entry point).
 bool make_pool_tensor_map(CUtensorMap* map, void* base, pkv_kv_dtype dtype, int head_dim,
                           int64_t rows) {
   const int esz = scaled_dtype(dtype) ? 1 : 2;
-  if ((head_dim * esz) % 128 != 0 || rows >= (int64_t(1) << 31)) return false;
+  const int row_bytes = head_dim * esz;
+  const bool pairs = row_bytes == 64;
+  if ((row_bytes % 128 != 0 && !pairs) || rows >= (int64_t(1) << 31)) return false;
   auto encode = tensor_map_encoder();
   if (!encode) return false;
-  const cuuint64_t dims[2] = {cuuint64_t(head_dim), cuuint64_t(rows)};
-  const cuuint64_t strides[1] = {cuuint64_t(head_dim) * esz};
-  const cuuint32_t box[2] = {cuuint32_t(128 / esz), cuuint32_t(pkv::kBlockSize)};
+  const int64_t map_rows = pairs ? rows / 2 : rows;  // rows is a multiple of 16
+  const int64_t map_cols = pairs ? 128 / esz : head_dim;
+  const cuuint64_t dims[2] = {cuuint64_t(map_cols), cuuint64_t(map_rows)};
+  const cuuint64_t strides[1] = {cuuint64_t(map_cols) * esz};
+  const cuuint32_t box[2] = {cuuint32_t(128 / esz), cuuint32_t(pairs ? pkv::kBlockSize / 2 : pkv::kBlockSize)};
   const cuuint32_t elem_strides[2] = {1, 1};
   const CUresult r = encode(
       map, scaled_dtype(dtype) ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,

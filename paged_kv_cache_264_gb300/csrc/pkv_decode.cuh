@@ -1,7 +1,7 @@
 // pkv_decode.cuh -- PagedAttention decode on the CUDA cores (paged_decode_kernel), the
 // work scheduling and partition merge shared with the tensor-core kernel
-// (pkv_decode_mma.cuh), for sm_103a.  The tensor-core kernel is the automatic choice
-// wherever it is built; this one covers INT8 and FP8 pools at head_dim 64 and can be forced.
+// (pkv_decode_mma.cuh), for sm_103a.  The tensor-core kernel is the automatic choice for
+// every built shape; this one computes the same function and can be forced.
 //
 // What is computed ("Lesson 4: Model deployment and inference acceleration", 4.2,
 // attention-invariance equation): for sequence b and query head h,

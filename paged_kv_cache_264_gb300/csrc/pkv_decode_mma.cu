@@ -8,11 +8,14 @@ namespace pkv {
 
 bool mma_supported(KvType kv, int head_dim, int cols) {
   if (cols != 2 && cols != 4 && cols != 8 && cols != 16) return false;
-  if (kv == KvType::kBf16) return head_dim == 128 || head_dim == 64;
-  return head_dim == 128;  // INT8, FP8
+  return head_dim == 128 || head_dim == 64;  // bf16, INT8 and FP8 pools alike
 }
 
 static int shapes_of(KvType kv, int head_dim, const RingShape** out) {
+  if (kv != KvType::kBf16 && head_dim == 64) {
+    *out = kShapesQuantD64;
+    return int(sizeof(kShapesQuantD64) / sizeof(kShapesQuantD64[0]));
+  }
   if (kv != KvType::kBf16) {
     *out = kShapesQuant;
     return int(sizeof(kShapesQuant) / sizeof(kShapesQuant[0]));
@@ -39,23 +42,26 @@ cudaError_t launch_decode_mma(const DecodeParams& p, const CUtensorMap* tk, cons
                               KvType kv, int cols, int shape, cudaStream_t stream) {
   if (!mma_supported(kv, p.head_dim, cols)) return cudaErrorInvalidValue;
   const bool gen = mma_needs_general(p.num_queries, p.window, cols);
+  if (kv != KvType::kBf16 && p.head_dim == 64) return launch_mma_quant_d64(kv, p, *tk, *tv, cols, shape, gen, stream);
   if (kv == KvType::kInt8) return launch_mma_int8(p, *tk, *tv, cols, shape, gen, stream);
   if (kv == KvType::kFp8) return launch_mma_fp8(p, *tk, *tv, cols, shape, gen, stream);
   return launch_mma_bf16(p, *tk, *tv, cols, shape, gen, stream);
 }
 
 int mma_ctas_per_sm(KvType kv, int head_dim, int cols, int shape, bool gen) {
-  if (!mma_supported(kv, head_dim, cols) || shape < 0 || shape > 3) return 0;
-  // [pool type][shape][column slots][gen]; 0 = not yet queried (or not built).  Threads may
-  // fill an entry concurrently; they store the same value.
-  static std::atomic<int> cache[4][4][17][2];
-  const int ti = kv == KvType::kFp8 ? 3 : kv == KvType::kInt8 ? 2 : (head_dim == 128 ? 0 : 1);
-  std::atomic<int>& slot = cache[ti][shape][cols][gen ? 1 : 0];
+  const RingShape* sh;
+  if (!mma_supported(kv, head_dim, cols) || shape < 0 || shape >= shapes_of(kv, head_dim, &sh)) return 0;
+  // [pool type][head_dim 128 | 64][shape][column slots][gen]; 0 = not yet queried (or not
+  // built).  Threads may fill an entry concurrently; they store the same value.
+  static std::atomic<int> cache[3][2][4][17][2];
+  const int ki = static_cast<int>(kv), di = head_dim == 128 ? 0 : 1;
+  std::atomic<int>& slot = cache[ki][di][shape][cols][gen ? 1 : 0];
   int n = slot.load(std::memory_order_relaxed);
   if (n) return n;
-  n = kv == KvType::kInt8  ? occupancy_mma_int8(cols, shape, gen)
-      : kv == KvType::kFp8 ? occupancy_mma_fp8(cols, shape, gen)
-                           : occupancy_mma_bf16(head_dim, cols, shape, gen);
+  n = kv != KvType::kBf16 && head_dim == 64 ? occupancy_mma_quant_d64(kv, cols, shape, gen)
+      : kv == KvType::kInt8                 ? occupancy_mma_int8(cols, shape, gen)
+      : kv == KvType::kFp8                  ? occupancy_mma_fp8(cols, shape, gen)
+                                            : occupancy_mma_bf16(head_dim, cols, shape, gen);
   slot.store(n, std::memory_order_relaxed);
   return n;
 }

@@ -1,7 +1,7 @@
 // pkv_decode_mma.cuh -- PagedAttention decode on the tensor cores (mma.sync) for tiles of
 // 2, 4, 8 or 16 query columns per kv head (the GQA group's heads times the query tokens of
-// a multi-query call; a single column, MHA decode, uses 2), head_dim 128 (bf16, INT8 or
-// FP8 pools) or 64 (bf16).
+// a multi-query call; a single column, MHA decode, uses 2), head_dim 128 or 64, bf16,
+// INT8 or FP8 pools.
 //
 // Same work decomposition and result as paged_decode_kernel (pkv_decode.cuh): one CTA
 // per (sequence, kv head, context partition), NW warps taking the item's blocks in turn,
@@ -9,8 +9,9 @@
 // What changes is how a 16-token block is consumed:
 //
 //  * Tiles arrive by TMA tensor copies (cp.async.bulk.tensor.2d) through a tensor map of
-//    the pool viewed as rows of head_dim elements, in 128-byte boxes with the 128-byte
-//    swizzle, so that the shared-memory reads below are free of bank conflicts.
+//    the pool viewed as rows of head_dim elements (two 64-byte token rows to a row for
+//    INT8/FP8 at head_dim 64), in 128-byte boxes with the 128-byte swizzle, so that the
+//    shared-memory reads below are free of bank conflicts.
 //  * Logits for all query columns come from m16n8k16 MMAs with fp32 accumulation:
 //    S[16 tokens x 8 columns] = K[16 x d] q^T[d x 8] per n-tile of 8 columns (columns past
 //    the active ones are zero).  Each K fragment feeds every n-tile.  A column is one
@@ -53,9 +54,13 @@ struct MmaCfg {
   static constexpr bool kQuant = KvTraits<KV>::kQuant;
   static constexpr bool kFp8 = KV == KvType::kFp8;     // E4M3 codes (else INT8 when kQuant)
   static constexpr int kRowBytes = D * kEsz;           // one token row of one tile
+  // 64-byte token rows (INT8/FP8 at head_dim 64) travel two to a 128-byte box row, so that
+  // every tile keeps the 128-byte swizzle: token t is box row t / 2, bytes 64 (t % 2) on.
+  static constexpr bool kPairRows = kRowBytes == 64;
   static constexpr int kBoxCols = 128 / kEsz;          // elements in a 128-byte box row
-  static constexpr int kBoxes = kRowBytes / 128;       // boxes per tile
-  static constexpr int kBoxBytes = kBlockSize * 128;   // 2 KiB, 1 KiB aligned in the ring
+  static constexpr int kBoxRows = kPairRows ? kBlockSize / 2 : kBlockSize;
+  static constexpr int kBoxes = kPairRows ? 1 : kRowBytes / 128;  // boxes per tile
+  static constexpr int kBoxBytes = kBoxRows * 128;     // 2 KiB (1 KiB for pair rows), 1 KiB aligned
   static constexpr int kTileBytes = kBoxes * kBoxBytes;
   static constexpr int kStageBytes = 2 * BPS * kTileBytes;   // BPS K tiles, then BPS V tiles
   static constexpr int kScaleStage = kQuant ? 2 * BPS * kBlockSize * 4 : 0;  // K then V scales
@@ -71,16 +76,17 @@ struct MmaCfg {
            sched_smem_bytes(sched_seqs, kThreads);
   }
 
-  static_assert(kRowBytes % 128 == 0, "rows must be whole 128-byte swizzle spans");
-  static_assert(!kQuant || D == 128, "INT8/FP8 tensor-core path is built for head_dim 128");
+  static_assert(kRowBytes % 128 == 0 || kPairRows, "rows must be whole 128-byte swizzle spans or pairs");
+  static_assert(!kQuant || D == 128 || D == 64, "INT8/FP8 tensor-core path is built for head_dim 64 and 128");
+  static_assert(!kPairRows || kQuant, "pair rows are the quantised head_dim 64 layout");
   static_assert(NC == 2 || NC == 4 || NC == 8 || NC == 16, "2, 4, 8 or 16 query columns");
   static_assert(BPS == 1 || BPS == 2, "one or two blocks per ring stage");
   static_assert(size_t(NC) * record_stride(D) * 4 <= size_t(S) * kStageBytes, "merge record fits the ring");
 };
 
 // Warps per CTA and the built ring shapes: (stages S, blocks per stage BPS).  A block's K
-// and V tiles take 8 KiB (bf16, head_dim 128) or 4 KiB (bf16 64, INT8/FP8 128).  The first
-// shape listed for a pool type is its default.
+// and V tiles take 8 KiB (bf16, head_dim 128), 4 KiB (bf16 64, INT8/FP8 128) or 2 KiB
+// (INT8/FP8 64).  The first shape listed for a pool type is its default.
 constexpr int kNwMma = 4;
 struct RingShape {
   int stages, bps;
@@ -91,6 +97,9 @@ constexpr RingShape kShapesBf16D64[] = {{3, 1}, {2, 2}};
 // 3x1 195 / 187, 2x2 203 / 192, 3x2 260 / 241.  Forcing more CTAs per SM through launch
 // bounds (fewer registers) never helped.
 constexpr RingShape kShapesQuant[] = {{2, 1}, {3, 1}, {2, 2}, {3, 2}};
+// INT8 and FP8 at head_dim 64 (2 KiB per block).  Measured on GB300 (int8_cb lengths at
+// head_dim 64, microseconds per call): 2x2 122.8, 3x1 138.2 (the CUDA-core kernel: 246.0).
+constexpr RingShape kShapesQuantD64[] = {{2, 2}, {3, 1}};
 
 // Launch / occupancy of one pool type's variants (defined in pkv_decode_mma_<type>.cu):
 // cols = column slots (2, 4, 8, 16), shape = index into the type's shape list, gen = kGen.
@@ -103,11 +112,24 @@ cudaError_t launch_mma_fp8(const DecodeParams& p, const CUtensorMap& tk, const C
 int occupancy_mma_bf16(int head_dim, int cols, int shape, bool gen);
 int occupancy_mma_int8(int cols, int shape, bool gen);
 int occupancy_mma_fp8(int cols, int shape, bool gen);
+// INT8 / FP8 pools at head_dim 64 (pkv_decode_mma_quant_d64.cu).
+cudaError_t launch_mma_quant_d64(KvType kv, const DecodeParams& p, const CUtensorMap& tk,
+                                 const CUtensorMap& tv, int cols, int shape, bool gen, cudaStream_t stream);
+int occupancy_mma_quant_d64(KvType kv, int cols, int shape, bool gen);
 
 // Byte offset of 16-byte chunk `c` of token row `t` in a tile whose 128-byte boxes were
 // written with the 128-byte swizzle (chunk index xor row index mod 8).
 __device__ __forceinline__ int swz_off(int t, int c) {
   return (c >> 3) * 2048 + t * 128 + (((c & 7) ^ (t & 7)) << 4);
+}
+
+// The same for a tile of 64-byte token rows held two to a 128-byte box row: token t is box
+// row t / 2, its chunk c (0..3) is chunk 4 (t % 2) + c of that row before the swizzle.  The
+// 8 tokens of an ldmatrix matrix then cover the 8 chunk positions of 4 box rows, so the
+// reads stay free of bank conflicts.
+__device__ __forceinline__ int swz_off_pair(int t, int c) {
+  const int r = t >> 1;
+  return r * 128 + (((((t & 1) << 2) | c) ^ (r & 7)) << 4);
 }
 
 // A ring stage known at compile time (the stage of an unrolled loop body), a loop over
@@ -187,7 +209,8 @@ __global__ void __launch_bounds__(NW * 32, (KvTraits<KV>::kQuant && NC <= 8 && B
   const uint32_t ring_a = smem_addr(ring);
   uint32_t kaddr[4];
 #pragma unroll
-  for (int m2 = 0; m2 < 4; ++m2) kaddr[m2] = ring_a + tok_k * 128 + ((((2 * m2) | ck) ^ (tok_k & 7)) << 4);
+  for (int m2 = 0; m2 < 4; ++m2)
+    kaddr[m2] = ring_a + (C::kPairRows ? swz_off_pair(tok_k, ((2 * m2) | ck) & 3) : swz_off(tok_k, (2 * m2) | ck));
   const uint32_t scl_a = smem_addr(scl) + gi * 4;  // this lane's token row gi in the scales
 
   for (int item = first_item<C::kThreads>(p, ss); item >= 0;) {
@@ -253,7 +276,7 @@ __global__ void __launch_bounds__(NW * 32, (KvTraits<KV>::kQuant && NC <= 8 && B
 #pragma unroll
     for (int j = 0; j < BPS; ++j) {
       if (tiles[j] < 0) continue;
-      const int row = tiles[j] * kBlockSize;
+      const int row = tiles[j] * C::kBoxRows;  // row of the tensor map's view of the pool
 #pragma unroll
       for (int x = 0; x < C::kBoxes; ++x) {
         tma_load_2d(st + j * C::kTileBytes + x * C::kBoxBytes, &tmap_k, x * C::kBoxCols, row,

@@ -26,6 +26,7 @@ llama3_8b_gqa_   128   as llama3_8b_gqa                 32/8     128   bf16   k 
 verify4
 long_32k_       8     as long_32k                      32/32    128   bf16   window 4096
 window4k
+int8_cb_d64      256   as int8_cb                       32/8     64    int8
 ===============  ====  ===============================  =======  ====  =====  ================
 
 The two ``verify4`` workloads are multi-query decode batches for speculative decoding
@@ -36,7 +37,8 @@ reuse their base workload's context lengths and block pool (its seed), so a veri
 and a decode step over the same cache compare directly.  ``long_32k_window4k`` is the
 long_32k cache decoded with a sliding window of 4096 tokens ("LLM/MLLM inference
 optimisation", 2.3: keep only the most recent window): each query reads its last 4096
-tokens.
+tokens.  ``int8_cb_d64`` is the int8_cb batch at head_dim 64 (two 64-byte token rows to each
+128-byte swizzled row on the tensor-core path).
 
 Pools other than ``tiny`` hold ``ceil(1.25 * sum_b ceil(T_b / 16))`` blocks; the blocks
 that sequences use are drawn from a seeded permutation of the pool.  Everything is drawn
@@ -107,6 +109,9 @@ SPECS: dict[str, Spec] = {
         Spec("long_32k_window4k", 9, "long-context sliding window: the long_32k cache (8 x 32768 "
              "tokens, 32/32 heads, head_dim 128, bf16) decoded with a 4096-token window", 8, 32, 32, 128,
              "bf16", ("const", 32768), outlier_key_channel_frac=0.01, base_index=4, window=4096),
+        Spec("int8_cb_d64", 10, "INT8 continuous batching at head_dim 64: the int8_cb lengths "
+             "with 32/8 heads of 64 dims", 256, 32, 8, 64,
+             "int8", ("lognormal", 1024.0, 1.0, 16, 16384), base_index=5),
     )
 }
 

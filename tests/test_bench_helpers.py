@@ -29,3 +29,4 @@ def test_recorded_traffic_needs_the_current_hash(tmp_path, monkeypatch):
     assert bench.recorded_traffic("w1", "tensor_core") == 123
     assert bench.recorded_traffic("w2", "tensor_core") is None  # taken on other sources
     assert bench.recorded_traffic("w3", "tensor_core") is None
+    assert bench.recorded_traffic("w1", "cuda_core") is None  # another kernel family's record

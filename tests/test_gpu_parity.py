@@ -241,7 +241,7 @@ def _sample(w, k=6):
     return sorted(picks)
 
 
-@pytest.mark.parametrize("name", ["llama2_7b", "llama3_8b_gqa", "long_32k", "int8_cb", "fp8_cb"])
+@pytest.mark.parametrize("name", ["llama2_7b", "llama3_8b_gqa", "long_32k", "int8_cb", "fp8_cb", "int8_cb_d64"])
 def test_named_workload_full_size(name):
     """Full-size workloads in the launch configuration the benchmark times (automatic
     plan); the oracle checks sampled sequences (shortest, longest, median, random)."""
@@ -251,7 +251,7 @@ def test_named_workload_full_size(name):
     check_all(w, kv, 0, seqs)
 
 
-@pytest.mark.parametrize("name", ["llama2_7b", "llama3_8b_gqa", "long_32k", "int8_cb", "fp8_cb"])
+@pytest.mark.parametrize("name", ["llama2_7b", "llama3_8b_gqa", "long_32k", "int8_cb", "fp8_cb", "int8_cb_d64"])
 def test_named_workload_cuda_core_kernel(name):
     """The full-size workloads through the CUDA-core kernel too (auto picks the tensor
     cores wherever they are built)."""

@@ -142,12 +142,12 @@ def test_plan_limits():
     with pytest.raises(pkv.PagedKVError, match="invalid"):
         pkv.decode_plan(pool, 2, 8, 3, num_queries=4)                  # max_context_len < k
     pool.close()
-    pool = pkv.PagedKVPool(4, 4, 64, "int8", fill=0)                   # no tensor-core INT8 at d=64
-    assert pkv.decode_plan(pool, 2, 8, 64, num_queries=4)["kernel"] == "cuda_core"
-    assert pkv.decode_plan(pool, 2, 16, 64, num_queries=4)["kernel"] == "cuda_core"  # 16 columns, 2 chunks
-    with pytest.raises(pkv.PagedKVError, match="unsupported"):
-        pkv.decode_plan(pool, 2, 16, 64, num_queries=4, kernel="tensor_core")
-    pool.close()
+    for kv in ("int8", "fp8"):
+        pool = pkv.PagedKVPool(4, 4, 64, kv, fill=0)                   # quantised pools at d = 64
+        assert pkv.decode_plan(pool, 2, 8, 64, num_queries=4)["kernel"] == "tensor_core"
+        assert pkv.decode_plan(pool, 2, 16, 64, num_queries=4)["kernel"] == "tensor_core"  # 16 columns
+        assert pkv.decode_plan(pool, 2, 16, 64, num_queries=4, kernel="cuda_core")["kernel"] == "cuda_core"
+        pool.close()
 
 
 @pytest.mark.parametrize("name", ["llama2_7b_verify4", "llama3_8b_gqa_verify4"])

@@ -38,6 +38,8 @@ def test_variants_share_their_base_lengths():
     assert (W.context_lens_of("long_32k") == 32768).all()
     assert W.SPECS["long_32k_window4k"].window == 4096
     assert W.SPECS["llama2_7b_verify4"].num_queries == 4
+    assert torch.equal(W.context_lens_of("int8_cb_d64"), W.context_lens_of("int8_cb"))
+    assert W.SPECS["int8_cb_d64"].head_dim == 64
 
 
 @pytest.mark.parametrize("lens,k", [([17, 40], 1), ([1, 16, 33, 100, 257], 1), ([4, 20, 65], 4)])
