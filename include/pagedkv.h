@@ -327,7 +327,9 @@ PKV_API pkv_status pkv_decode_plan(const pkv_pool* pool, int num_seqs, int num_q
  * rounded to bf16 (round to nearest even).
  *   q            (device): bf16 [num_seqs, num_q_heads, head_dim], 16-byte aligned.
  *   block_tables (device): int32 [num_seqs, max_blocks_per_seq]; entries past
- *                          ceil(T_b / 16) are never read.
+ *                          ceil(T_b / 16) are never used and may hold anything (a
+ *                          kernel may load them along with the used ones, so every row
+ *                          must be max_blocks_per_seq entries long).
  *   context_lens (device): int32 [num_seqs], 1 <= T_b <= max_context_len (k <= T_b with
  *                          k query tokens per sequence).
  *   max_context_len (host int): an upper bound on every T_b; it sizes the plan and the

@@ -132,6 +132,25 @@ def test_window_plan_reads_fewer_blocks():
     pool.close()
 
 
+def test_window_bound_plan_runs_one_wave():
+    """When the window, not the lengths, bounds every unit's blocks and the units fit on the
+    GPU at once, the automatic plan splits each unit into equal items that run in one wave
+    on the grid; with more units than fit, the general rule applies."""
+    pool = pkv.PagedKVPool(4, 32, 128, "bf16", fill=0)
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    one = pkv.decode_plan(pool, 8, 32, 32768, window=4096)      # 256 units, 257-block bound
+    parts = one["max_partitions"]
+    assert parts >= 1 and 256 * parts <= 4 * sms                 # one wave (at most 4 CTAs per SM)
+    assert one["partition_blocks"] == -(-257 // parts)             # equal items, no short tail
+    if parts == 1:
+        assert one["kernels_per_call"] == 1                        # no partials, no merge kernel
+    many = pkv.decode_plan(pool, 256, 32, 32768, window=4096)   # 8192 units: more than one wave
+    assert many["max_partitions"] > 1 and many["partition_blocks"] <= 128
+    nowin = pkv.decode_plan(pool, 8, 32, 32768)                   # no window: lengths unknown
+    assert nowin["max_partitions"] > parts
+    pool.close()
+
+
 @pytest.mark.parametrize("kv", ["bf16", "int8"])
 def test_sliding_window_generation_with_block_manager(kv):
     """A generation loop under a 40-token window: each step appends one token per sequence,
