@@ -542,10 +542,13 @@ __global__ void __launch_bounds__(NW * 32)
   const char* kbase = static_cast<const char*>(p.k_cache);
   const char* vbase = static_cast<const char*>(p.v_cache);
 
-  auto issue = [&](int k) {  // lane 0 only: fetch the warp's k-th block of the item
+  // Fetch the warp's k-th block of the item: the whole warp runs this with warp-uniform
+  // values, one elected lane issues the copies.
+  auto issue = [&](int k) {
     const int s = (kb + k) % S;
     unsigned char* st = ring + size_t(s) * C::kStageBytes;
     const int phys = tbl[warp + k * NW];
+    if (!elect_one()) return;
     if (phys < 0 || phys >= p.num_blocks) {
       set_error(p.err, kErrBlockId);
       mbar_arrive(bars + s);  // complete the phase with no data; the block is skipped
@@ -565,9 +568,7 @@ __global__ void __launch_bounds__(NW * 32)
                     C::kScaleBytes, bars + s, policy);
     }
   };
-  if (lane == 0) {
-    for (int k = 0; k < S && k < nw; ++k) issue(k);
-  }
+  for (int k = 0; k < S && k < nw; ++k) issue(k);
 
   // ---- q for this lane's dims of all G query columns, pre-multiplied by scale * log2(e)
   const int tok = lane / C::kLPT;    // token within a pass
@@ -733,7 +734,7 @@ __global__ void __launch_bounds__(NW * 32)
       }
     }
     __syncwarp();  // every lane is done with this stage and with `prob`
-    if (lane == 0 && k + S < nw) {
+    if (k + S < nw) {
       fence_proxy_async_smem();
       issue(k + S);
     }

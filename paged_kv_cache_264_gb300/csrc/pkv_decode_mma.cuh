@@ -249,7 +249,9 @@ __global__ void __launch_bounds__(NW * 32, (KvTraits<KV>::kQuant && NC <= 8 && B
   // other chunks' CTAs read them again right away, so keep them in L2.
   const uint64_t policy = p.chunks > 1 ? l2_evict_last_policy() : l2_evict_first_policy();
 
-  auto issue = [&](auto s_c, int k) {  // lane 0 only: fetch the warp's k-th stage of the item
+  // Fetch the warp's k-th stage of the item.  The whole warp runs this with warp-uniform
+  // values; one elected lane issues the copies.
+  auto issue = [&](auto s_c, int k) {
     const int s = s_c.value;  // (kb + k) % S
     unsigned char* st = ring + s * C::kStageBytes;
     float* sc = scl + s * (C::kScaleStage / 4);
@@ -262,12 +264,13 @@ __global__ void __launch_bounds__(NW * 32, (KvTraits<KV>::kQuant && NC <= 8 && B
       if (ib0 + j >= nb_item) continue;
       const int phys = tbl[ib0 + j];
       if (phys < 0 || phys >= p.num_blocks) {
-        set_error(p.err, kErrBlockId);
+        if (lane == 0) set_error(p.err, kErrBlockId);
         continue;
       }
       tiles[j] = phys * p.kv_heads + kvh;  // pools with tensor maps have < 2^27 tiles
       bytes += 2 * C::kTileBytes + (C::kQuant ? 2 * kBlockSize * 4 : 0);
     }
+    if (!elect_one()) return;
     if (bytes == 0) {
       mbar_arrive(bars + s);  // complete the phase with no data; the blocks are skipped
       return;
@@ -292,7 +295,7 @@ __global__ void __launch_bounds__(NW * 32, (KvTraits<KV>::kQuant && NC <= 8 && B
       }
     }
   };
-  if (lane == 0) {
+  {
     if constexpr (kGen) {
       for (int k = 0; k < S && k < nw; ++k) issue(StageRt{int((kb + k) % S)}, k);
     } else {
@@ -759,7 +762,7 @@ __global__ void __launch_bounds__(NW * 32, (KvTraits<KV>::kQuant && NC <= 8 && B
       }
     }
     __syncwarp();
-    if (lane == 0 && k + S < nw) {
+    if (k + S < nw) {
       fence_proxy_async_smem();
       issue(s_c, k + S);
     }

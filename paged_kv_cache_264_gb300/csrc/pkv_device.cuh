@@ -202,6 +202,21 @@ __device__ __forceinline__ uint32_t f16x2_biased(uint32_t u, uint32_t sel) {
   return __byte_perm(u, 0x64646464u, sel);
 }
 
+// True in exactly one lane of the (fully active) warp: elect.sync picks a leader.  Copy
+// issue code runs on the whole warp with warp-uniform values and only the copy
+// instructions sit under this test; measured on GB300 that costs fewer instructions than
+// running the whole issue path in lane 0 alone (int8_cb decode 172.9 -> 166.9 us, 6 %
+// fewer instructions).
+__device__ __forceinline__ bool elect_one() {
+  uint32_t pred = 0;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "elect.sync _|p, 0xffffffff;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(pred));
+  return pred != 0;
+}
+
 // Programmatic dependent launch.  A kernel launched with programmatic stream serialisation
 // may start while the previous kernel in the stream is still finishing; griddep_wait()
 // returns once that kernel has completed and its writes are visible, so it must precede
