@@ -93,10 +93,10 @@ struct RingShape {
 };
 constexpr RingShape kShapesBf16D128[] = {{2, 1}, {3, 1}};
 constexpr RingShape kShapesBf16D64[] = {{3, 1}, {2, 2}};
-// INT8 and FP8.  Measured on GB300 (int8_cb / fp8_cb, microseconds per call): 2x1 194 / 185,
-// 3x1 195 / 187, 2x2 203 / 192, 3x2 260 / 241.  Forcing more CTAs per SM through launch
-// bounds (fewer registers) never helped.
-constexpr RingShape kShapesQuant[] = {{2, 1}, {3, 1}, {2, 2}, {3, 2}};
+// INT8 and FP8.  Measured on GB300 (int8_cb / fp8_cb, microseconds per call, median of 3
+// interleaved runs): 3x1 168.2 / 162.0, 2x1 169.6 / 162.1, 2x2 172.1 / -, 3x2 ~250 / ~246.
+// Forcing more CTAs per SM through launch bounds (fewer registers) never helped.
+constexpr RingShape kShapesQuant[] = {{3, 1}, {2, 1}, {2, 2}, {3, 2}};
 // INT8 and FP8 at head_dim 64 (2 KiB per block).  Measured on GB300 (int8_cb lengths at
 // head_dim 64, microseconds per call): 2x2 122.8, 3x1 138.2 (the CUDA-core kernel: 246.0).
 constexpr RingShape kShapesQuantD64[] = {{2, 2}, {3, 1}};

@@ -419,7 +419,8 @@ def test_scheduler_counters_reset_between_calls(kv):
 
 RING_SHAPES = [("bf16", 128, 2, 1), ("bf16", 128, 3, 1), ("bf16", 64, 3, 1), ("bf16", 64, 2, 2),
                ("int8", 128, 3, 1), ("int8", 128, 2, 2), ("int8", 128, 3, 2), ("int8", 128, 2, 1),
-               ("fp8", 128, 3, 1), ("fp8", 128, 2, 2), ("fp8", 128, 3, 2), ("fp8", 128, 2, 1)]
+               ("fp8", 128, 3, 1), ("fp8", 128, 2, 2), ("fp8", 128, 3, 2), ("fp8", 128, 2, 1),
+               ("int8", 64, 2, 2), ("int8", 64, 3, 1), ("fp8", 64, 2, 2), ("fp8", 64, 3, 1)]
 
 
 @pytest.mark.parametrize("partition_blocks", [0, 3, 5])
