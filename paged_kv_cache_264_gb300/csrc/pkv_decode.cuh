@@ -14,11 +14,11 @@
 // partition covers P consecutive logical blocks.  One CTA of NW warps runs one item and
 // serves all query columns of its kv head (the G query heads of the group, times the query
 // tokens of a multi-query call; template parameter G counts column slots), so each K/V
-// block is read from HBM once per group.  Warp w takes the item's blocks w, w + NW, ...; each warp owns a ring of S
-// shared-memory stages, and its lane 0 fills a stage with one bulk asynchronous copy
-// per tile (the [phys][kvh] K tile and V tile are each one contiguous 16*D-element
-// run, so no tensor map is needed), completing on the stage's mbarrier.  The block
-// table slice of the item is staged in shared memory first.
+// block is read from HBM once per group.  Warp w takes the item's blocks w, w + NW, ...;
+// each warp owns a ring of S shared-memory stages, and one elected lane fills a stage with
+// one bulk asynchronous copy per tile (the [phys][kvh] K tile and V tile are each one
+// contiguous 16*D-element run, so no tensor map is needed), completing on the stage's
+// mbarrier.  The block table slice of the item is staged in shared memory first.
 //
 // Per block a warp computes 16 tokens x G columns of logits with fp32 FMAs: lanes split
 // a token's D dims (DPL dims each) and hold q for all G columns in registers; a
