@@ -302,7 +302,7 @@ def run_ours(args, rank, world, local):
 
     # ---- end to end through the public API with host buffers
     e2e = run_e2e(args, pkv, pool, w, new_k, new_v, new_slots, q, tables, lens, max_ctx, ws, sb,
-                  stream, dev, world, win, kern)
+                  stream, dev, world, win, kern, out_ref=out)
 
     peak, peak_kind = measured_peaks()
     achieved = sb.decode / (dec_ms * 1e-3) / 1e9
@@ -352,11 +352,18 @@ def run_ours(args, rank, world, local):
 
 
 def run_e2e(args, pkv, pool, w, new_k, new_v, new_slots, q, tables, lens, max_ctx, ws, sb, stream,
-            dev, world, win=0, kern="auto"):
+            dev, world, win=0, kern="auto", out_ref=None):
     """Same step through the public API, but every step copies its inputs from pinned
     host memory and reads the output back.  The step's inputs (q, the appended K/V rows,
     their slots, the page tables and lengths) sit in one pinned staging buffer and go to
-    the device in one copy."""
+    the device in one copy; the output comes back in one copy.
+
+    Reported twice: ``value`` with the copies double-buffered (two device input buffers and
+    two outputs; step i + 1's inputs travel on an upload stream and step i's output on a
+    download stream while step i computes, as a serving loop would run it), and
+    ``serial_value`` with upload, compute and download in order on one stream.  Either way
+    every step moves all of its bytes, and the last output read back must equal the device
+    path's output bit for bit."""
     parts = [("q", q), ("k", new_k), ("v", new_v), ("slots", new_slots), ("tables", tables), ("lens", lens)]
     offs, size = {}, 0
     for name, t in parts:
@@ -364,40 +371,78 @@ def run_e2e(args, pkv, pool, w, new_k, new_v, new_slots, q, tables, lens, max_ct
         offs[name] = (size, nbytes)
         size += (nbytes + 255) // 256 * 256  # 256-byte aligned views
     host_buf = torch.empty(size, dtype=torch.uint8).pin_memory()
-    dev_buf = torch.empty(size, dtype=torch.uint8, device=dev)
-    dbuf = {}
     for name, t in parts:
         o, nbytes = offs[name]
         host_buf[o:o + nbytes].copy_(t.contiguous().cpu().view(torch.uint8).reshape(-1))
-        dbuf[name] = dev_buf[o:o + nbytes].view(t.dtype).view(t.shape)
-    out_d = torch.empty_like(q)
-    out_h = torch.empty(q.shape, dtype=q.dtype).pin_memory()
+    dev_buf = [torch.empty(size, dtype=torch.uint8, device=dev) for _ in range(2)]
+    dbuf = [{name: dev_buf[j][o:o + nb].view(t.dtype).view(t.shape)
+             for (name, t), (o, nb) in zip(parts, (offs[n] for n, _ in parts))} for j in range(2)]
+    out_d = [torch.empty_like(q) for _ in range(2)]
+    out_h = [torch.empty(q.shape, dtype=q.dtype).pin_memory() for _ in range(2)]
     h2d = size
-    d2h = out_h.numel() * out_h.element_size()
+    d2h = out_h[0].numel() * out_h[0].element_size()
+    up, down = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+    in_ready = [torch.cuda.Event() for _ in range(2)]
+    done = [torch.cuda.Event() for _ in range(2)]
+    out_back = [torch.cuda.Event() for _ in range(2)]
 
-    def step():
-        dev_buf.copy_(host_buf, non_blocking=True)
-        pkv.reshape_and_cache(pool, dbuf["k"], dbuf["v"], dbuf["slots"], stream)
-        pkv.paged_attention_decode(pool, dbuf["q"], dbuf["tables"], dbuf["lens"], w.scale, max_ctx,
-                                   out=out_d, workspace=ws, kernel=kern, window=win, stream=stream)
-        out_h.copy_(out_d, non_blocking=True)
+    def compute(j):
+        d = dbuf[j]
+        pkv.reshape_and_cache(pool, d["k"], d["v"], d["slots"], stream)
+        pkv.paged_attention_decode(pool, d["q"], d["tables"], d["lens"], w.scale, max_ctx,
+                                   out=out_d[j], workspace=ws, kernel=kern, window=win, stream=stream)
 
-    for _ in range(max(3, args.warmup)):
-        step()
-    torch.cuda.synchronize(dev)
+    def step_serial(i):
+        dev_buf[0].copy_(host_buf, non_blocking=True)
+        compute(0)
+        out_h[0].copy_(out_d[0], non_blocking=True)
+
+    def step_overlap(i):
+        j = i % 2
+        with torch.cuda.stream(up):
+            up.wait_event(done[j])  # step i - 2 has consumed this input buffer
+            dev_buf[j].copy_(host_buf, non_blocking=True)
+            in_ready[j].record(up)
+        stream.wait_event(in_ready[j])
+        stream.wait_event(out_back[j])  # step i - 2's output has left this buffer
+        compute(j)
+        done[j].record(stream)
+        with torch.cuda.stream(down):
+            down.wait_event(done[j])
+            out_h[j].copy_(out_d[j], non_blocking=True)
+            out_back[j].record(down)
+
+    def timed(step, n):
+        for i in range(max(3, args.warmup)):
+            step(i)
+        torch.cuda.synchronize(dev)
+        barrier(world)
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        up.wait_event(a)
+        down.wait_event(a)
+        for i in range(n):
+            step(i)
+        if step is step_overlap:
+            stream.wait_event(out_back[(n - 1) % 2])  # the last output is back on the host
+        b.record(stream)
+        torch.cuda.synchronize(dev)
+        barrier(world)
+        return max_over_ranks(a.elapsed_time(b), world, dev)
+
     n = max(10, min(args.steps, 500))
-    barrier(world)
-    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    a.record(stream)
-    for _ in range(n):
-        step()
-    b.record(stream)
-    torch.cuda.synchronize(dev)
-    barrier(world)
-    ms = max_over_ranks(a.elapsed_time(b), world, dev)
+    ms_serial = timed(step_serial, n)
+    if out_ref is not None and not torch.equal(out_h[0], out_ref.cpu()):
+        raise RuntimeError("the serial end-to-end output differs from the device path's")
+    ms = timed(step_overlap, n)
+    if out_ref is not None and not torch.equal(out_h[(n - 1) % 2], out_ref.cpu()):
+        raise RuntimeError("the double-buffered end-to-end output differs from the device path's")
     total = sum_over_ranks(float(sb.step) * n, world, dev)
     return {"value": round(total / (ms * 1e-3) / 1e9, 2), "unit": UNIT, "steps": n,
-            "ms_per_step": round(ms / n, 5), "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
+            "ms_per_step": round(ms / n, 5), "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+            "copies": "double-buffered on upload/download streams",
+            "serial_value": round(total / (ms_serial * 1e-3) / 1e9, 2),
+            "serial_ms_per_step": round(ms_serial / n, 5)}
 
 
 # ------------------------------------------------------------------ oracle legs
