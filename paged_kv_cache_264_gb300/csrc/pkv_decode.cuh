@@ -534,6 +534,9 @@ __global__ void __launch_bounds__(NW * 32)
   const int nb_item = min(nblk, blk0 + P) - blk0;
   const int32_t* trow = p.block_tables + size_t(b) * p.max_blocks_per_seq + blk0;
   for (int i = threadIdx.x; i < nb_item; i += C::kThreads) tbl[i] = __ldg(trow + i);
+  // The previous item's merge record sits in the rings (generic-proxy stores and loads);
+  // order those accesses before this item's tensor / bulk copies (async proxy) refill them.
+  fence_proxy_async_smem();
   __syncthreads();
 
   // Blocks of this warp: item blocks warp, warp + NW, ...

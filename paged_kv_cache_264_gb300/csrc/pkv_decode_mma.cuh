@@ -239,6 +239,9 @@ __global__ void __launch_bounds__(NW * 32, (KvTraits<KV>::kQuant && NC <= 8 && B
   } else {
     for (int i = threadIdx.x; i < nb_item; i += C::kThreads) tbl[i] = __ldg(trow + i);
   }
+  // The previous item's merge record sits in the rings (generic-proxy stores and loads);
+  // order those accesses before this item's tensor / bulk copies (async proxy) refill them.
+  fence_proxy_async_smem();
   __syncthreads();
 
   // The item's blocks are taken BPS at a time (one ring stage); warp w takes stages
