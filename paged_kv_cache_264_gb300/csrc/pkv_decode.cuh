@@ -502,7 +502,6 @@ __global__ void __launch_bounds__(NW * 32)
   constexpr uint32_t kFull = 0xffffffffu;
   extern __shared__ __align__(128) unsigned char smem[];
   griddep_wait();  // inputs may come from the previous kernel in the stream
-  griddep_launch_dependents();
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -773,6 +772,10 @@ __global__ void __launch_bounds__(NW * 32)
   }  // item located
   item = next_item(p, ss, ticket);
   }  // items
+  // The next kernel's CTAs may launch once every CTA of this one has passed here: a
+  // trigger at the start let a grid that leaves CTA slots free (the one-wave window
+  // plan) have the next call's CTAs placed early and unevenly across the SMs.
+  griddep_launch_dependents();
   finish_items(p);
 }
 

@@ -163,7 +163,6 @@ __global__ void __launch_bounds__(NW * 32, (KvTraits<KV>::kQuant && NC <= 8 && B
   constexpr int NT = C::kNT;
   constexpr uint32_t kFull = 0xffffffffu;
   griddep_wait();  // inputs may come from the previous kernel in the stream
-  griddep_launch_dependents();
   extern __shared__ unsigned char smem_raw[];
   unsigned char* smem = reinterpret_cast<unsigned char*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -863,6 +862,10 @@ __global__ void __launch_bounds__(NW * 32, (KvTraits<KV>::kQuant && NC <= 8 && B
   }  // item located
   item = next_item(p, ss, ticket);
   }  // items
+  // The next kernel's CTAs may launch once every CTA of this one has passed here: a
+  // trigger at the start let a grid that leaves CTA slots free (the one-wave window
+  // plan) have the next call's CTAs placed early and unevenly across the SMs.
+  griddep_launch_dependents();
   finish_items(p);
 }
 

@@ -221,9 +221,9 @@ __device__ __forceinline__ bool elect_one() {
 // may start while the previous kernel in the stream is still finishing; griddep_wait()
 // returns once that kernel has completed and its writes are visible, so it must precede
 // every read of data a previous kernel may have written.  griddep_launch_dependents()
-// lets the next kernel's launch begin; that kernel is only scheduled once every CTA of this
-// one has started, so it can never take resources this kernel still needs.  Both are no-ops
-// for ordinary launches.
+// lets the next kernel's launch begin once every CTA of this one has called it (or exited);
+// the decode kernels call it when a CTA has no more work, the append kernels at their
+// start.  Both are no-ops for ordinary launches.
 __device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 __device__ __forceinline__ void griddep_launch_dependents() {
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
