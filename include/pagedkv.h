@@ -241,10 +241,12 @@ PKV_API int32_t pkv_block_manager_refcount(const pkv_block_manager* manager, int
 
 /*
  * Decode-plan knobs.  Zero-initialise and set what you need; zero means automatic.
- *   partition_blocks: context partition (split-K) size in 16-token blocks; each
+ *   partition_blocks: context partition (split-K) size P in 16-token blocks; each
  *     (sequence, kv head, partition) becomes one work item, and sequences longer than
- *     one partition are combined by a log-sum-exp reduce.  0 = chosen from the batch
- *     shape and the device's SM count.
+ *     one partition are combined by a log-sum-exp reduce.  Partitions start at multiples
+ *     of P; a sequence's last partition also takes a remainder of at most P / 4 blocks
+ *     (so a partition holds up to P + P / 4 blocks).  0 = chosen from the batch shape and
+ *     the device's SM count.
  *   kernel: which decode kernel family runs.  Both serve, per (sequence, kv head), a tile
  *     of group * num_queries query columns, in chunks of up to 16 (tensor cores) or 8
  *     (CUDA cores) columns, each chunk one work unit that reads the kv head's blocks.

@@ -197,7 +197,7 @@ pkv_status make_plan(const pkv_pool* pool, int num_seqs, int num_q_heads, int ma
     P = static_cast<int>(ceil_div(max_nblk, ceil_div(max_nblk, P)));
   }
   plan->partition_blocks = P;
-  plan->max_parts = static_cast<int>(ceil_div(max_nblk, P));
+  plan->max_parts = pkv::partition_count(static_cast<int>(max_nblk), P);
   // Persistent CTAs pay off when the grid would hold idle slots, i.e. when sequences split
   // into different numbers of partitions; with one partition each, or one wave of equal
   // items under a window bound, the grid is exact.

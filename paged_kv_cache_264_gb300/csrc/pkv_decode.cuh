@@ -64,7 +64,7 @@
 
 namespace pkv {
 
-constexpr int kMaxPartitionBlocks = 1024;  // largest P (the staged table slice is 4 KiB)
+constexpr int kMaxPartitionBlocks = 1024;  // largest P
 
 template <KvType KV>
 struct KvTraits;
@@ -132,7 +132,7 @@ struct DecodeCfg {
   static constexpr size_t kBarOff = align_up(kProbOff + kProbBytes, 16);
   static constexpr size_t kTableOff = kBarOff + size_t(NW) * S * 8;
   static size_t smem_bytes(int partition_blocks, int sched_seqs) {
-    return kTableOff + size_t(partition_blocks) * 4 + sched_smem_bytes(sched_seqs, kThreads);
+    return kTableOff + size_t(partition_cap(partition_blocks)) * 4 + sched_smem_bytes(sched_seqs, kThreads);
   }
 
   static_assert(D % 32 == 0 && (D == 64 || D == 128), "head_dim 64 or 128");
@@ -235,7 +235,7 @@ __device__ __forceinline__ int first_block(const DecodeParams& p, int T) {
 __device__ __forceinline__ int seq_parts(const DecodeParams& p, int T) {
   if (T < p.num_queries || T > p.max_context_len) return 1;
   const int nblk = (T + kBlockSize - 1) / kBlockSize - first_block(p, T);
-  return (nblk + p.partition_blocks - 1) / p.partition_blocks;
+  return partition_count(nblk, p.partition_blocks);
 }
 
 // Whether token t of a block is visible to a column: lim = the column's visible tokens
@@ -507,7 +507,7 @@ __global__ void __launch_bounds__(NW * 32)
   const int lane = threadIdx.x & 31;
 
   int* tbl = reinterpret_cast<int*>(smem + C::kTableOff);
-  const SchedSmem ss = sched_smem(smem + C::kTableOff + size_t(p.partition_blocks) * 4,
+  const SchedSmem ss = sched_smem(smem + C::kTableOff + size_t(partition_cap(p.partition_blocks)) * 4,
                                   p.persistent ? p.num_seqs : 0);
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::kBarOff) + warp * S;
   unsigned char* ring = smem + size_t(warp) * S * C::kStageBytes;
@@ -530,7 +530,7 @@ __global__ void __launch_bounds__(NW * 32)
   } else {
   const int nblk = (T + kBlockSize - 1) / kBlockSize;
   const int blk0 = first_block(p, T) + part * P;
-  const int nb_item = min(nblk, blk0 + P) - blk0;
+  const int nb_item = (part == nparts - 1 ? nblk : min(nblk, blk0 + P)) - blk0;  // the last takes the rest
   const int32_t* trow = p.block_tables + size_t(b) * p.max_blocks_per_seq + blk0;
   for (int i = threadIdx.x; i < nb_item; i += C::kThreads) tbl[i] = __ldg(trow + i);
   // The previous item's merge record sits in the rings (generic-proxy stores and loads);

@@ -72,7 +72,7 @@ struct MmaCfg {
   static constexpr size_t kBarOff = align_up(kScaleOff + size_t(NW) * S * kScaleStage, 16);
   static constexpr size_t kTableOff = kBarOff + size_t(NW) * S * 8;
   static size_t smem_bytes(int partition_blocks, int sched_seqs) {
-    return 1024 /* alignment slack */ + kTableOff + size_t(partition_blocks) * 4 +
+    return 1024 /* alignment slack */ + kTableOff + size_t(partition_cap(partition_blocks)) * 4 +
            sched_smem_bytes(sched_seqs, kThreads);
   }
 
@@ -173,7 +173,7 @@ __global__ void __launch_bounds__(NW * 32, (KvTraits<KV>::kQuant && NC <= 8 && B
   const int gj = lane & 3;   // fragment column pair
 
   int* tbl = reinterpret_cast<int*>(smem + C::kTableOff);
-  const SchedSmem ss = sched_smem(smem + C::kTableOff + size_t(p.partition_blocks) * 4,
+  const SchedSmem ss = sched_smem(smem + C::kTableOff + size_t(partition_cap(p.partition_blocks)) * 4,
                                   p.persistent ? p.num_seqs : 0);
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::kBarOff) + warp * S;
   unsigned char* ring = smem + size_t(warp) * S * C::kStageBytes;
@@ -222,7 +222,8 @@ __global__ void __launch_bounds__(NW * 32, (KvTraits<KV>::kQuant && NC <= 8 && B
   // still lie inside the table row (part * P < max_blocks_per_seq) and are never used.
   const int32_t* trow0 = p.block_tables + size_t(it.b) * p.max_blocks_per_seq + it.part * P;
   int tpre = 0;
-  if (!kGen && int(threadIdx.x) < min(P, p.max_blocks_per_seq - it.part * P)) tpre = __ldg(trow0 + threadIdx.x);
+  if (!kGen && int(threadIdx.x) < min(partition_cap(P), p.max_blocks_per_seq - it.part * P))
+    tpre = __ldg(trow0 + threadIdx.x);
   if (locate_len(p, __ldg(p.context_lens + it.b), it)) {
   const int b = it.b, kvh = it.kvh, part = it.part, nparts = it.nparts, T = it.T;
   if (it.bad_len) {
@@ -230,7 +231,7 @@ __global__ void __launch_bounds__(NW * 32, (KvTraits<KV>::kQuant && NC <= 8 && B
   } else {
   const int nblk = (T + kBlockSize - 1) / kBlockSize;
   const int blk0 = (kGen ? first_block(p, T) : 0) + part * P;
-  const int nb_item = min(nblk, blk0 + P) - blk0;
+  const int nb_item = (part == nparts - 1 ? nblk : min(nblk, blk0 + P)) - blk0;  // the last takes the rest
   const int32_t* trow = p.block_tables + size_t(b) * p.max_blocks_per_seq + blk0;
   if constexpr (!kGen) {
     if (int(threadIdx.x) < nb_item) tbl[threadIdx.x] = tpre;

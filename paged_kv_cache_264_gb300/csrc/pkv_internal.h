@@ -15,6 +15,19 @@ constexpr uint64_t kWaitTimeoutNs = 2000000000ull;  // bounded waits give up aft
 constexpr int kMaxSchedSeqs = 4096;  // largest batch scheduled by the persistent grid
 constexpr int kNoWindow = 1 << 30;   // window value meaning "no window" (contexts are shorter)
 
+// Partitions of a sequence's nblk blocks for partition size P (decode kernels, partition
+// reduce and host plan alike).  They start at multiples of P, so that an item's slice of the
+// block table can be requested before its context length is known, and the last one also
+// takes a remainder of at most P / 4 blocks instead of leaving it to an item of its own
+// (with its own partial to merge): a partition holds up to partition_cap(P) blocks.
+__host__ __device__ constexpr int partition_count(int nblk, int P) {
+  return nblk - P / 4 <= P ? 1 : (nblk - P / 4 + P - 1) / P;
+}
+__host__ __device__ constexpr int partition_cap(int P) { return P + P / 4; }
+static_assert(partition_count(64, 64) == 1 && partition_count(80, 64) == 1 && partition_count(81, 64) == 2 &&
+                  partition_count(1024, 64) == 16 && partition_count(7, 1) == 7 && partition_count(5, 4) == 1,
+              "partition_count");
+
 // Device error word bits (mirror PKV_DEVERR_* of the public header).
 constexpr uint32_t kErrBlockId = 0x1u;
 constexpr uint32_t kErrContextLen = 0x2u;

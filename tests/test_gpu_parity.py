@@ -328,6 +328,25 @@ def test_host_validation_errors():
     pool.close()
 
 
+@pytest.mark.parametrize("kernel", KERNELS)
+@pytest.mark.parametrize("kv", ["bf16", "int8", "fp8"])
+def test_small_remainder_joins_last_partition(kv, kernel):
+    """With partition size P, a remainder of at most P / 4 blocks is taken by a sequence's
+    last partition (which then holds up to P + P / 4 blocks) instead of an item of its own.
+    P = 16: 20 blocks are one item; 21 blocks two (16 + 5); 36 blocks two (16 + 20); 37
+    blocks three (16 + 16 + 5); 15.4 blocks one; a one-token tail past 20 blocks two."""
+    blocks = [20, 21, 36, 37]
+    lens = [16 * n for n in blocks] + [15 * 16 + 7, 20 * 16 + 1, 20 * 16 - 9]
+    w = custom(lens, 8, 2, 128, kv, seed=67)
+    pool = pkv.PagedKVPool(w.num_blocks, w.num_kv_heads, w.head_dim, kv, fill=0)
+    for nblk, parts in ((20, 1), (21, 2), (36, 2), (37, 3)):
+        plan = pkv.decode_plan(pool, 1, 8, 16 * nblk, partition_blocks=16, kernel=kernel)
+        assert plan["max_partitions"] == parts, (nblk, plan)
+        assert plan["kernels_per_call"] == (1 if parts == 1 else 2)
+    pool.close()
+    check_all(w, kv, 16, kernel=kernel)
+
+
 def test_launch_count_and_plan():
     w = custom([300, 40], 8, 2, 128, "bf16", seed=61)
     pool = gpu_pool_from(w, "bf16", garbage=False)

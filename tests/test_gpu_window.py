@@ -124,7 +124,9 @@ def test_window_plan_reads_fewer_blocks():
     pool = pkv.PagedKVPool(4, 32, 128, "bf16", fill=0)
     full = pkv.decode_plan(pool, 8, 32, 32768, partition_blocks=64)
     win = pkv.decode_plan(pool, 8, 32, 32768, partition_blocks=64, window=4096)
-    assert full["max_partitions"] == 32 and win["max_partitions"] == 5  # ceil((256 + 1) / 64)
+    # 2048 blocks: 32 partitions of 64; the window's 257 blocks: 4, the last taking the
+    # 1-block remainder (a remainder of at most P / 4 joins the last partition)
+    assert full["max_partitions"] == 32 and win["max_partitions"] == 4
     assert pkv.decode_workspace_bytes(pool, 8, 32, 32768, 64, window=4096) < \
         pkv.decode_workspace_bytes(pool, 8, 32, 32768, 64)
     with pytest.raises(pkv.PagedKVError, match="invalid"):
