@@ -177,12 +177,14 @@ pkv_status make_plan(const pkv_pool* pool, int num_seqs, int num_q_heads, int ma
     P = static_cast<int>(ceil_div(max_nblk, parts));
     one_wave = true;
   } else {
-    // Measured on GB300: items of 128 blocks (CUDA-core kernel) or 64 blocks (tensor-core
-    // kernel, which consumes a block faster) balance fewer partials against load balance.
-    // The tensor-core kernel takes 128-block items too when that leaves every sequence in
-    // one item (no partials, no reduce kernel) and for 16-column tiles (twice the work per
-    // block).
-    P = plan->kernel == PKV_KERNEL_TENSOR_CORE ? kItemBlocksTensorCore : kItemBlocksCudaCore;
+    // Measured on GB300: items of 128 blocks (CUDA-core kernel, bf16 pools) or 64 blocks
+    // (tensor-core kernel, which consumes a block faster, and CUDA-core kernel on INT8/FP8
+    // pools, whose items carry half the bytes: 409.6 against 428.0 us on the 256-sequence
+    // INT8 batch) balance fewer partials against load balance.  The tensor-core kernel takes
+    // 128-block items too when that leaves every sequence in one item (no partials, no
+    // reduce kernel) and for 16-column tiles (twice the work per block).
+    P = plan->kernel == PKV_KERNEL_TENSOR_CORE || pool->dtype != PKV_KV_BF16 ? kItemBlocksTensorCore
+                                                                            : kItemBlocksCudaCore;
     if (plan->kernel == PKV_KERNEL_TENSOR_CORE && (max_nblk <= 128 || plan->cols == 16)) P = 128;
     // Shrink the partition while the batch would not fill the GPU twice over.
     while (P > 4 && units * ceil_div(max_nblk, P) < 2 * resident) P /= 2;
