@@ -414,6 +414,20 @@ def test_large_batch_classic_grid(kernel, partition_blocks):
     check_all(w, "bf16", partition_blocks, kernel=kernel, seqs=list(range(0, 4200, 97)))
 
 
+@pytest.mark.parametrize("kernel", KERNELS)
+def test_batch_at_the_persistent_scheduler_limit(kernel):
+    """Exactly 4096 sequences, the largest batch the persistent scheduler serves: its prefix
+    sum then takes 16 KiB of shared memory per CTA.  Split sequences make the plan take it."""
+    g = torch.Generator().manual_seed(93)
+    lens = torch.randint(1, 200, (4096,), generator=g)
+    w = custom(lens, 8, 2, 64, "int8", seed=94)
+    pool = pkv.PagedKVPool(1, 2, 64, "int8", fill=0)
+    plan = pkv.decode_plan(pool, 4096, 8, int(lens.max()), 4, kernel=kernel)
+    pool.close()
+    assert plan["kernels_per_call"] == 2
+    check_all(w, "int8", 4, kernel=kernel, seqs=list(range(0, 4096, 61)) + [4095])
+
+
 @pytest.mark.parametrize("kv", ["bf16", "int8"])
 def test_scheduler_counters_reset_between_calls(kv):
     """The persistent scheduler's counters live in the pool's device memory and reset
