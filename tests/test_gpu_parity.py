@@ -417,12 +417,14 @@ def test_large_batch_classic_grid(kernel, partition_blocks):
 @pytest.mark.parametrize("kernel", KERNELS)
 @pytest.mark.parametrize("kv", ["bf16", "int8"])
 @pytest.mark.parametrize("partition_blocks", [1, 2, 3])
-def test_reduce_over_many_partitions(kv, kernel, partition_blocks):
+@pytest.mark.parametrize("d", [64, 128])
+def test_reduce_over_many_partitions(kv, kernel, partition_blocks, d):
     """More than 32 partitions per row: the reduce kernel's lanes then hold several
     partitions each and its accumulator loop runs past its look-ahead (125 blocks in 125, 63
-    or 42 partitions), next to short sequences that do not split."""
-    w = custom([2000, 33, 1999, 700], 8, 2, 128, kv, seed=97)
-    pool = pkv.PagedKVPool(1, 2, 128, kv, fill=0)
+    or 42 partitions), next to short sequences that do not split; both head sizes (the
+    reduce reads 4 or 2 floats per lane)."""
+    w = custom([2000, 33, 1999, 700], 8, 2, d, kv, seed=97)
+    pool = pkv.PagedKVPool(1, 2, d, kv, fill=0)
     plan = pkv.decode_plan(pool, w.num_seqs, w.num_q_heads, w.max_context_len, partition_blocks, kernel=kernel)
     pool.close()
     assert plan["max_partitions"] > 32
